@@ -1,0 +1,233 @@
+/*
+ * qsa.h -- C ABI of libqsa.so: QSA (Qwen Sparse Attention) block-sparse GQA
+ * on one GB300 (sm_103a).
+ *
+ * Four entry points make up the hot path:
+ *   qsa_indexer_prefill  -- weight-free block indexer over a padded prefill batch
+ *   qsa_indexer_decode   -- the same indexer for one new token per sequence,
+ *                           reading and updating its state in the paged KV pool
+ *   qsa_sparse_prefill   -- sparse GQA attention over dense padded BSND Q/K/V
+ *   qsa_sparse_decode    -- split-K sparse GQA decode attention over the pool
+ *
+ * Where each operation is defined (page title, then section):
+ *   "Cute Dsl Qsa Sparse Runner" (TensorRT-Edge-LLM C++ API): the runner
+ *       classes, struct QsaSparsePrefillParams, struct QsaSparseDecodeParams,
+ *       kMaxSplits = 8, kPartialRows = 16.
+ *   "Qsa Attention Plugin" (TensorRT-Edge-LLM C++ API): class
+ *       QsaAttentionPlugin -- fused step 2 (prefill indexer, top-512 blocks,
+ *       expand + causal tail, [B, S, 2051] lists), step 3 (decode indexer
+ *       B1/B2/B3), the attributes of the constructor, and the "KV pool
+ *       contract" (widened rows, tail state of head 0).
+ *   "spark_model/layers/ops/qsa.rs" (Atlas Inference API docs): doc comments
+ *       of qsa_block_pool, qsa_qprep, qsa_qprep_rows, qsa_score, qsa_score_rows
+ *       (block pooling, query prep, block score sum_h relu(q_h . k_b)/sqrt(hd)).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers (cudaMalloc'd or equivalent) of
+ *     the GPU that is current on the calling thread; the caller owns every
+ *     buffer.  The library allocates nothing and never synchronises the host:
+ *     each call only enqueues kernels on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream).
+ *   - fp16 means IEEE binary16.  Layouts are row-major, innermost index last.
+ *   - Parameters are validated on the host before anything is launched.  A
+ *     non-QSA_OK status means nothing was enqueued, except QSA_ERR_CUDA, which
+ *     reports a failed launch (the CUDA error is left for cudaGetLastError and
+ *     described by qsa_last_error_message()).
+ *   - No C++ exception crosses this boundary.
+ */
+#ifndef QSA_H
+#define QSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QSA_OK = 0,
+  QSA_ERR_INVALID_ARG = 1, /* null pointer, negative or inconsistent size        */
+  QSA_ERR_UNSUPPORTED = 2, /* valid shape that these kernels do not implement   */
+  QSA_ERR_WORKSPACE = 3,   /* workspace missing, too small or misaligned        */
+  QSA_ERR_CUDA = 4         /* a kernel launch failed                            */
+} qsa_status_t;
+
+/* ------------------------------------------------------------------ indexer */
+
+/* Prefill indexer ("Qsa Attention Plugin", fused step 2; "qsa.rs",
+ * qsa_block_pool / qsa_qprep_rows / qsa_score_rows).  Normal prefill from
+ * position 0 (no chunked prefill).  For each sequence b with live length
+ * L = contextLengths[b] and each row t < L it writes the -1-padded list
+ *   { r*g .. r*g + r-1 : g among the top-`budget` complete blocks }
+ *     U { r*n_c .. t },      n_c = floor((t+1)/r),
+ * where block keys are mean(r raw keys) -> RMSNorm*(1+kNormW) -> RoPE at r*g
+ * (stored fp16), queries are RMSNorm*(1+qNormW) -> RoPE at t (fp32), and the
+ * score of block g is sum_h relu(q_h . kbar_g) / sqrt(headDim).  When
+ * n_c <= budget every block is kept; exact score ties go to the lower block
+ * id.  Lists are written in ascending token order; rows t >= L are all -1. */
+typedef struct {
+  const void* idxQ;              /* fp16 [B, S, numHeads, headDim] raw index queries     */
+  const void* idxK;              /* fp16 [B, S, headDim] raw index keys (one shared head)  */
+  const float* qNormW;           /* fp32 [headDim]; the norm multiplies by (1 + w)         */
+  const float* kNormW;           /* fp32 [headDim]                                          */
+  const int32_t* contextLengths; /* int32 [B], 0 <= L <= S                                  */
+  int32_t* indices;              /* out int32 [B, S, topK]                                  */
+  void* workspace;               /* >= qsa_indexer_prefill_workspace_size(), 256-B aligned */
+  size_t workspaceBytes;
+  int32_t batchSize;             /* B                                                       */
+  int32_t seqLen;                /* S (padded length)                                       */
+  int32_t numHeads;              /* indexer heads Hi, 1..8                                  */
+  int32_t headDim;               /* indexer head dim di: 64 or 128                          */
+  int32_t rotDim;                /* rotated dims: even, <= headDim                           */
+  int32_t compressRatio;         /* r (tokens per block); 4 on the pages                    */
+  int32_t budget;                /* blocks kept per row; 512 on the pages                    */
+  int32_t topK;                  /* list width, must equal budget*r + r - 1                  */
+  float ropeTheta;               /* RoPE base                                                */
+  float rmsNormEps;              /* RMSNorm epsilon                                          */
+  void* stream;                  /* cudaStream_t                                             */
+} QsaIndexerPrefillParams;
+
+/* Decode indexer ("Qsa Attention Plugin", step 3: B1 fused q-prep + predicated
+ * tail write / compress, B2 block scores from the kbar tails, B3 deterministic
+ * top-`budget` + expand).  One new token per sequence at t = L-1 where
+ * L = contextLengths[b] is the TOTAL length including that token.  Indexer
+ * state lives in head 0 of the pool rows, columns [kvHeadDim, kvHeadDim+headDim)
+ * ("KV pool contract"): block g's key in the V-row tail of token r*g, the raw
+ * index key of each token of the trailing incomplete block in its K-row tail.
+ * This call (B1) stores the new raw key in the K-row tail of token t when t
+ * leaves its block incomplete; when t completes block g = (t+1)/r - 1 it
+ * instead computes that block's key from the K-row tails of tokens
+ * r*g .. t-1 plus the new raw key and stores it in the V-row tail of token r*g.
+ * No other pool byte is written.  Then it scores every complete block and
+ * writes the row's list exactly as the prefill indexer would for row t.
+ * A sequence with L == 0 gets an all -1 list and no pool write. */
+typedef struct {
+  const void* idxQ;              /* fp16 [B, numHeads, headDim] raw index query of the new token */
+  const void* idxK;              /* fp16 [B, headDim] raw index key of the new token             */
+  const float* qNormW;           /* fp32 [headDim]                                                */
+  const float* kNormW;           /* fp32 [headDim]                                                */
+  void* kvPool;                  /* fp16 [numFlatPages, 128, numKVHeads, poolHeadDim]; tails R/W  */
+  const int32_t* pageTable;      /* int32 [B, 2, maxPagesPerSeq]: row 0 K page ids, row 1 V page
+                                    ids (absolute pool page ids, i.e. pre-offset by numPages)     */
+  const int32_t* contextLengths; /* int32 [B], total lengths, 0 <= L <= 128*maxPagesPerSeq        */
+  int32_t* indices;              /* out int32 [B, 1, topK]                                        */
+  void* workspace;               /* >= qsa_indexer_decode_workspace_size(), 256-B aligned, and
+                                    ZERO-FILLED before its first use; every call leaves its
+                                    counters at zero again                                         */
+  size_t workspaceBytes;
+  int32_t batchSize;             /* B                                                              */
+  int32_t numKVHeads;            /* Hkv of the pool                                                */
+  int32_t kvHeadDim;             /* attention head dim D: the tail starts at column D              */
+  int32_t poolHeadDim;           /* >= kvHeadDim + headDim                                         */
+  int32_t numFlatPages;          /* pages in the pool (both planes)                                */
+  int32_t maxPagesPerSeq;        /* page-table row length                                          */
+  int32_t numHeads;              /* indexer heads Hi, 1..8                                         */
+  int32_t headDim;               /* indexer head dim di: 64 or 128                                 */
+  int32_t rotDim;
+  int32_t compressRatio;         /* r; must divide 128                                              */
+  int32_t budget;
+  int32_t topK;                  /* must equal budget*r + r - 1                                    */
+  float ropeTheta;
+  float rmsNormEps;
+  void* stream;
+} QsaIndexerDecodeParams;
+
+/* --------------------------------------------------------------- attention */
+
+/* Sparse GQA prefill ("Cute Dsl Qsa Sparse Runner", struct
+ * QsaSparsePrefillParams, field for field).  For each live row t < L and query
+ * head h (KV head g = h / (numQHeads/numKVHeads)):
+ *   o[b,t,h] = sum_{j in list} softmax_j(attentionScale * q[b,t,h] . k[b,j,g]) v[b,j,g]
+ * over the entries j >= 0 of indices[b,t,:].  Causality lives entirely in the
+ * list: no positional mask is applied.  Output rows t >= L are exact zeros;
+ * a live row whose list has no valid entry is zero too.  K/V rows are only
+ * read where a list names them; an entry outside [0, L) is skipped (a list
+ * must only name live tokens). */
+typedef struct {
+  const void* qPtr;              /* fp16 [B, S, numQHeads, headDim]  */
+  const void* kPtr;              /* fp16 [B, S, numKVHeads, headDim] */
+  const void* vPtr;              /* fp16 [B, S, numKVHeads, headDim] */
+  void* oPtr;                    /* out fp16 [B, S, numQHeads, headDim] */
+  const int32_t* indices;        /* int32 [B, S, topK], -1 padded on the right */
+  const int32_t* contextLengths; /* int32 [B], 0 <= L <= S */
+  int32_t batchSize;
+  int32_t seqLen;
+  int32_t numQHeads;
+  int32_t numKVHeads;            /* numQHeads / numKVHeads must be 1..16 */
+  int32_t headDim;               /* 128 */
+  int32_t topK;
+  float attentionScale;          /* multiplier of q . k (not assumed 1/sqrt(D)) */
+  void* stream;
+} QsaSparsePrefillParams;
+
+/* Split-K sparse GQA decode ("Cute Dsl Qsa Sparse Runner", struct
+ * QsaSparseDecodeParams, field for field).  One query token per sequence;
+ * K/V rows come from the pool through the page table, and only columns
+ * [0, headDim) of a pool row are read.  The list of each (sequence, KV head)
+ * is cut into kMaxSplits = 8 contiguous slices; each slice writes an fp32
+ * partial (O, m, l) and the last slice to finish merges the eight partials
+ * into oPtr and resets its counter to zero.  splitCounters MUST be zero on
+ * entry (zero-fill the buffer once; every call leaves it zeroed). */
+typedef struct {
+  const void* qPtr;              /* fp16 [B, 1, numQHeads, headDim] */
+  const void* kvPoolPtr;         /* fp16 [numFlatPages, 128, numKVHeads, poolHeadDim] */
+  const int32_t* pageTable;      /* int32 [B, 2, maxPagesPerSeq] (row 1 pre-offset by numPages) */
+  const int32_t* indices;        /* int32 [B, 1, topK], -1 padded */
+  const int32_t* contextLengths; /* int32 [B], total lengths including the new token */
+  void* oPtr;                    /* out fp16 [B, 1, numQHeads, headDim] */
+  float* partialO;               /* fp32 [B*numKVHeads*8, 16, headDim] */
+  float* partialStats;           /* fp32 [B*numKVHeads*8, 2, 16] */
+  int32_t* splitCounters;        /* int32 [B*numKVHeads], zero on entry */
+  int32_t batchSize;
+  int32_t numQHeads;
+  int32_t numKVHeads;            /* numQHeads / numKVHeads must be 1..16 */
+  int32_t headDim;               /* 128 */
+  int32_t poolHeadDim;           /* >= headDim, multiple of 8 */
+  int32_t numFlatPages;          /* 2 * numPages (both planes) */
+  int32_t maxPagesPerSeq;
+  int32_t topK;
+  float attentionScale;
+  void* stream;
+} QsaSparseDecodeParams;
+
+/* ------------------------------------------------------------ entry points */
+
+qsa_status_t qsa_indexer_prefill(const QsaIndexerPrefillParams* params);
+qsa_status_t qsa_indexer_decode(const QsaIndexerDecodeParams* params);
+qsa_status_t qsa_sparse_prefill(const QsaSparsePrefillParams* params);
+qsa_status_t qsa_sparse_decode(const QsaSparseDecodeParams* params);
+
+/* Workspace bytes of the indexers (0 when the sizes are invalid). */
+size_t qsa_indexer_prefill_workspace_size(int32_t batchSize, int32_t seqLen, int32_t headDim,
+                                          int32_t compressRatio);
+size_t qsa_indexer_decode_workspace_size(int32_t batchSize, int32_t maxPagesPerSeq,
+                                         int32_t compressRatio, int32_t budget);
+
+/* Element counts of the split-K decode workspace ("Cute Dsl Qsa Sparse Runner",
+ * QsaSparseDecodeParams: partialO, partialStats, splitCounters). */
+size_t qsa_sparse_decode_partial_o_elems(int32_t batchSize, int32_t numKVHeads, int32_t headDim);
+size_t qsa_sparse_decode_partial_stats_elems(int32_t batchSize, int32_t numKVHeads);
+size_t qsa_sparse_decode_counter_elems(int32_t batchSize, int32_t numKVHeads);
+int32_t qsa_sparse_decode_max_splits(void);   /* kMaxSplits = 8   */
+int32_t qsa_sparse_decode_partial_rows(void); /* kPartialRows = 16 */
+
+/* Whether these kernels cover a shape (the runners' canImplement): 1 or 0. */
+int32_t qsa_sparse_prefill_can_implement(int32_t numQHeads, int32_t numKVHeads, int32_t headDim);
+int32_t qsa_sparse_decode_can_implement(int32_t numQHeads, int32_t numKVHeads, int32_t headDim,
+                                        int32_t poolHeadDim);
+
+/* Longest padded prefill length the prefill indexer accepts (it keeps a row
+ * group's block scores on chip). */
+int32_t qsa_indexer_prefill_max_seq_len(void);
+
+/* Human-readable name of a status, and the detail of the last failure on the
+ * calling thread (never NULL; empty when there was none). */
+const char* qsa_status_string(qsa_status_t status);
+const char* qsa_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_H */
