@@ -1,0 +1,388 @@
+#!/usr/bin/env python3
+"""Benchmark of the QSA hot path on GB300; prints ONE JSON line.
+
+Headline: prefill tokens/s on the 8K workload (B=1, S=8192, Hq=32, Hkv=4,
+D=128, indexer 8 x 128, rot 64, ratio 4, budget 512, topK 2051): one step is
+qsa_indexer_prefill + qsa_sparse_prefill over one batch already resident in
+HBM, timed with CUDA events per step on the launching stream, L2 flushed
+(a 512 MB write) between steps outside the timed events.  The same line
+carries the decode us/step of the two decode workloads (one CUDA-graph replay
+of qsa_indexer_decode + qsa_sparse_decode), the roofline of the dominant
+kernel, an end-to-end figure through the C ABI with host buffers, the CPU
+oracle baseline and the SM clocks sampled during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs the same
+workload on its own GPU (replicas: the path shards by sequence with no
+exchange); value is the sum over ranks, time the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from block_sparse_gqa_qsa_gb300 import synthetic as syn  # noqa: E402
+
+METRIC = "QSA prefill tokens/s & decode us/step; % of HBM/tensor roofline on 1 GB300"
+UNIT = "tokens/s"
+HEADLINE = syn.PREFILL_8K
+DECODES = (syn.DECODE_32, syn.DECODE_LONG)
+FLUSH_BYTES = 512 << 20  # > 129 MB L2
+
+
+def f32(x):
+    return float(np.float32(x))
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p.get("bf16_tflops"), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------ algorithmic work
+def prefill_work(cfg, ctx):
+    """Sum of live tokens, sum of list lengths cnt(t), gathered bytes and MMA flops of the attention."""
+    r, beta = cfg.ratio, cfg.budget
+    tok = 0
+    cnt = 0
+    for L in ctx:
+        L = int(L)
+        t = np.arange(L, dtype=np.int64)
+        n_c = (t + 1) // r
+        cnt += int(np.sum(np.minimum(n_c, beta) * r + (t + 1 - n_c * r)))
+        tok += L
+    kv = cfg.Hkv * cnt * 2 * cfg.D * 2
+    qo = 2 * tok * cfg.Hq * cfg.D * 2
+    lists = cfg.B * cfg.S * cfg.topK * 4
+    flops = 4 * cnt * cfg.Hq * cfg.D
+    return tok, cnt, kv + qo + lists, flops
+
+
+def decode_work(cfg, ctx):
+    """Bytes one decode step must move: block keys, gathered K/V rows, q/o/lists."""
+    r, beta = cfg.ratio, cfg.budget
+    kbar = sum((int(L) // r) * cfg.di * 2 for L in ctx)
+    cnt = sum(min(int(L) // r, beta) * r + (int(L) - (int(L) // r) * r) for L in ctx)
+    kv = cfg.Hkv * cnt * 2 * cfg.D * 2
+    small = cfg.B * (2 * cfg.Hq * cfg.D * 2 + cfg.Hi * cfg.di * 2 + cfg.topK * 4 * 2)
+    return kbar, kv, kbar + kv + small
+
+
+# ------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling during the timed region (read-only queries)."""
+    FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active"
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        else:
+            self.lines = []
+
+    def summary(self):
+        sm, mx, reasons = [], [], 0
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                reasons |= int(parts[3], 16) if parts[3].startswith("0x") else int(parts[3])
+            except (ValueError, IndexError):
+                pass
+        names = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+                 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+                 0x100: "display_clock_setting"}
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": [n for b, n in names.items() if reasons & b], "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+class Prefill:
+    def __init__(self, cfg, dev):
+        from block_sparse_gqa_qsa_gb300 import _binding as qb
+        self.qb, self.cfg, self.dev = qb, cfg, dev
+        self.host = syn.make_prefill(cfg)
+        self.t = {k: v.to(dev) for k, v in self.host.items()}
+        self.ws = qb.alloc_workspace(qb.indexer_prefill_workspace_size(cfg.B, cfg.S, cfg.di, cfg.ratio), dev)
+        self.ind = torch.empty((cfg.B, cfg.S, cfg.topK), dtype=torch.int32, device=dev)
+        self.out = torch.empty((cfg.B, cfg.S, cfg.Hq, cfg.D), dtype=torch.float16, device=dev)
+
+    def indexer(self, t=None):
+        c, t = self.cfg, t or self.t
+        self.qb.indexer_prefill(t["idxQ"], t["idxK"], t["wq"], t["wk"], t["ctx"], self.ind, self.ws, rot=c.rot,
+                                ratio=c.ratio, budget=c.budget, topK=c.topK, theta=c.theta, eps=c.eps)
+
+    def attention(self, t=None):
+        c, t = self.cfg, t or self.t
+        self.qb.sparse_prefill(t["q"], t["k"], t["v"], self.ind, t["ctx"], self.out, f32(c.scale))
+
+
+class Decode:
+    def __init__(self, cfg, dev):
+        from block_sparse_gqa_qsa_gb300 import _binding as qb
+        self.qb, self.cfg, self.dev = qb, cfg, dev
+        d = syn.make_decode(cfg, device=dev)
+        self.ctx_host = d["ctx"].clone()
+        self.d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+        self.ws = qb.alloc_workspace(qb.indexer_decode_workspace_size(cfg.B, cfg.maxPagesPerSeq, cfg.ratio,
+                                                                      cfg.budget), dev)
+        po, ps, pc = qb.sparse_decode_workspace_elems(cfg.B, cfg.Hkv, cfg.D)
+        self.parts = (torch.zeros(po, device=dev), torch.zeros(ps, device=dev),
+                      torch.zeros(pc, dtype=torch.int32, device=dev))
+        self.ind = torch.empty((cfg.B, 1, cfg.topK), dtype=torch.int32, device=dev)
+        self.out = torch.empty((cfg.B, 1, cfg.Hq, cfg.D), dtype=torch.float16, device=dev)
+
+    def step(self):
+        c, d = self.cfg, self.d
+        self.qb.indexer_decode(d["idxQ"], d["idxK"], d["wq"], d["wk"], d["pool"], d["page_table"], d["ctx"],
+                               self.ind, self.ws, D=c.D, rot=c.rot, ratio=c.ratio, budget=c.budget, topK=c.topK,
+                               theta=c.theta, eps=c.eps)
+        self.qb.sparse_decode(d["q"], d["pool"], d["page_table"], self.ind, d["ctx"], self.out, *self.parts, D=c.D,
+                              scale=f32(c.scale))
+
+
+def time_decode(dec, flush, reps=50, warm=10):
+    for _ in range(3):
+        dec.step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        dec.step()
+    for _ in range(warm):
+        g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        flush.add_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) * 1000.0)
+    return statistics.median(times), times
+
+
+def run_ours(args, rank, world, dev):
+    from block_sparse_gqa_qsa_gb300 import _binding as qb
+    qb.lib()
+    hbm_peak, _, peak_kind = peaks()
+    cfg = HEADLINE
+    pf = Prefill(cfg, dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(max(args.warmup, 3)):
+        pf.indexer()
+        pf.attention()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_idx, t_att, t_step = [], [], []
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for _ in range(args.steps):
+            flush.add_(1)  # L2 flush, outside the timed events
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record()
+            pf.indexer()
+            e[1].record()
+            pf.attention()
+            e[2].record()
+            e[2].synchronize()
+            t_idx.append(e[0].elapsed_time(e[1]))
+            t_att.append(e[1].elapsed_time(e[2]))
+            t_step.append(e[0].elapsed_time(e[2]))
+    torch.cuda.synchronize()
+    ms = statistics.mean(t_step)
+    if world > 1:
+        torch.distributed.barrier()
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    tok, cnt, gbytes, flops = prefill_work(cfg, pf.host["ctx"].tolist())
+    value = world * tok / (ms / 1000.0)
+    att_ms = statistics.mean(t_att)
+    achieved = gbytes / (att_ms / 1000.0) / 1e9
+
+    # end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    pinned = {k: v.pin_memory() for k, v in pf.host.items()}
+    out_host = torch.empty(pf.out.shape, dtype=pf.out.dtype).pin_memory()
+    dev_bufs = {k: torch.empty_like(v, device=dev) for k, v in pf.host.items()}
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_ms = []
+    for i in range(max(args.steps // 2, 3) + 2):
+        flush.add_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for k in dev_bufs:
+            dev_bufs[k].copy_(pinned[k], non_blocking=True)
+        pf.indexer(dev_bufs)
+        pf.attention(dev_bufs)
+        out_host.copy_(pf.out, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        if i >= 2:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_value = world * tok / (statistics.mean(e2e_ms) / 1000.0)
+
+    # decode workloads: one graph replay per step
+    decode = []
+    for dc in DECODES:
+        dec = Decode(dc, dev)
+        us, _ = time_decode(dec, flush)
+        kbar, kv, total = decode_work(dc, dec.ctx_host.tolist())
+        decode.append({"workload": dc.name, "us_per_step": round(us, 2), "bytes_per_step": total,
+                       "roofline_us": round(total / (hbm_peak * 1e9) * 1e6, 2),
+                       "frac": round(total / (hbm_peak * 1e9) * 1e6 / us, 4), "kernels_per_step": 2})
+        del dec
+        torch.cuda.empty_cache()
+    return {
+        "value": value, "ms": ms, "tok": tok, "t_idx": statistics.mean(t_idx), "t_att": att_ms,
+        "achieved": achieved, "gbytes": gbytes, "flops": flops, "cnt": cnt, "hbm_peak": hbm_peak,
+        "peak_kind": peak_kind, "e2e": e2e_value, "h2d": h2d, "d2h": d2h, "clocks": clk.summary(),
+        "decode": decode, "launches": 3 * args.steps,
+    }
+
+
+# --------------------------------------------------------- the CPU oracle
+def oracle_sample(cfg, t_np, nrows, nthreads=0):
+    """Oracle prefill (indexer + attention) on `nrows` rows spread over the sequence; returns (rows, seconds)."""
+    import oracle
+    rows = np.linspace(0, cfg.S - 1, nrows).astype(np.int64)
+    t0 = time.perf_counter()
+    ind = oracle.indexer_prefill(t_np["idxQ"], t_np["idxK"], t_np["wq"], t_np["wk"], t_np["ctx"], rot=cfg.rot,
+                                 ratio=cfg.ratio, budget=cfg.budget, topK=cfg.topK, theta=cfg.theta,
+                                 eps=f32(cfg.eps), rows=rows, nthreads=nthreads)
+    oracle.sparse_prefill(t_np["q"], t_np["k"], t_np["v"], ind, t_np["ctx"], f32(cfg.scale), rows=rows,
+                          nthreads=nthreads)
+    return nrows, time.perf_counter() - t0
+
+
+def cpu_baseline(cfg, t_np, target_s=12.0):
+    cores = os.cpu_count() or 1
+    n, s = oracle_sample(cfg, t_np, 64)
+    nrows = int(min(cfg.S, max(64, 64 * target_s / max(s, 1e-3))))
+    n, s = oracle_sample(cfg, t_np, nrows)
+    return {"value": n / s, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {cfg.S} rows of {cfg.name} (indexer + attention for those rows, "
+                      f"f64, {cores} threads), {s:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the fp64 CPU oracle on the host cores, same metric and workload."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    cfg = HEADLINE
+    t = syn.make_prefill(cfg)
+    t_np = {k: v.numpy() for k, v in t.items()}
+    cores = os.cpu_count() or 1
+    # each step: a bounded sample of the workload's rows
+    nrows = 192
+    for _ in range(args.warmup):
+        oracle_sample(cfg, t_np, 32)
+    times = []
+    for _ in range(args.steps):
+        n, s = oracle_sample(cfg, t_np, nrows)
+        times.append(s)
+    per = statistics.mean(times)
+    value = nrows / per
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": per * 1000.0, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": cfg.name, "B": cfg.B, "S": cfg.S, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "D": cfg.D,
+                       "indexer": f"{cfg.Hi}x{cfg.di} rot {cfg.rot}", "ratio": cfg.ratio, "budget": cfg.budget,
+                       "topK": cfg.topK, "sample_rows_per_step": nrows},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{nrows} of {cfg.S} rows per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device(dev))
+    r = run_ours(args, rank, world, dev)
+    if rank == 0:
+        cfg = HEADLINE
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            t_np = {k: v.numpy() for k, v in syn.make_prefill(cfg).items()}
+            cpu = cpu_baseline(cfg, t_np)
+        line = {
+            "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": r["ms"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
+            "config": {"workload": cfg.name, "B": cfg.B, "S": cfg.S, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "D": cfg.D,
+                       "indexer": f"{cfg.Hi}x{cfg.di} rot {cfg.rot}", "ratio": cfg.ratio, "budget": cfg.budget,
+                       "topK": cfg.topK, "l2": "flushed between steps (512 MB write)", "parallelism": "replicas"},
+            "stages_ms": {"indexer_prefill": round(r["t_idx"], 4), "sparse_prefill": round(r["t_att"], 4)},
+            "roofline": {"kernel": "sparse_prefill_kernel", "bound": "hbm", "achieved": round(r["achieved"], 1),
+                         "peak": r["hbm_peak"], "unit": "GB/s", "frac": round(r["achieved"] / r["hbm_peak"], 4),
+                         "traffic": None, "algorithmic_bytes": r["gbytes"], "sum_cnt": r["cnt"],
+                         "peak_source": r["peak_kind"],
+                         "note": "gathered K/V rows are largely L2 hits, so frac may exceed 1"},
+            "decode": r["decode"],
+            "e2e": {"value": r["e2e"], "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+            "cpu_baseline": cpu, "clocks": r["clocks"], "gpu_launches": r["launches"],
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

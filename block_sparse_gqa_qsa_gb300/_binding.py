@@ -1,0 +1,229 @@
+"""ctypes binding of libqsa.so (the C ABI declared in include/qsa.h).
+
+Argument marshalling only: every function checks dtypes, devices and
+contiguity of torch tensors, fills the C params struct and calls the entry
+point of the same name; all computation happens in the library's kernels.
+A non-QSA_OK status raises ``QsaError`` with the library's message.  There is
+no CPU fallback: a missing library raises ``RuntimeError`` on first use.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqsa.so")
+
+QSA_OK, QSA_ERR_INVALID_ARG, QSA_ERR_UNSUPPORTED, QSA_ERR_WORKSPACE, QSA_ERR_CUDA = range(5)
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_f32 = ctypes.c_float
+_sz = ctypes.c_size_t
+
+
+class QsaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_status_names.get(status, status)}: {message}")
+        self.status = status
+
+
+_status_names = {0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED", 3: "QSA_ERR_WORKSPACE",
+                 4: "QSA_ERR_CUDA"}
+
+
+class QsaIndexerPrefillParams(ctypes.Structure):
+    _fields_ = [("idxQ", _vp), ("idxK", _vp), ("qNormW", _vp), ("kNormW", _vp), ("contextLengths", _vp),
+                ("indices", _vp), ("workspace", _vp), ("workspaceBytes", _sz), ("batchSize", _i32),
+                ("seqLen", _i32), ("numHeads", _i32), ("headDim", _i32), ("rotDim", _i32),
+                ("compressRatio", _i32), ("budget", _i32), ("topK", _i32), ("ropeTheta", _f32),
+                ("rmsNormEps", _f32), ("stream", _vp)]
+
+
+class QsaIndexerDecodeParams(ctypes.Structure):
+    _fields_ = [("idxQ", _vp), ("idxK", _vp), ("qNormW", _vp), ("kNormW", _vp), ("kvPool", _vp),
+                ("pageTable", _vp), ("contextLengths", _vp), ("indices", _vp), ("workspace", _vp),
+                ("workspaceBytes", _sz), ("batchSize", _i32), ("numKVHeads", _i32), ("kvHeadDim", _i32),
+                ("poolHeadDim", _i32), ("numFlatPages", _i32), ("maxPagesPerSeq", _i32), ("numHeads", _i32),
+                ("headDim", _i32), ("rotDim", _i32), ("compressRatio", _i32), ("budget", _i32), ("topK", _i32),
+                ("ropeTheta", _f32), ("rmsNormEps", _f32), ("stream", _vp)]
+
+
+class QsaSparsePrefillParams(ctypes.Structure):
+    _fields_ = [("qPtr", _vp), ("kPtr", _vp), ("vPtr", _vp), ("oPtr", _vp), ("indices", _vp),
+                ("contextLengths", _vp), ("batchSize", _i32), ("seqLen", _i32), ("numQHeads", _i32),
+                ("numKVHeads", _i32), ("headDim", _i32), ("topK", _i32), ("attentionScale", _f32),
+                ("stream", _vp)]
+
+
+class QsaSparseDecodeParams(ctypes.Structure):
+    _fields_ = [("qPtr", _vp), ("kvPoolPtr", _vp), ("pageTable", _vp), ("indices", _vp),
+                ("contextLengths", _vp), ("oPtr", _vp), ("partialO", _vp), ("partialStats", _vp),
+                ("splitCounters", _vp), ("batchSize", _i32), ("numQHeads", _i32), ("numKVHeads", _i32),
+                ("headDim", _i32), ("poolHeadDim", _i32), ("numFlatPages", _i32), ("maxPagesPerSeq", _i32),
+                ("topK", _i32), ("attentionScale", _f32), ("stream", _vp)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises RuntimeError when it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libqsa.so is missing ({LIB_PATH}); build it with "
+                                   "`python -m block_sparse_gqa_qsa_gb300.build` -- there is no fallback")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, st in (("qsa_indexer_prefill", QsaIndexerPrefillParams),
+                             ("qsa_indexer_decode", QsaIndexerDecodeParams),
+                             ("qsa_sparse_prefill", QsaSparsePrefillParams),
+                             ("qsa_sparse_decode", QsaSparseDecodeParams)):
+                f = getattr(L, name)
+                f.argtypes = [ctypes.POINTER(st)]
+                f.restype = ctypes.c_int
+            L.qsa_indexer_prefill_workspace_size.argtypes = [_i32] * 4
+            L.qsa_indexer_prefill_workspace_size.restype = _sz
+            L.qsa_indexer_decode_workspace_size.argtypes = [_i32] * 4
+            L.qsa_indexer_decode_workspace_size.restype = _sz
+            L.qsa_sparse_decode_partial_o_elems.argtypes = [_i32] * 3
+            L.qsa_sparse_decode_partial_o_elems.restype = _sz
+            L.qsa_sparse_decode_partial_stats_elems.argtypes = [_i32] * 2
+            L.qsa_sparse_decode_partial_stats_elems.restype = _sz
+            L.qsa_sparse_decode_counter_elems.argtypes = [_i32] * 2
+            L.qsa_sparse_decode_counter_elems.restype = _sz
+            for n in ("qsa_sparse_decode_max_splits", "qsa_sparse_decode_partial_rows",
+                      "qsa_indexer_prefill_max_blocks"):
+                getattr(L, n).argtypes = []
+                getattr(L, n).restype = _i32
+            L.qsa_sparse_prefill_can_implement.argtypes = [_i32] * 3
+            L.qsa_sparse_prefill_can_implement.restype = _i32
+            L.qsa_sparse_decode_can_implement.argtypes = [_i32] * 4
+            L.qsa_sparse_decode_can_implement.restype = _i32
+            L.qsa_status_string.argtypes = [ctypes.c_int]
+            L.qsa_status_string.restype = ctypes.c_char_p
+            L.qsa_last_error_message.argtypes = []
+            L.qsa_last_error_message.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != QSA_OK:
+        raise QsaError(status, lib().qsa_last_error_message().decode())
+
+
+def _ptr(t: torch.Tensor | None, dtype=None, name: str = "tensor") -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+# ------------------------------------------------------------------ sizes
+def indexer_prefill_workspace_size(B: int, S: int, di: int, ratio: int) -> int:
+    return lib().qsa_indexer_prefill_workspace_size(B, S, di, ratio)
+
+
+def indexer_decode_workspace_size(B: int, max_pages_per_seq: int, ratio: int, budget: int) -> int:
+    return lib().qsa_indexer_decode_workspace_size(B, max_pages_per_seq, ratio, budget)
+
+
+def sparse_decode_workspace_elems(B: int, Hkv: int, D: int) -> tuple[int, int, int]:
+    L = lib()
+    return (L.qsa_sparse_decode_partial_o_elems(B, Hkv, D), L.qsa_sparse_decode_partial_stats_elems(B, Hkv),
+            L.qsa_sparse_decode_counter_elems(B, Hkv))
+
+
+def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """Zero-filled byte buffer (torch allocations are 256-byte aligned)."""
+    return torch.zeros(max(nbytes, 1), dtype=torch.uint8, device=device)
+
+
+# ------------------------------------------------------------- entry points
+def indexer_prefill(idxQ, idxK, wq, wk, ctx, indices, workspace, *, rot, ratio, budget, topK, theta, eps,
+                    stream=None):
+    """qsa_indexer_prefill: idxQ fp16 [B,S,Hi,di], idxK fp16 [B,S,di] -> indices int32 [B,S,topK]."""
+    B, S, Hi, di = idxQ.shape
+    p = QsaIndexerPrefillParams(
+        idxQ=_ptr(idxQ, torch.float16, "idxQ"), idxK=_ptr(idxK, torch.float16, "idxK"),
+        qNormW=_ptr(wq, torch.float32, "qNormW"), kNormW=_ptr(wk, torch.float32, "kNormW"),
+        contextLengths=_ptr(ctx, torch.int32, "contextLengths"), indices=_ptr(indices, torch.int32, "indices"),
+        workspace=_ptr(workspace, None, "workspace"), workspaceBytes=workspace.numel() * workspace.element_size(),
+        batchSize=B, seqLen=S, numHeads=Hi, headDim=di, rotDim=rot, compressRatio=ratio, budget=budget,
+        topK=topK, ropeTheta=theta, rmsNormEps=eps, stream=_stream(stream))
+    if tuple(idxK.shape) != (B, S, di) or tuple(indices.shape[-1:]) != (topK,) or indices.numel() != B * S * topK:
+        raise ValueError("indexer_prefill: shape mismatch")
+    _check(lib().qsa_indexer_prefill(ctypes.byref(p)))
+
+
+def indexer_decode(idxQ, idxK, wq, wk, pool, page_table, ctx, indices, workspace, *, D, rot, ratio, budget,
+                   topK, theta, eps, stream=None):
+    """qsa_indexer_decode: one new token per sequence; updates the pool's tail state in place."""
+    B, Hi, di = idxQ.shape
+    nflat, tpp, Hkv, phd = pool.shape
+    p = QsaIndexerDecodeParams(
+        idxQ=_ptr(idxQ, torch.float16, "idxQ"), idxK=_ptr(idxK, torch.float16, "idxK"),
+        qNormW=_ptr(wq, torch.float32, "qNormW"), kNormW=_ptr(wk, torch.float32, "kNormW"),
+        kvPool=_ptr(pool, torch.float16, "kvPool"), pageTable=_ptr(page_table, torch.int32, "pageTable"),
+        contextLengths=_ptr(ctx, torch.int32, "contextLengths"), indices=_ptr(indices, torch.int32, "indices"),
+        workspace=_ptr(workspace, None, "workspace"), workspaceBytes=workspace.numel() * workspace.element_size(),
+        batchSize=B, numKVHeads=Hkv, kvHeadDim=D, poolHeadDim=phd, numFlatPages=nflat,
+        maxPagesPerSeq=page_table.shape[-1], numHeads=Hi, headDim=di, rotDim=rot, compressRatio=ratio,
+        budget=budget, topK=topK, ropeTheta=theta, rmsNormEps=eps, stream=_stream(stream))
+    if tpp != 128 or tuple(page_table.shape[:2]) != (B, 2) or indices.numel() != B * topK:
+        raise ValueError("indexer_decode: shape mismatch")
+    _check(lib().qsa_indexer_decode(ctypes.byref(p)))
+
+
+def sparse_prefill(q, k, v, indices, ctx, out, scale, stream=None):
+    """qsa_sparse_prefill: q/out fp16 [B,S,Hq,D], k/v fp16 [B,S,Hkv,D], indices int32 [B,S,topK]."""
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    topK = indices.shape[-1]
+    if tuple(k.shape) != (B, S, Hkv, D) or tuple(v.shape) != (B, S, Hkv, D) or tuple(out.shape) != (B, S, Hq, D) \
+            or indices.numel() != B * S * topK:
+        raise ValueError("sparse_prefill: shape mismatch")
+    p = QsaSparsePrefillParams(
+        qPtr=_ptr(q, torch.float16, "q"), kPtr=_ptr(k, torch.float16, "k"), vPtr=_ptr(v, torch.float16, "v"),
+        oPtr=_ptr(out, torch.float16, "out"), indices=_ptr(indices, torch.int32, "indices"),
+        contextLengths=_ptr(ctx, torch.int32, "contextLengths"), batchSize=B, seqLen=S, numQHeads=Hq,
+        numKVHeads=Hkv, headDim=D, topK=topK, attentionScale=scale, stream=_stream(stream))
+    _check(lib().qsa_sparse_prefill(ctypes.byref(p)))
+
+
+def sparse_decode(q, pool, page_table, indices, ctx, out, partial_o, partial_stats, counters, *, D, scale,
+                  stream=None):
+    """qsa_sparse_decode: q/out fp16 [B,1,Hq,D]; split-K over the pool through the page table."""
+    B = q.shape[0]
+    Hq = q.shape[-2]
+    nflat, tpp, Hkv, phd = pool.shape
+    topK = indices.shape[-1]
+    if q.numel() != B * Hq * D or out.numel() != B * Hq * D or indices.numel() != B * topK or tpp != 128:
+        raise ValueError("sparse_decode: shape mismatch")
+    p = QsaSparseDecodeParams(
+        qPtr=_ptr(q, torch.float16, "q"), kvPoolPtr=_ptr(pool, torch.float16, "kvPool"),
+        pageTable=_ptr(page_table, torch.int32, "pageTable"), indices=_ptr(indices, torch.int32, "indices"),
+        contextLengths=_ptr(ctx, torch.int32, "contextLengths"), oPtr=_ptr(out, torch.float16, "out"),
+        partialO=_ptr(partial_o, torch.float32, "partialO"),
+        partialStats=_ptr(partial_stats, torch.float32, "partialStats"),
+        splitCounters=_ptr(counters, torch.int32, "splitCounters"), batchSize=B, numQHeads=Hq, numKVHeads=Hkv,
+        headDim=D, poolHeadDim=phd, numFlatPages=nflat, maxPagesPerSeq=page_table.shape[-1], topK=topK,
+        attentionScale=scale, stream=_stream(stream))
+    _check(lib().qsa_sparse_decode(ctypes.byref(p)))

@@ -1,0 +1,249 @@
+// qsa_api.cu -- the C ABI of libqsa.so (declared in include/qsa.h): host-side
+// validation, workspace arithmetic, RoPE frequency tables, the TMA tensor map
+// of the decode indexer, and the kernel launches.  Nothing here allocates or
+// synchronises; a failed check returns before anything is enqueued.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "qsa_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+qsa_status_t fail(qsa_status_t s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+qsa_status_t ok() {
+  g_last_error.clear();
+  return QSA_OK;
+}
+
+qsa_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(QSA_ERR_CUDA, "%s: CUDA error %d (%s)", what, static_cast<int>(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+qsa::RopeFreqs rope_freqs(float theta, int rot) {
+  qsa::RopeFreqs r;
+  std::memset(&r, 0, sizeof(r));
+  for (int i = 0; i < rot / 2; ++i) r.inv_freq[i] = std::pow(static_cast<double>(theta), -2.0 * i / rot);
+  return r;
+}
+
+constexpr int kMaxListWidth = 10240;     // prefill indexer stages one list in shared memory
+constexpr int kMaxAttnListWidth = 16384;  // attention stages one list (or slice) in shared memory
+constexpr int kMaxDecodeBudget = 512;     // decode merge holds 8 * budget candidates per CTA
+
+// Indexer arguments shared by both indexers ("Qsa Attention Plugin" constructor
+// attributes: indexerNumHeads, indexerHeadDim, indexerBudget, indexerCompressRatio).
+qsa_status_t check_indexer_shape(int Hi, int di, int rot, int ratio, int budget, int topK, float theta,
+                                 float eps) {
+  if (Hi < 1 || di < 1 || rot < 0 || rot > di || (rot & 1) || ratio < 1 || budget < 1 || !(theta > 0.f) ||
+      !(eps >= 0.f))
+    return fail(QSA_ERR_INVALID_ARG, "indexer: invalid numHeads/headDim/rotDim/compressRatio/budget/theta/eps");
+  if (static_cast<long long>(topK) < static_cast<long long>(budget) * ratio + ratio - 1)
+    return fail(QSA_ERR_INVALID_ARG, "indexer: topK %d < budget*ratio + ratio - 1 = %lld", topK,
+                static_cast<long long>(budget) * ratio + ratio - 1);
+  if (Hi > 8) return fail(QSA_ERR_UNSUPPORTED, "indexer: numHeads %d > 8", Hi);
+  if (di != 64 && di != 128) return fail(QSA_ERR_UNSUPPORTED, "indexer: headDim %d not 64 or 128", di);
+  if (rot > 128) return fail(QSA_ERR_UNSUPPORTED, "indexer: rotDim %d > 128", rot);
+  return QSA_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qsa_status_string(qsa_status_t s) {
+  switch (s) {
+    case QSA_OK: return "QSA_OK";
+    case QSA_ERR_INVALID_ARG: return "QSA_ERR_INVALID_ARG";
+    case QSA_ERR_UNSUPPORTED: return "QSA_ERR_UNSUPPORTED";
+    case QSA_ERR_WORKSPACE: return "QSA_ERR_WORKSPACE";
+    case QSA_ERR_CUDA: return "QSA_ERR_CUDA";
+  }
+  return "QSA_ERR_UNKNOWN";
+}
+
+const char* qsa_last_error_message(void) { return g_last_error.c_str(); }
+
+int32_t qsa_indexer_prefill_max_blocks(void) { return qsa::kPrefillMaxBlocks; }
+
+size_t qsa_indexer_prefill_workspace_size(int32_t B, int32_t S, int32_t di, int32_t ratio) {
+  if (B < 1 || S < 1 || di < 1 || ratio < 1) return 0;
+  return qsa::indexer_prefill_workspace_bytes(B, S, di, ratio);
+}
+
+size_t qsa_indexer_decode_workspace_size(int32_t B, int32_t maxPagesPerSeq, int32_t ratio, int32_t budget) {
+  if (B < 1 || maxPagesPerSeq < 1 || ratio < 1 || qsa::kTokensPerPageHost % ratio != 0 || budget < 1) return 0;
+  return qsa::indexer_decode_workspace_bytes(B, maxPagesPerSeq, ratio, budget);
+}
+
+size_t qsa_sparse_decode_partial_o_elems(int32_t B, int32_t Hkv, int32_t D) {
+  if (B < 1 || Hkv < 1 || D < 1) return 0;
+  return static_cast<size_t>(B) * Hkv * 8 * 16 * D;
+}
+size_t qsa_sparse_decode_partial_stats_elems(int32_t B, int32_t Hkv) {
+  if (B < 1 || Hkv < 1) return 0;
+  return static_cast<size_t>(B) * Hkv * 8 * 2 * 16;
+}
+size_t qsa_sparse_decode_counter_elems(int32_t B, int32_t Hkv) {
+  if (B < 1 || Hkv < 1) return 0;
+  return static_cast<size_t>(B) * Hkv;
+}
+int32_t qsa_sparse_decode_max_splits(void) { return 8; }
+int32_t qsa_sparse_decode_partial_rows(void) { return 16; }
+
+int32_t qsa_sparse_prefill_can_implement(int32_t Hq, int32_t Hkv, int32_t D) {
+  return Hq >= 1 && Hkv >= 1 && Hq % Hkv == 0 && Hq / Hkv <= 16 && D == 128;
+}
+int32_t qsa_sparse_decode_can_implement(int32_t Hq, int32_t Hkv, int32_t D, int32_t poolHeadDim) {
+  return qsa_sparse_prefill_can_implement(Hq, Hkv, D) && poolHeadDim >= D && poolHeadDim % 8 == 0;
+}
+
+qsa_status_t qsa_indexer_prefill(const QsaIndexerPrefillParams* p) {
+  if (!p) return fail(QSA_ERR_INVALID_ARG, "qsa_indexer_prefill: params is NULL");
+  if (!p->idxQ || !p->idxK || !p->qNormW || !p->kNormW || !p->contextLengths || !p->indices)
+    return fail(QSA_ERR_INVALID_ARG, "qsa_indexer_prefill: a tensor pointer is NULL");
+  if (p->batchSize < 1 || p->seqLen < 1)
+    return fail(QSA_ERR_INVALID_ARG, "qsa_indexer_prefill: batchSize/seqLen must be >= 1");
+  qsa_status_t s = check_indexer_shape(p->numHeads, p->headDim, p->rotDim, p->compressRatio, p->budget, p->topK,
+                                       p->ropeTheta, p->rmsNormEps);
+  if (s != QSA_OK) return s;
+  if (p->batchSize > 65535) return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_prefill: batchSize > 65535");
+  if (p->seqLen / p->compressRatio > qsa::kPrefillMaxBlocks)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_prefill: seqLen/compressRatio = %d blocks > %d",
+                p->seqLen / p->compressRatio, qsa::kPrefillMaxBlocks);
+  if (p->topK > kMaxListWidth) return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_prefill: topK > %d", kMaxListWidth);
+  const size_t need = qsa::indexer_prefill_workspace_bytes(p->batchSize, p->seqLen, p->headDim, p->compressRatio);
+  if (!p->workspace || p->workspaceBytes < need || !aligned(p->workspace, 256))
+    return fail(QSA_ERR_WORKSPACE, "qsa_indexer_prefill: workspace needs %zu bytes, 256-byte aligned", need);
+  const cudaError_t e = qsa::launch_indexer_prefill(*p, rope_freqs(p->ropeTheta, p->rotDim));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "qsa_indexer_prefill");
+}
+
+qsa_status_t qsa_indexer_decode(const QsaIndexerDecodeParams* p) {
+  if (!p) return fail(QSA_ERR_INVALID_ARG, "qsa_indexer_decode: params is NULL");
+  if (!p->idxQ || !p->idxK || !p->qNormW || !p->kNormW || !p->kvPool || !p->pageTable || !p->contextLengths ||
+      !p->indices)
+    return fail(QSA_ERR_INVALID_ARG, "qsa_indexer_decode: a tensor pointer is NULL");
+  if (p->batchSize < 1 || p->numKVHeads < 1 || p->kvHeadDim < 1 || p->numFlatPages < 1 || p->maxPagesPerSeq < 1)
+    return fail(QSA_ERR_INVALID_ARG, "qsa_indexer_decode: batchSize/numKVHeads/kvHeadDim/numFlatPages/"
+                                     "maxPagesPerSeq must be >= 1");
+  if (p->poolHeadDim < p->kvHeadDim + p->headDim)
+    return fail(QSA_ERR_INVALID_ARG, "qsa_indexer_decode: poolHeadDim %d < kvHeadDim + headDim", p->poolHeadDim);
+  qsa_status_t s = check_indexer_shape(p->numHeads, p->headDim, p->rotDim, p->compressRatio, p->budget, p->topK,
+                                       p->ropeTheta, p->rmsNormEps);
+  if (s != QSA_OK) return s;
+  if (qsa::kTokensPerPageHost % p->compressRatio != 0)
+    return fail(QSA_ERR_INVALID_ARG, "qsa_indexer_decode: compressRatio %d does not divide the 128-token page",
+                p->compressRatio);
+  if (p->budget > kMaxDecodeBudget)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_decode: budget %d > %d", p->budget, kMaxDecodeBudget);
+  if (p->batchSize > 65535) return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_decode: batchSize > 65535");
+  if (p->kvHeadDim % 8 || p->poolHeadDim % 8 || !aligned(p->kvPool, 16))
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_decode: kvHeadDim and poolHeadDim must be multiples of 8 and "
+                                     "kvPool 16-byte aligned (TMA rows)");
+  if (static_cast<long long>(p->maxPagesPerSeq) * 128 > 0x7fffffffLL)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_decode: maxPagesPerSeq too large");
+  const size_t need = qsa::indexer_decode_workspace_bytes(p->batchSize, p->maxPagesPerSeq, p->compressRatio, p->budget);
+  if (!p->workspace || p->workspaceBytes < need || !aligned(p->workspace, 256))
+    return fail(QSA_ERR_WORKSPACE, "qsa_indexer_decode: workspace needs %zu bytes, 256-byte aligned", need);
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return fail(QSA_ERR_CUDA, "qsa_indexer_decode: cuTensorMapEncodeTiled is unavailable");
+  // Strided view of the key tails: [numFlatPages][128/r block-start rows][headDim] starting at column kvHeadDim
+  // of head 0 ("KV pool contract": block g's key in the V-row tail of token r*g).
+  const int bpp = qsa::kTokensPerPageHost / p->compressRatio;
+  const size_t row_bytes = static_cast<size_t>(p->numKVHeads) * p->poolHeadDim * 2;
+  CUtensorMap map;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(p->headDim), static_cast<cuuint64_t>(bpp),
+                        static_cast<cuuint64_t>(p->numFlatPages)};
+  cuuint64_t strides[2] = {row_bytes * p->compressRatio, row_bytes * qsa::kTokensPerPageHost};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(p->headDim), static_cast<cuuint32_t>(bpp), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  void* base = static_cast<char*>(p->kvPool) + static_cast<size_t>(p->kvHeadDim) * 2;
+  const CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_decode: tensor map rejected (CUresult %d)", r);
+  const cudaError_t e = qsa::launch_indexer_decode(*p, rope_freqs(p->ropeTheta, p->rotDim), map);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "qsa_indexer_decode");
+}
+
+qsa_status_t qsa_sparse_prefill(const QsaSparsePrefillParams* p) {
+  if (!p) return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_prefill: params is NULL");
+  if (!p->qPtr || !p->kPtr || !p->vPtr || !p->oPtr || !p->indices || !p->contextLengths)
+    return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_prefill: a tensor pointer is NULL");
+  if (p->batchSize < 1 || p->seqLen < 1 || p->numQHeads < 1 || p->numKVHeads < 1 || p->headDim < 1 || p->topK < 1)
+    return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_prefill: sizes must be >= 1");
+  if (p->numQHeads % p->numKVHeads)
+    return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_prefill: numQHeads %% numKVHeads != 0");
+  if (!qsa_sparse_prefill_can_implement(p->numQHeads, p->numKVHeads, p->headDim))
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_sparse_prefill: needs headDim 128 and a GQA group of at most 16");
+  if (p->topK > kMaxAttnListWidth)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_sparse_prefill: topK > %d", kMaxAttnListWidth);
+  if (static_cast<long long>(p->batchSize) * p->seqLen * p->numKVHeads > 0x7fffffffLL)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_sparse_prefill: batchSize*seqLen*numKVHeads exceeds the grid");
+  if (!aligned(p->qPtr, 16) || !aligned(p->kPtr, 16) || !aligned(p->vPtr, 16) || !aligned(p->oPtr, 16))
+    return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_prefill: Q/K/V/O must be 16-byte aligned");
+  const cudaError_t e = qsa::launch_sparse_prefill(*p);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "qsa_sparse_prefill");
+}
+
+qsa_status_t qsa_sparse_decode(const QsaSparseDecodeParams* p) {
+  if (!p) return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_decode: params is NULL");
+  if (!p->qPtr || !p->kvPoolPtr || !p->pageTable || !p->indices || !p->contextLengths || !p->oPtr)
+    return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_decode: a tensor pointer is NULL");
+  if (!p->partialO || !p->partialStats || !p->splitCounters)
+    return fail(QSA_ERR_WORKSPACE, "qsa_sparse_decode: partialO/partialStats/splitCounters is NULL");
+  if (p->batchSize < 1 || p->numQHeads < 1 || p->numKVHeads < 1 || p->headDim < 1 || p->topK < 1 ||
+      p->numFlatPages < 1 || p->maxPagesPerSeq < 1)
+    return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_decode: sizes must be >= 1");
+  if (p->numQHeads % p->numKVHeads)
+    return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_decode: numQHeads %% numKVHeads != 0");
+  if (p->poolHeadDim < p->headDim) return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_decode: poolHeadDim < headDim");
+  if (!qsa_sparse_decode_can_implement(p->numQHeads, p->numKVHeads, p->headDim, p->poolHeadDim))
+    return fail(QSA_ERR_UNSUPPORTED,
+                "qsa_sparse_decode: needs headDim 128, a GQA group of at most 16, poolHeadDim a multiple of 8");
+  if (p->topK > kMaxAttnListWidth) return fail(QSA_ERR_UNSUPPORTED, "qsa_sparse_decode: topK > %d", kMaxAttnListWidth);
+  if (p->batchSize > 65535 || p->numKVHeads > 65535)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_sparse_decode: batchSize/numKVHeads > 65535");
+  if (static_cast<long long>(p->maxPagesPerSeq) * 128 > 0x7fffffffLL)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_sparse_decode: maxPagesPerSeq too large");
+  if (!aligned(p->qPtr, 16) || !aligned(p->kvPoolPtr, 16) || !aligned(p->oPtr, 16) || !aligned(p->partialO, 16) ||
+      !aligned(p->partialStats, 4) || !aligned(p->splitCounters, 4))
+    return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_decode: q/pool/o/partialO must be 16-byte aligned");
+  const cudaError_t e = qsa::launch_sparse_decode(*p);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "qsa_sparse_decode");
+}
+
+}  // extern "C"

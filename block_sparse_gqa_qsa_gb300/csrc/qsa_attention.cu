@@ -1,0 +1,530 @@
+// qsa_attention.cu -- sparse GQA attention over QSA index lists.
+//
+//   sparse_prefill_kernel  one CTA per (query token, KV head) over dense padded
+//                          BSND Q/K/V ("Cute Dsl Qsa Sparse Runner",
+//                          QsaSparsePrefillParams)
+//   sparse_decode_kernel   one CTA per (split, KV head, sequence) over the paged
+//                          pool, fp32 partials, and the last split to finish
+//                          merges them and resets its counter
+//                          (QsaSparseDecodeParams, kMaxSplits = 8,
+//                          kPartialRows = 16)
+//
+// Both stream the K/V rows named by the list through a cp.async ring in shared
+// memory (16-byte copies, one 256-byte row per key, zero-filled for skipped
+// entries).  The GQA head group is one MMA operand: each warp takes 16 keys of
+// a 64-key tile and computes S^T = K Q^T with the keys as the M side and the
+// group's heads as N (m16n8k16, no padding of the group to 16 rows), online
+// softmax in fp32 (log2 domain), and O^T += V^T P^T with P^T formed from the S
+// fragments by an in-register 8x8 transpose.  Warps keep independent running
+// (m, l, O) and are merged once at the end.
+#include "qsa_device.cuh"
+#include "qsa_internal.h"
+
+namespace qsa {
+namespace {
+
+constexpr int kThreads = 128;  // 4 warps
+constexpr int kKeys = 64;      // keys per tile (16 per warp)
+constexpr int kD = 128;        // attention head dim
+constexpr int kTileBytes = kKeys * kD * 2;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kOStride = 132;  // padded fp32 row of the warp-merge buffer
+
+// Byte offset of 16-byte chunk `c` of row `r` in a [rows][256 B] tile (XOR swizzle
+// over 8-row groups so ldmatrix reads are bank-conflict free).
+__device__ __forceinline__ uint32_t swz(int r, int c) { return r * 256 + ((c ^ (r & 7)) << 4); }
+
+template <int NT>
+struct WarpAcc {
+  float o[8][NT][4];  // O^T fragments: dims 16*mt + (g, g+8), heads 8*nt + (2q, 2q+1)
+  float m[NT][2];     // running max (log2 units) of heads 8*nt + 2q, 8*nt + 2q + 1
+  float l[NT][2];     // this thread's share of the running sum
+};
+
+template <int NT>
+__device__ __forceinline__ void acc_init(WarpAcc<NT>& A) {
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) A.o[mt][nt][i] = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    A.m[nt][0] = A.m[nt][1] = -INFINITY;
+    A.l[nt][0] = A.l[nt][1] = 0.f;
+  }
+}
+
+// Q^T B-fragments of all 8 k-steps (128 dims) from the swizzled Q tile.
+template <int NT>
+__device__ __forceinline__ void load_q_frags(uint32_t q_tile, uint32_t (&qf)[NT][8][2]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int ks = 0; ks < 8; ks += 2) {
+      const int row = 8 * nt + (lane & 7);
+      const int chunk = 2 * ks + (lane >> 3);
+      ldsm_x4(q_tile + swz(row, chunk), qf[nt][ks][0], qf[nt][ks][1], qf[nt][ks + 1][0], qf[nt][ks + 1][1]);
+    }
+}
+
+// One warp, 16 keys (tile rows 16*warp ..): S^T = K Q^T, online softmax, O^T += V^T P^T.
+template <int NT>
+__device__ __forceinline__ void attend16(WarpAcc<NT>& A, uint32_t k_tile, uint32_t v_tile,
+                                         const uint32_t (&qf)[NT][8][2], bool valid0, bool valid1, float sl2) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int kr0 = warp * 16;
+  const int mi = lane >> 3;
+  float s[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    uint32_t a[4];
+    ldsm_x4(k_tile + swz(kr0 + (lane & 7) + 8 * (mi & 1), 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) mma16816(s[nt], a, qf[nt][ks][0], qf[nt][ks][1]);
+  }
+  uint32_t pb[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const float x0 = valid0 ? s[nt][0] * sl2 : -INFINITY;  // key g,   head 2q
+    const float x1 = valid0 ? s[nt][1] * sl2 : -INFINITY;  // key g,   head 2q+1
+    const float x2 = valid1 ? s[nt][2] * sl2 : -INFINITY;  // key g+8, head 2q
+    const float x3 = valid1 ? s[nt][3] * sl2 : -INFINITY;  // key g+8, head 2q+1
+    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o));
+    }
+    const float mn0 = fmaxf(A.m[nt][0], mx0), mn1 = fmaxf(A.m[nt][1], mx1);
+    const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = exp2f(A.m[nt][0] - mu0), al1 = exp2f(A.m[nt][1] - mu1);
+    A.m[nt][0] = mn0;
+    A.m[nt][1] = mn1;
+    const float p0 = exp2f(x0 - mu0), p1 = exp2f(x1 - mu1), p2 = exp2f(x2 - mu0), p3 = exp2f(x3 - mu1);
+    A.l[nt][0] = A.l[nt][0] * al0 + (p0 + p2);
+    A.l[nt][1] = A.l[nt][1] * al1 + (p1 + p3);
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      A.o[mt][nt][0] *= al0;
+      A.o[mt][nt][1] *= al1;
+      A.o[mt][nt][2] *= al0;
+      A.o[mt][nt][3] *= al1;
+    }
+    pb[nt][0] = movmatrix_t(pack_half2(p0, p1));  // keys 0..7  -> (k = 2q..2q+1, n = g)
+    pb[nt][1] = movmatrix_t(pack_half2(p2, p3));  // keys 8..15
+  }
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    uint32_t a[4];
+    ldsm_x4_t(v_tile + swz(kr0 + (lane & 7) + 8 * (mi >> 1), 2 * mt + (mi & 1)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) mma16816(A.o[mt][nt], a, pb[nt][0], pb[nt][1]);
+  }
+}
+
+// Writes each warp's (m, l, O^T) to shared memory: mw/lw [4][16], ow [4][16][kOStride].
+template <int NT>
+__device__ __forceinline__ void stash_warp(const WarpAcc<NT>& A, float* mw, float* lw, float* ow) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float l = A.l[nt][j];
+      l += __shfl_xor_sync(kFull, l, 4);
+      l += __shfl_xor_sync(kFull, l, 8);
+      l += __shfl_xor_sync(kFull, l, 16);
+      if (g == 0) {
+        mw[warp * 16 + 8 * nt + 2 * q + j] = A.m[nt][j];
+        lw[warp * 16 + 8 * nt + 2 * q + j] = l;
+      }
+    }
+  float* o = ow + warp * 16 * kOStride;
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int h = 8 * nt + 2 * q, d = 16 * mt + g;
+      o[h * kOStride + d] = A.o[mt][nt][0];
+      o[(h + 1) * kOStride + d] = A.o[mt][nt][1];
+      o[h * kOStride + d + 8] = A.o[mt][nt][2];
+      o[(h + 1) * kOStride + d + 8] = A.o[mt][nt][3];
+    }
+}
+
+// Merged (M, L) of one head over the 4 warps, and the warps' weights 2^(m_w - M).
+__device__ __forceinline__ float merge_weights(const float* mw, const float* lw, int h, float (&f)[4], float& L) {
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) M = fmaxf(M, mw[w * 16 + h]);
+  L = 0.f;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const float m = mw[w * 16 + h];
+    f[w] = m == -INFINITY ? 0.f : exp2f(m - M);
+    L += f[w] * lw[w * 16 + h];
+  }
+  return M;
+}
+
+// ------------------------------------------------------------------ prefill
+struct PrefillArgs {
+  const __half* q;
+  const __half* k;
+  const __half* v;
+  __half* o;
+  const int32_t* indices;
+  const int32_t* ctx;
+  int S, Hq, Hkv, G, topK, topKpad;
+  float sl2;  // attentionScale * log2(e)
+};
+
+template <int NT, int STAGES>
+__global__ void __launch_bounds__(kThreads, 2) sparse_prefill_kernel(const PrefillArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const uint32_t ring = smem_addr(smem);                       // [STAGES][K 16 KB | V 16 KB]
+  const uint32_t q_tile = ring + STAGES * 2 * kTileBytes;      // [8*NT][256 B]
+  int* idx_s = reinterpret_cast<int*>(smem + STAGES * 2 * kTileBytes + NT * 8 * 256);
+  int* misc = idx_s + a.topKpad;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long bid = blockIdx.x;
+  const int kvh = static_cast<int>(bid % a.Hkv);
+  const long long bt = bid / a.Hkv;
+  const int t = static_cast<int>(bt % a.S);
+  const int b = static_cast<int>(bt / a.S);
+  const int L = max(0, min(a.ctx[b], a.S));
+  __half* out = a.o + (static_cast<size_t>(bt) * a.Hq + static_cast<size_t>(kvh) * a.G) * kD;
+  if (t >= L) {  // rows at or past the live length are exact zeros
+    for (int e = tid; e < a.G * kD / 8; e += kThreads) reinterpret_cast<uint4*>(out)[e] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  // Stage the list; entries outside [0, L) are skipped.
+  const int32_t* lst = a.indices + static_cast<size_t>(bt) * a.topK;
+  int last = -1;
+  for (int i = tid; i < a.topKpad; i += kThreads) {
+    const int j = i < a.topK ? __ldg(lst + i) : -1;
+    const bool ok = static_cast<unsigned>(j) < static_cast<unsigned>(L);
+    idx_s[i] = ok ? j : -1;
+    last = ok ? i : last;
+  }
+  last = __reduce_max_sync(kFull, last);
+  if (lane == 0) misc[warp] = last;
+  // Q rows of the group (rows >= G zero).
+  const __half* qsrc = a.q + (static_cast<size_t>(bt) * a.Hq + static_cast<size_t>(kvh) * a.G) * kD;
+  for (int e = tid; e < NT * 8 * 16; e += kThreads) {
+    const int r = e >> 4, c = e & 15;
+    const bool ok = r < a.G;
+    cp_async16(q_tile + swz(r, c), qsrc + (ok ? r : 0) * kD + c * 8, ok);
+  }
+  cp_async_commit();
+  __syncthreads();
+  const int nslots = max(max(misc[0], misc[1]), max(misc[2], misc[3])) + 1;
+  const int ntiles = (nslots + kKeys - 1) / kKeys;
+
+  const size_t kv_b = static_cast<size_t>(b) * a.S;
+  auto issue = [&](int tile, int stage) {
+    const int key = tid >> 1, part = tid & 1;
+    const int j = idx_s[tile * kKeys + key];
+    const bool ok = j >= 0;
+    const size_t row = ((kv_b + (ok ? j : 0)) * a.Hkv + kvh) * kD;
+    const uint32_t kdst = ring + stage * 2 * kTileBytes;
+    const uint32_t vdst = kdst + kTileBytes;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int ch = part * 8 + c;
+      cp_async16(kdst + swz(key, ch), a.k + row + ch * 8, ok);
+      cp_async16(vdst + swz(key, ch), a.v + row + ch * 8, ok);
+    }
+  };
+#pragma unroll
+  for (int s = 0; s < STAGES - 1; ++s) {
+    if (s < ntiles) issue(s, s);
+    cp_async_commit();
+  }
+  cp_async_wait<STAGES - 1>();  // the Q group (oldest) has landed
+  __syncthreads();
+  uint32_t qf[NT][8][2];
+  load_q_frags<NT>(q_tile, qf);
+
+  WarpAcc<NT> A;
+  acc_init(A);
+  for (int i = 0; i < ntiles; ++i) {
+    cp_async_wait<STAGES - 2>();
+    __syncthreads();
+    if (i + STAGES - 1 < ntiles) issue(i + STAGES - 1, (i + STAGES - 1) % STAGES);
+    cp_async_commit();
+    const int stage = i % STAGES;
+    const int slot = i * kKeys + warp * 16 + (lane >> 2);
+    attend16<NT>(A, ring + stage * 2 * kTileBytes, ring + stage * 2 * kTileBytes + kTileBytes, qf,
+                 idx_s[slot] >= 0, idx_s[slot + 8] >= 0, a.sl2);
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  float* mw = reinterpret_cast<float*>(smem);
+  float* lw = mw + 64;
+  float* ow = lw + 64;
+  stash_warp<NT>(A, mw, lw, ow);
+  __syncthreads();
+  for (int e = tid; e < a.G * (kD / 2); e += kThreads) {
+    const int h = e / (kD / 2), d = 2 * (e % (kD / 2));
+    float f[4], Lsum;
+    merge_weights(mw, lw, h, f, Lsum);
+    float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      o0 += f[w] * ow[(w * 16 + h) * kOStride + d];
+      o1 += f[w] * ow[(w * 16 + h) * kOStride + d + 1];
+    }
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    reinterpret_cast<__half2*>(out + h * kD)[d / 2] = __floats2half2_rn(o0 * inv, o1 * inv);
+  }
+}
+
+// ------------------------------------------------------------------- decode
+struct DecodeArgs {
+  const __half* q;
+  const __half* pool;
+  const int32_t* pageTable;
+  const int32_t* indices;
+  const int32_t* ctx;
+  __half* o;
+  float* partialO;
+  float* partialStats;
+  int32_t* counters;
+  int Hq, Hkv, G, poolHeadDim, numFlatPages, maxPagesPerSeq, topK, sliceLen, slicePad;
+  float sl2;
+};
+
+template <int NT, int STAGES>
+__global__ void __launch_bounds__(kThreads, 3) sparse_decode_kernel(const DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const uint32_t ring = smem_addr(smem);
+  const uint32_t q_tile = ring + STAGES * 2 * kTileBytes;
+  long long* kofs = reinterpret_cast<long long*>(smem + STAGES * 2 * kTileBytes + NT * 8 * 256);
+  long long* vofs = kofs + a.slicePad;
+  int* misc = reinterpret_cast<int*>(vofs + a.slicePad);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int L = max(0, min(a.ctx[b], a.maxPagesPerSeq * kTokensPerPage));
+  const int s0 = split * a.sliceLen;
+  const int s1 = min(a.topK, s0 + a.sliceLen);
+  const int32_t* lst = a.indices + static_cast<size_t>(b) * a.topK;
+  const int32_t* ptK = a.pageTable + static_cast<size_t>(b) * 2 * a.maxPagesPerSeq;
+  const int32_t* ptV = ptK + a.maxPagesPerSeq;
+  int last = -1;
+  for (int i = tid; i < a.slicePad; i += kThreads) {
+    const int slot = s0 + i;
+    const int j = slot < s1 ? __ldg(lst + slot) : -1;
+    bool ok = static_cast<unsigned>(j) < static_cast<unsigned>(L);
+    long long ko = -1, vo = -1;
+    if (ok) {
+      const int kp = __ldg(ptK + (j >> 7)), vp = __ldg(ptV + (j >> 7));
+      ok = static_cast<unsigned>(kp) < static_cast<unsigned>(a.numFlatPages) &&
+           static_cast<unsigned>(vp) < static_cast<unsigned>(a.numFlatPages);
+      const long long within = static_cast<long long>((j & 127) * a.Hkv + kvh) * a.poolHeadDim;
+      ko = static_cast<long long>(kp) * kTokensPerPage * a.Hkv * a.poolHeadDim + within;
+      vo = static_cast<long long>(vp) * kTokensPerPage * a.Hkv * a.poolHeadDim + within;
+    }
+    kofs[i] = ok ? ko : -1;
+    vofs[i] = ok ? vo : -1;
+    last = ok ? i : last;
+  }
+  last = __reduce_max_sync(kFull, last);
+  if (lane == 0) misc[warp] = last;
+  const __half* qsrc = a.q + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(kvh) * a.G) * kD;
+  for (int e = tid; e < NT * 8 * 16; e += kThreads) {
+    const int r = e >> 4, c = e & 15;
+    const bool ok = r < a.G;
+    cp_async16(q_tile + swz(r, c), qsrc + (ok ? r : 0) * kD + c * 8, ok);
+  }
+  cp_async_commit();
+  __syncthreads();
+  const int nslots = max(max(misc[0], misc[1]), max(misc[2], misc[3])) + 1;
+  const int ntiles = (nslots + kKeys - 1) / kKeys;
+
+  auto issue = [&](int tile, int stage) {
+    const int key = tid >> 1, part = tid & 1;
+    const long long ko = kofs[tile * kKeys + key], vo = vofs[tile * kKeys + key];
+    const bool ok = ko >= 0;
+    const uint32_t kdst = ring + stage * 2 * kTileBytes;
+    const uint32_t vdst = kdst + kTileBytes;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int ch = part * 8 + c;
+      cp_async16(kdst + swz(key, ch), a.pool + (ok ? ko : 0) + ch * 8, ok);
+      cp_async16(vdst + swz(key, ch), a.pool + (ok ? vo : 0) + ch * 8, ok);
+    }
+  };
+#pragma unroll
+  for (int s = 0; s < STAGES - 1; ++s) {
+    if (s < ntiles) issue(s, s);
+    cp_async_commit();
+  }
+  cp_async_wait<STAGES - 1>();
+  __syncthreads();
+  uint32_t qf[NT][8][2];
+  load_q_frags<NT>(q_tile, qf);
+  WarpAcc<NT> A;
+  acc_init(A);
+  for (int i = 0; i < ntiles; ++i) {
+    cp_async_wait<STAGES - 2>();
+    __syncthreads();
+    if (i + STAGES - 1 < ntiles) issue(i + STAGES - 1, (i + STAGES - 1) % STAGES);
+    cp_async_commit();
+    const int stage = i % STAGES;
+    const int slot = i * kKeys + warp * 16 + (lane >> 2);
+    attend16<NT>(A, ring + stage * 2 * kTileBytes, ring + stage * 2 * kTileBytes + kTileBytes, qf,
+                 kofs[slot] >= 0, kofs[slot + 8] >= 0, a.sl2);
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  float* mw = reinterpret_cast<float*>(smem);
+  float* lw = mw + 64;
+  float* ow = lw + 64;
+  stash_warp<NT>(A, mw, lw, ow);
+  __syncthreads();
+
+  // This split's partial: O unnormalised relative to its max M, stats (M, L).
+  const size_t part = (static_cast<size_t>(b) * a.Hkv + kvh) * kMaxSplits + split;
+  float* pO = a.partialO + part * kPartialRows * kD;
+  float* pS = a.partialStats + part * 2 * kPartialRows;
+  for (int e = tid; e < kPartialRows * (kD / 2); e += kThreads) {
+    const int h = e / (kD / 2), d = 2 * (e % (kD / 2));
+    float f[4] = {0.f, 0.f, 0.f, 0.f}, Lsum = 0.f, M = -INFINITY;
+    if (h < a.G) M = merge_weights(mw, lw, h, f, Lsum);
+    float o0 = 0.f, o1 = 0.f;
+    if (h < a.G) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        o0 += f[w] * ow[(w * 16 + h) * kOStride + d];
+        o1 += f[w] * ow[(w * 16 + h) * kOStride + d + 1];
+      }
+    }
+    reinterpret_cast<float2*>(pO + h * kD)[d / 2] = make_float2(o0, o1);
+    if (d == 0) {
+      pS[h] = h < a.G ? M : -INFINITY;
+      pS[kPartialRows + h] = h < a.G ? Lsum : 0.f;
+    }
+  }
+  // Last split to arrive merges the kMaxSplits partials and re-arms the counter.
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) misc[4] = atomicAdd(a.counters + b * a.Hkv + kvh, 1) == kMaxSplits - 1;
+  __syncthreads();
+  if (!misc[4]) return;
+  __threadfence();
+  const float* pO0 = a.partialO + (static_cast<size_t>(b) * a.Hkv + kvh) * kMaxSplits * kPartialRows * kD;
+  const float* pS0 = a.partialStats + (static_cast<size_t>(b) * a.Hkv + kvh) * kMaxSplits * 2 * kPartialRows;
+  __half* out = a.o + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(kvh) * a.G) * kD;
+  for (int e = tid; e < a.G * (kD / 2); e += kThreads) {
+    const int h = e / (kD / 2), d = 2 * (e % (kD / 2));
+    float M = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) M = fmaxf(M, __ldcg(pS0 + s * 2 * kPartialRows + h));
+    float Lsum = 0.f, o0 = 0.f, o1 = 0.f;
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) {
+      const float m = __ldcg(pS0 + s * 2 * kPartialRows + h);
+      const float f = m == -INFINITY ? 0.f : exp2f(m - M);
+      Lsum += f * __ldcg(pS0 + s * 2 * kPartialRows + kPartialRows + h);
+      const float2 ov = __ldcg(reinterpret_cast<const float2*>(pO0 + (s * kPartialRows + h) * kD + d));
+      o0 += f * ov.x;
+      o1 += f * ov.y;
+    }
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    reinterpret_cast<__half2*>(out + h * kD)[d / 2] = __floats2half2_rn(o0 * inv, o1 * inv);
+  }
+  if (tid == 0) a.counters[b * a.Hkv + kvh] = 0;
+}
+
+constexpr int kPrefillStages = 3;
+constexpr int kDecodeStages = 2;
+
+template <int NT>
+size_t prefill_smem(int topKpad) {
+  return static_cast<size_t>(kPrefillStages) * 2 * kTileBytes + NT * 8 * 256 + static_cast<size_t>(topKpad) * 4 + 64;
+}
+template <int NT>
+size_t decode_smem(int slicePad) {
+  return static_cast<size_t>(kDecodeStages) * 2 * kTileBytes + NT * 8 * 256 + static_cast<size_t>(slicePad) * 16 + 64;
+}
+
+constexpr int kMaxDynSmem = 227 * 1024;  // per-CTA opt-in limit; the launch asks only for what it uses
+
+template <int NT>
+cudaError_t prefill_nt(const PrefillArgs& a, long long nblocks, cudaStream_t st) {
+  const size_t smem = prefill_smem<NT>(a.topKpad);
+  static const cudaError_t attr = cudaFuncSetAttribute(sparse_prefill_kernel<NT, kPrefillStages>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+  if (attr != cudaSuccess) return attr;
+  sparse_prefill_kernel<NT, kPrefillStages><<<static_cast<unsigned>(nblocks), kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int NT>
+cudaError_t decode_nt(const DecodeArgs& a, int B, cudaStream_t st) {
+  const size_t smem = decode_smem<NT>(a.slicePad);
+  static const cudaError_t attr = cudaFuncSetAttribute(sparse_decode_kernel<NT, kDecodeStages>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+  if (attr != cudaSuccess) return attr;
+  dim3 grid(kMaxSplits, a.Hkv, B);
+  sparse_decode_kernel<NT, kDecodeStages><<<grid, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_sparse_prefill(const QsaSparsePrefillParams& p) {
+  PrefillArgs a;
+  a.q = static_cast<const __half*>(p.qPtr);
+  a.k = static_cast<const __half*>(p.kPtr);
+  a.v = static_cast<const __half*>(p.vPtr);
+  a.o = static_cast<__half*>(p.oPtr);
+  a.indices = p.indices;
+  a.ctx = p.contextLengths;
+  a.S = p.seqLen;
+  a.Hq = p.numQHeads;
+  a.Hkv = p.numKVHeads;
+  a.G = p.numQHeads / p.numKVHeads;
+  a.topK = p.topK;
+  a.topKpad = (p.topK + kKeys - 1) / kKeys * kKeys;
+  a.sl2 = p.attentionScale * kLog2e;
+  const long long nblocks = static_cast<long long>(p.batchSize) * p.seqLen * p.numKVHeads;
+  cudaStream_t st = static_cast<cudaStream_t>(p.stream);
+  return a.G <= 8 ? prefill_nt<1>(a, nblocks, st) : prefill_nt<2>(a, nblocks, st);
+}
+
+cudaError_t launch_sparse_decode(const QsaSparseDecodeParams& p) {
+  DecodeArgs a;
+  a.q = static_cast<const __half*>(p.qPtr);
+  a.pool = static_cast<const __half*>(p.kvPoolPtr);
+  a.pageTable = p.pageTable;
+  a.indices = p.indices;
+  a.ctx = p.contextLengths;
+  a.o = static_cast<__half*>(p.oPtr);
+  a.partialO = p.partialO;
+  a.partialStats = p.partialStats;
+  a.counters = p.splitCounters;
+  a.Hq = p.numQHeads;
+  a.Hkv = p.numKVHeads;
+  a.G = p.numQHeads / p.numKVHeads;
+  a.poolHeadDim = p.poolHeadDim;
+  a.numFlatPages = p.numFlatPages;
+  a.maxPagesPerSeq = p.maxPagesPerSeq;
+  a.topK = p.topK;
+  a.sliceLen = (p.topK + kMaxSplits - 1) / kMaxSplits;
+  a.slicePad = (a.sliceLen + kKeys - 1) / kKeys * kKeys;
+  a.sl2 = p.attentionScale * kLog2e;
+  cudaStream_t st = static_cast<cudaStream_t>(p.stream);
+  return a.G <= 8 ? decode_nt<1>(a, p.batchSize, st) : decode_nt<2>(a, p.batchSize, st);
+}
+
+}  // namespace qsa

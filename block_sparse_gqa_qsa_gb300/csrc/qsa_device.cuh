@@ -1,0 +1,218 @@
+// qsa_device.cuh -- device helpers shared by the QSA kernels (sm_103a):
+// inline-PTX wrappers (cp.async, ldmatrix, mma.sync, movmatrix, mbarrier, TMA),
+// CTA-wide reductions and scans, RoPE angles, and the deterministic top-k
+// selection used by both indexers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qsa {
+
+constexpr int kTokensPerPage = 128;  // pool page size ("Cute Dsl Qsa Sparse Runner", QsaSparseDecodeParams)
+constexpr int kMaxSplits = 8;        // kMaxSplits of CuteDslQsaSparseDecodeRunner
+constexpr int kPartialRows = 16;     // kPartialRows of CuteDslQsaSparseDecodeRunner
+constexpr unsigned kFull = 0xffffffffu;
+
+// Error bits recorded in the status word of an indexer workspace.
+constexpr int kErrWaitTimeout = 1;  // a bounded wait on a TMA barrier expired
+constexpr int kErrBadPage = 2;      // a page-table entry fell outside the pool
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte global->shared async copy; zero-fills the destination when !pred.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
+  const int n = pred ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// D = A(16x16, row) * B(16x8, col) + D, fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Transpose of an 8x8 b16 matrix held one row-pair per thread (fragment layout).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// mbarrier + TMA (cp.async.bulk.tensor) ---------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+  return t;
+}
+// Bounded wait: gives up after `limit_ns` of wall time and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];\n" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// -------------------------------------------------------- CTA reductions
+// Sum of one int per thread over a CTA of NT threads.  `red` holds 2*NT/32
+// ints; `phase` alternates so that one barrier per call suffices.
+template <int NT>
+__device__ __forceinline__ int cta_sum(int v, int* red, int& phase) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  v = __reduce_add_sync(kFull, v);
+  int* r = red + phase * (NT / 32);
+  if (lane == 0) r[w] = v;
+  __syncthreads();
+  int s = 0;
+#pragma unroll
+  for (int i = 0; i < NT / 32; ++i) s += r[i];
+  phase ^= 1;
+  return s;
+}
+
+// Exclusive prefix sum over the CTA in thread order; `total` gets the sum.
+template <int NT>
+__device__ __forceinline__ int cta_exclusive_scan(int v, int* scratch, int& total) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[w] = x;
+  __syncthreads();
+  int base = 0, tot = 0;
+#pragma unroll
+  for (int i = 0; i < NT / 32; ++i) {
+    const int s = scratch[i];
+    base += i < w ? s : 0;
+    tot += s;
+  }
+  __syncthreads();
+  total = tot;
+  return base + x - v;
+}
+
+// ------------------------------------------------------------ top-k select
+// Deterministic top-`budget` selection by (key desc, id asc) over a CTA.
+// Thread i holds elements [i*VPT, i*VPT + VPT) of an id-ascending sequence;
+// only the first `nv` (<= VPT) of a thread's elements are valid.  Keys are
+// the bit patterns of non-negative floats, so unsigned order is value order.
+// The threshold T (the budget-th largest key) is found by bisection on the
+// key space with one CTA-wide count per step; keys > T are kept, and of the
+// keys == T the lowest ids (a prefix in thread order) fill the rest.
+// Requires total valid elements > budget.  Sets sel[v] for kept elements.
+template <int NT, int VPT>
+__device__ __forceinline__ void cta_topk(const uint32_t (&key)[VPT], int nv, int budget, bool (&sel)[VPT],
+                                         int* red, int* scratch) {
+  int phase = 0;
+  uint32_t lo = 0u, hi = 0x7f800001u;  // count(>= lo) >= budget > count(>= hi)
+  int cnt_hi = 0;
+  while (hi - lo > 1u) {
+    const uint32_t mid = lo + ((hi - lo) >> 1);
+    int c = 0;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) c += (v < nv && key[v] >= mid) ? 1 : 0;
+    const int tot = cta_sum<NT>(c, red, phase);
+    if (tot >= budget) {
+      lo = mid;
+    } else {
+      hi = mid;
+      cnt_hi = tot;
+    }
+  }
+  const uint32_t T = lo;
+  const int need = budget - cnt_hi;  // how many keys equal to T are kept
+  int eq = 0;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) eq += (v < nv && key[v] == T) ? 1 : 0;
+  int tot_eq;
+  int rank = cta_exclusive_scan<NT>(eq, scratch, tot_eq);
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    bool s = false;
+    if (v < nv) {
+      if (key[v] > T) {
+        s = true;
+      } else if (key[v] == T) {
+        s = rank < need;
+        ++rank;
+      }
+    }
+    sel[v] = s;
+  }
+}
+
+// ------------------------------------------------------------------- RoPE
+// cos/sin of pos * inv_freq with the angle formed and reduced modulo 2*pi in
+// f64, then evaluated in fp32 (|r| <= pi): an fp32 product pos * inv_freq
+// would be off by up to 0.03 rad at pos ~ 5e5.
+__device__ __forceinline__ void rope_cos_sin_f32(double pos, double inv_freq, float& c, float& s) {
+  const double a = pos * inv_freq;
+  const double k = rint(a * 0.15915494309189535);           // 1 / (2 pi)
+  double r = fma(-k, 6.283185307179586, a);                   // 2 pi, high part
+  r = fma(-k, 2.4492935982947064e-16, r);                     // 2 pi - high part
+  sincosf(static_cast<float>(r), &s, &c);
+}
+
+}  // namespace qsa

@@ -1,0 +1,44 @@
+// qsa_internal.h -- launch interface between the C ABI (qsa_api.cu) and the
+// kernel translation units.  Host-side only; not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/qsa.h"
+
+namespace qsa {
+
+constexpr int kTokensPerPageHost = 128;  // pool page size of the decode contract
+
+// theta^(-2i/rot) for i < rot/2, formed in f64 on the host once per call.
+struct RopeFreqs {
+  double inv_freq[64];
+};
+
+// Prefill indexer -----------------------------------------------------------
+constexpr int kPrefillRowsPerCta = 8;      // query rows sharing one CTA's block-key tiles
+constexpr int kPrefillMaxBlocks = 4096;    // block scores of a row group kept in shared memory
+size_t indexer_prefill_workspace_bytes(int B, int S, int di, int ratio);
+cudaError_t launch_indexer_prefill(const QsaIndexerPrefillParams& p, const RopeFreqs& rf);
+
+// Decode indexer ------------------------------------------------------------
+struct DecodePlan {
+  int pagesPerChunk;   // pages of block keys one CTA streams
+  int chunksMax;       // chunks of the longest possible sequence
+  int levels;          // merge levels above the chunks (fan-in 8)
+  int slotsPerSeq;     // candidate slots per sequence over all levels
+  int countersPerSeq;  // last-arriver counters per sequence
+};
+DecodePlan plan_indexer_decode(int B, int maxPagesPerSeq, int ratio);
+size_t indexer_decode_workspace_bytes(int B, int maxPagesPerSeq, int ratio, int budget);
+cudaError_t launch_indexer_decode(const QsaIndexerDecodeParams& p, const RopeFreqs& rf,
+                                  const CUtensorMap& kbarMap);
+
+// Attention -----------------------------------------------------------------
+cudaError_t launch_sparse_prefill(const QsaSparsePrefillParams& p);
+cudaError_t launch_sparse_decode(const QsaSparseDecodeParams& p);
+
+}  // namespace qsa

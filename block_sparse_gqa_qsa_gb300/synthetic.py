@@ -205,3 +205,46 @@ def random_lists(B: int, S: int, topK: int, ctx, seed: int, fill: float = 1.0,
             pick = torch.randperm(span, generator=g)[:n].to(torch.int32)
             out[b, t, :n] = pick
     return out
+
+
+def qsa_like_lists(B: int, S: int, ctx, ratio: int, budget: int, topK: int, seed: int,
+                   device="cpu", chunk_rows: int = 1024) -> torch.Tensor:
+    """Index lists with the indexer's structure but a random block choice.
+
+    Row t < L keeps every complete block when n_c(t) <= budget, else `budget`
+    complete blocks drawn uniformly; the blocks expand to their `ratio` tokens
+    and the causal tail follows; ascending, -1 padded.  Rows t >= L are -1.
+    For attention inputs at sizes where a CPU reference selection is slow."""
+    g = _gen(seed, device=device)
+    out = torch.full((B, S, topK), -1, dtype=torch.int32, device=device)
+    nbmax = max(S // ratio, 1)
+    big = 1 << 30
+    for b in range(B):
+        L = int(ctx[b])
+        for r0 in range(0, L, chunk_rows):
+            r1 = min(L, r0 + chunk_rows)
+            t = torch.arange(r0, r1, device=device)
+            n_c = (t + 1) // ratio
+            blk = torch.arange(nbmax, device=device)
+            valid = blk[None, :] < n_c[:, None]
+            key = torch.rand((r1 - r0, nbmax), generator=g, device=device)
+            key = torch.where(valid, key, torch.full_like(key, -1.0))
+            k = min(budget, nbmax)
+            top = torch.topk(key, k, dim=1).indices
+            chosen = torch.zeros_like(valid)
+            chosen.scatter_(1, top, True)
+            chosen &= valid
+            tok = torch.arange(S, device=device)
+            tmask = chosen.repeat_interleave(ratio, dim=1)
+            if tmask.shape[1] < S:
+                tmask = torch.cat([tmask, torch.zeros((r1 - r0, S - tmask.shape[1]), dtype=torch.bool,
+                                                      device=device)], dim=1)
+            tmask = tmask[:, :S] | ((tok[None, :] >= (n_c * ratio)[:, None]) & (tok[None, :] <= t[:, None]))
+            keyed = torch.where(tmask, tok[None, :].expand(r1 - r0, S), torch.full((1, 1), big, device=device))
+            srt = torch.sort(keyed, dim=1).values[:, :topK]
+            srt = torch.where(srt == big, torch.full_like(srt, -1), srt)
+            if srt.shape[1] < topK:
+                srt = torch.cat([srt, torch.full((r1 - r0, topK - srt.shape[1]), -1, device=device,
+                                                 dtype=srt.dtype)], dim=1)
+            out[b, r0:r1] = srt.to(torch.int32)
+    return out

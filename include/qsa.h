@@ -41,6 +41,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define QSA_API __attribute__((visibility("default")))
+#else
+#define QSA_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -82,7 +88,7 @@ typedef struct {
   int32_t rotDim;                /* rotated dims: even, <= headDim                           */
   int32_t compressRatio;         /* r (tokens per block); 4 on the pages                    */
   int32_t budget;                /* blocks kept per row; 512 on the pages                    */
-  int32_t topK;                  /* list width, must equal budget*r + r - 1                  */
+  int32_t topK;                  /* list width, >= budget*r + r - 1 (2051 on the pages)      */
   float ropeTheta;               /* RoPE base                                                */
   float rmsNormEps;              /* RMSNorm epsilon                                          */
   void* stream;                  /* cudaStream_t                                             */
@@ -127,7 +133,7 @@ typedef struct {
   int32_t rotDim;
   int32_t compressRatio;         /* r; must divide 128                                              */
   int32_t budget;
-  int32_t topK;                  /* must equal budget*r + r - 1                                    */
+  int32_t topK;                  /* >= budget*r + r - 1                                            */
   float ropeTheta;
   float rmsNormEps;
   void* stream;
@@ -193,38 +199,39 @@ typedef struct {
 
 /* ------------------------------------------------------------ entry points */
 
-qsa_status_t qsa_indexer_prefill(const QsaIndexerPrefillParams* params);
-qsa_status_t qsa_indexer_decode(const QsaIndexerDecodeParams* params);
-qsa_status_t qsa_sparse_prefill(const QsaSparsePrefillParams* params);
-qsa_status_t qsa_sparse_decode(const QsaSparseDecodeParams* params);
+QSA_API qsa_status_t qsa_indexer_prefill(const QsaIndexerPrefillParams* params);
+QSA_API qsa_status_t qsa_indexer_decode(const QsaIndexerDecodeParams* params);
+QSA_API qsa_status_t qsa_sparse_prefill(const QsaSparsePrefillParams* params);
+QSA_API qsa_status_t qsa_sparse_decode(const QsaSparseDecodeParams* params);
 
 /* Workspace bytes of the indexers (0 when the sizes are invalid). */
-size_t qsa_indexer_prefill_workspace_size(int32_t batchSize, int32_t seqLen, int32_t headDim,
+QSA_API size_t qsa_indexer_prefill_workspace_size(int32_t batchSize, int32_t seqLen, int32_t headDim,
                                           int32_t compressRatio);
-size_t qsa_indexer_decode_workspace_size(int32_t batchSize, int32_t maxPagesPerSeq,
+QSA_API size_t qsa_indexer_decode_workspace_size(int32_t batchSize, int32_t maxPagesPerSeq,
                                          int32_t compressRatio, int32_t budget);
 
 /* Element counts of the split-K decode workspace ("Cute Dsl Qsa Sparse Runner",
  * QsaSparseDecodeParams: partialO, partialStats, splitCounters). */
-size_t qsa_sparse_decode_partial_o_elems(int32_t batchSize, int32_t numKVHeads, int32_t headDim);
-size_t qsa_sparse_decode_partial_stats_elems(int32_t batchSize, int32_t numKVHeads);
-size_t qsa_sparse_decode_counter_elems(int32_t batchSize, int32_t numKVHeads);
-int32_t qsa_sparse_decode_max_splits(void);   /* kMaxSplits = 8   */
-int32_t qsa_sparse_decode_partial_rows(void); /* kPartialRows = 16 */
+QSA_API size_t qsa_sparse_decode_partial_o_elems(int32_t batchSize, int32_t numKVHeads, int32_t headDim);
+QSA_API size_t qsa_sparse_decode_partial_stats_elems(int32_t batchSize, int32_t numKVHeads);
+QSA_API size_t qsa_sparse_decode_counter_elems(int32_t batchSize, int32_t numKVHeads);
+QSA_API int32_t qsa_sparse_decode_max_splits(void);   /* kMaxSplits = 8   */
+QSA_API int32_t qsa_sparse_decode_partial_rows(void); /* kPartialRows = 16 */
 
 /* Whether these kernels cover a shape (the runners' canImplement): 1 or 0. */
-int32_t qsa_sparse_prefill_can_implement(int32_t numQHeads, int32_t numKVHeads, int32_t headDim);
-int32_t qsa_sparse_decode_can_implement(int32_t numQHeads, int32_t numKVHeads, int32_t headDim,
+QSA_API int32_t qsa_sparse_prefill_can_implement(int32_t numQHeads, int32_t numKVHeads, int32_t headDim);
+QSA_API int32_t qsa_sparse_decode_can_implement(int32_t numQHeads, int32_t numKVHeads, int32_t headDim,
                                         int32_t poolHeadDim);
 
-/* Longest padded prefill length the prefill indexer accepts (it keeps a row
- * group's block scores on chip). */
-int32_t qsa_indexer_prefill_max_seq_len(void);
+/* The prefill indexer keeps a row group's block scores in shared memory:
+ * floor(seqLen / compressRatio) may not exceed this many blocks (4096, i.e.
+ * seqLen up to 16384 at ratio 4); larger shapes return QSA_ERR_UNSUPPORTED. */
+QSA_API int32_t qsa_indexer_prefill_max_blocks(void);
 
 /* Human-readable name of a status, and the detail of the last failure on the
  * calling thread (never NULL; empty when there was none). */
-const char* qsa_status_string(qsa_status_t status);
-const char* qsa_last_error_message(void);
+QSA_API const char* qsa_status_string(qsa_status_t status);
+QSA_API const char* qsa_last_error_message(void);
 
 #ifdef __cplusplus
 }

@@ -71,6 +71,17 @@ double half_to_double(uint16_t h) {
   return sign ? -mag : mag;
 }
 
+// The same widening for all 65536 patterns, built once; the passes below read
+// fp16 tensors through it.
+const double* half_table() {
+  static const std::vector<double> tab = [] {
+    std::vector<double> t(65536);
+    for (int h = 0; h < 65536; ++h) t[h] = half_to_double(static_cast<uint16_t>(h));
+    return t;
+  }();
+  return tab.data();
+}
+
 // Round-to-nearest-even of a double to binary16.
 uint16_t double_to_half(double x) {
   if (std::isnan(x)) return 0x7e00;
@@ -119,13 +130,14 @@ void partial_rope(double* y, int rot, int64_t pos, double theta) {
   }
 }
 
-bool rope_args_ok(int di, int rot) { return di > 0 && rot >= 0 && rot <= di && rot % 2 == 0; }
+bool rope_args_ok(int di, int rot) { return di > 0 && di <= 512 && rot >= 0 && rot <= di && rot % 2 == 0; }
 
 // Index query of one (row, head): RMSNorm*(1+w), then RoPE at pos.
 void index_q(const uint16_t* x, const float* w, int di, int rot, int64_t pos, double theta,
              double eps, double* q) {
+  const double* H = half_table();
   std::vector<double> xd(di);
-  for (int i = 0; i < di; ++i) xd[i] = half_to_double(x[i]);
+  for (int i = 0; i < di; ++i) xd[i] = H[x[i]];
   rms_norm_one_plus_w(xd.data(), w, di, eps, q);
   partial_rope(q, rot, pos, theta);
 }
@@ -133,9 +145,10 @@ void index_q(const uint16_t* x, const float* w, int di, int rot, int64_t pos, do
 // Block key: mean of r raw keys -> RMSNorm*(1+w) -> RoPE at the block start pos -> fp16.
 void block_key(const uint16_t* raw, int r, const float* w, int di, int rot, int64_t pos,
                double theta, double eps, uint16_t* kbar, double* y64) {
+  const double* H = half_table();
   std::vector<double> m(di, 0.0), y(di);
   for (int j = 0; j < r; ++j)
-    for (int i = 0; i < di; ++i) m[i] += half_to_double(raw[static_cast<size_t>(j) * di + i]);
+    for (int i = 0; i < di; ++i) m[i] += H[raw[static_cast<size_t>(j) * di + i]];
   for (int i = 0; i < di; ++i) m[i] /= r;
   rms_norm_one_plus_w(m.data(), w, di, eps, y.data());
   partial_rope(y.data(), rot, pos, theta);
@@ -145,10 +158,13 @@ void block_key(const uint16_t* raw, int r, const float* w, int di, int rot, int6
 
 // sum_h relu(q_h . kbar) / sqrt(di)   ([RS] qsa_score)
 double block_score(const double* q, const uint16_t* kbar, int Hi, int di) {
+  const double* H = half_table();
+  double k[512];
+  for (int i = 0; i < di; ++i) k[i] = H[kbar[i]];
   double s = 0.0;
   for (int h = 0; h < Hi; ++h) {
     double dot = 0.0;
-    for (int i = 0; i < di; ++i) dot += q[static_cast<size_t>(h) * di + i] * half_to_double(kbar[i]);
+    for (int i = 0; i < di; ++i) dot += q[static_cast<size_t>(h) * di + i] * k[i];
     s += dot > 0.0 ? dot : 0.0;
   }
   return s / std::sqrt(static_cast<double>(di));
@@ -189,12 +205,13 @@ void attend_head(const uint16_t* q, const uint16_t* const* krows, const uint16_t
                  int64_t n, int D, double scale, double* o) {
   for (int d = 0; d < D; ++d) o[d] = 0.0;
   if (n == 0) return;
+  const double* H = half_table();
   std::vector<double> qd(D), s(n);
-  for (int d = 0; d < D; ++d) qd[d] = half_to_double(q[d]);
+  for (int d = 0; d < D; ++d) qd[d] = H[q[d]];
   double m = -std::numeric_limits<double>::infinity();
   for (int64_t j = 0; j < n; ++j) {
     double dot = 0.0;
-    for (int d = 0; d < D; ++d) dot += qd[d] * half_to_double(krows[j][d]);
+    for (int d = 0; d < D; ++d) dot += qd[d] * H[krows[j][d]];
     s[j] = scale * dot;
     m = std::max(m, s[j]);
   }
@@ -202,7 +219,7 @@ void attend_head(const uint16_t* q, const uint16_t* const* krows, const uint16_t
   for (int64_t j = 0; j < n; ++j) {
     const double p = std::exp(s[j] - m);
     l += p;
-    for (int d = 0; d < D; ++d) o[d] += p * half_to_double(vrows[j][d]);
+    for (int d = 0; d < D; ++d) o[d] += p * H[vrows[j][d]];
   }
   for (int d = 0; d < D; ++d) o[d] /= l;
 }

@@ -1,0 +1,233 @@
+"""GPU parity of the decode path through the C ABI: qsa_indexer_decode (state
+update in the pool tails, then scoring, selection and expansion) and the
+split-K qsa_sparse_decode, against the fp64 CPU oracle."""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_gqa_qsa_gb300 import _binding as qb
+from block_sparse_gqa_qsa_gb300 import synthetic as syn
+from qsa_testlib import check_attention, check_list, compare_selection, f32, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TPP = syn.TOKENS_PER_PAGE
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_sparse_gqa_qsa_gb300 import build
+    build.build()
+    qb.lib()
+
+
+def _gpu_indexer(d_dev, cfg, ws=None):
+    B = cfg.B
+    if ws is None:
+        ws = qb.alloc_workspace(qb.indexer_decode_workspace_size(B, cfg.maxPagesPerSeq, cfg.ratio, cfg.budget), DEV)
+    ind = torch.full((B, 1, cfg.topK), 7, dtype=torch.int32, device=DEV)
+    qb.indexer_decode(d_dev["idxQ"], d_dev["idxK"], d_dev["wq"], d_dev["wk"], d_dev["pool"], d_dev["page_table"],
+                      d_dev["ctx"], ind, ws, D=cfg.D, rot=cfg.rot, ratio=cfg.ratio, budget=cfg.budget, topK=cfg.topK,
+                      theta=cfg.theta, eps=cfg.eps)
+    torch.cuda.synchronize()
+    return ind, ws
+
+
+def _gpu_attention(d_dev, lists_dev, cfg, scale, ws=None):
+    B = cfg.B
+    if ws is None:
+        po, ps, pc = qb.sparse_decode_workspace_elems(B, cfg.Hkv, cfg.D)
+        ws = (torch.zeros(po, dtype=torch.float32, device=DEV), torch.zeros(ps, dtype=torch.float32, device=DEV),
+              torch.zeros(pc, dtype=torch.int32, device=DEV))
+    out = torch.full((B, 1, cfg.Hq, cfg.D), float("nan"), dtype=torch.float16, device=DEV)
+    qb.sparse_decode(d_dev["q"], d_dev["pool"], d_dev["page_table"], lists_dev, d_dev["ctx"], out, *ws, D=cfg.D,
+                     scale=scale)
+    torch.cuda.synchronize()
+    return out, ws
+
+
+def _to_dev(d):
+    return {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+def _oracle_indexer(d_np, pool_np, cfg):
+    ind, sc = oracle.indexer_decode(d_np["idxQ"], d_np["idxK"], d_np["wq"], d_np["wk"], pool_np, d_np["page_table"],
+                                    d_np["ctx"], D=cfg.D, rot=cfg.rot, ratio=cfg.ratio, budget=cfg.budget,
+                                    topK=cfg.topK, theta=cfg.theta, eps=f32(cfg.eps), want_scores=True)
+    return ind, sc
+
+
+def _np(d):
+    return {k: (v.numpy() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+def test_indexer_decode_parity_and_state_update():
+    cfg = syn.DECODE_PARITY
+    d = syn.make_decode(cfg)
+    d_np = _np(d)
+    pool_np = d_np["pool"].copy()
+    d_dev = _to_dev(d)
+    ind, ws = _gpu_indexer(d_dev, cfg)
+    ref, sc = _oracle_indexer(d_np, pool_np, cfg)
+    g = to_np(ind)[:, 0]
+    for b in range(cfg.B):
+        L = int(d_np["ctx"][b])
+        check_list(g[b], L - 1, L, cfg.ratio, cfg.budget)
+        compare_selection(g[b], ref[b], sc[b], L - 1, cfg.ratio, cfg.budget)
+    # the pool after the step: identical bytes (tails of head 0 only were written)
+    assert np.array_equal(to_np(d_dev["pool"]).view(np.uint16), pool_np.view(np.uint16))
+    assert not np.array_equal(pool_np.view(np.uint16), d_np["pool"].view(np.uint16))
+    assert int(to_np(ws[:4]).view(np.int32)[0]) == 0, "workspace status word"
+    # a second call on the updated state gives the same lists and leaves the pool unchanged
+    ind2, _ = _gpu_indexer(d_dev, cfg, ws)
+    assert torch.equal(ind2, ind)
+    assert np.array_equal(to_np(d_dev["pool"]).view(np.uint16), pool_np.view(np.uint16))
+
+
+def test_indexer_decode_edges():
+    """Dense rows (n_c <= budget), L = 0, a block completed on a page boundary, ties."""
+    cfg = dataclasses.replace(syn.DECODE_PARITY, B=5, budget=40, ctx_list=(0, 3, 128, 160, 4096), max_ctx=4096,
+                              seed=21)
+    d = syn.make_decode(cfg)
+    d_np = _np(d)
+    pool_np = d_np["pool"].copy()
+    d_dev = _to_dev(d)
+    ind, _ = _gpu_indexer(d_dev, cfg)
+    ref, sc = _oracle_indexer(d_np, pool_np, cfg)
+    g = to_np(ind)[:, 0]
+    assert np.all(g[0] == -1)
+    for b in range(1, cfg.B):
+        L = int(d_np["ctx"][b])
+        check_list(g[b], L - 1, L, cfg.ratio, cfg.budget)
+        compare_selection(g[b], ref[b], sc[b], L - 1, cfg.ratio, cfg.budget)
+    assert np.array_equal(to_np(d_dev["pool"]).view(np.uint16), pool_np.view(np.uint16))
+    # exact ties: every block-key tail identical and no RoPE -> lowest ids on both sides
+    cfg0 = dataclasses.replace(cfg, rot=0, ctx_list=(3001, 4000, 2, 515, 4095))
+    d = syn.make_decode(cfg0)
+    pool = d["pool"]
+    pool[:, :, 0, cfg0.D:] = pool[0, 0, 0, cfg0.D:]
+    d_np = _np(d)
+    pool_np = d_np["pool"].copy()
+    d_dev = _to_dev(d)
+    ind, _ = _gpu_indexer(d_dev, cfg0)
+    ref, _ = _oracle_indexer(d_np, pool_np, cfg0)
+    assert np.array_equal(to_np(ind)[:, 0], ref)
+
+
+def _state(pool, pt, b, L, cfg):
+    """Compact indexer state of sequence b before decoding token L-1 (torch gathers of input data)."""
+    t = L - 1
+    n_prev = t // cfg.ratio
+    tok = torch.arange(n_prev, device=pool.device) * cfg.ratio
+    kb = pool[pt[b, 1, tok // TPP].long(), tok % TPP, 0, cfg.D:cfg.D + cfg.di]
+    first = n_prev * cfg.ratio
+    tt = torch.arange(first, t, device=pool.device)
+    tail = pool[pt[b, 0, tt // TPP].long(), tt % TPP, 0, cfg.D:cfg.D + cfg.di]
+    return to_np(kb), to_np(tail)
+
+
+def _rows(pool, pt, b, lst, cfg):
+    j = torch.from_numpy(lst[lst >= 0].astype(np.int64)).to(pool.device)
+    kr = pool[pt[b, 0, j // TPP].long(), j % TPP, :, :cfg.D]
+    vr = pool[pt[b, 1, j // TPP].long(), j % TPP, :, :cfg.D]
+    return to_np(kr), to_np(vr)
+
+
+@pytest.mark.parametrize("cfg", [syn.DECODE_32, syn.DECODE_LONG], ids=lambda c: c.name)
+def test_decode_full_size(cfg):
+    d = syn.make_decode(cfg, device=DEV)
+    d_dev = _to_dev(d)
+    pool, pt = d_dev["pool"], d_dev["page_table"]
+    ctx = d["ctx"].numpy()
+    d_np = _np({k: v for k, v in d.items() if k != "pool"})
+    # oracle on the compact state of every sequence, taken before the GPU updates the tails
+    ref_lists, ref_new, ref_sc = [], [], []
+    for b in range(cfg.B):
+        kb, tail = _state(pool, pt, b, int(ctx[b]), cfg)
+        lst, knew, sc = oracle.indexer_decode_state(d_np["idxQ"][b], d_np["idxK"][b], d_np["wq"], d_np["wk"], kb,
+                                                    tail if len(tail) else None, int(ctx[b]), rot=cfg.rot,
+                                                    ratio=cfg.ratio, budget=cfg.budget, topK=cfg.topK,
+                                                    theta=cfg.theta, eps=f32(cfg.eps))
+        ref_lists.append(lst)
+        ref_new.append(knew)
+        ref_sc.append(sc)
+    ind, ws = _gpu_indexer(d_dev, cfg)
+    g = to_np(ind)[:, 0]
+    for b in range(cfg.B):
+        L = int(ctx[b])
+        check_list(g[b], L - 1, L, cfg.ratio, cfg.budget)
+        compare_selection(g[b], ref_lists[b], ref_sc[b], L - 1, cfg.ratio, cfg.budget)
+        t = L - 1
+        if ref_new[b] is not None:  # completed block: its key in the V-row tail of its first token
+            first = (L // cfg.ratio - 1) * cfg.ratio
+            got = pool[pt[b, 1, first // TPP].long(), first % TPP, 0, cfg.D:cfg.D + cfg.di]
+            assert np.array_equal(to_np(got).view(np.uint16), ref_new[b].view(np.uint16))
+        else:  # raw key in token t's K-row tail
+            got = pool[pt[b, 0, t // TPP].long(), t % TPP, 0, cfg.D:cfg.D + cfg.di]
+            assert np.array_equal(to_np(got).view(np.uint16), d_np["idxK"][b].view(np.uint16))
+    assert int(to_np(ws[:4]).view(np.int32)[0]) == 0
+    # attention over the oracle's lists
+    lists_dev = torch.from_numpy(np.stack(ref_lists)[:, None, :]).to(DEV)
+    out, _ = _gpu_attention(d_dev, lists_dev, cfg, f32(cfg.scale))
+    for b in range(cfg.B):
+        kr, vr = _rows(pool, pt, b, ref_lists[b], cfg)
+        ref = oracle.attend_rows(d_np["q"][b, 0], kr, vr, f32(cfg.scale))
+        check_attention(to_np(out)[b, 0], ref, f"{cfg.name} seq {b}")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(16, 2), (32, 4), (32, 2), (12, 1)])
+def test_sparse_decode_parity(Hq, Hkv):
+    cfg = dataclasses.replace(syn.DECODE_PARITY, Hq=Hq, Hkv=Hkv, seed=Hq + Hkv)
+    d = syn.make_decode(cfg)
+    d_np = _np(d)
+    lists = oracle.indexer_decode(d_np["idxQ"], d_np["idxK"], d_np["wq"], d_np["wk"], d_np["pool"].copy(),
+                                  d_np["page_table"], d_np["ctx"], D=cfg.D, rot=cfg.rot, ratio=cfg.ratio,
+                                  budget=cfg.budget, topK=cfg.topK, theta=cfg.theta, eps=f32(cfg.eps))
+    d_dev = _to_dev(d)
+    lists_dev = torch.from_numpy(lists[:, None, :].copy()).to(DEV)
+    out, ws = _gpu_attention(d_dev, lists_dev, cfg, f32(cfg.scale))
+    ref = oracle.sparse_decode(d_np["q"][:, 0], d_np["pool"], d_np["page_table"], lists, d_np["ctx"], D=cfg.D,
+                               scale=f32(cfg.scale))
+    check_attention(to_np(out)[:, 0], ref, "decode parity")
+    assert int(ws[2].abs().sum()) == 0, "split counters must be re-armed to zero"
+    out2, _ = _gpu_attention(d_dev, lists_dev, cfg, f32(cfg.scale), ws)
+    assert torch.equal(out2.view(torch.int16), out.view(torch.int16)), "back-to-back calls must agree bitwise"
+    # only columns [0, D) are read: NaN tails change nothing
+    d_dev["pool"][..., cfg.D:] = float("nan")
+    out3, _ = _gpu_attention(d_dev, lists_dev, cfg, f32(cfg.scale), ws)
+    assert torch.equal(out3.view(torch.int16), out.view(torch.int16))
+
+
+def test_sparse_decode_page_permutation_and_empty():
+    cfg = dataclasses.replace(syn.DECODE_PARITY, B=3, ctx_list=(0, 700, 1500), max_ctx=1536, seed=5)
+    d = syn.make_decode(cfg)
+    d_np = _np(d)
+    rng = np.random.default_rng(1)
+    lists = np.full((cfg.B, cfg.topK), -1, np.int32)
+    for b, L in enumerate(cfg.ctx_list):
+        n = min(L, 450)
+        lists[b, :n] = rng.permutation(L)[:n]
+    d_dev = _to_dev(d)
+    lists_dev = torch.from_numpy(lists[:, None, :].copy()).to(DEV)
+    out, ws = _gpu_attention(d_dev, lists_dev, cfg, 0.08)
+    o = to_np(out)[:, 0]
+    assert np.all(o[0].view(np.uint16) == 0), "L = 0: zero output"
+    ref = oracle.sparse_decode(d_np["q"][:, 0], d_np["pool"], d_np["page_table"], lists, d_np["ctx"], D=cfg.D,
+                               scale=f32(0.08))
+    check_attention(o, ref, "random lists")
+    # the same logical cache under another page permutation
+    npg = d["num_pages"]
+    perm = torch.from_numpy(rng.permutation(npg)).to(DEV)
+    mapping = torch.cat([perm, perm + npg])  # new id of every old page, V plane kept at +numPages
+    pool2 = torch.empty_like(d_dev["pool"])
+    pool2[mapping] = d_dev["pool"]
+    d2 = dict(d_dev, pool=pool2, page_table=mapping[d_dev["page_table"].long()].int())
+    out2, _ = _gpu_attention(d2, lists_dev, cfg, 0.08, ws)
+    assert torch.equal(out2.view(torch.int16), out.view(torch.int16))
