@@ -44,7 +44,6 @@ qsa::RopeFreqs rope_freqs(float theta, int rot) {
 
 constexpr int kMaxListWidth = 10240;     // prefill indexer stages one list in shared memory
 constexpr int kMaxAttnListWidth = 16384;  // attention stages one list (or slice) in shared memory
-constexpr int kMaxDecodeBudget = 512;     // decode merge holds 8 * budget candidates per CTA
 
 // Indexer arguments shared by both indexers ("Qsa Attention Plugin" constructor
 // attributes: indexerNumHeads, indexerHeadDim, indexerBudget, indexerCompressRatio).
@@ -167,9 +166,11 @@ qsa_status_t qsa_indexer_decode(const QsaIndexerDecodeParams* p) {
   if (qsa::kTokensPerPageHost % p->compressRatio != 0)
     return fail(QSA_ERR_INVALID_ARG, "qsa_indexer_decode: compressRatio %d does not divide the 128-token page",
                 p->compressRatio);
-  if (p->budget > kMaxDecodeBudget)
-    return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_decode: budget %d > %d", p->budget, kMaxDecodeBudget);
-  if (p->batchSize > 65535) return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_decode: batchSize > 65535");
+  if (p->compressRatio < 4)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_decode: compressRatio %d < 4 (a page's key tails must fit one "
+                                     "ring stage)", p->compressRatio);
+  if (p->batchSize > qsa::kDecodeMaxBatch)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_decode: batchSize > %d", qsa::kDecodeMaxBatch);
   if (p->kvHeadDim % 8 || p->poolHeadDim % 8 || !aligned(p->kvPool, 16))
     return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_decode: kvHeadDim and poolHeadDim must be multiples of 8 and "
                                      "kvPool 16-byte aligned (TMA rows)");

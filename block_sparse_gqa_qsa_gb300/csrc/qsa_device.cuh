@@ -60,6 +60,19 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
   return y;
 }
+// Paired fp32 FMA (two independent lanes of a 64-bit register pair): the same
+// FMA throughput as two scalar FMAs in half the issue slots.
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t pack_f2(float lo, float hi) {
+  return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
+}
+__device__ __forceinline__ float lo_f2(uint64_t x) { return __uint_as_float(static_cast<uint32_t>(x)); }
+__device__ __forceinline__ float hi_f2(uint64_t x) { return __uint_as_float(static_cast<uint32_t>(x >> 32)); }
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);

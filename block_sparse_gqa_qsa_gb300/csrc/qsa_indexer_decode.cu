@@ -3,22 +3,29 @@
 // predicated tail write / compress, B2 block scores from the kbar tails, B3
 // deterministic top-512 + expand; "KV pool contract" for where the state lives).
 //
-// One launch.  A sequence's complete blocks are cut into chunks of
-// `pagesPerChunk` pages; one CTA per (chunk, sequence):
-//   B1  index-query prep at t = L-1 (fp32, f64 angles), redundantly per CTA;
-//       chunk 0 stores the new raw key in token t's K-row tail when t leaves
-//       its block incomplete; the CTA owning the page of a block that t
-//       completes forms that block's key in f64 (from the K-row tails of its
-//       first r-1 tokens and the new key), stores it in the V-row tail of the
-//       block's first token and scores it from shared memory.
-//   B2  streams the chunk's block keys: one 3-D TMA copy fetches the 128/r
-//       key tails of a page (box {di, 128/r, 1} over a strided view of the
-//       pool) into a 4-stage ring; each key is scored by di/8 lanes of a warp
-//       (8 dims x 8 heads each), reduced with transposing warp shuffles.
-//   B3  keeps the chunk's top-`budget` (key desc, id asc) as candidates; the
-//       last CTA of each group of 8 (an atomic ticket, no waiting) merges the
-//       group's candidates, up a tree, and the root writes the index list.
-// Every wait on a TMA barrier is bounded; on expiry the CTA records
+// Three launches on the caller's stream:
+//   decode_prep_kernel    (B1) one CTA per sequence: index-query prep at
+//       t = L-1 (fp32, f64 angles) into the workspace; then the state update:
+//       the new raw key into token t's K-row tail when t leaves its block
+//       incomplete, else the block t completes is pooled in f64 (from the
+//       K-row tails of its first r-1 tokens and the new key) and its key is
+//       stored in the V-row tail of the block's first token.
+//   decode_score_kernel   (B2) persistent, one CTA per SM, warp-specialised:
+//       a producer warp streams the key tails of every page that holds
+//       complete blocks (one 3-D TMA copy per page: box {di, 128/r, 1} over a
+//       strided view of the pool) into a 24-stage ring; 15 consumer warps
+//       score one page each (8 dims x 8 heads per lane with paired fp32 FMA, a
+//       transposing shuffle reduction whose head order is pre-permuted per
+//       lane so that no select is needed), write the scores and add them to a
+//       4096-bin histogram of the score bits per sequence.  Pages are split
+//       evenly over the CTAs, so HBM streams without per-chunk stalls.
+//   decode_select_kernel  (B3) per sequence: the histogram gives the bin that
+//       holds the budget-th largest score; CTAs over 8192-block slices mark
+//       every block above that bin in a bitmap and append the blocks inside
+//       it; the last CTA to finish picks the exact top of those by (score
+//       desc, id asc), expands the bitmap in ascending order with the causal
+//       tail, and re-arms the histogram and counters.
+// Waits on TMA barriers are bounded; on expiry the kernel records
 // kErrWaitTimeout in the workspace status word and stops.
 #include "qsa_device.cuh"
 #include "qsa_internal.h"
@@ -27,15 +34,53 @@ namespace qsa {
 namespace {
 
 constexpr size_t kStatusBytes = 256;
-constexpr int kThreads = 256;
-constexpr int kStages = 4;
-constexpr int kVPT = 16;         // selection elements per thread (4096 per CTA)
-constexpr int kFanIn = 8;        // children merged per tree node
-constexpr int kMaxChunkBlocks = kThreads * kVPT;
+constexpr int kNumBins = 4096;       // histogram of (score bits >> 19): exponent + 4 mantissa bits
+constexpr int kBinShift = 19;
+constexpr int kSliceBlocks = 8192;   // blocks one select CTA filters
+constexpr int kConsumerWarps = 15;  // + 1 producer warp = 16 warps, up to 128 registers each
+constexpr int kScoreThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 24;
+constexpr int kSelThreads = 256;
+constexpr int kTieVPT = 16;          // tie candidates per thread held in registers
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;  // 0.2 s
 constexpr int kMaxDynSmem = 227 * 1024;
 
-struct DecIdxArgs {
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct WsLayout {
+  size_t q, scores, hist, bitmap, tieKey, tieId, counters, total;
+};
+WsLayout ws_layout(int B, int nbmax) {
+  WsLayout l;
+  size_t off = kStatusBytes;
+  l.q = off;
+  off += up256(static_cast<size_t>(B) * 8 * 128 * 4);  // prepared queries fp32 [B][8][128]
+  l.scores = off;
+  off += up256(static_cast<size_t>(B) * nbmax * 4);     // block scores fp32 [B][nbmax]
+  l.hist = off;
+  off += up256(static_cast<size_t>(B) * kNumBins * 4);  // int32 [B][kNumBins], zero between calls
+  l.bitmap = off;
+  off += up256(static_cast<size_t>(B) * ((nbmax + 31) / 32) * 4);
+  l.tieKey = off;
+  off += up256(static_cast<size_t>(B) * nbmax * 4);
+  l.tieId = off;
+  off += up256(static_cast<size_t>(B) * nbmax * 4);
+  l.counters = off;
+  off += up256(static_cast<size_t>(B) * 2 * 4);         // tie count, ticket: zero between calls
+  l.total = off;
+  return l;
+}
+
+__device__ __forceinline__ size_t pool_row(int page, int tok_in_page, int Hkv, int poolHeadDim) {
+  return (static_cast<size_t>(page) * kTokensPerPage + tok_in_page) * Hkv * poolHeadDim;  // head 0
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// ------------------------------------------------------------------ B1
+struct PrepArgs {
   const __half* idxQ;
   const __half* idxK;
   const float* wq;
@@ -43,150 +88,34 @@ struct DecIdxArgs {
   __half* pool;
   const int32_t* pageTable;
   const int32_t* ctx;
-  int32_t* indices;
-  uint32_t* candKey;  // [B][slotsPerSeq][budget]
-  int32_t* candId;    // [B][slotsPerSeq][budget]
-  int32_t* candCnt;   // [B][slotsPerSeq]
-  int32_t* counters;  // [B][countersPerSeq]
+  float* q;
   int32_t* status;
-  int Hkv, D, poolHeadDim, numFlatPages, maxPagesPerSeq, Hi, rot, ratio, budget, topK;
-  int pagesPerChunk, chunksMax, slotsPerSeq, countersPerSeq;
+  int Hi, Hkv, D, poolHeadDim, numFlatPages, maxPagesPerSeq, rot, ratio;
   float eps;
   RopeFreqs rf;
 };
 
-__device__ __forceinline__ size_t pool_row(int page, int tok_in_page, int Hkv, int poolHeadDim) {
-  return (static_cast<size_t>(page) * kTokensPerPage + tok_in_page) * Hkv * poolHeadDim;  // head 0
-}
-
-// Writes the selected (ascending-id) elements either as the candidates of a
-// tree slot or, at the root, as the sequence's expanded index list.
-template <int VPT>
-__device__ __forceinline__ void emit(const DecIdxArgs& a, int b, const uint32_t (&key)[VPT],
-                                     const int (&id)[VPT], const bool (&sel)[VPT], bool root, int slot,
-                                     int n_c, int t, int* scan) {
-  int ns = 0;
-#pragma unroll
-  for (int v = 0; v < VPT; ++v) ns += sel[v] ? 1 : 0;
-  int tot;
-  int pos = cta_exclusive_scan<kThreads>(ns, scan, tot);
-  if (!root) {
-    const size_t base = (static_cast<size_t>(b) * a.slotsPerSeq + slot) * a.budget;
-#pragma unroll
-    for (int v = 0; v < VPT; ++v)
-      if (sel[v]) {
-        a.candKey[base + pos] = key[v];
-        a.candId[base + pos] = id[v];
-        ++pos;
-      }
-    if (threadIdx.x == 0) a.candCnt[static_cast<size_t>(b) * a.slotsPerSeq + slot] = tot;
-    return;
-  }
-  int32_t* out = a.indices + static_cast<size_t>(b) * a.topK;
-#pragma unroll
-  for (int v = 0; v < VPT; ++v)
-    if (sel[v]) {
-      for (int j = 0; j < a.ratio; ++j) out[pos * a.ratio + j] = id[v] * a.ratio + j;
-      ++pos;
-    }
-  const int head = tot * a.ratio;
-  for (int i = head + threadIdx.x; i < a.topK; i += kThreads) {
-    const int j = n_c * a.ratio + (i - head);
-    out[i] = j <= t ? j : -1;
-  }
-}
-
-__host__ __device__ __forceinline__ int align_up(int x, int a) { return (x + a - 1) / a * a; }
-
-// Shared-memory carve-up of the decode indexer (byte offsets), used by host and device.
-struct DecSmem {
-  int bars, q, sc, m, y, knew, red, total;
-};
-__host__ __device__ __forceinline__ DecSmem dec_smem_layout(int di, int ratio, int pagesPerChunk) {
-  const int bpp = kTokensPerPage / ratio;
-  DecSmem l;
-  int off = kStages * bpp * di * 2;  // the TMA ring starts at offset 0
-  l.bars = off = align_up(off, 16);
-  off += kStages * 8;
-  l.q = off = align_up(off, 16);
-  off += 8 * di * 4;
-  l.sc = off = align_up(off, 16);
-  off += pagesPerChunk * bpp * 4;
-  l.m = off = align_up(off, 16);
-  off += di * 8;
-  l.y = off;
-  off += di * 8;
-  l.knew = off = align_up(off, 16);
-  off += di * 2;
-  l.red = off = align_up(off, 16);
-  off += 32 * 4;
-  l.total = off;
-  return l;
-}
-
 template <int DI>
-__global__ void __launch_bounds__(kThreads) decode_indexer_kernel(const DecIdxArgs a,
-                                                                  const __grid_constant__ CUtensorMap kmap) {
-  constexpr int LPB = DI / 8;    // lanes per block key (8 dims each)
-  constexpr int BPW = 32 / LPB;  // block keys per warp pass
-  extern __shared__ __align__(1024) uint8_t smem[];
-  const int bpp = kTokensPerPage / a.ratio;       // block keys per page
-  const int stage_bytes = bpp * DI * 2;
-  const DecSmem lay = dec_smem_layout(DI, a.ratio, a.pagesPerChunk);
-  uint8_t* ring = smem;                                            // [kStages][bpp][DI] fp16
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bars);
-  float* q_s = reinterpret_cast<float*>(smem + lay.q);             // [8][DI]
-  float* sc_s = reinterpret_cast<float*>(smem + lay.sc);           // [pagesPerChunk * bpp]
-  double* m_s = reinterpret_cast<double*>(smem + lay.m);           // [DI] f64 scratch
-  double* y_s = reinterpret_cast<double*>(smem + lay.y);           // [DI]
-  __half* knew_s = reinterpret_cast<__half*>(smem + lay.knew);     // [DI]
-  int* red = reinterpret_cast<int*>(smem + lay.red);               // 16 + 8 + 8 ints
-  int* scan = red + 16;
-  int* misc = scan + 8;
-
+__global__ void __launch_bounds__(256) decode_prep_kernel(const PrepArgs a) {
+  constexpr int PER = DI / 32;
+  __shared__ float y_s[8][DI];
+  __shared__ double m_s[DI];
+  __shared__ double y2_s[DI];
+  __shared__ double part_s[8];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int c = blockIdx.x, b = blockIdx.y;
+  const int b = blockIdx.x;
   const int L = max(0, min(a.ctx[b], a.maxPagesPerSeq * kTokensPerPage));
-  if (L == 0) {  // no token: empty list, no state change
-    if (c == 0)
-      for (int i = tid; i < a.topK; i += kThreads) a.indices[static_cast<size_t>(b) * a.topK + i] = -1;
-    return;
-  }
+  if (L == 0) return;
   const int t = L - 1;
   const int n_c = L / a.ratio;
   const bool completes = (L % a.ratio) == 0;
-  const int npg = (n_c + bpp - 1) / bpp;  // pages holding complete blocks
-  const int nch = max(1, (npg + a.pagesPerChunk - 1) / a.pagesPerChunk);
-  if (c >= nch) return;
-  const int p0 = c * a.pagesPerChunk, p1 = min(p0 + a.pagesPerChunk, npg);
-  const int npages = max(0, p1 - p0);
-  const int g0 = p0 * bpp;
-  const int nloc = max(0, min(p1 * bpp, n_c) - g0);
   const int32_t* ptK = a.pageTable + static_cast<size_t>(b) * 2 * a.maxPagesPerSeq;
   const int32_t* ptV = ptK + a.maxPagesPerSeq;
 
-  // ---- start the key stream early
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
-    fence_barrier_init();
-  }
-  __syncthreads();
-  if (tid == 0) {
-    for (int s = 0; s < kStages && s < npages; ++s) {
-      int vp = __ldg(ptV + p0 + s);
-      if (static_cast<unsigned>(vp) >= static_cast<unsigned>(a.numFlatPages)) {
-        atomicOr(a.status, kErrBadPage);
-        vp = 0;
-      }
-      mbar_arrive_expect_tx(&bars[s], stage_bytes);
-      tma_load_3d(ring + s * stage_bytes, &kmap, 0, 0, vp, &bars[s]);
-    }
-  }
-
-  // ---- B1: index-query prep at pos t (warp h -> head h)
+  // index-query prep: warp h -> head h (heads >= Hi are zero)
   {
-    constexpr int PER = DI / 32;
     const int h = warp;
+    float* qo = a.q + (static_cast<size_t>(b) * 8 + h) * 128;
     if (h < a.Hi) {
       const __half* x = a.idxQ + (static_cast<size_t>(b) * a.Hi + h) * DI;
       float y[PER];
@@ -203,343 +132,605 @@ __global__ void __launch_bounds__(kThreads) decode_indexer_kernel(const DecIdxAr
       for (int p = 0; p < PER; ++p) {
         const int i = lane + 32 * p;
         y[p] = y[p] * inv * (1.0f + a.wq[i]);
-        q_s[h * DI + i] = y[p];
+        y_s[h][i] = y[p];
       }
       __syncwarp();
       const int half = a.rot >> 1;
-      float v[PER];
 #pragma unroll
       for (int p = 0; p < PER; ++p) {
         const int i = lane + 32 * p;
-        v[p] = y[p];
+        float v = y[p];
         if (i < half) {
           float cs, sn;
           rope_cos_sin_f32(static_cast<double>(t), a.rf.inv_freq[i], cs, sn);
-          v[p] = y[p] * cs - q_s[h * DI + i + half] * sn;
+          v = y[p] * cs - y_s[h][i + half] * sn;
         } else if (i < a.rot) {
           const int k = i - half;
           float cs, sn;
           rope_cos_sin_f32(static_cast<double>(t), a.rf.inv_freq[k], cs, sn);
-          v[p] = y[p] * cs + q_s[h * DI + k] * sn;
+          v = y[p] * cs + y_s[h][k] * sn;
         }
+        qo[i] = v;
       }
-      __syncwarp();
-#pragma unroll
-      for (int p = 0; p < PER; ++p) q_s[h * DI + lane + 32 * p] = v[p];
     } else {
 #pragma unroll
-      for (int p = 0; p < PER; ++p) q_s[h * DI + lane + 32 * p] = 0.f;
+      for (int p = 0; p < PER; ++p) qo[lane + 32 * p] = 0.f;
     }
   }
 
-  // ---- B1: predicated tail write / compress
-  int g_new = -1;
+  // state update
   if (!completes) {
-    if (c == 0 && tid < DI) {
+    if (tid < DI) {
       const int kp = __ldg(ptK + (t >> 7));
       if (static_cast<unsigned>(kp) < static_cast<unsigned>(a.numFlatPages))
         a.pool[pool_row(kp, t & 127, a.Hkv, a.poolHeadDim) + a.D + tid] = a.idxK[static_cast<size_t>(b) * DI + tid];
       else if (tid == 0)
         atomicOr(a.status, kErrBadPage);
     }
-  } else {
-    const int gn = n_c - 1;
-    const int first = gn * a.ratio;  // block's first token; all r tokens share its page
-    if ((first >> 7) / a.pagesPerChunk == c) {
-      g_new = gn;
-      if (warp == 0) {
-        const int kp = __ldg(ptK + (first >> 7));
-        const int vp = __ldg(ptV + (first >> 7));
-        const bool okp = static_cast<unsigned>(kp) < static_cast<unsigned>(a.numFlatPages) &&
-                         static_cast<unsigned>(vp) < static_cast<unsigned>(a.numFlatPages);
-        if (!okp && lane == 0) atomicOr(a.status, kErrBadPage);
-        for (int i = lane; i < DI; i += 32) {
-          double acc = 0.0;
-          for (int j = 0; j < a.ratio; ++j) {
-            const int tok = first + j;
-            const __half hv = (tok == t || !okp)
-                                  ? a.idxK[static_cast<size_t>(b) * DI + i]
-                                  : a.pool[pool_row(kp, tok & 127, a.Hkv, a.poolHeadDim) + a.D + i];
-            acc = __dadd_rn(acc, static_cast<double>(__half2float(hv)));
-          }
-          m_s[i] = __ddiv_rn(acc, static_cast<double>(a.ratio));
-        }
-        __syncwarp();
-        double inv = 0.0;
-        if (lane == 0) {
-          double ss = 0.0;
-          for (int i = 0; i < DI; ++i) ss = __dadd_rn(ss, __dmul_rn(m_s[i], m_s[i]));
-          inv = __ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(__ddiv_rn(ss, static_cast<double>(DI)), static_cast<double>(a.eps))));
-        }
-        inv = __shfl_sync(kFull, inv, 0);
-        for (int i = lane; i < DI; i += 32)
-          y_s[i] = __dmul_rn(__dmul_rn(m_s[i], inv), __dadd_rn(1.0, static_cast<double>(a.wk[i])));
-        __syncwarp();
-        const int half = a.rot >> 1;
-        const double pos = static_cast<double>(first);
-        for (int i = lane; i < DI; i += 32) {
-          double r = y_s[i];
-          if (i < half) {
-            double s, cc;
-            sincos(__dmul_rn(pos, a.rf.inv_freq[i]), &s, &cc);
-            r = __dsub_rn(__dmul_rn(y_s[i], cc), __dmul_rn(y_s[i + half], s));
-          } else if (i < a.rot) {
-            const int k = i - half;
-            double s, cc;
-            sincos(__dmul_rn(pos, a.rf.inv_freq[k]), &s, &cc);
-            r = __dadd_rn(__dmul_rn(y_s[i], cc), __dmul_rn(y_s[k], s));
-          }
-          const __half hk = __double2half(r);
-          knew_s[i] = hk;
-          if (okp) a.pool[pool_row(vp, first & 127, a.Hkv, a.poolHeadDim) + a.D + i] = hk;
-        }
+    return;
+  }
+  const int first = (n_c - 1) * a.ratio;  // all r tokens of the block share this page
+  const int kp = __ldg(ptK + (first >> 7)), vp = __ldg(ptV + (first >> 7));
+  const bool okp = static_cast<unsigned>(kp) < static_cast<unsigned>(a.numFlatPages) &&
+                   static_cast<unsigned>(vp) < static_cast<unsigned>(a.numFlatPages);
+  if (!okp) {
+    if (tid == 0) atomicOr(a.status, kErrBadPage);
+    return;
+  }
+  double sq = 0.0;
+  if (tid < DI) {
+    double acc = 0.0;
+    for (int j = 0; j < a.ratio; ++j) {
+      const int tok = first + j;
+      const __half hv = tok == t ? a.idxK[static_cast<size_t>(b) * DI + tid]
+                                 : a.pool[pool_row(kp, tok & 127, a.Hkv, a.poolHeadDim) + a.D + tid];
+      acc = __dadd_rn(acc, static_cast<double>(__half2float(hv)));
+    }
+    const double m = __ddiv_rn(acc, static_cast<double>(a.ratio));
+    m_s[tid] = m;
+    sq = __dmul_rn(m, m);
+  }
+  if (warp < DI / 32) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sq = __dadd_rn(sq, __shfl_xor_sync(kFull, sq, o));
+    if (lane == 0) part_s[warp] = sq;
+  }
+  __syncthreads();
+  if (tid < DI) {
+    double ss = 0.0;
+    for (int w = 0; w < DI / 32; ++w) ss = __dadd_rn(ss, part_s[w]);
+    const double inv = __ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(__ddiv_rn(ss, static_cast<double>(DI)),
+                                                           static_cast<double>(a.eps))));
+    y2_s[tid] = __dmul_rn(__dmul_rn(m_s[tid], inv), __dadd_rn(1.0, static_cast<double>(a.wk[tid])));
+  }
+  __syncthreads();
+  if (tid < DI) {
+    const int i = tid, half = a.rot >> 1;
+    const double pos = static_cast<double>(first);
+    double r = y2_s[i];
+    if (i < half) {
+      double s, c;
+      sincos(__dmul_rn(pos, a.rf.inv_freq[i]), &s, &c);
+      r = __dsub_rn(__dmul_rn(y2_s[i], c), __dmul_rn(y2_s[i + half], s));
+    } else if (i < a.rot) {
+      const int k = i - half;
+      double s, c;
+      sincos(__dmul_rn(pos, a.rf.inv_freq[k]), &s, &c);
+      r = __dadd_rn(__dmul_rn(y2_s[i], c), __dmul_rn(y2_s[k], s));
+    }
+    a.pool[pool_row(vp, first & 127, a.Hkv, a.poolHeadDim) + a.D + i] = __double2half(r);
+  }
+}
+
+// ------------------------------------------------------------------ B2
+struct ScoreArgs {
+  const int32_t* ctx;
+  const int32_t* pageTable;
+  const float* q;
+  float* scores;
+  int32_t* hist;
+  int32_t* status;
+  int B, maxPagesPerSeq, numFlatPages, ratio, nbmax;
+};
+
+__host__ __device__ __forceinline__ int score_smem_bytes(int di, int ratio, int B) {
+  const int stage = (kTokensPerPage / ratio) * di * 2;
+  return kStages * stage + 2 * kStages * 8 + ((B + 1 + 3) / 4) * 16 + kConsumerWarps * 128 * 4;
+}
+
+template <int DI>
+__global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const ScoreArgs a,
+                                                                        const __grid_constant__ CUtensorMap kmap) {
+  constexpr int LPB = DI / 8;          // lanes per block key (8 dims each)
+  constexpr int BPW = 32 / LPB;        // block keys per warp pass
+  constexpr int LOGL = LPB == 16 ? 4 : 3;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int bpp = kTokensPerPage / a.ratio;
+  const int stage_bytes = bpp * DI * 2;
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * stage_bytes);
+  uint64_t* empty = full + kStages;
+  int* pref = reinterpret_cast<int*>(empty + kStages);  // pages of complete blocks, exclusive prefix [B+1]
+  float* scr = reinterpret_cast<float*>(pref + (a.B + 1 + 3) / 4 * 4);  // [kConsumerWarps][128]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int MAXL = a.maxPagesPerSeq * kTokensPerPage;
+
+  for (int b = tid; b < a.B; b += blockDim.x) {
+    const int L = max(0, min(a.ctx[b], MAXL));
+    pref[b + 1] = (L / a.ratio + bpp - 1) / bpp;
+  }
+  if (tid == 0) {
+    pref[0] = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < a.B; base += 32) {
+      const int i = base + lane;
+      int v = i < a.B ? pref[i + 1] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, v, o);
+        if (lane >= o) v += y;
       }
+      if (i < a.B) pref[i + 1] = v + carry;
+      carry += __shfl_sync(kFull, v, 31);
     }
   }
   __syncthreads();
+  const long long W = pref[a.B];
+  const long long lo = W * blockIdx.x / gridDim.x, hi = W * (blockIdx.x + 1) / gridDim.x;
+  if (lo >= hi) return;
 
-  // ---- B2: stream and score the chunk's block keys
-  const int sub = lane % LPB;
-  float qr[8][8];
-#pragma unroll
-  for (int h = 0; h < 8; ++h) {
-    const float4 x0 = *reinterpret_cast<const float4*>(q_s + h * DI + sub * 8);
-    const float4 x1 = *reinterpret_cast<const float4*>(q_s + h * DI + sub * 8 + 4);
-    qr[h][0] = x0.x; qr[h][1] = x0.y; qr[h][2] = x0.z; qr[h][3] = x0.w;
-    qr[h][4] = x1.x; qr[h][5] = x1.y; qr[h][6] = x1.z; qr[h][7] = x1.w;
-  }
-  bool alive = true;
-  int failed_at = npages;
-  for (int pi = 0; pi < npages; ++pi) {
-    const int s = pi % kStages;
-    const bool ok = mbar_wait_bounded(&bars[s], (pi / kStages) & 1, kWaitLimitNs);
-    if (!__syncthreads_and(ok)) {
-      alive = false;
-      failed_at = pi;
-      break;
-    }
-    const __half* tile = reinterpret_cast<const __half*>(ring + s * stage_bytes);
-    for (int blk0 = warp * BPW; blk0 < bpp; blk0 += 8 * BPW) {
-      const int blk = blk0 + lane / LPB;
-      const int g = (p0 + pi) * bpp + blk;
-      const bool valid = blk < bpp && g < n_c;
-      const __half* src = g == g_new ? knew_s : tile + (valid ? blk : 0) * DI;
-      const uint4 raw = *reinterpret_cast<const uint4*>(src + sub * 8);
-      const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
-      float kv[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __half22float2(h2[i]);
-        kv[2 * i] = f.x;
-        kv[2 * i + 1] = f.y;
-      }
-      float d[8];
-#pragma unroll
-      for (int h = 0; h < 8; ++h) {
-        float acc = qr[h][0] * kv[0];
-#pragma unroll
-        for (int i = 1; i < 8; ++i) acc = fmaf(qr[h][i], kv[i], acc);
-        d[h] = acc;
-      }
-      // Transposing reduction over the LPB lanes of this key: after three
-      // halvings each lane holds one head's partial; LPB = 16 needs one more
-      // exchange to complete the sum.
-      int n = 8;
-#pragma unroll
-      for (int o = LPB / 2; o >= LPB / 8; o >>= 1) {
-        const bool upper = (lane & o) != 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (i < n / 2) {
-            const float send = upper ? d[i] : d[i + n / 2];
-            const float keep = upper ? d[i + n / 2] : d[i];
-            d[i] = keep + __shfl_xor_sync(kFull, send, o);
-          }
+  if (warp == kConsumerWarps) {  // ---- producer
+    if (lane == 0) {
+      int b = 0;
+      for (long long i = lo; i < hi; ++i) {
+        while (i >= pref[b + 1]) ++b;
+        const int p = static_cast<int>(i - pref[b]);
+        int vp = __ldg(a.pageTable + (static_cast<size_t>(b) * 2 + 1) * a.maxPagesPerSeq + p);
+        if (static_cast<unsigned>(vp) >= static_cast<unsigned>(a.numFlatPages)) {
+          atomicOr(a.status, kErrBadPage);
+          vp = 0;
         }
-        n >>= 1;
+        const int j = static_cast<int>(i - lo), s = j % kStages, n = j / kStages;
+        if (!mbar_wait_bounded(&empty[s], (n & 1) ^ 1, kWaitLimitNs)) {
+          atomicOr(a.status, kErrWaitTimeout);
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        tma_load_3d(ring + s * stage_bytes, &kmap, 0, 0, vp, &full[s]);
       }
-      float dot = d[0];
-      if (LPB == 16) dot += __shfl_xor_sync(kFull, dot, 1);
-      float sc = dot > 0.f ? dot : 0.f;
-#pragma unroll
-      for (int o = LPB / 8; o < LPB; o <<= 1) sc += __shfl_xor_sync(kFull, sc, o);
-      if (valid && sub == 0) sc_s[pi * bpp + blk] = sc;
-    }
-    __syncthreads();  // stage s fully read
-    if (tid == 0 && pi + kStages < npages) {
-      int vp = __ldg(ptV + p0 + pi + kStages);
-      if (static_cast<unsigned>(vp) >= static_cast<unsigned>(a.numFlatPages)) {
-        atomicOr(a.status, kErrBadPage);
-        vp = 0;
-      }
-      fence_proxy_async();
-      mbar_arrive_expect_tx(&bars[s], stage_bytes);
-      tma_load_3d(ring + s * stage_bytes, &kmap, 0, 0, vp, &bars[s]);
-    }
-  }
-  if (!alive) {
-    // Pages failed_at .. failed_at + kStages - 1 may still be in flight: let
-    // each land (bounded) before the CTA exits.
-    if (tid == 0) {
-      atomicOr(a.status, kErrWaitTimeout);
-      const int issued = min(npages, failed_at + kStages);
-      for (int pi = failed_at; pi < issued; ++pi)
-        mbar_wait_bounded(&bars[pi % kStages], (pi / kStages) & 1, kWaitLimitNs);
     }
     return;
   }
 
-  // ---- B3: chunk top-k, then the merge tree
-  uint32_t key[kVPT];
-  int id[kVPT];
-  bool sel[kVPT];
-  {
-    const int base = tid * kVPT;
-    const int nv = max(0, min(kVPT, nloc - base));
+  // ---- consumers: warp w takes pages lo + w, lo + w + kConsumerWarps, ...
+  const int sub = lane % LPB;
+  const int m = (sub >> (LOGL - 3)) & 7;  // this lane's head order is h ^ m (see the reduction)
+  uint64_t q2[8][4];
+  int cached_b = -1, n_c = 0;
+  int b = 0;
+  float* myscr = scr + warp * 128;
+  for (long long i = lo + warp; i < hi; i += kConsumerWarps) {
+    while (i >= pref[b + 1]) ++b;
+    const int p = static_cast<int>(i - pref[b]);
+    const int j = static_cast<int>(i - lo), s = j % kStages, n = j / kStages;
+    if (b != cached_b) {
+      const float* qb = a.q + static_cast<size_t>(b) * 8 * 128;
 #pragma unroll
-    for (int v = 0; v < kVPT; ++v) {
-      key[v] = v < nv ? __float_as_uint(sc_s[base + v]) : 0u;
-      id[v] = g0 + base + v;
-      sel[v] = v < nv;
+      for (int h = 0; h < 8; ++h) {
+        const float4 x0 = *reinterpret_cast<const float4*>(qb + (h ^ m) * 128 + sub * 8);
+        const float4 x1 = *reinterpret_cast<const float4*>(qb + (h ^ m) * 128 + sub * 8 + 4);
+        q2[h][0] = pack_f2(x0.x, x0.y);
+        q2[h][1] = pack_f2(x0.z, x0.w);
+        q2[h][2] = pack_f2(x1.x, x1.y);
+        q2[h][3] = pack_f2(x1.z, x1.w);
+      }
+      n_c = max(0, min(a.ctx[b], MAXL)) / a.ratio;
+      cached_b = b;
     }
-    if (nloc > a.budget) cta_topk<kThreads, kVPT>(key, nv, a.budget, sel, red, scan);
-  }
-  int cnt = nch, lvl_off = 0, lvl_n = a.chunksMax, node = c;
-  bool root = cnt == 1;
-  emit<kVPT>(a, b, key, id, sel, root, lvl_off + node, n_c, t, scan);
-  while (!root) {
-    const int parent = node / kFanIn;
-    const int nsib = min(kFanIn, cnt - parent * kFanIn);
-    const int next_off = lvl_off + lvl_n;
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-      int32_t* ctr = a.counters + static_cast<size_t>(b) * a.countersPerSeq + (next_off - a.chunksMax) + parent;
-      const bool last = atomicAdd(ctr, 1) == nsib - 1;
-      if (last) *ctr = 0;  // re-armed for the next call
-      misc[0] = last;
+    if (!mbar_wait_bounded(&full[s], n & 1, kWaitLimitNs)) {
+      if (lane == 0) atomicOr(a.status, kErrWaitTimeout);
+      break;
     }
-    __syncthreads();
-    if (!misc[0]) return;
-    __threadfence();
-    // Children's candidates, concatenated in child order (ascending ids).
-    const size_t slot0 = static_cast<size_t>(b) * a.slotsPerSeq + lvl_off + parent * kFanIn;
-    int offs[kFanIn + 1];
-    offs[0] = 0;
+    const __half* tile = reinterpret_cast<const __half*>(ring + s * stage_bytes);
+    for (int pass = 0; pass < bpp / BPW; ++pass) {
+      const int blk = pass * BPW + lane / LPB;
+      const uint4 raw = *reinterpret_cast<const uint4*>(tile + blk * DI + sub * 8);
+      const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+      uint64_t kp[4];
 #pragma unroll
-    for (int k = 0; k < kFanIn; ++k) offs[k + 1] = offs[k] + (k < nsib ? __ldcg(a.candCnt + slot0 + k) : 0);
-    const int total = offs[kFanIn];
-    const int base = tid * kVPT;
-    const int nv = max(0, min(kVPT, total - base));
+      for (int jj = 0; jj < 4; ++jj) {
+        const float2 f = __half22float2(h2[jj]);
+        kp[jj] = pack_f2(f.x, f.y);
+      }
+      float d[8];
 #pragma unroll
-    for (int v = 0; v < kVPT; ++v) {
-      const int e = base + v;
-      key[v] = 0u;
-      id[v] = 0;
-      sel[v] = v < nv;
-      if (v < nv) {
-        int k = 0;
-        while (e >= offs[k + 1]) ++k;
-        const size_t at = (slot0 + k) * a.budget + (e - offs[k]);
-        key[v] = __ldcg(a.candKey + at);
-        id[v] = __ldcg(a.candId + at);
+      for (int h = 0; h < 8; ++h) {
+        uint64_t acc = ffma2(q2[h][0], kp[0], 0ull);
+        acc = ffma2(q2[h][1], kp[1], acc);
+        acc = ffma2(q2[h][2], kp[2], acc);
+        acc = ffma2(q2[h][3], kp[3], acc);
+        d[h] = lo_f2(acc) + hi_f2(acc);
+      }
+      // Transposing reduction over the LPB lanes of this key.  Lane head order
+      // h ^ m makes the partner's upper half hold the same heads as this
+      // lane's lower half at every step, so each step is add(shuffle).
+#pragma unroll
+      for (int i2 = 0; i2 < 4; ++i2) d[i2] += __shfl_xor_sync(kFull, d[i2 + 4], LPB / 2);
+#pragma unroll
+      for (int i2 = 0; i2 < 2; ++i2) d[i2] += __shfl_xor_sync(kFull, d[i2 + 2], LPB / 4);
+      d[0] += __shfl_xor_sync(kFull, d[1], LPB / 8);
+      if (LPB == 16) d[0] += __shfl_xor_sync(kFull, d[0], 1);
+      float sc = d[0] > 0.f ? d[0] : 0.f;  // relu of head m's dot
+      sc += __shfl_xor_sync(kFull, sc, LPB / 8);
+      sc += __shfl_xor_sync(kFull, sc, LPB / 4);
+      sc += __shfl_xor_sync(kFull, sc, LPB / 2);
+      if (sub == 0) myscr[blk] = sc;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);  // the stage may be refilled
+    float* sc_row = a.scores + static_cast<size_t>(b) * a.nbmax;
+    int32_t* hrow = a.hist + static_cast<size_t>(b) * kNumBins;
+    for (int r0 = 0; r0 < bpp; r0 += 32) {
+      const int jb = r0 + lane;
+      const int g = p * bpp + jb;
+      const bool valid = jb < bpp && g < n_c;
+      const float sc = valid ? myscr[jb] : 0.f;
+      const int bin = static_cast<int>(__float_as_uint(sc) >> kBinShift);
+      if (valid) sc_row[g] = sc;
+      const unsigned act = __ballot_sync(kFull, valid);
+      if (valid) {
+        const unsigned peers = __match_any_sync(act, bin);
+        if (lane == __ffs(peers) - 1) atomicAdd(hrow + bin, __popc(peers));
       }
     }
-    if (total > a.budget) cta_topk<kThreads, kVPT>(key, nv, a.budget, sel, red, scan);
-    node = parent;
-    cnt = (cnt + kFanIn - 1) / kFanIn;
-    lvl_off = next_off;
-    lvl_n = (lvl_n + kFanIn - 1) / kFanIn;
-    root = cnt == 1;
-    emit<kVPT>(a, b, key, id, sel, root, lvl_off + node, n_c, t, scan);
+    __syncwarp();
   }
 }
 
-size_t decode_smem_bytes(int di, int ratio, int pagesPerChunk) {
-  return static_cast<size_t>(dec_smem_layout(di, ratio, pagesPerChunk).total);
+// ------------------------------------------------------------------ B3
+struct SelectArgs {
+  const int32_t* ctx;
+  const float* scores;
+  int32_t* hist;
+  uint32_t* bitmap;
+  uint32_t* tieKey;
+  int32_t* tieId;
+  int32_t* tieCnt;
+  int32_t* ticket;
+  int32_t* indices;
+  int maxPagesPerSeq, ratio, budget, topK, nbmax, words;
+};
+
+__global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const SelectArgs a) {
+  __shared__ int red[2 * kSelThreads / 32];
+  __shared__ int scan[kSelThreads / 32];
+  __shared__ int info[4];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int s = blockIdx.x, b = blockIdx.y;
+  const int L = max(0, min(a.ctx[b], a.maxPagesPerSeq * kTokensPerPage));
+  const int t = L - 1;
+  const int n_c = L / a.ratio;
+  int32_t* out = a.indices + static_cast<size_t>(b) * a.topK;
+  int32_t* hrow = a.hist + static_cast<size_t>(b) * kNumBins;
+  if (L == 0) {
+    if (s == 0)
+      for (int i = tid; i < a.topK; i += kSelThreads) out[i] = -1;
+    return;
+  }
+  if (n_c <= a.budget) {  // every block kept: the list is 0..t
+    if (s == 0) {
+      for (int i = tid; i < a.topK; i += kSelThreads) out[i] = i <= t ? i : -1;
+      for (int i = tid; i < kNumBins; i += kSelThreads) hrow[i] = 0;
+    }
+    return;
+  }
+  const int nsplit = (n_c + kSliceBlocks - 1) / kSliceBlocks;
+  if (s >= nsplit) return;
+
+  // ---- the bin holding the budget-th largest score
+  constexpr int BPT = kNumBins / kSelThreads;  // 16 bins per thread
+  int h[BPT];
+  int own = 0;
+#pragma unroll
+  for (int k = 0; k < BPT; ++k) {
+    h[k] = __ldcg(hrow + tid * BPT + k);
+    own += h[k];
+  }
+  if (tid == 0) {
+    info[0] = 0;  // threshold bin
+    info[1] = 0;  // blocks in higher bins
+  }
+  int total;
+  const int excl = cta_exclusive_scan<kSelThreads>(own, scan, total);
+  int running = total - excl - own;  // blocks in bins of higher threads
+#pragma unroll
+  for (int k = BPT - 1; k >= 0; --k) {
+    if (running < a.budget && running + h[k] >= a.budget) {
+      info[0] = tid * BPT + k;
+      info[1] = running;
+    }
+    running += h[k];
+  }
+  __syncthreads();
+  const int T = info[0], c_above = info[1];
+
+  // ---- mark blocks above the bin, collect the blocks inside it
+  const float* srow = a.scores + static_cast<size_t>(b) * a.nbmax;
+  uint32_t* brow = a.bitmap + static_cast<size_t>(b) * a.words;
+  const int g1 = min((s + 1) * kSliceBlocks, n_c);
+  for (int base = s * kSliceBlocks + warp * 32; base < g1; base += kSelThreads) {
+    const int g = base + lane;
+    const bool valid = g < g1;
+    const uint32_t key = valid ? __float_as_uint(__ldcg(srow + g)) : 0u;
+    const int bin = static_cast<int>(key >> kBinShift);
+    const unsigned sure = __ballot_sync(kFull, valid && bin > T);
+    if (lane == 0) brow[base >> 5] = sure;
+    const bool tie = valid && bin == T;
+    const unsigned tm = __ballot_sync(kFull, tie);
+    if (tm) {
+      int pos0 = 0;
+      if (lane == 0) pos0 = atomicAdd(a.tieCnt + b, __popc(tm));
+      pos0 = __shfl_sync(kFull, pos0, 0);
+      if (tie) {
+        const int at = pos0 + __popc(tm & ((1u << lane) - 1u));
+        a.tieKey[static_cast<size_t>(b) * a.nbmax + at] = key;
+        a.tieId[static_cast<size_t>(b) * a.nbmax + at] = g;
+      }
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) info[2] = atomicAdd(a.ticket + b, 1) == nsplit - 1;
+  __syncthreads();
+  if (!info[2]) return;
+  __threadfence();
+
+  // ---- last CTA: exact top of the tie bin by (score desc, id asc)
+  const int need = a.budget - c_above;
+  const int nt = __ldcg(a.tieCnt + b);
+  const uint32_t* tk = a.tieKey + static_cast<size_t>(b) * a.nbmax;
+  const int32_t* ti = a.tieId + static_cast<size_t>(b) * a.nbmax;
+  if (nt <= need) {
+    for (int e = tid; e < nt; e += kSelThreads) {
+      const int id = __ldcg(ti + e);
+      atomicOr(brow + (id >> 5), 1u << (id & 31));
+    }
+  } else if (nt <= kTieVPT * kSelThreads) {
+    uint32_t key[kTieVPT];
+    int id[kTieVPT];
+    const int nv = max(0, min(kTieVPT, nt - tid * kTieVPT));
+#pragma unroll
+    for (int v = 0; v < kTieVPT; ++v) {
+      key[v] = v < nv ? __ldcg(tk + tid * kTieVPT + v) : 0u;
+      id[v] = v < nv ? __ldcg(ti + tid * kTieVPT + v) : 0;
+    }
+    int phase = 0;
+    // every tie key lies in bin T: count(>= lo) >= need > count(>= hi)
+    uint32_t lo = static_cast<uint32_t>(T) << kBinShift, hi = static_cast<uint32_t>(T + 1) << kBinShift;
+    int cnt_lo = nt, cnt_hi = 0;
+    while (hi - lo > 1u) {
+      const uint32_t mid = lo + ((hi - lo) >> 1);
+      int c = 0;
+#pragma unroll
+      for (int v = 0; v < kTieVPT; ++v) c += (v < nv && key[v] >= mid) ? 1 : 0;
+      const int tot = cta_sum<kSelThreads>(c, red, phase);
+      if (tot >= need) {
+        lo = mid;
+        cnt_lo = tot;
+      } else {
+        hi = mid;
+        cnt_hi = tot;
+      }
+    }
+    const uint32_t Tk = lo;
+    const int n_eq = need - cnt_hi;  // keys equal to Tk to keep, lowest ids first
+    int ilo = -1, ihi = a.nbmax;     // count(== Tk, id <= ilo) < n_eq <= count(== Tk, id <= ihi)
+    if (cnt_lo - cnt_hi == n_eq) ilo = ihi - 1;  // no exact tie at the cut: keep every key == Tk
+    while (ihi - ilo > 1) {
+      const int mid = ilo + ((ihi - ilo) >> 1);
+      int c = 0;
+#pragma unroll
+      for (int v = 0; v < kTieVPT; ++v) c += (v < nv && key[v] == Tk && id[v] <= mid) ? 1 : 0;
+      const int tot = cta_sum<kSelThreads>(c, red, phase);
+      if (tot >= n_eq)
+        ihi = mid;
+      else
+        ilo = mid;
+    }
+#pragma unroll
+    for (int v = 0; v < kTieVPT; ++v)
+      if (v < nv && (key[v] > Tk || (key[v] == Tk && id[v] <= ihi))) atomicOr(brow + (id[v] >> 5), 1u << (id[v] & 31));
+  } else {
+    // Degenerate case (very many scores in one bin, e.g. all zero): the same
+    // two bisections, counting straight from global memory.
+    int phase = 0;
+    uint32_t lo = static_cast<uint32_t>(T) << kBinShift, hi = static_cast<uint32_t>(T + 1) << kBinShift;
+    int cnt_lo = nt, cnt_hi = 0;
+    while (hi - lo > 1u) {
+      const uint32_t mid = lo + ((hi - lo) >> 1);
+      int c = 0;
+      for (int e = tid; e < nt; e += kSelThreads) c += __ldcg(tk + e) >= mid ? 1 : 0;
+      const int tot = cta_sum<kSelThreads>(c, red, phase);
+      if (tot >= need) {
+        lo = mid;
+        cnt_lo = tot;
+      } else {
+        hi = mid;
+        cnt_hi = tot;
+      }
+    }
+    const uint32_t Tk = lo;
+    const int n_eq = need - cnt_hi;
+    int ilo = -1, ihi = a.nbmax;
+    if (cnt_lo - cnt_hi == n_eq) ilo = ihi - 1;
+    while (ihi - ilo > 1) {
+      const int mid = ilo + ((ihi - ilo) >> 1);
+      int c = 0;
+      for (int e = tid; e < nt; e += kSelThreads) c += (__ldcg(tk + e) == Tk && __ldcg(ti + e) <= mid) ? 1 : 0;
+      const int tot = cta_sum<kSelThreads>(c, red, phase);
+      if (tot >= n_eq)
+        ihi = mid;
+      else
+        ilo = mid;
+    }
+    for (int e = tid; e < nt; e += kSelThreads) {
+      const uint32_t k = __ldcg(tk + e);
+      const int id = __ldcg(ti + e);
+      if (k > Tk || (k == Tk && id <= ihi)) atomicOr(brow + (id >> 5), 1u << (id & 31));
+    }
+  }
+  __threadfence();
+  __syncthreads();
+
+  // ---- expand the bitmap in ascending order, then the causal tail
+  const int nw = (n_c + 31) / 32;
+  const int wpt = (nw + kSelThreads - 1) / kSelThreads;
+  const int w0 = min(tid * wpt, nw), w1 = min(w0 + wpt, nw);
+  int cnt = 0;
+  for (int w = w0; w < w1; ++w) cnt += __popc(__ldcg(brow + w));
+  int tot;
+  int pos = cta_exclusive_scan<kSelThreads>(cnt, scan, tot);
+  for (int w = w0; w < w1; ++w) {
+    uint32_t bits = __ldcg(brow + w);
+    while (bits) {
+      const int id = w * 32 + __ffs(bits) - 1;
+      bits &= bits - 1;
+      for (int jj = 0; jj < a.ratio; ++jj)
+        if (pos * a.ratio + jj < a.topK) out[pos * a.ratio + jj] = id * a.ratio + jj;
+      ++pos;
+    }
+  }
+  const int head = tot * a.ratio;
+  for (int i = head + tid; i < a.topK; i += kSelThreads) {
+    const int j = n_c * a.ratio + (i - head);
+    out[i] = j <= t ? j : -1;
+  }
+  // re-arm for the next call
+  for (int i = tid; i < kNumBins; i += kSelThreads) hrow[i] = 0;
+  if (tid == 0) {
+    a.tieCnt[b] = 0;
+    a.ticket[b] = 0;
+  }
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
 }
 
 }  // namespace
 
-DecodePlan plan_indexer_decode(int B, int maxPagesPerSeq, int ratio) {
-  DecodePlan pl;
-  const int bpp = kTokensPerPage / ratio;
-  const long long total_pages = static_cast<long long>(B) * maxPagesPerSeq;
-  const int target_ctas = 640;  // ~4 resident CTAs on each of the 152 SMs
-  long long cp = (total_pages + target_ctas - 1) / target_ctas;
-  cp = cp < 1 ? 1 : cp;
-  const int cap = kMaxChunkBlocks / bpp;  // chunk scores must fit one selection pass
-  pl.pagesPerChunk = static_cast<int>(cp > cap ? cap : cp);
-  pl.chunksMax = (maxPagesPerSeq + pl.pagesPerChunk - 1) / pl.pagesPerChunk;
-  pl.levels = 0;
-  pl.slotsPerSeq = pl.chunksMax;
-  for (int n = pl.chunksMax; n > 1;) {
-    n = (n + kFanIn - 1) / kFanIn;
-    pl.slotsPerSeq += n;
-    ++pl.levels;
-  }
-  pl.countersPerSeq = pl.slotsPerSeq - pl.chunksMax;
-  return pl;
-}
-
 size_t indexer_decode_workspace_bytes(int B, int maxPagesPerSeq, int ratio, int budget) {
-  const DecodePlan pl = plan_indexer_decode(B, maxPagesPerSeq, ratio);
-  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  const size_t slots = static_cast<size_t>(B) * pl.slotsPerSeq;
-  return kStatusBytes + up(slots * budget * 4) * 2 + up(slots * 4) + up(static_cast<size_t>(B) * pl.countersPerSeq * 4);
+  (void)budget;
+  const int nbmax = maxPagesPerSeq * (kTokensPerPageHost / ratio);
+  return ws_layout(B, nbmax).total;
 }
 
 cudaError_t launch_indexer_decode(const QsaIndexerDecodeParams& p, const RopeFreqs& rf,
                                   const CUtensorMap& kbarMap) {
-  const DecodePlan pl = plan_indexer_decode(p.batchSize, p.maxPagesPerSeq, p.compressRatio);
-  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  const size_t slots = static_cast<size_t>(p.batchSize) * pl.slotsPerSeq;
+  const int B = p.batchSize;
+  const int bpp = kTokensPerPageHost / p.compressRatio;
+  const int nbmax = p.maxPagesPerSeq * bpp;
+  const WsLayout l = ws_layout(B, nbmax);
   uint8_t* ws = static_cast<uint8_t*>(p.workspace);
-  DecIdxArgs a;
-  a.status = reinterpret_cast<int32_t*>(ws);
-  a.candKey = reinterpret_cast<uint32_t*>(ws + kStatusBytes);
-  a.candId = reinterpret_cast<int32_t*>(ws + kStatusBytes + up(slots * p.budget * 4));
-  a.candCnt = reinterpret_cast<int32_t*>(ws + kStatusBytes + 2 * up(slots * p.budget * 4));
-  a.counters = reinterpret_cast<int32_t*>(ws + kStatusBytes + 2 * up(slots * p.budget * 4) + up(slots * 4));
-  a.idxQ = static_cast<const __half*>(p.idxQ);
-  a.idxK = static_cast<const __half*>(p.idxK);
-  a.wq = p.qNormW;
-  a.wk = p.kNormW;
-  a.pool = static_cast<__half*>(p.kvPool);
-  a.pageTable = p.pageTable;
-  a.ctx = p.contextLengths;
-  a.indices = p.indices;
-  a.Hkv = p.numKVHeads;
-  a.D = p.kvHeadDim;
-  a.poolHeadDim = p.poolHeadDim;
-  a.numFlatPages = p.numFlatPages;
-  a.maxPagesPerSeq = p.maxPagesPerSeq;
-  a.Hi = p.numHeads;
-  a.rot = p.rotDim;
-  a.ratio = p.compressRatio;
-  a.budget = p.budget;
-  a.topK = p.topK;
-  a.pagesPerChunk = pl.pagesPerChunk;
-  a.chunksMax = pl.chunksMax;
-  a.slotsPerSeq = pl.slotsPerSeq;
-  a.countersPerSeq = pl.countersPerSeq;
-  a.eps = p.rmsNormEps;
-  a.rf = rf;
-  const size_t smem = decode_smem_bytes(p.headDim, p.compressRatio, pl.pagesPerChunk);
-  if (smem > static_cast<size_t>(kMaxDynSmem)) return cudaErrorInvalidValue;
-  dim3 grid(pl.chunksMax, p.batchSize);
+  int32_t* status = reinterpret_cast<int32_t*>(ws);
+  float* q = reinterpret_cast<float*>(ws + l.q);
+  float* scores = reinterpret_cast<float*>(ws + l.scores);
+  int32_t* hist = reinterpret_cast<int32_t*>(ws + l.hist);
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(ws + l.bitmap);
+  int32_t* counters = reinterpret_cast<int32_t*>(ws + l.counters);
   cudaStream_t st = static_cast<cudaStream_t>(p.stream);
+
+  PrepArgs pa;
+  pa.idxQ = static_cast<const __half*>(p.idxQ);
+  pa.idxK = static_cast<const __half*>(p.idxK);
+  pa.wq = p.qNormW;
+  pa.wk = p.kNormW;
+  pa.pool = static_cast<__half*>(p.kvPool);
+  pa.pageTable = p.pageTable;
+  pa.ctx = p.contextLengths;
+  pa.q = q;
+  pa.status = status;
+  pa.Hi = p.numHeads;
+  pa.Hkv = p.numKVHeads;
+  pa.D = p.kvHeadDim;
+  pa.poolHeadDim = p.poolHeadDim;
+  pa.numFlatPages = p.numFlatPages;
+  pa.maxPagesPerSeq = p.maxPagesPerSeq;
+  pa.rot = p.rotDim;
+  pa.ratio = p.compressRatio;
+  pa.eps = p.rmsNormEps;
+  pa.rf = rf;
+  if (p.headDim == 64)
+    decode_prep_kernel<64><<<B, 256, 0, st>>>(pa);
+  else
+    decode_prep_kernel<128><<<B, 256, 0, st>>>(pa);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  ScoreArgs sa;
+  sa.ctx = p.contextLengths;
+  sa.pageTable = p.pageTable;
+  sa.q = q;
+  sa.scores = scores;
+  sa.hist = hist;
+  sa.status = status;
+  sa.B = B;
+  sa.maxPagesPerSeq = p.maxPagesPerSeq;
+  sa.numFlatPages = p.numFlatPages;
+  sa.ratio = p.compressRatio;
+  sa.nbmax = nbmax;
+  const int smem = score_smem_bytes(p.headDim, p.compressRatio, B);
+  if (smem > kMaxDynSmem) return cudaErrorInvalidValue;
+  const long long maxPages = static_cast<long long>(B) * p.maxPagesPerSeq;
+  const int grid = static_cast<int>(maxPages < sm_count() ? maxPages : sm_count());
   if (p.headDim == 64) {
     static const cudaError_t attr = cudaFuncSetAttribute(
-        decode_indexer_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+        decode_score_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
     if (attr != cudaSuccess) return attr;
-    decode_indexer_kernel<64><<<grid, kThreads, smem, st>>>(a, kbarMap);
+    decode_score_kernel<64><<<grid, kScoreThreads, smem, st>>>(sa, kbarMap);
   } else {
     static const cudaError_t attr = cudaFuncSetAttribute(
-        decode_indexer_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+        decode_score_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
     if (attr != cudaSuccess) return attr;
-    decode_indexer_kernel<128><<<grid, kThreads, smem, st>>>(a, kbarMap);
+    decode_score_kernel<128><<<grid, kScoreThreads, smem, st>>>(sa, kbarMap);
   }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  SelectArgs se;
+  se.ctx = p.contextLengths;
+  se.scores = scores;
+  se.hist = hist;
+  se.bitmap = bitmap;
+  se.tieKey = reinterpret_cast<uint32_t*>(ws + l.tieKey);
+  se.tieId = reinterpret_cast<int32_t*>(ws + l.tieId);
+  se.tieCnt = counters;
+  se.ticket = counters + B;
+  se.indices = p.indices;
+  se.maxPagesPerSeq = p.maxPagesPerSeq;
+  se.ratio = p.compressRatio;
+  se.budget = p.budget;
+  se.topK = p.topK;
+  se.nbmax = nbmax;
+  se.words = (nbmax + 31) / 32;
+  dim3 sgrid((nbmax + kSliceBlocks - 1) / kSliceBlocks, B);
+  decode_select_kernel<<<sgrid, kSelThreads, 0, st>>>(se);
   return cudaGetLastError();
 }
 

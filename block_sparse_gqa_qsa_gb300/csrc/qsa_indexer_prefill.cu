@@ -53,14 +53,12 @@ __global__ void __launch_bounds__(256) block_pool_kernel(const PoolArgs a) {
     m_s[warp][i] = __ddiv_rn(acc, static_cast<double>(a.ratio));
   }
   __syncwarp();
-  // Sum of squares in index order (one lane), so the norm is formed exactly as written.
-  double inv = 0.0;
-  if (lane == 0) {
-    double ss = 0.0;
-    for (int i = 0; i < DI; ++i) ss = __dadd_rn(ss, __dmul_rn(m_s[warp][i], m_s[warp][i]));
-    inv = __ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(__ddiv_rn(ss, static_cast<double>(DI)), a.eps)));
-  }
-  inv = __shfl_sync(kFull, inv, 0);
+  double ss = 0.0;
+#pragma unroll
+  for (int p = 0; p < PER; ++p) ss = __dadd_rn(ss, __dmul_rn(m_s[warp][lane + 32 * p], m_s[warp][lane + 32 * p]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss = __dadd_rn(ss, __shfl_xor_sync(kFull, ss, o));
+  const double inv = __ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(__ddiv_rn(ss, static_cast<double>(DI)), a.eps)));
 #pragma unroll
   for (int p = 0; p < PER; ++p) {
     const int i = lane + 32 * p;

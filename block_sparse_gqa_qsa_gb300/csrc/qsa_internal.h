@@ -25,14 +25,7 @@ size_t indexer_prefill_workspace_bytes(int B, int S, int di, int ratio);
 cudaError_t launch_indexer_prefill(const QsaIndexerPrefillParams& p, const RopeFreqs& rf);
 
 // Decode indexer ------------------------------------------------------------
-struct DecodePlan {
-  int pagesPerChunk;   // pages of block keys one CTA streams
-  int chunksMax;       // chunks of the longest possible sequence
-  int levels;          // merge levels above the chunks (fan-in 8)
-  int slotsPerSeq;     // candidate slots per sequence over all levels
-  int countersPerSeq;  // last-arriver counters per sequence
-};
-DecodePlan plan_indexer_decode(int B, int maxPagesPerSeq, int ratio);
+constexpr int kDecodeMaxBatch = 4096;   // the streaming scorer keeps a per-sequence page prefix on chip
 size_t indexer_decode_workspace_bytes(int B, int maxPagesPerSeq, int ratio, int budget);
 cudaError_t launch_indexer_decode(const QsaIndexerDecodeParams& p, const RopeFreqs& rf,
                                   const CUtensorMap& kbarMap);

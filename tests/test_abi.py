@@ -73,7 +73,8 @@ def test_constants_and_sizes(binding):
     assert (po, ps, pc) == (B * Hkv * 8 * 16 * D, B * Hkv * 8 * 2 * 16, B * Hkv)
     assert binding.indexer_prefill_workspace_size(2, 1000, 128, 4) == 256 + 2 * 250 * 128 * 2
     assert binding.indexer_prefill_workspace_size(0, 1000, 128, 4) == 0
-    assert binding.indexer_decode_workspace_size(8, 4096, 4, 512) > 8 * 4096 // 52 * 512 * 8
+    # scores, tie keys and tie ids: 12 bytes per possible block of every sequence, at least
+    assert binding.indexer_decode_workspace_size(8, 4096, 4, 512) >= 8 * 4096 * 32 * 12
     assert binding.indexer_decode_workspace_size(8, 4096, 3, 512) == 0  # 3 does not divide a page
     assert L.qsa_sparse_prefill_can_implement(32, 4, 128) == 1
     assert L.qsa_sparse_prefill_can_implement(64, 2, 128) == 0  # group 32 > 16
@@ -134,7 +135,9 @@ def test_validation_rejects_before_launch(binding):
     assert _call(binding, "qsa_indexer_decode", dp) == binding.QSA_ERR_WORKSPACE
     dp.compressRatio, dp.topK = 3, 2051
     assert _call(binding, "qsa_indexer_decode", dp) == binding.QSA_ERR_INVALID_ARG
-    dp.compressRatio, dp.budget, dp.topK = 4, 1024, 4099
+    dp.compressRatio, dp.topK = 2, 1025  # a page's 64 key tails exceed one ring stage
+    assert _call(binding, "qsa_indexer_decode", dp) == binding.QSA_ERR_UNSUPPORTED
+    dp.compressRatio, dp.topK, dp.batchSize = 4, 2051, 5000
     assert _call(binding, "qsa_indexer_decode", dp) == binding.QSA_ERR_UNSUPPORTED
 
     sd = binding.QsaSparseDecodeParams(qPtr=fake, kvPoolPtr=fake, pageTable=fake, indices=fake,
