@@ -166,9 +166,11 @@ qsa_status_t qsa_indexer_decode(const QsaIndexerDecodeParams* p) {
   if (qsa::kTokensPerPageHost % p->compressRatio != 0)
     return fail(QSA_ERR_INVALID_ARG, "qsa_indexer_decode: compressRatio %d does not divide the 128-token page",
                 p->compressRatio);
-  if (p->compressRatio < 4)
-    return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_decode: compressRatio %d < 4 (a page's key tails must fit one "
-                                     "ring stage)", p->compressRatio);
+  if (p->compressRatio < 4 || p->compressRatio > 16)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_decode: compressRatio %d outside 4..16 (a page's key tails are "
+                                     "one swizzled TMA tile of 8..32 rows)", p->compressRatio);
+  if (p->budget > 4096)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_decode: budget %d > 4096", p->budget);
   if (p->batchSize > qsa::kDecodeMaxBatch)
     return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_decode: batchSize > %d", qsa::kDecodeMaxBatch);
   if (p->kvHeadDim % 8 || p->poolHeadDim % 8 || !aligned(p->kvPool, 16))
@@ -189,11 +191,11 @@ qsa_status_t qsa_indexer_decode(const QsaIndexerDecodeParams* p) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(p->headDim), static_cast<cuuint64_t>(bpp),
                         static_cast<cuuint64_t>(p->numFlatPages)};
   cuuint64_t strides[2] = {row_bytes * p->compressRatio, row_bytes * qsa::kTokensPerPageHost};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(p->headDim), static_cast<cuuint32_t>(bpp), 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(bpp), 1};  // one 128-byte swizzled half per copy
   cuuint32_t estr[3] = {1, 1, 1};
   void* base = static_cast<char*>(p->kvPool) + static_cast<size_t>(p->kvHeadDim) * 2;
   const CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_decode: tensor map rejected (CUresult %d)", r);
   const cudaError_t e = qsa::launch_indexer_decode(*p, rope_freqs(p->ropeTheta, p->rotDim), map);

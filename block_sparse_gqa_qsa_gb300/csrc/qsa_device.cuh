@@ -217,6 +217,17 @@ __device__ __forceinline__ void cta_topk(const uint32_t (&key)[VPT], int nv, int
 }
 
 // ------------------------------------------------------------------- RoPE
+// cos/sin of the f64 angle pos * inv_freq, reduced to [-pi, pi] first (2 pi in
+// two parts, each product taken with one rounding by fma) so that the f64
+// sincos stays on its short path even at positions ~5e5.
+__device__ __forceinline__ void rope_cos_sin_f64(double pos, double inv_freq, double& c, double& s) {
+  const double a = __dmul_rn(pos, inv_freq);
+  const double k = rint(a * 0.15915494309189535);
+  double r = fma(-k, 6.283185307179586, a);
+  r = fma(-k, 2.4492935982947064e-16, r);
+  sincos(r, &s, &c);
+}
+
 // cos/sin of pos * inv_freq with the angle formed and reduced modulo 2*pi in
 // f64, then evaluated in fp32 (|r| <= pi): an fp32 product pos * inv_freq
 // would be off by up to 0.03 rad at pos ~ 5e5.

@@ -12,19 +12,21 @@
 //       stored in the V-row tail of the block's first token.
 //   decode_score_kernel   (B2) persistent, one CTA per SM, warp-specialised:
 //       a producer warp streams the key tails of every page that holds
-//       complete blocks (one 3-D TMA copy per page: box {di, 128/r, 1} over a
-//       strided view of the pool) into a 24-stage ring; 15 consumer warps
-//       score one page each (8 dims x 8 heads per lane with paired fp32 FMA, a
-//       transposing shuffle reduction whose head order is pre-permuted per
-//       lane so that no select is needed), write the scores and add them to a
-//       4096-bin histogram of the score bits per sequence.  Pages are split
-//       evenly over the CTAs, so HBM streams without per-chunk stalls.
+//       complete blocks (3-D TMA copies, box {64, 128/r, 1} with the 128-byte
+//       swizzle over a strided view of the pool, page ids fetched 32 at a time)
+//       into a 24-stage ring; 15 consumer warps score one page each: 16 lanes
+//       per key, 8 dims x 8 heads per lane (dims paired in fp32x2 FMAs), then
+//       a transposing shuffle reduction whose head order is pre-permuted per
+//       lane (h ^ m) so that every step is one add of one shuffle; they write
+//       the scores and add them to a 4096-bin histogram of the score bits per
+//       sequence.  Pages are split evenly over the CTAs.
 //   decode_select_kernel  (B3) per sequence: the histogram gives the bin that
-//       holds the budget-th largest score; CTAs over 8192-block slices mark
-//       every block above that bin in a bitmap and append the blocks inside
-//       it; the last CTA to finish picks the exact top of those by (score
-//       desc, id asc), expands the bitmap in ascending order with the causal
-//       tail, and re-arms the histogram and counters.
+//       holds the budget-th largest score; CTAs over 2048-block slices collect
+//       the blocks above that bin and the blocks inside it (gathered in shared
+//       memory, one global reservation per CTA); the last CTA to finish keeps
+//       the top of the tie bin by (score desc, id asc), sorts the kept ids
+//       (bitonic, in shared memory), expands them with the causal tail, and
+//       re-arms the histogram and counters.
 // Waits on TMA barriers are bounded; on expiry the kernel records
 // kErrWaitTimeout in the workspace status word and stops.
 #include "qsa_device.cuh"
@@ -36,7 +38,8 @@ namespace {
 constexpr size_t kStatusBytes = 256;
 constexpr int kNumBins = 4096;       // histogram of (score bits >> 19): exponent + 4 mantissa bits
 constexpr int kBinShift = 19;
-constexpr int kSliceBlocks = 8192;   // blocks one select CTA filters
+constexpr int kSliceBlocks = 2048;   // blocks one select CTA filters (8 per thread, one round of loads)
+constexpr int kMaxSelect = 4096;     // budget cap: the final CTA sorts the kept block ids in shared memory
 constexpr int kConsumerWarps = 15;  // + 1 producer warp = 16 warps, up to 128 registers each
 constexpr int kScoreThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 24;
@@ -48,9 +51,9 @@ constexpr int kMaxDynSmem = 227 * 1024;
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
-  size_t q, scores, hist, bitmap, tieKey, tieId, counters, total;
+  size_t q, scores, hist, sureId, tieKey, tieId, counters, total;
 };
-WsLayout ws_layout(int B, int nbmax) {
+WsLayout ws_layout(int B, int nbmax, int budget) {
   WsLayout l;
   size_t off = kStatusBytes;
   l.q = off;
@@ -59,14 +62,14 @@ WsLayout ws_layout(int B, int nbmax) {
   off += up256(static_cast<size_t>(B) * nbmax * 4);     // block scores fp32 [B][nbmax]
   l.hist = off;
   off += up256(static_cast<size_t>(B) * kNumBins * 4);  // int32 [B][kNumBins], zero between calls
-  l.bitmap = off;
-  off += up256(static_cast<size_t>(B) * ((nbmax + 31) / 32) * 4);
+  l.sureId = off;
+  off += up256(static_cast<size_t>(B) * budget * 4);    // blocks above the threshold bin [B][budget]
   l.tieKey = off;
-  off += up256(static_cast<size_t>(B) * nbmax * 4);
+  off += up256(static_cast<size_t>(B) * nbmax * 4);     // blocks inside it [B][nbmax]
   l.tieId = off;
   off += up256(static_cast<size_t>(B) * nbmax * 4);
   l.counters = off;
-  off += up256(static_cast<size_t>(B) * 2 * 4);         // tie count, ticket: zero between calls
+  off += up256(static_cast<size_t>(B) * 3 * 4);         // sure count, tie count, ticket: zero between calls
   l.total = off;
   return l;
 }
@@ -210,12 +213,12 @@ __global__ void __launch_bounds__(256) decode_prep_kernel(const PrepArgs a) {
     double r = y2_s[i];
     if (i < half) {
       double s, c;
-      sincos(__dmul_rn(pos, a.rf.inv_freq[i]), &s, &c);
+      rope_cos_sin_f64(pos, a.rf.inv_freq[i], c, s);
       r = __dsub_rn(__dmul_rn(y2_s[i], c), __dmul_rn(y2_s[i + half], s));
     } else if (i < a.rot) {
       const int k = i - half;
       double s, c;
-      sincos(__dmul_rn(pos, a.rf.inv_freq[k]), &s, &c);
+      rope_cos_sin_f64(pos, a.rf.inv_freq[k], c, s);
       r = __dadd_rn(__dmul_rn(y2_s[i], c), __dmul_rn(y2_s[k], s));
     }
     a.pool[pool_row(vp, first & 127, a.Hkv, a.poolHeadDim) + a.D + i] = __double2half(r);
@@ -238,12 +241,28 @@ __host__ __device__ __forceinline__ int score_smem_bytes(int di, int ratio, int 
   return kStages * stage + 2 * kStages * 8 + ((B + 1 + 3) / 4) * 16 + kConsumerWarps * 128 * 4;
 }
 
+// One lane per key row: byte offset of 16-byte chunk c (dims 8c..8c+7 of a
+// 64-dim half) of row r in a TMA tile written with the 128-byte swizzle.
+__device__ __forceinline__ int swz128(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
+
+// Writes one page's scores (lane j = block j of the page) and adds them to the
+// sequence's histogram, one atomic per distinct bin of the warp.
+__device__ __forceinline__ void page_epilogue(const ScoreArgs& a, int b, int p, int n_c, int bpp, float sc) {
+  const int lane = threadIdx.x & 31;
+  const int g = p * bpp + lane;
+  const bool valid = lane < bpp && g < n_c;
+  const int bin = static_cast<int>(__float_as_uint(sc) >> kBinShift);
+  if (valid) a.scores[static_cast<size_t>(b) * a.nbmax + g] = sc;
+  const unsigned act = __ballot_sync(kFull, valid);
+  if (valid) {
+    const unsigned peers = __match_any_sync(act, bin);
+    if (lane == __ffs(peers) - 1) atomicAdd(a.hist + static_cast<size_t>(b) * kNumBins + bin, __popc(peers));
+  }
+}
+
 template <int DI>
 __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const ScoreArgs a,
                                                                         const __grid_constant__ CUtensorMap kmap) {
-  constexpr int LPB = DI / 8;          // lanes per block key (8 dims each)
-  constexpr int BPW = 32 / LPB;        // block keys per warp pass
-  constexpr int LOGL = LPB == 16 ? 4 : 3;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int bpp = kTokensPerPage / a.ratio;
   const int stage_bytes = bpp * DI * 2;
@@ -251,7 +270,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * stage_bytes);
   uint64_t* empty = full + kStages;
   int* pref = reinterpret_cast<int*>(empty + kStages);  // pages of complete blocks, exclusive prefix [B+1]
-  float* scr = reinterpret_cast<float*>(pref + (a.B + 1 + 3) / 4 * 4);  // [kConsumerWarps][128]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int MAXL = a.maxPagesPerSeq * kTokensPerPage;
 
@@ -287,40 +305,59 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
   const long long lo = W * blockIdx.x / gridDim.x, hi = W * (blockIdx.x + 1) / gridDim.x;
   if (lo >= hi) return;
 
-  if (warp == kConsumerWarps) {  // ---- producer
-    if (lane == 0) {
-      int b = 0;
-      for (long long i = lo; i < hi; ++i) {
-        while (i >= pref[b + 1]) ++b;
-        const int p = static_cast<int>(i - pref[b]);
-        int vp = __ldg(a.pageTable + (static_cast<size_t>(b) * 2 + 1) * a.maxPagesPerSeq + p);
+  if (warp == kConsumerWarps) {  // ---- producer: page ids 32 at a time, one TMA per 64-dim half
+    int bw = 0;  // sequence of the batch's first page
+    bool alive = true;
+    for (long long base = lo; base < hi && alive; base += 32) {
+      while (base >= pref[bw + 1]) ++bw;
+      const long long i = base + lane;
+      int vp = 0;
+      if (i < hi) {
+        int bl = bw;
+        while (i >= pref[bl + 1]) ++bl;
+        vp = __ldg(a.pageTable + (static_cast<size_t>(bl) * 2 + 1) * a.maxPagesPerSeq + (i - pref[bl]));
         if (static_cast<unsigned>(vp) >= static_cast<unsigned>(a.numFlatPages)) {
           atomicOr(a.status, kErrBadPage);
           vp = 0;
         }
-        const int j = static_cast<int>(i - lo), s = j % kStages, n = j / kStages;
-        if (!mbar_wait_bounded(&empty[s], (n & 1) ^ 1, kWaitLimitNs)) {
-          atomicOr(a.status, kErrWaitTimeout);
+      }
+      const int cnt = static_cast<int>(hi - base < 32 ? hi - base : 32);
+      for (int k = 0; k < cnt; ++k) {
+        const int vpk = __shfl_sync(kFull, vp, k);
+        int ok = 1;
+        if (lane == 0) {
+          const int jdx = static_cast<int>(base + k - lo), s = jdx % kStages, n = jdx / kStages;
+          if (!mbar_wait_bounded(&empty[s], (n & 1) ^ 1, kWaitLimitNs)) {
+            atomicOr(a.status, kErrWaitTimeout);
+            ok = 0;
+          } else {
+            mbar_arrive_expect_tx(&full[s], stage_bytes);
+#pragma unroll
+            for (int hh = 0; hh < DI / 64; ++hh)
+              tma_load_3d(ring + s * stage_bytes + hh * bpp * 128, &kmap, 64 * hh, 0, vpk, &full[s]);
+          }
+        }
+        if (!__shfl_sync(kFull, ok, 0)) {
+          alive = false;
           break;
         }
-        mbar_arrive_expect_tx(&full[s], stage_bytes);
-        tma_load_3d(ring + s * stage_bytes, &kmap, 0, 0, vp, &full[s]);
       }
     }
     return;
   }
 
-  // ---- consumers: warp w takes pages lo + w, lo + w + kConsumerWarps, ...
+  // ---- consumers: warp w takes pages lo + w, lo + w + kConsumerWarps, ...; 16 lanes per key
+  constexpr int LPB = DI / 8, BPW = 32 / LPB, LOGL = LPB == 16 ? 4 : 3;
   const int sub = lane % LPB;
-  const int m = (sub >> (LOGL - 3)) & 7;  // this lane's head order is h ^ m (see the reduction)
+  const int m = (sub >> (LOGL - 3)) & 7;
   uint64_t q2[8][4];
   int cached_b = -1, n_c = 0;
   int b = 0;
-  float* myscr = scr + warp * 128;
+  float* myscr = reinterpret_cast<float*>(pref + (a.B + 1 + 3) / 4 * 4) + warp * 128;
   for (long long i = lo + warp; i < hi; i += kConsumerWarps) {
     while (i >= pref[b + 1]) ++b;
     const int p = static_cast<int>(i - pref[b]);
-    const int j = static_cast<int>(i - lo), s = j % kStages, n = j / kStages;
+    const int jx = static_cast<int>(i - lo), s = jx % kStages, n = jx / kStages;
     if (b != cached_b) {
       const float* qb = a.q + static_cast<size_t>(b) * 8 * 128;
 #pragma unroll
@@ -339,10 +376,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
       if (lane == 0) atomicOr(a.status, kErrWaitTimeout);
       break;
     }
-    const __half* tile = reinterpret_cast<const __half*>(ring + s * stage_bytes);
+    const uint8_t* tile = ring + s * stage_bytes;
+#pragma unroll 2
     for (int pass = 0; pass < bpp / BPW; ++pass) {
       const int blk = pass * BPW + lane / LPB;
-      const uint4 raw = *reinterpret_cast<const uint4*>(tile + blk * DI + sub * 8);
+      const uint4 raw = *reinterpret_cast<const uint4*>(tile + (sub >> 3) * bpp * 128 + swz128(blk, sub & 7));
       const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
       uint64_t kp[4];
 #pragma unroll
@@ -359,38 +397,21 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
         acc = ffma2(q2[h][3], kp[3], acc);
         d[h] = lo_f2(acc) + hi_f2(acc);
       }
-      // Transposing reduction over the LPB lanes of this key.  Lane head order
-      // h ^ m makes the partner's upper half hold the same heads as this
-      // lane's lower half at every step, so each step is add(shuffle).
 #pragma unroll
       for (int i2 = 0; i2 < 4; ++i2) d[i2] += __shfl_xor_sync(kFull, d[i2 + 4], LPB / 2);
 #pragma unroll
       for (int i2 = 0; i2 < 2; ++i2) d[i2] += __shfl_xor_sync(kFull, d[i2 + 2], LPB / 4);
       d[0] += __shfl_xor_sync(kFull, d[1], LPB / 8);
       if (LPB == 16) d[0] += __shfl_xor_sync(kFull, d[0], 1);
-      float sc = d[0] > 0.f ? d[0] : 0.f;  // relu of head m's dot
+      float sc = d[0] > 0.f ? d[0] : 0.f;
       sc += __shfl_xor_sync(kFull, sc, LPB / 8);
       sc += __shfl_xor_sync(kFull, sc, LPB / 4);
       sc += __shfl_xor_sync(kFull, sc, LPB / 2);
       if (sub == 0) myscr[blk] = sc;
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);  // the stage may be refilled
-    float* sc_row = a.scores + static_cast<size_t>(b) * a.nbmax;
-    int32_t* hrow = a.hist + static_cast<size_t>(b) * kNumBins;
-    for (int r0 = 0; r0 < bpp; r0 += 32) {
-      const int jb = r0 + lane;
-      const int g = p * bpp + jb;
-      const bool valid = jb < bpp && g < n_c;
-      const float sc = valid ? myscr[jb] : 0.f;
-      const int bin = static_cast<int>(__float_as_uint(sc) >> kBinShift);
-      if (valid) sc_row[g] = sc;
-      const unsigned act = __ballot_sync(kFull, valid);
-      if (valid) {
-        const unsigned peers = __match_any_sync(act, bin);
-        if (lane == __ffs(peers) - 1) atomicAdd(hrow + bin, __popc(peers));
-      }
-    }
+    if (lane == 0) mbar_arrive(&empty[s]);
+    page_epilogue(a, b, p, n_c, bpp, myscr[lane < bpp ? lane : 0]);
     __syncwarp();
   }
 }
@@ -400,19 +421,21 @@ struct SelectArgs {
   const int32_t* ctx;
   const float* scores;
   int32_t* hist;
-  uint32_t* bitmap;
+  int32_t* sureId;
   uint32_t* tieKey;
   int32_t* tieId;
-  int32_t* tieCnt;
-  int32_t* ticket;
+  int32_t* counters;  // [B][3]: sure count, tie count, ticket
   int32_t* indices;
-  int maxPagesPerSeq, ratio, budget, topK, nbmax, words;
+  int maxPagesPerSeq, ratio, budget, topK, nbmax;
 };
 
 __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const SelectArgs a) {
   __shared__ int red[2 * kSelThreads / 32];
   __shared__ int scan[kSelThreads / 32];
-  __shared__ int info[4];
+  __shared__ int info[8];
+  __shared__ int buf_s[kMaxSelect];            // filter: sure ids | final: kept ids to sort
+  __shared__ uint32_t tkey_s[kSliceBlocks];    // filter: this slice's ties
+  __shared__ int tid_s[kSliceBlocks];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int s = blockIdx.x, b = blockIdx.y;
   const int L = max(0, min(a.ctx[b], a.maxPagesPerSeq * kTokensPerPage));
@@ -420,6 +443,7 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
   const int n_c = L / a.ratio;
   int32_t* out = a.indices + static_cast<size_t>(b) * a.topK;
   int32_t* hrow = a.hist + static_cast<size_t>(b) * kNumBins;
+  int32_t* ctr = a.counters + static_cast<size_t>(b) * 3;
   if (L == 0) {
     if (s == 0)
       for (int i = tid; i < a.topK; i += kSelThreads) out[i] = -1;
@@ -447,6 +471,8 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
   if (tid == 0) {
     info[0] = 0;  // threshold bin
     info[1] = 0;  // blocks in higher bins
+    info[2] = 0;  // sure blocks gathered by this CTA
+    info[3] = 0;  // ties gathered by this CTA
   }
   int total;
   const int excl = cta_exclusive_scan<kSelThreads>(own, scan, total);
@@ -462,66 +488,118 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
   __syncthreads();
   const int T = info[0], c_above = info[1];
 
-  // ---- mark blocks above the bin, collect the blocks inside it
+  // ---- classify this slice: above the bin (kept) or inside it (tie)
   const float* srow = a.scores + static_cast<size_t>(b) * a.nbmax;
-  uint32_t* brow = a.bitmap + static_cast<size_t>(b) * a.words;
-  const int g1 = min((s + 1) * kSliceBlocks, n_c);
-  for (int base = s * kSliceBlocks + warp * 32; base < g1; base += kSelThreads) {
-    const int g = base + lane;
+  const int g0 = s * kSliceBlocks, g1 = min(g0 + kSliceBlocks, n_c);
+  constexpr int U = kSliceBlocks / kSelThreads;
+  uint32_t keys[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int g = g0 + u * kSelThreads + tid;
+    keys[u] = g < g1 ? __float_as_uint(__ldcg(srow + g)) : 0u;
+  }
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int g = g0 + u * kSelThreads + tid;
     const bool valid = g < g1;
-    const uint32_t key = valid ? __float_as_uint(__ldcg(srow + g)) : 0u;
-    const int bin = static_cast<int>(key >> kBinShift);
-    const unsigned sure = __ballot_sync(kFull, valid && bin > T);
-    if (lane == 0) brow[base >> 5] = sure;
-    const bool tie = valid && bin == T;
-    const unsigned tm = __ballot_sync(kFull, tie);
-    if (tm) {
-      int pos0 = 0;
-      if (lane == 0) pos0 = atomicAdd(a.tieCnt + b, __popc(tm));
-      pos0 = __shfl_sync(kFull, pos0, 0);
-      if (tie) {
-        const int at = pos0 + __popc(tm & ((1u << lane) - 1u));
-        a.tieKey[static_cast<size_t>(b) * a.nbmax + at] = key;
-        a.tieId[static_cast<size_t>(b) * a.nbmax + at] = g;
+    const int bin = static_cast<int>(keys[u] >> kBinShift);
+    const bool sure = valid && bin > T, tie = valid && bin == T;
+    const unsigned sm = __ballot_sync(kFull, sure), tm = __ballot_sync(kFull, tie);
+    const unsigned lt = (1u << lane) - 1u;
+    if (sm) {
+      int p0 = 0;
+      if (lane == 0) p0 = atomicAdd(&info[2], __popc(sm));
+      p0 = __shfl_sync(kFull, p0, 0);
+      if (sure) {
+        const int at = p0 + __popc(sm & lt);
+        if (at < kMaxSelect) buf_s[at] = g;
       }
+    }
+    if (tm) {
+      int p0 = 0;
+      if (lane == 0) p0 = atomicAdd(&info[3], __popc(tm));
+      p0 = __shfl_sync(kFull, p0, 0);
+      if (tie) {
+        const int at = p0 + __popc(tm & lt);
+        tkey_s[at] = keys[u];
+        tid_s[at] = g;
+      }
+    }
+  }
+  __syncthreads();
+  {  // one global reservation per list per CTA
+    const int ns = min(info[2], kMaxSelect), nts = info[3];
+    if (tid == 0) {
+      info[4] = ns ? atomicAdd(ctr + 0, ns) : 0;
+      info[5] = nts ? atomicAdd(ctr + 1, nts) : 0;
+    }
+    __syncthreads();
+    const int as = info[4], at = info[5];
+    for (int e = tid; e < ns; e += kSelThreads)
+      if (as + e < a.budget) a.sureId[static_cast<size_t>(b) * a.budget + as + e] = buf_s[e];
+    for (int e = tid; e < nts; e += kSelThreads) {
+      a.tieKey[static_cast<size_t>(b) * a.nbmax + at + e] = tkey_s[e];
+      a.tieId[static_cast<size_t>(b) * a.nbmax + at + e] = tid_s[e];
     }
   }
   __threadfence();
   __syncthreads();
-  if (tid == 0) info[2] = atomicAdd(a.ticket + b, 1) == nsplit - 1;
+  if (tid == 0) info[6] = atomicAdd(ctr + 2, 1) == nsplit - 1;
   __syncthreads();
-  if (!info[2]) return;
+  if (!info[6]) return;
   __threadfence();
 
-  // ---- last CTA: exact top of the tie bin by (score desc, id asc)
+  // ---- last CTA: kept blocks = the sure ones + the top of the tie bin by (score desc, id asc)
   const int need = a.budget - c_above;
-  const int nt = __ldcg(a.tieCnt + b);
+  const int nt = __ldcg(ctr + 1);
   const uint32_t* tk = a.tieKey + static_cast<size_t>(b) * a.nbmax;
   const int32_t* ti = a.tieId + static_cast<size_t>(b) * a.nbmax;
+  for (int e = tid; e < c_above; e += kSelThreads) buf_s[e] = __ldcg(a.sureId + static_cast<size_t>(b) * a.budget + e);
+  if (tid == 0) info[7] = c_above;  // next free slot of buf_s
+  __syncthreads();
+  auto keep = [&](int id) {
+    const int at = atomicAdd(&info[7], 1);
+    if (at < kMaxSelect) buf_s[at] = id;
+  };
   if (nt <= need) {
-    for (int e = tid; e < nt; e += kSelThreads) {
-      const int id = __ldcg(ti + e);
-      atomicOr(brow + (id >> 5), 1u << (id & 31));
-    }
-  } else if (nt <= kTieVPT * kSelThreads) {
+    for (int e = tid; e < nt; e += kSelThreads) keep(__ldcg(ti + e));
+  } else {
+    // bisection on the score bits inside bin T, then on the id among exact ties at the cut
+    const bool regs = nt <= kTieVPT * kSelThreads;
     uint32_t key[kTieVPT];
     int id[kTieVPT];
-    const int nv = max(0, min(kTieVPT, nt - tid * kTieVPT));
+    const int nv = regs ? max(0, min(kTieVPT, nt - tid * kTieVPT)) : 0;
 #pragma unroll
     for (int v = 0; v < kTieVPT; ++v) {
       key[v] = v < nv ? __ldcg(tk + tid * kTieVPT + v) : 0u;
       id[v] = v < nv ? __ldcg(ti + tid * kTieVPT + v) : 0;
     }
+    auto count_ge = [&](uint32_t x) {
+      int c = 0;
+      if (regs) {
+#pragma unroll
+        for (int v = 0; v < kTieVPT; ++v) c += (v < nv && key[v] >= x) ? 1 : 0;
+      } else {
+        for (int e = tid; e < nt; e += kSelThreads) c += __ldcg(tk + e) >= x ? 1 : 0;
+      }
+      return c;
+    };
+    auto count_eq_le = [&](uint32_t x, int y) {
+      int c = 0;
+      if (regs) {
+#pragma unroll
+        for (int v = 0; v < kTieVPT; ++v) c += (v < nv && key[v] == x && id[v] <= y) ? 1 : 0;
+      } else {
+        for (int e = tid; e < nt; e += kSelThreads) c += (__ldcg(tk + e) == x && __ldcg(ti + e) <= y) ? 1 : 0;
+      }
+      return c;
+    };
     int phase = 0;
-    // every tie key lies in bin T: count(>= lo) >= need > count(>= hi)
     uint32_t lo = static_cast<uint32_t>(T) << kBinShift, hi = static_cast<uint32_t>(T + 1) << kBinShift;
-    int cnt_lo = nt, cnt_hi = 0;
+    int cnt_lo = nt, cnt_hi = 0;  // count(>= lo) >= need > count(>= hi)
     while (hi - lo > 1u) {
       const uint32_t mid = lo + ((hi - lo) >> 1);
-      int c = 0;
-#pragma unroll
-      for (int v = 0; v < kTieVPT; ++v) c += (v < nv && key[v] >= mid) ? 1 : 0;
-      const int tot = cta_sum<kSelThreads>(c, red, phase);
+      const int tot = cta_sum<kSelThreads>(count_ge(mid), red, phase);
       if (tot >= need) {
         lo = mid;
         cnt_lo = tot;
@@ -532,83 +610,53 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
     }
     const uint32_t Tk = lo;
     const int n_eq = need - cnt_hi;  // keys equal to Tk to keep, lowest ids first
-    int ilo = -1, ihi = a.nbmax;     // count(== Tk, id <= ilo) < n_eq <= count(== Tk, id <= ihi)
-    if (cnt_lo - cnt_hi == n_eq) ilo = ihi - 1;  // no exact tie at the cut: keep every key == Tk
-    while (ihi - ilo > 1) {
-      const int mid = ilo + ((ihi - ilo) >> 1);
-      int c = 0;
-#pragma unroll
-      for (int v = 0; v < kTieVPT; ++v) c += (v < nv && key[v] == Tk && id[v] <= mid) ? 1 : 0;
-      const int tot = cta_sum<kSelThreads>(c, red, phase);
-      if (tot >= n_eq)
-        ihi = mid;
-      else
-        ilo = mid;
-    }
-#pragma unroll
-    for (int v = 0; v < kTieVPT; ++v)
-      if (v < nv && (key[v] > Tk || (key[v] == Tk && id[v] <= ihi))) atomicOr(brow + (id[v] >> 5), 1u << (id[v] & 31));
-  } else {
-    // Degenerate case (very many scores in one bin, e.g. all zero): the same
-    // two bisections, counting straight from global memory.
-    int phase = 0;
-    uint32_t lo = static_cast<uint32_t>(T) << kBinShift, hi = static_cast<uint32_t>(T + 1) << kBinShift;
-    int cnt_lo = nt, cnt_hi = 0;
-    while (hi - lo > 1u) {
-      const uint32_t mid = lo + ((hi - lo) >> 1);
-      int c = 0;
-      for (int e = tid; e < nt; e += kSelThreads) c += __ldcg(tk + e) >= mid ? 1 : 0;
-      const int tot = cta_sum<kSelThreads>(c, red, phase);
-      if (tot >= need) {
-        lo = mid;
-        cnt_lo = tot;
-      } else {
-        hi = mid;
-        cnt_hi = tot;
+    int ilo = -1, ihi = a.nbmax;
+    if (cnt_lo - cnt_hi != n_eq) {
+      while (ihi - ilo > 1) {
+        const int mid = ilo + ((ihi - ilo) >> 1);
+        if (cta_sum<kSelThreads>(count_eq_le(Tk, mid), red, phase) >= n_eq)
+          ihi = mid;
+        else
+          ilo = mid;
       }
     }
-    const uint32_t Tk = lo;
-    const int n_eq = need - cnt_hi;
-    int ilo = -1, ihi = a.nbmax;
-    if (cnt_lo - cnt_hi == n_eq) ilo = ihi - 1;
-    while (ihi - ilo > 1) {
-      const int mid = ilo + ((ihi - ilo) >> 1);
-      int c = 0;
-      for (int e = tid; e < nt; e += kSelThreads) c += (__ldcg(tk + e) == Tk && __ldcg(ti + e) <= mid) ? 1 : 0;
-      const int tot = cta_sum<kSelThreads>(c, red, phase);
-      if (tot >= n_eq)
-        ihi = mid;
-      else
-        ilo = mid;
-    }
-    for (int e = tid; e < nt; e += kSelThreads) {
-      const uint32_t k = __ldcg(tk + e);
-      const int id = __ldcg(ti + e);
-      if (k > Tk || (k == Tk && id <= ihi)) atomicOr(brow + (id >> 5), 1u << (id & 31));
+    if (regs) {
+#pragma unroll
+      for (int v = 0; v < kTieVPT; ++v)
+        if (v < nv && (key[v] > Tk || (key[v] == Tk && id[v] <= ihi))) keep(id[v]);
+    } else {
+      for (int e = tid; e < nt; e += kSelThreads) {
+        const uint32_t k = __ldcg(tk + e);
+        const int i2 = __ldcg(ti + e);
+        if (k > Tk || (k == Tk && i2 <= ihi)) keep(i2);
+      }
     }
   }
-  __threadfence();
   __syncthreads();
-
-  // ---- expand the bitmap in ascending order, then the causal tail
-  const int nw = (n_c + 31) / 32;
-  const int wpt = (nw + kSelThreads - 1) / kSelThreads;
-  const int w0 = min(tid * wpt, nw), w1 = min(w0 + wpt, nw);
-  int cnt = 0;
-  for (int w = w0; w < w1; ++w) cnt += __popc(__ldcg(brow + w));
-  int tot;
-  int pos = cta_exclusive_scan<kSelThreads>(cnt, scan, tot);
-  for (int w = w0; w < w1; ++w) {
-    uint32_t bits = __ldcg(brow + w);
-    while (bits) {
-      const int id = w * 32 + __ffs(bits) - 1;
-      bits &= bits - 1;
-      for (int jj = 0; jj < a.ratio; ++jj)
-        if (pos * a.ratio + jj < a.topK) out[pos * a.ratio + jj] = id * a.ratio + jj;
-      ++pos;
+  // ---- sort the kept ids ascending (bitonic, padded to a power of two), expand with the tail
+  const int nk = min(info[7], kMaxSelect);
+  int np2 = 1;
+  while (np2 < nk) np2 <<= 1;
+  for (int e = nk + tid; e < np2; e += kSelThreads) buf_s[e] = 0x7fffffff;
+  __syncthreads();
+  for (int k = 2; k <= np2; k <<= 1) {
+    for (int jb = k >> 1; jb > 0; jb >>= 1) {
+      for (int e = tid; e < np2; e += kSelThreads) {
+        const int f = e ^ jb;
+        if (f > e) {
+          const int x = buf_s[e], y = buf_s[f];
+          const bool up = (e & k) == 0;
+          if ((x > y) == up) {
+            buf_s[e] = y;
+            buf_s[f] = x;
+          }
+        }
+      }
+      __syncthreads();
     }
   }
-  const int head = tot * a.ratio;
+  for (int e = tid; e < nk * a.ratio && e < a.topK; e += kSelThreads) out[e] = buf_s[e / a.ratio] * a.ratio + e % a.ratio;
+  const int head = nk * a.ratio;
   for (int i = head + tid; i < a.topK; i += kSelThreads) {
     const int j = n_c * a.ratio + (i - head);
     out[i] = j <= t ? j : -1;
@@ -616,8 +664,9 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
   // re-arm for the next call
   for (int i = tid; i < kNumBins; i += kSelThreads) hrow[i] = 0;
   if (tid == 0) {
-    a.tieCnt[b] = 0;
-    a.ticket[b] = 0;
+    ctr[0] = 0;
+    ctr[1] = 0;
+    ctr[2] = 0;
   }
 }
 
@@ -636,9 +685,8 @@ int sm_count() {
 }  // namespace
 
 size_t indexer_decode_workspace_bytes(int B, int maxPagesPerSeq, int ratio, int budget) {
-  (void)budget;
   const int nbmax = maxPagesPerSeq * (kTokensPerPageHost / ratio);
-  return ws_layout(B, nbmax).total;
+  return ws_layout(B, nbmax, budget).total;
 }
 
 cudaError_t launch_indexer_decode(const QsaIndexerDecodeParams& p, const RopeFreqs& rf,
@@ -646,13 +694,12 @@ cudaError_t launch_indexer_decode(const QsaIndexerDecodeParams& p, const RopeFre
   const int B = p.batchSize;
   const int bpp = kTokensPerPageHost / p.compressRatio;
   const int nbmax = p.maxPagesPerSeq * bpp;
-  const WsLayout l = ws_layout(B, nbmax);
+  const WsLayout l = ws_layout(B, nbmax, p.budget);
   uint8_t* ws = static_cast<uint8_t*>(p.workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
   float* q = reinterpret_cast<float*>(ws + l.q);
   float* scores = reinterpret_cast<float*>(ws + l.scores);
   int32_t* hist = reinterpret_cast<int32_t*>(ws + l.hist);
-  uint32_t* bitmap = reinterpret_cast<uint32_t*>(ws + l.bitmap);
   int32_t* counters = reinterpret_cast<int32_t*>(ws + l.counters);
   cudaStream_t st = static_cast<cudaStream_t>(p.stream);
 
@@ -717,18 +764,16 @@ cudaError_t launch_indexer_decode(const QsaIndexerDecodeParams& p, const RopeFre
   se.ctx = p.contextLengths;
   se.scores = scores;
   se.hist = hist;
-  se.bitmap = bitmap;
+  se.sureId = reinterpret_cast<int32_t*>(ws + l.sureId);
   se.tieKey = reinterpret_cast<uint32_t*>(ws + l.tieKey);
   se.tieId = reinterpret_cast<int32_t*>(ws + l.tieId);
-  se.tieCnt = counters;
-  se.ticket = counters + B;
+  se.counters = counters;
   se.indices = p.indices;
   se.maxPagesPerSeq = p.maxPagesPerSeq;
   se.ratio = p.compressRatio;
   se.budget = p.budget;
   se.topK = p.topK;
   se.nbmax = nbmax;
-  se.words = (nbmax + 31) / 32;
   dim3 sgrid((nbmax + kSliceBlocks - 1) / kSliceBlocks, B);
   decode_select_kernel<<<sgrid, kSelThreads, 0, st>>>(se);
   return cudaGetLastError();

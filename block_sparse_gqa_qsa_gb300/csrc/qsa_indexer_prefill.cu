@@ -75,12 +75,12 @@ __global__ void __launch_bounds__(256) block_pool_kernel(const PoolArgs a) {
     double r = y;
     if (i < half) {
       double s, c;
-      sincos(__dmul_rn(pos, a.rf.inv_freq[i]), &s, &c);
+      rope_cos_sin_f64(pos, a.rf.inv_freq[i], c, s);
       r = __dsub_rn(__dmul_rn(y, c), __dmul_rn(y_s[warp][i + half], s));
     } else if (i < a.rot) {
       const int k = i - half;
       double s, c;
-      sincos(__dmul_rn(pos, a.rf.inv_freq[k]), &s, &c);
+      rope_cos_sin_f64(pos, a.rf.inv_freq[k], c, s);
       r = __dadd_rn(__dmul_rn(y, c), __dmul_rn(y_s[warp][k], s));
     }
     out[i] = __double2half(r);

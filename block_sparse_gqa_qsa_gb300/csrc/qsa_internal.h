@@ -25,7 +25,7 @@ size_t indexer_prefill_workspace_bytes(int B, int S, int di, int ratio);
 cudaError_t launch_indexer_prefill(const QsaIndexerPrefillParams& p, const RopeFreqs& rf);
 
 // Decode indexer ------------------------------------------------------------
-constexpr int kDecodeMaxBatch = 4096;   // the streaming scorer keeps a per-sequence page prefix on chip
+constexpr int kDecodeMaxBatch = 1024;   // the streaming scorer keeps a per-sequence page prefix on chip
 size_t indexer_decode_workspace_bytes(int B, int maxPagesPerSeq, int ratio, int budget);
 cudaError_t launch_indexer_decode(const QsaIndexerDecodeParams& p, const RopeFreqs& rf,
                                   const CUtensorMap& kbarMap);
