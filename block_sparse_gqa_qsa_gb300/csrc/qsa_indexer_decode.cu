@@ -14,12 +14,12 @@
 //       a producer warp streams the key tails of every page that holds
 //       complete blocks (3-D TMA copies, box {64, 128/r, 1} with the 128-byte
 //       swizzle over a strided view of the pool, page ids fetched 32 at a time)
-//       into a 24-stage ring; consumer warps score one page each on the
-//       tensor cores (mma m16n8k16: 16 block keys x 8 index heads per step,
-//       q split into fp16 hi + lo parts, fp32 accumulation), apply relu per
-//       head and sum over heads, write the scores and add them to a 4096-bin
-//       histogram of the score bits per sequence.  Pages are split evenly
-//       over the CTAs.
+//       into a 24-stage ring; 15 consumer warps score one page each: 16 lanes
+//       per key, 8 dims x 8 heads per lane (dims paired in fp32x2 FMAs), then
+//       a transposing shuffle reduction whose head order is pre-permuted per
+//       lane (h ^ m) so that every step is one add of one shuffle; they write
+//       the scores and add them to a 4096-bin histogram of the score bits per
+//       sequence.  Pages are split evenly over the CTAs.
 //   decode_select_kernel  (B3) per sequence: the histogram gives the bin that
 //       holds the budget-th largest score; CTAs over 2048-block slices collect
 //       the blocks above that bin and the blocks inside it (gathered in shared
@@ -40,7 +40,7 @@ constexpr int kNumBins = 4096;       // histogram of (score bits >> 19): exponen
 constexpr int kBinShift = 19;
 constexpr int kSliceBlocks = 2048;   // blocks one select CTA filters (8 per thread, one round of loads)
 constexpr int kMaxSelect = 4096;     // budget cap: the final CTA sorts the kept block ids in shared memory
-constexpr int kConsumerWarps = 8;   // + 1 producer warp
+constexpr int kConsumerWarps = 15;  // + 1 producer warp = 16 warps, up to 128 registers each
 constexpr int kScoreThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 24;
 constexpr int kSelThreads = 256;
@@ -346,33 +346,28 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
     return;
   }
 
-  // ---- consumers: warp w scores pages lo + w, lo + w + kConsumerWarps, ... on the tensor cores.
-  // Per 16 blocks, S[block][head] = K[block][:] . q[head][:] is a 16x8 m16n8k16 product with the
-  // block keys as A (ldmatrix from the swizzled tile) and the 8 index heads as N.  q is carried
-  // as two fp16 parts, hi = fp16(q) and lo = fp16(q - hi), both multiplied by the exact fp16 key
-  // into one fp32 accumulator, so q keeps ~22 of its 24 bits.
-  constexpr int KS = DI / 16;
-  uint32_t qh[KS][2], ql[KS][2];
+  // ---- consumers: warp w takes pages lo + w, lo + w + kConsumerWarps, ...; 16 lanes per key
+  constexpr int LPB = DI / 8, BPW = 32 / LPB, LOGL = LPB == 16 ? 4 : 3;
+  const int sub = lane % LPB;
+  const int m = (sub >> (LOGL - 3)) & 7;
+  uint64_t q2[8][4];
   int cached_b = -1, n_c = 0;
   int b = 0;
   float* myscr = reinterpret_cast<float*>(pref + (a.B + 1 + 3) / 4 * 4) + warp * 128;
-  const int arow = ((lane >> 3) & 1) * 8 + (lane & 7), achunk = lane >> 4;
   for (long long i = lo + warp; i < hi; i += kConsumerWarps) {
     while (i >= pref[b + 1]) ++b;
     const int p = static_cast<int>(i - pref[b]);
     const int jx = static_cast<int>(i - lo), s = jx % kStages, n = jx / kStages;
     if (b != cached_b) {
-      const float* qn = a.q + (static_cast<size_t>(b) * 8 + (lane >> 2)) * 128 + 2 * (lane & 3);
+      const float* qb = a.q + static_cast<size_t>(b) * 8 * 128;
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const float2 x = *reinterpret_cast<const float2*>(qn + ks * 16 + j * 8);
-          const __half2 h = __floats2half2_rn(x.x, x.y);
-          const float2 hf = __half22float2(h);
-          qh[ks][j] = *reinterpret_cast<const uint32_t*>(&h);
-          ql[ks][j] = pack_half2(x.x - hf.x, x.y - hf.y);
-        }
+      for (int h = 0; h < 8; ++h) {
+        const float4 x0 = *reinterpret_cast<const float4*>(qb + (h ^ m) * 128 + sub * 8);
+        const float4 x1 = *reinterpret_cast<const float4*>(qb + (h ^ m) * 128 + sub * 8 + 4);
+        q2[h][0] = pack_f2(x0.x, x0.y);
+        q2[h][1] = pack_f2(x0.z, x0.w);
+        q2[h][2] = pack_f2(x1.x, x1.y);
+        q2[h][3] = pack_f2(x1.z, x1.w);
       }
       n_c = max(0, min(a.ctx[b], MAXL)) / a.ratio;
       cached_b = b;
@@ -381,27 +376,38 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
       if (lane == 0) atomicOr(a.status, kErrWaitTimeout);
       break;
     }
-    const uint32_t tile = smem_addr(ring + s * stage_bytes);
-    for (int mt = 0; mt * 16 < bpp; ++mt) {
-      const int r = (mt * 16 + arow) & (bpp - 1);  // with 8 blocks a page, rows 8..15 repeat 0..7
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint8_t* tile = ring + s * stage_bytes;
+#pragma unroll 2
+    for (int pass = 0; pass < bpp / BPW; ++pass) {
+      const int blk = pass * BPW + lane / LPB;
+      const uint4 raw = *reinterpret_cast<const uint4*>(tile + (sub >> 3) * bpp * 128 + swz128(blk, sub & 7));
+      const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+      uint64_t kp[4];
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        uint32_t af[4];
-        ldsm_x4(tile + (ks >> 2) * bpp * 128 + swz128(r, (ks & 3) * 2 + achunk), af[0], af[1], af[2], af[3]);
-        mma16816(c, af, qh[ks][0], qh[ks][1]);
-        mma16816(c, af, ql[ks][0], ql[ks][1]);
+      for (int jj = 0; jj < 4; ++jj) {
+        const float2 f = __half22float2(h2[jj]);
+        kp[jj] = pack_f2(f.x, f.y);
       }
-      // c0, c1: block mt*16 + lane/4, heads 2(lane%4) + {0,1}; c2, c3: the block 8 rows down
-      float s0 = fmaxf(c[0], 0.f) + fmaxf(c[1], 0.f), s1 = fmaxf(c[2], 0.f) + fmaxf(c[3], 0.f);
-      s0 += __shfl_xor_sync(kFull, s0, 1);
-      s1 += __shfl_xor_sync(kFull, s1, 1);
-      s0 += __shfl_xor_sync(kFull, s0, 2);
-      s1 += __shfl_xor_sync(kFull, s1, 2);
-      if ((lane & 3) == 0) {
-        myscr[mt * 16 + (lane >> 2)] = s0;
-        myscr[mt * 16 + 8 + (lane >> 2)] = s1;
+      float d[8];
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        uint64_t acc = ffma2(q2[h][0], kp[0], 0ull);
+        acc = ffma2(q2[h][1], kp[1], acc);
+        acc = ffma2(q2[h][2], kp[2], acc);
+        acc = ffma2(q2[h][3], kp[3], acc);
+        d[h] = lo_f2(acc) + hi_f2(acc);
       }
+#pragma unroll
+      for (int i2 = 0; i2 < 4; ++i2) d[i2] += __shfl_xor_sync(kFull, d[i2 + 4], LPB / 2);
+#pragma unroll
+      for (int i2 = 0; i2 < 2; ++i2) d[i2] += __shfl_xor_sync(kFull, d[i2 + 2], LPB / 4);
+      d[0] += __shfl_xor_sync(kFull, d[1], LPB / 8);
+      if (LPB == 16) d[0] += __shfl_xor_sync(kFull, d[0], 1);
+      float sc = d[0] > 0.f ? d[0] : 0.f;
+      sc += __shfl_xor_sync(kFull, sc, LPB / 8);
+      sc += __shfl_xor_sync(kFull, sc, LPB / 4);
+      sc += __shfl_xor_sync(kFull, sc, LPB / 2);
+      if (sub == 0) myscr[blk] = sc;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
