@@ -107,7 +107,13 @@ typedef struct {
  * r*g .. t-1 plus the new raw key and stores it in the V-row tail of token r*g.
  * No other pool byte is written.  Then it scores every complete block and
  * writes the row's list exactly as the prefill indexer would for row t.
- * A sequence with L == 0 gets an all -1 list and no pool write. */
+ * A sequence with L == 0 gets an all -1 list and no pool write.
+ * Device-side errors do not fault: the first int32 of the workspace is a
+ * status word that the kernels OR bits into and never clear -- bit 0: a
+ * wait on a TMA copy ran past 0.2 s and the scorer stopped early (the lists
+ * of that call are then not valid); bit 1: a page id outside
+ * [0, numFlatPages) was met and skipped.  Limits: batchSize <= 1024,
+ * budget <= 4096, compressRatio 4, 8 or 16. */
 typedef struct {
   const void* idxQ;              /* fp16 [B, numHeads, headDim] raw index query of the new token */
   const void* idxK;              /* fp16 [B, headDim] raw index key of the new token             */
@@ -131,8 +137,8 @@ typedef struct {
   int32_t numHeads;              /* indexer heads Hi, 1..8                                         */
   int32_t headDim;               /* indexer head dim di: 64 or 128                                 */
   int32_t rotDim;
-  int32_t compressRatio;         /* r; must divide 128                                              */
-  int32_t budget;
+  int32_t compressRatio;         /* r: 4, 8 or 16 (divides the 128-token page)                     */
+  int32_t budget;                /* 1..4096                                                        */
   int32_t topK;                  /* >= budget*r + r - 1                                            */
   float ropeTheta;
   float rmsNormEps;
