@@ -83,7 +83,8 @@ def lib() -> ctypes.CDLL:
             for name, st in (("qsa_indexer_prefill", QsaIndexerPrefillParams),
                              ("qsa_indexer_decode", QsaIndexerDecodeParams),
                              ("qsa_sparse_prefill", QsaSparsePrefillParams),
-                             ("qsa_sparse_decode", QsaSparseDecodeParams)):
+                             ("qsa_sparse_decode", QsaSparseDecodeParams),
+                             ("qsa_sparse_decode_noalloc", QsaSparseDecodeParams)):
                 f = getattr(L, name)
                 f.argtypes = [ctypes.POINTER(st)]
                 f.restype = ctypes.c_int
@@ -227,3 +228,22 @@ def sparse_decode(q, pool, page_table, indices, ctx, out, partial_o, partial_sta
         headDim=D, poolHeadDim=phd, numFlatPages=nflat, maxPagesPerSeq=page_table.shape[-1], topK=topK,
         attentionScale=scale, stream=_stream(stream))
     _check(lib().qsa_sparse_decode(ctypes.byref(p)))
+
+
+def sparse_decode_noalloc(q, pool, page_table, indices, ctx, out, *, D, scale, stream=None):
+    """qsa_sparse_decode_noalloc: sparse_decode with the library's own fixed scratch (no workspace
+    arguments; batch * KV heads <= 256).  Concurrent calls on one GPU race on that scratch."""
+    B = q.shape[0]
+    Hq = q.shape[-2]
+    nflat, tpp, Hkv, phd = pool.shape
+    topK = indices.shape[-1]
+    if q.numel() != B * Hq * D or out.numel() != B * Hq * D or indices.numel() != B * topK or tpp != 128:
+        raise ValueError("sparse_decode_noalloc: shape mismatch")
+    p = QsaSparseDecodeParams(
+        qPtr=_ptr(q, torch.float16, "q"), kvPoolPtr=_ptr(pool, torch.float16, "kvPool"),
+        pageTable=_ptr(page_table, torch.int32, "pageTable"), indices=_ptr(indices, torch.int32, "indices"),
+        contextLengths=_ptr(ctx, torch.int32, "contextLengths"), oPtr=_ptr(out, torch.float16, "out"),
+        partialO=None, partialStats=None, splitCounters=None, batchSize=B, numQHeads=Hq, numKVHeads=Hkv,
+        headDim=D, poolHeadDim=phd, numFlatPages=nflat, maxPagesPerSeq=page_table.shape[-1], topK=topK,
+        attentionScale=scale, stream=_stream(stream))
+    _check(lib().qsa_sparse_decode_noalloc(ctypes.byref(p)))

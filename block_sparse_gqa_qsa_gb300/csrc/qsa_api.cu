@@ -33,6 +33,12 @@ qsa_status_t cuda_fail(cudaError_t e, const char* what) {
   return fail(QSA_ERR_CUDA, "%s: CUDA error %d (%s)", what, static_cast<int>(e), cudaGetErrorString(e));
 }
 
+}  // namespace
+
+qsa_status_t qsa::record_error(qsa_status_t s, const char* msg) { return fail(s, "%s", msg); }
+
+namespace {
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 qsa::RopeFreqs rope_freqs(float theta, int rot) {

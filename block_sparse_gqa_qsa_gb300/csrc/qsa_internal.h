@@ -34,4 +34,7 @@ cudaError_t launch_indexer_decode(const QsaIndexerDecodeParams& p, const RopeFre
 cudaError_t launch_sparse_prefill(const QsaSparsePrefillParams& p);
 cudaError_t launch_sparse_decode(const QsaSparseDecodeParams& p);
 
+// Stores msg as the calling thread's qsa_last_error_message() and returns s.
+qsa_status_t record_error(qsa_status_t s, const char* msg);
+
 }  // namespace qsa

@@ -210,6 +210,29 @@ QSA_API qsa_status_t qsa_indexer_decode(const QsaIndexerDecodeParams* params);
 QSA_API qsa_status_t qsa_sparse_prefill(const QsaSparsePrefillParams* params);
 QSA_API qsa_status_t qsa_sparse_decode(const QsaSparseDecodeParams* params);
 
+/* Split-K sparse decode with no caller workspace.  The pages have no
+ * counterpart to this entry point.  It serves callers that cannot hand device
+ * memory to a library call on their decode path: an engine whose memory is
+ * planned once up front and offers plugins no workspace, or a serving loop
+ * that must not reach an allocator per token (an allocator may synchronise
+ * the device, or fail under memory pressure, in the middle of a step).
+ *
+ * It computes exactly what qsa_sparse_decode computes, with these differences:
+ *   - partialO, partialStats and splitCounters must be NULL.  The fp32
+ *     partials and the split counters live in one fixed scratch array inside
+ *     the library (16.25 MiB of device memory per GPU, placed by the driver
+ *     when the library's code is loaded onto that GPU).  It holds
+ *     batchSize * numKVHeads <= 256 (sequence, KV head) pairs at headDim 128;
+ *     larger shapes return QSA_ERR_UNSUPPORTED and launch nothing.
+ *   - The first call on each GPU (made with that GPU current) looks up the
+ *     scratch's address and clears its counters on `stream`.  Make that first
+ *     call before any stream capture.  Later calls only launch the kernels.
+ *   - All calls on one GPU within a process share that scratch.  Two calls
+ *     whose kernels may run at the same time (different streams, or
+ *     different threads) race and corrupt each other's outputs: issue them on
+ *     one stream. */
+QSA_API qsa_status_t qsa_sparse_decode_noalloc(const QsaSparseDecodeParams* params);
+
 /* Workspace bytes of the indexers (0 when the sizes are invalid). */
 QSA_API size_t qsa_indexer_prefill_workspace_size(int32_t batchSize, int32_t seqLen, int32_t headDim,
                                           int32_t compressRatio);
