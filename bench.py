@@ -88,24 +88,33 @@ def decode_work(cfg, ctx):
 
 # ------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi sampling during the timed region (read-only queries)."""
-    FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active"
+    """nvidia-smi sampling (read-only queries) around the timed regions.
+
+    The sampler runs from before the warm-up to after the last timed region;
+    `window()` brackets each timed region with host timestamps, and the summary
+    keeps the samples that fall inside a window (all samples if the windows are
+    too short to contain one, which the summary then says)."""
+    FIELDS = "timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active"
 
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.windows = []
+        self.lines = []
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.5)  # let the first samples arrive before anything is timed
         except Exception:
             self.proc = None
         return self
 
     def __exit__(self, *a):
         if self.proc:
+            time.sleep(0.2)
             self.proc.terminate()
             try:
                 out, _ = self.proc.communicate(timeout=5)
@@ -113,24 +122,43 @@ class ClockSampler:
                 self.proc.kill()
                 out = ""
             self.lines = [ln for ln in out.splitlines() if ln.strip()]
-        else:
-            self.lines = []
+
+    class _Window:
+        def __init__(self, owner):
+            self.owner = owner
+
+        def __enter__(self):
+            self.t0 = time.time()
+
+        def __exit__(self, *a):
+            self.owner.windows.append((self.t0, time.time()))
+
+    def window(self):
+        return ClockSampler._Window(self)
 
     def summary(self):
-        sm, mx, reasons = [], [], 0
-        for ln in getattr(self, "lines", []):
+        import datetime
+        rows = []
+        for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-                reasons |= int(parts[3], 16) if parts[3].startswith("0x") else int(parts[3])
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                r = int(parts[4], 16) if parts[4].startswith("0x") else int(parts[4])
+                rows.append((ts, float(parts[1]), float(parts[2]), r))
             except (ValueError, IndexError):
                 pass
+        inside = [r for r in rows if any(t0 - 0.05 <= r[0] <= t1 + 0.05 for t0, t1 in self.windows)]
+        use = inside or rows
         names = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
                  0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
                  0x100: "display_clock_setting"}
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": [n for b, n in names.items() if reasons & b], "samples": len(sm)}
+        reasons = 0
+        for r in use:
+            reasons |= r[3]
+        return {"sm_mhz": statistics.median(r[1] for r in use) if use else None,
+                "sm_max_mhz": max(r[2] for r in use) if use else None,
+                "reasons": [n for bit, n in names.items() if reasons & bit], "samples": len(use),
+                "samples_in_timed_windows": len(inside)}
 
 
 # ------------------------------------------------------------------ our arm
@@ -178,7 +206,7 @@ class Decode:
                               scale=f32(c.scale))
 
 
-def time_decode(dec, flush, reps=50, warm=10):
+def time_decode(dec, flush, clk, reps=50, warm=10):
     for _ in range(3):
         dec.step()
     torch.cuda.synchronize()
@@ -189,14 +217,15 @@ def time_decode(dec, flush, reps=50, warm=10):
         g.replay()
     torch.cuda.synchronize()
     times = []
-    for _ in range(reps):
-        flush.add_(1)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        g.replay()
-        e1.record()
-        e1.synchronize()
-        times.append(e0.elapsed_time(e1) * 1000.0)
+    with clk.window():
+        for _ in range(reps):
+            flush.add_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1) * 1000.0)
     return statistics.median(times), times
 
 
@@ -207,6 +236,8 @@ def run_ours(args, rank, world, dev):
     cfg = HEADLINE
     pf = Prefill(cfg, dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    clk = ClockSampler(torch.cuda.current_device())
+    clk.__enter__()
     for _ in range(max(args.warmup, 3)):
         pf.indexer()
         pf.attention()
@@ -215,7 +246,7 @@ def run_ours(args, rank, world, dev):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_idx, t_att, t_step = [], [], []
-    with ClockSampler(torch.cuda.current_device()) as clk:
+    with clk.window():
         for _ in range(args.steps):
             flush.add_(1)  # L2 flush, outside the timed events
             e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
@@ -248,6 +279,9 @@ def run_ours(args, rank, world, dev):
     d2h = out_host.numel() * out_host.element_size()
     e2e_ms = []
     for i in range(max(args.steps // 2, 3) + 2):
+        if i == 2:
+            w = clk.window()
+            w.__enter__()
         flush.add_(1)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
@@ -260,19 +294,21 @@ def run_ours(args, rank, world, dev):
         e1.synchronize()
         if i >= 2:
             e2e_ms.append(e0.elapsed_time(e1))
+    w.__exit__(None, None, None)
     e2e_value = world * tok / (statistics.mean(e2e_ms) / 1000.0)
 
     # decode workloads: one graph replay per step
     decode = []
     for dc in DECODES:
         dec = Decode(dc, dev)
-        us, _ = time_decode(dec, flush)
+        us, _ = time_decode(dec, flush, clk)
         kbar, kv, total = decode_work(dc, dec.ctx_host.tolist())
         decode.append({"workload": dc.name, "us_per_step": round(us, 2), "bytes_per_step": total,
                        "roofline_us": round(total / (hbm_peak * 1e9) * 1e6, 2),
-                       "frac": round(total / (hbm_peak * 1e9) * 1e6 / us, 4), "kernels_per_step": 2})
+                       "frac": round(total / (hbm_peak * 1e9) * 1e6 / us, 4), "kernels_per_step": 4})
         del dec
         torch.cuda.empty_cache()
+    clk.__exit__(None, None, None)
     return {
         "value": value, "ms": ms, "tok": tok, "t_idx": statistics.mean(t_idx), "t_att": att_ms,
         "achieved": achieved, "gbytes": gbytes, "flops": flops, "cnt": cnt, "hbm_peak": hbm_peak,
