@@ -48,6 +48,25 @@ def f32(x):
     return float(np.float32(x))
 
 
+# DRAM read+write bytes of one sparse_prefill_kernel launch on the 8K prefill workload, from the ncu
+# capture summarised in profiles/sparse_prefill_kernel__prefill_S8192.md.  Reported only while the
+# kernel's sources hash to the value they had when the counters were taken.
+PROFILED_TRAFFIC = {"bytes": 201_838_080, "sources": ("qsa_attention.cu", "qsa_device.cuh"),
+                    "sha256": "38119e0ee8d81749ce9f93e3afc958ae7be1d37e40dc7cf0ed991272112d0975"}
+
+
+def profiled_traffic():
+    import hashlib
+    h = hashlib.sha256()
+    try:
+        for name in PROFILED_TRAFFIC["sources"]:
+            with open(os.path.join(ROOT, "block_sparse_gqa_qsa_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+    except OSError:
+        return None
+    return PROFILED_TRAFFIC["bytes"] if h.hexdigest() == PROFILED_TRAFFIC["sha256"] else None
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -408,7 +427,7 @@ def main():
             "stages_ms": {"indexer_prefill": round(r["t_idx"], 4), "sparse_prefill": round(r["t_att"], 4)},
             "roofline": {"kernel": "sparse_prefill_kernel", "bound": "hbm", "achieved": round(r["achieved"], 1),
                          "peak": r["hbm_peak"], "unit": "GB/s", "frac": round(r["achieved"] / r["hbm_peak"], 4),
-                         "traffic": None, "algorithmic_bytes": r["gbytes"], "sum_cnt": r["cnt"],
+                         "traffic": profiled_traffic(), "algorithmic_bytes": r["gbytes"], "sum_cnt": r["cnt"],
                          "peak_source": r["peak_kind"],
                          "note": "gathered K/V rows are largely L2 hits, so frac may exceed 1"},
             "decode": r["decode"],
