@@ -186,7 +186,7 @@ struct PrefillArgs {
 };
 
 template <int NT, int STAGES>
-__global__ void __launch_bounds__(kThreads, 2) sparse_prefill_kernel(const PrefillArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) sparse_prefill_kernel(const PrefillArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t ring = smem_addr(smem);                       // [STAGES][K 16 KB | V 16 KB]
   const uint32_t q_tile = ring + STAGES * 2 * kTileBytes;      // [8*NT][256 B]
@@ -229,16 +229,18 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_prefill_kernel(const Prefi
   const int ntiles = (nslots + kKeys - 1) / kKeys;
 
   const size_t kv_b = static_cast<size_t>(b) * a.S;
+  // 16 consecutive lanes copy one 256-byte row, so every warp instruction reads
+  // whole 128-byte lines (two rows of K, then the same two rows of V).
   auto issue = [&](int tile, int stage) {
-    const int key = tid >> 1, part = tid & 1;
-    const int j = idx_s[tile * kKeys + key];
-    const bool ok = j >= 0;
-    const size_t row = ((kv_b + (ok ? j : 0)) * a.Hkv + kvh) * kD;
     const uint32_t kdst = ring + stage * 2 * kTileBytes;
     const uint32_t vdst = kdst + kTileBytes;
+    const int ch = tid & 15;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const int ch = part * 8 + c;
+    for (int r = 0; r < kKeys / 8; ++r) {
+      const int key = r * 8 + (tid >> 4);
+      const int j = idx_s[tile * kKeys + key];
+      const bool ok = j >= 0;
+      const size_t row = ((kv_b + (ok ? j : 0)) * a.Hkv + kvh) * kD;
       cp_async16(kdst + swz(key, ch), a.k + row + ch * 8, ok);
       cp_async16(vdst + swz(key, ch), a.v + row + ch * 8, ok);
     }
@@ -350,15 +352,15 @@ __global__ void __launch_bounds__(kThreads, 3) sparse_decode_kernel(const Decode
   const int nslots = max(max(misc[0], misc[1]), max(misc[2], misc[3])) + 1;
   const int ntiles = (nslots + kKeys - 1) / kKeys;
 
-  auto issue = [&](int tile, int stage) {
-    const int key = tid >> 1, part = tid & 1;
-    const long long ko = kofs[tile * kKeys + key], vo = vofs[tile * kKeys + key];
-    const bool ok = ko >= 0;
+  auto issue = [&](int tile, int stage) {  // one 256-byte row per 16 lanes, as in prefill
     const uint32_t kdst = ring + stage * 2 * kTileBytes;
     const uint32_t vdst = kdst + kTileBytes;
+    const int ch = tid & 15;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const int ch = part * 8 + c;
+    for (int r = 0; r < kKeys / 8; ++r) {
+      const int key = r * 8 + (tid >> 4);
+      const long long ko = kofs[tile * kKeys + key], vo = vofs[tile * kKeys + key];
+      const bool ok = ko >= 0;
       cp_async16(kdst + swz(key, ch), a.pool + (ok ? ko : 0) + ch * 8, ok);
       cp_async16(vdst + swz(key, ch), a.pool + (ok ? vo : 0) + ch * 8, ok);
     }
@@ -445,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 3) sparse_decode_kernel(const Decode
   if (tid == 0) a.counters[b * a.Hkv + kvh] = 0;
 }
 
-constexpr int kPrefillStages = 3;
+constexpr int kPrefillStages = 2;  // 74 KB of shared memory: 3 CTAs per SM
 constexpr int kDecodeStages = 2;
 
 template <int NT>
