@@ -166,56 +166,6 @@ __device__ __forceinline__ int cta_exclusive_scan(int v, int* scratch, int& tota
   return base + x - v;
 }
 
-// ------------------------------------------------------------ top-k select
-// Deterministic top-`budget` selection by (key desc, id asc) over a CTA.
-// Thread i holds elements [i*VPT, i*VPT + VPT) of an id-ascending sequence;
-// only the first `nv` (<= VPT) of a thread's elements are valid.  Keys are
-// the bit patterns of non-negative floats, so unsigned order is value order.
-// The threshold T (the budget-th largest key) is found by bisection on the
-// key space with one CTA-wide count per step; keys > T are kept, and of the
-// keys == T the lowest ids (a prefix in thread order) fill the rest.
-// Requires total valid elements > budget.  Sets sel[v] for kept elements.
-template <int NT, int VPT>
-__device__ __forceinline__ void cta_topk(const uint32_t (&key)[VPT], int nv, int budget, bool (&sel)[VPT],
-                                         int* red, int* scratch) {
-  int phase = 0;
-  uint32_t lo = 0u, hi = 0x7f800001u;  // count(>= lo) >= budget > count(>= hi)
-  int cnt_hi = 0;
-  while (hi - lo > 1u) {
-    const uint32_t mid = lo + ((hi - lo) >> 1);
-    int c = 0;
-#pragma unroll
-    for (int v = 0; v < VPT; ++v) c += (v < nv && key[v] >= mid) ? 1 : 0;
-    const int tot = cta_sum<NT>(c, red, phase);
-    if (tot >= budget) {
-      lo = mid;
-    } else {
-      hi = mid;
-      cnt_hi = tot;
-    }
-  }
-  const uint32_t T = lo;
-  const int need = budget - cnt_hi;  // how many keys equal to T are kept
-  int eq = 0;
-#pragma unroll
-  for (int v = 0; v < VPT; ++v) eq += (v < nv && key[v] == T) ? 1 : 0;
-  int tot_eq;
-  int rank = cta_exclusive_scan<NT>(eq, scratch, tot_eq);
-#pragma unroll
-  for (int v = 0; v < VPT; ++v) {
-    bool s = false;
-    if (v < nv) {
-      if (key[v] > T) {
-        s = true;
-      } else if (key[v] == T) {
-        s = rank < need;
-        ++rank;
-      }
-    }
-    sel[v] = s;
-  }
-}
-
 // ------------------------------------------------------------------- RoPE
 // cos/sin of the f64 angle pos * inv_freq, reduced to [-pi, pi] first (2 pi in
 // two parts, each product taken with one rounding by fma) so that the f64

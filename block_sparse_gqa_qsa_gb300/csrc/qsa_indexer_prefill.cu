@@ -13,9 +13,11 @@
 //                          scores on the CUDA cores (fp32 FMA, a register-tiled
 //                          contraction of 8 rows x 8 heads against 256-block
 //                          tiles staged in shared memory), the relu/head sum,
-//                          then per row a deterministic top-`budget` select and
-//                          the expansion into the row's index list.  A row
-//                          group's scores never leave shared memory.
+//                          then one warp per row: a deterministic top-`budget`
+//                          select (bisection on the score bits with warp
+//                          reductions, exact ties to the lower block id) and
+//                          the expansion into the row's ascending index list.
+//                          A row group's scores never leave shared memory.
 #include "qsa_device.cuh"
 #include "qsa_internal.h"
 
@@ -108,8 +110,7 @@ constexpr int kHI = 8;                      // heads per thread tile (Hi <= 8, e
 template <int DI, int VPT>
 constexpr size_t select_smem_bytes() {
   return sizeof(float) * (static_cast<size_t>(DI) * kRows * kHI + 2 * kTile * kKS + kRows * kThreads * VPT +
-                          kRows * DI + kRows * 128) +
-         sizeof(int) * 32;
+                          kRows * DI + kRows * 128);
 }
 
 template <int DI, int VPT>
@@ -121,9 +122,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_select_kernel(const SelAr
   float* sc_s = kb_s + 2 * kTile * kKS;       // [kRows][NBMAX]   block scores
   float* ys_s = sc_s + kRows * NBMAX;         // [kRows][DI]      per-warp RoPE scratch
   float* cs_s = ys_s + kRows * DI;            // [kRows][64][2]   cos/sin per row
-  int* red = reinterpret_cast<int*>(cs_s + kRows * 128);
-  int* scan = red + 16;
-  int* list_s = reinterpret_cast<int*>(kb_s);  // list staging after scoring
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.y;
@@ -276,43 +274,65 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_select_kernel(const SelAr
     __syncthreads();
   }
 
-  // ------------------------------------------------ select + expand per row
-  for (int r = 0; r < nlive; ++r) {
-    const int t = t0 + r;
+  // ------------------------------------ select + expand, one warp per row
+  // Lane l holds the scores of blocks l + 32 m.  Keys are the score bits + 1
+  // (order-preserving for scores >= 0; 0 marks blocks past the row's n_c).
+  // Bisection on the key finds T with count(key >= T) >= budget >
+  // count(key > T); the blocks above T are kept, and of those equal to T the
+  // lowest ids, so the kept set is the top `budget` by (score desc, id asc).
+  // Walking m upwards visits ids in ascending order, so ballots compact the
+  // kept blocks straight into the ascending list.
+  if (warp < nlive) {
+    constexpr int KPL = NBMAX / 32;
+    const int t = t0 + warp;
     const int n_c = (t + 1) / a.ratio;
     int32_t* out = ind_b + static_cast<size_t>(t) * a.topK;
     if (n_c <= a.budget) {  // every block kept: the row lists 0..t
-      for (int i = tid; i < a.topK; i += kThreads) out[i] = i <= t ? i : -1;
-      continue;
-    }
-    const int base = tid * VPT;
-    const int nv = max(0, min(VPT, n_c - base));
-    uint32_t key[VPT];
+      for (int i = lane; i < a.topK; i += 32) out[i] = i <= t ? i : -1;
+    } else {
+      uint32_t key[KPL];
 #pragma unroll
-    for (int v = 0; v < VPT; ++v) key[v] = v < nv ? __float_as_uint(sc_s[r * NBMAX + base + v]) : 0u;
-    bool sel[VPT];
-    cta_topk<kThreads, VPT>(key, nv, a.budget, sel, red, scan);
-    int ns = 0;
+      for (int m = 0; m < KPL; ++m) {
+        const int g = lane + 32 * m;
+        key[m] = g < n_c ? __float_as_uint(sc_s[warp * NBMAX + g]) + 1u : 0u;
+      }
+      uint32_t lo = 1u, hi = 0x80000001u;  // count(>= lo) >= budget > count(>= hi)
+      int c_hi = 0;
+      while (hi - lo > 1u) {
+        const uint32_t mid = lo + ((hi - lo) >> 1);
+        int c = 0;
 #pragma unroll
-    for (int v = 0; v < VPT; ++v) ns += sel[v] ? 1 : 0;
-    int tot;
-    int pos = cta_exclusive_scan<kThreads>(ns, scan, tot);
+        for (int m = 0; m < KPL; ++m) c += key[m] >= mid ? 1 : 0;
+        c = static_cast<int>(__reduce_add_sync(kFull, static_cast<unsigned>(c)));
+        if (c >= a.budget) {
+          lo = mid;
+        } else {
+          hi = mid;
+          c_hi = c;
+        }
+      }
+      int quota = a.budget - c_hi;  // blocks with key == lo to keep, lowest ids first
+      int pos = 0;
+      const unsigned below = (1u << lane) - 1u;
 #pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-      if (sel[v]) {
-        const int g = base + v;
-        for (int j = 0; j < a.ratio; ++j) list_s[pos * a.ratio + j] = g * a.ratio + j;
-        ++pos;
+      for (int m = 0; m < KPL; ++m) {
+        const bool eq = key[m] == lo;
+        const unsigned eqm = __ballot_sync(kFull, eq);
+        const bool take = key[m] > lo || (eq && __popc(eqm & below) < quota);
+        quota = max(0, quota - __popc(eqm));
+        const unsigned tm = __ballot_sync(kFull, take);
+        if (take) {
+          const int at = (pos + __popc(tm & below)) * a.ratio, g = lane + 32 * m;
+          for (int j = 0; j < a.ratio; ++j) out[at + j] = g * a.ratio + j;
+        }
+        pos += __popc(tm);
+      }
+      const int head = pos * a.ratio;
+      for (int i = head + lane; i < a.topK; i += 32) {
+        const int j = n_c * a.ratio + (i - head);
+        out[i] = j <= t ? j : -1;
       }
     }
-    const int head = tot * a.ratio;
-    for (int i = head + tid; i < a.topK; i += kThreads) {
-      const int j = n_c * a.ratio + (i - head);
-      list_s[i] = j <= t ? j : -1;
-    }
-    __syncthreads();
-    for (int i = tid; i < a.topK; i += kThreads) out[i] = list_s[i];
-    __syncthreads();
   }
 }
 
