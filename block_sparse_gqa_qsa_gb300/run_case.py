@@ -1,0 +1,77 @@
+"""Runs a few steps of one named workload on cuda:0 through the C ABI.
+
+A step is the whole path for that workload: qsa_indexer_prefill +
+qsa_sparse_prefill for a prefill workload, qsa_indexer_decode +
+qsa_sparse_decode for a decode workload.  Inputs come from the seeded
+generators of `synthetic`.  The sizes can be overridden to get a case small
+enough for a profiler's multi-pass capture (a decode pool of a few GB instead
+of tens).
+
+    python -m block_sparse_gqa_qsa_gb300.run_case prefill_S8192 --steps 2
+    python -m block_sparse_gqa_qsa_gb300.run_case decode_long_B8_L512k --B 1 --steps 2
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import math
+
+import torch
+
+from . import _binding as qb
+from . import synthetic as syn
+
+
+def _prefill_steps(cfg, steps):
+    t = {k: v.cuda() for k, v in syn.make_prefill(cfg).items()}
+    ws = qb.alloc_workspace(qb.indexer_prefill_workspace_size(cfg.B, cfg.S, cfg.di, cfg.ratio))
+    ind = torch.empty((cfg.B, cfg.S, cfg.topK), dtype=torch.int32, device="cuda")
+    out = torch.empty((cfg.B, cfg.S, cfg.Hq, cfg.D), dtype=torch.float16, device="cuda")
+    scale = float(torch.tensor(1.0 / math.sqrt(cfg.D), dtype=torch.float32))
+    for _ in range(steps):
+        qb.indexer_prefill(t["idxQ"], t["idxK"], t["wq"], t["wk"], t["ctx"], ind, ws, rot=cfg.rot, ratio=cfg.ratio,
+                           budget=cfg.budget, topK=cfg.topK, theta=cfg.theta, eps=cfg.eps)
+        qb.sparse_prefill(t["q"], t["k"], t["v"], ind, t["ctx"], out, scale)
+
+
+def _decode_steps(cfg, steps):
+    d = syn.make_decode(cfg, device="cuda")
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    ws = qb.alloc_workspace(qb.indexer_decode_workspace_size(cfg.B, cfg.maxPagesPerSeq, cfg.ratio, cfg.budget))
+    po, ps, pc = qb.sparse_decode_workspace_elems(cfg.B, cfg.Hkv, cfg.D)
+    parts = (torch.zeros(po, device="cuda"), torch.zeros(ps, device="cuda"),
+             torch.zeros(pc, dtype=torch.int32, device="cuda"))
+    ind = torch.empty((cfg.B, 1, cfg.topK), dtype=torch.int32, device="cuda")
+    out = torch.empty((cfg.B, 1, cfg.Hq, cfg.D), dtype=torch.float16, device="cuda")
+    scale = float(torch.tensor(1.0 / math.sqrt(cfg.D), dtype=torch.float32))
+    for _ in range(steps):
+        qb.indexer_decode(d["idxQ"], d["idxK"], d["wq"], d["wk"], d["pool"], d["page_table"], d["ctx"], ind, ws,
+                          D=cfg.D, rot=cfg.rot, ratio=cfg.ratio, budget=cfg.budget, topK=cfg.topK, theta=cfg.theta,
+                          eps=cfg.eps)
+        qb.sparse_decode(d["q"], d["pool"], d["page_table"], ind, d["ctx"], out, *parts, D=cfg.D, scale=scale)
+
+
+def main(argv=None):
+    names = {c.name: c for c in syn.BENCH_CONFIGS}
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("workload", choices=sorted(names))
+    ap.add_argument("--steps", type=int, default=2)
+    ap.add_argument("--B", type=int, default=None, help="override the batch size")
+    ap.add_argument("--ctx", type=int, default=None, help="decode: every sequence gets this total length")
+    args = ap.parse_args(argv)
+    cfg = names[args.workload]
+    if args.B is not None:
+        cfg = dataclasses.replace(cfg, B=args.B)
+    qb.lib()
+    if isinstance(cfg, syn.DecodeConfig):
+        if args.ctx is not None:
+            cfg = dataclasses.replace(cfg, ctx_lo=args.ctx, ctx_hi=args.ctx, max_ctx=max(args.ctx, 1), ctx_list=None)
+        _decode_steps(cfg, args.steps)
+    else:
+        _prefill_steps(cfg, args.steps)
+    torch.cuda.synchronize()
+    print(f"ok: {args.steps} steps of {cfg.name} (B={cfg.B})")
+
+
+if __name__ == "__main__":
+    main()
