@@ -184,6 +184,8 @@ qsa_status_t qsa_indexer_decode(const QsaIndexerDecodeParams* p) {
                                      "kvPool 16-byte aligned (TMA rows)");
   if (static_cast<long long>(p->maxPagesPerSeq) * 128 > 0x7fffffffLL)
     return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_decode: maxPagesPerSeq too large");
+  if (static_cast<long long>(p->maxPagesPerSeq) * (qsa::kTokensPerPageHost / p->compressRatio) > (1LL << 21))
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_decode: more than 2097152 blocks per sequence");
   const size_t need = qsa::indexer_decode_workspace_bytes(p->batchSize, p->maxPagesPerSeq, p->compressRatio, p->budget);
   if (!p->workspace || p->workspaceBytes < need || !aligned(p->workspace, 256))
     return fail(QSA_ERR_WORKSPACE, "qsa_indexer_decode: workspace needs %zu bytes, 256-byte aligned", need);

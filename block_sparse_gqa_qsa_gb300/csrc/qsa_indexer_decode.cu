@@ -5,7 +5,8 @@
 //
 // Three launches on the caller's stream:
 //   decode_prep_kernel    (B1) one CTA per sequence: index-query prep at
-//       t = L-1 (fp32, f64 angles) into the workspace; then the state update:
+//       t = L-1 (fp32, f64 angles) into the workspace by 8 warps, and
+//       concurrently, by di/32 more warps, the state update:
 //       the new raw key into token t's K-row tail when t leaves its block
 //       incomplete, else the block t completes is pooled in f64 (from the
 //       K-row tails of its first r-1 tokens and the new key) and its key is
@@ -20,13 +21,15 @@
 //       lane (h ^ m) so that every step is one add of one shuffle; they write
 //       the scores and add them to a 4096-bin histogram of the score bits per
 //       sequence.  Pages are split evenly over the CTAs.
-//   decode_select_kernel  (B3) per sequence: the histogram gives the bin that
-//       holds the budget-th largest score; CTAs over 2048-block slices collect
-//       the blocks above that bin and the blocks inside it (gathered in shared
-//       memory, one global reservation per CTA); the last CTA to finish keeps
-//       the top of the tie bin by (score desc, id asc), sorts the kept ids
-//       (bitonic, in shared memory), expands them with the causal tail, and
-//       re-arms the histogram and counters.
+//   decode_select_kernel  (B3) per sequence: the histogram gives the bin T that
+//       holds the budget-th largest score; one CTA per 2048-block slice writes
+//       the slice's candidates (blocks in bins >= T) in ascending id order
+//       into the slice's own region (no global atomics); the last CTA to
+//       finish finds the exact cut inside bin T with two radix digits of the
+//       score bits in shared memory, keeps the blocks above the cut and, of
+//       those equal to it, the lowest ids, and emits the list by filtering the
+//       already ascending candidates; then the causal tail, and it re-arms
+//       the histogram and its ticket.
 // Waits on TMA barriers are bounded; on expiry the kernel records
 // kErrWaitTimeout in the workspace status word and stops.
 #include "qsa_device.cuh"
@@ -39,21 +42,23 @@ constexpr size_t kStatusBytes = 256;
 constexpr int kNumBins = 4096;       // histogram of (score bits >> 19): exponent + 4 mantissa bits
 constexpr int kBinShift = 19;
 constexpr int kSliceBlocks = 2048;   // blocks one select CTA filters (8 per thread, one round of loads)
-constexpr int kMaxSelect = 4096;     // budget cap: the final CTA sorts the kept block ids in shared memory
+constexpr int kMaxSlices = 1024;     // slices per sequence (blocks <= 2M): their bases live in shared memory
+constexpr int kStageCand = 4096;     // candidates the final CTA stages in shared memory (more: read from L2)
 constexpr int kConsumerWarps = 15;  // + 1 producer warp = 16 warps, up to 128 registers each
 constexpr int kScoreThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 24;
 constexpr int kSelThreads = 256;
-constexpr int kTieVPT = 16;          // tie candidates per thread held in registers
+constexpr int kPrepThreads = 256 + 128;  // 8 query-prep warps + up to 4 state-update warps
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;  // 0.2 s
 constexpr int kMaxDynSmem = 227 * 1024;
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
-  size_t q, scores, hist, sureId, tieKey, tieId, counters, total;
+  size_t q, scores, hist, candKey, candId, sliceCnt, ticket, total;
 };
-WsLayout ws_layout(int B, int nbmax, int budget) {
+WsLayout ws_layout(int B, int nbmax) {
+  const int nsplit = (nbmax + kSliceBlocks - 1) / kSliceBlocks;
   WsLayout l;
   size_t off = kStatusBytes;
   l.q = off;
@@ -62,20 +67,24 @@ WsLayout ws_layout(int B, int nbmax, int budget) {
   off += up256(static_cast<size_t>(B) * nbmax * 4);     // block scores fp32 [B][nbmax]
   l.hist = off;
   off += up256(static_cast<size_t>(B) * kNumBins * 4);  // int32 [B][kNumBins], zero between calls
-  l.sureId = off;
-  off += up256(static_cast<size_t>(B) * budget * 4);    // blocks above the threshold bin [B][budget]
-  l.tieKey = off;
-  off += up256(static_cast<size_t>(B) * nbmax * 4);     // blocks inside it [B][nbmax]
-  l.tieId = off;
+  l.candKey = off;
+  off += up256(static_cast<size_t>(B) * nbmax * 4);     // selection candidates, slice-major [B][nbmax]
+  l.candId = off;
   off += up256(static_cast<size_t>(B) * nbmax * 4);
-  l.counters = off;
-  off += up256(static_cast<size_t>(B) * 3 * 4);         // sure count, tie count, ticket: zero between calls
+  l.sliceCnt = off;
+  off += up256(static_cast<size_t>(B) * nsplit * 4);    // candidates per slice [B][nsplit]
+  l.ticket = off;
+  off += up256(static_cast<size_t>(B) * 4);             // slices done, zero between calls
   l.total = off;
   return l;
 }
 
 __device__ __forceinline__ size_t pool_row(int page, int tok_in_page, int Hkv, int poolHeadDim) {
   return (static_cast<size_t>(page) * kTokensPerPage + tok_in_page) * Hkv * poolHeadDim;  // head 0
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -99,7 +108,7 @@ struct PrepArgs {
 };
 
 template <int DI>
-__global__ void __launch_bounds__(256) decode_prep_kernel(const PrepArgs a) {
+__global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const PrepArgs a) {
   constexpr int PER = DI / 32;
   __shared__ float y_s[8][DI];
   __shared__ double m_s[DI];
@@ -115,8 +124,9 @@ __global__ void __launch_bounds__(256) decode_prep_kernel(const PrepArgs a) {
   const int32_t* ptK = a.pageTable + static_cast<size_t>(b) * 2 * a.maxPagesPerSeq;
   const int32_t* ptV = ptK + a.maxPagesPerSeq;
 
-  // index-query prep: warp h -> head h (heads >= Hi are zero)
-  {
+  // warps 0..7: index-query prep, warp h -> head h (heads >= Hi are zero);
+  // warps 8..: the state update, concurrently (named barrier 1 among them)
+  if (warp < 8) {
     const int h = warp;
     float* qo = a.q + (static_cast<size_t>(b) * 8 + h) * 128;
     if (h < a.Hi) {
@@ -159,15 +169,16 @@ __global__ void __launch_bounds__(256) decode_prep_kernel(const PrepArgs a) {
 #pragma unroll
       for (int p = 0; p < PER; ++p) qo[lane + 32 * p] = 0.f;
     }
+    return;
   }
-
-  // state update
+  const int u = tid - 256;  // dim handled by this thread of the state-update warps
+  const int uw = u >> 5;
   if (!completes) {
-    if (tid < DI) {
+    if (u < DI) {
       const int kp = __ldg(ptK + (t >> 7));
       if (static_cast<unsigned>(kp) < static_cast<unsigned>(a.numFlatPages))
-        a.pool[pool_row(kp, t & 127, a.Hkv, a.poolHeadDim) + a.D + tid] = a.idxK[static_cast<size_t>(b) * DI + tid];
-      else if (tid == 0)
+        a.pool[pool_row(kp, t & 127, a.Hkv, a.poolHeadDim) + a.D + u] = a.idxK[static_cast<size_t>(b) * DI + u];
+      else if (u == 0)
         atomicOr(a.status, kErrBadPage);
     }
     return;
@@ -177,38 +188,38 @@ __global__ void __launch_bounds__(256) decode_prep_kernel(const PrepArgs a) {
   const bool okp = static_cast<unsigned>(kp) < static_cast<unsigned>(a.numFlatPages) &&
                    static_cast<unsigned>(vp) < static_cast<unsigned>(a.numFlatPages);
   if (!okp) {
-    if (tid == 0) atomicOr(a.status, kErrBadPage);
+    if (u == 0) atomicOr(a.status, kErrBadPage);
     return;
   }
   double sq = 0.0;
-  if (tid < DI) {
+  {
     double acc = 0.0;
     for (int j = 0; j < a.ratio; ++j) {
       const int tok = first + j;
-      const __half hv = tok == t ? a.idxK[static_cast<size_t>(b) * DI + tid]
-                                 : a.pool[pool_row(kp, tok & 127, a.Hkv, a.poolHeadDim) + a.D + tid];
+      const __half hv = tok == t ? a.idxK[static_cast<size_t>(b) * DI + u]
+                                 : a.pool[pool_row(kp, tok & 127, a.Hkv, a.poolHeadDim) + a.D + u];
       acc = __dadd_rn(acc, static_cast<double>(__half2float(hv)));
     }
     const double m = __ddiv_rn(acc, static_cast<double>(a.ratio));
-    m_s[tid] = m;
+    m_s[u] = m;
     sq = __dmul_rn(m, m);
   }
-  if (warp < DI / 32) {
+  {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sq = __dadd_rn(sq, __shfl_xor_sync(kFull, sq, o));
-    if (lane == 0) part_s[warp] = sq;
+    if (lane == 0) part_s[uw] = sq;
   }
-  __syncthreads();
-  if (tid < DI) {
+  named_barrier_sync(1, DI);
+  {
     double ss = 0.0;
     for (int w = 0; w < DI / 32; ++w) ss = __dadd_rn(ss, part_s[w]);
     const double inv = __ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(__ddiv_rn(ss, static_cast<double>(DI)),
                                                            static_cast<double>(a.eps))));
-    y2_s[tid] = __dmul_rn(__dmul_rn(m_s[tid], inv), __dadd_rn(1.0, static_cast<double>(a.wk[tid])));
+    y2_s[u] = __dmul_rn(__dmul_rn(m_s[u], inv), __dadd_rn(1.0, static_cast<double>(a.wk[u])));
   }
-  __syncthreads();
-  if (tid < DI) {
-    const int i = tid, half = a.rot >> 1;
+  named_barrier_sync(1, DI);
+  {
+    const int i = u, half = a.rot >> 1;
     const double pos = static_cast<double>(first);
     double r = y2_s[i];
     if (i < half) {
@@ -421,21 +432,93 @@ struct SelectArgs {
   const int32_t* ctx;
   const float* scores;
   int32_t* hist;
-  int32_t* sureId;
-  uint32_t* tieKey;
-  int32_t* tieId;
-  int32_t* counters;  // [B][3]: sure count, tie count, ticket
+  uint32_t* candKey;  // [B][nbmax]: slice s keeps its candidates at [s*kSliceBlocks, ...), ascending ids
+  int32_t* candId;
+  int32_t* sliceCnt;  // [B][nsplitmax]
+  int32_t* ticket;    // [B], zero between calls
   int32_t* indices;
-  int maxPagesPerSeq, ratio, budget, topK, nbmax;
+  int maxPagesPerSeq, ratio, budget, topK, nbmax, nsplitmax;
 };
 
+// Bin T holding the budget-th largest score and the count of blocks in higher
+// bins, from the sequence's histogram (every thread gets both).
+__device__ __forceinline__ void threshold_bin(const int32_t* hrow, int budget, int* scan, int* info, int& T,
+                                              int& c_above) {
+  constexpr int BPT = kNumBins / kSelThreads;
+  const int tid = threadIdx.x;
+  int h[BPT];
+  int own = 0;
+  if (tid == 0) {
+    info[0] = 0;
+    info[1] = 0;
+  }
+  const int4* h4 = reinterpret_cast<const int4*>(hrow + tid * BPT);
+#pragma unroll
+  for (int k = 0; k < BPT / 4; ++k) {
+    const int4 v = __ldcg(h4 + k);
+    h[4 * k] = v.x;
+    h[4 * k + 1] = v.y;
+    h[4 * k + 2] = v.z;
+    h[4 * k + 3] = v.w;
+    own += v.x + v.y + v.z + v.w;
+  }
+  int total;
+  const int excl = cta_exclusive_scan<kSelThreads>(own, scan, total);
+  int running = total - excl - own;  // blocks in the bins of higher threads
+#pragma unroll
+  for (int k = BPT - 1; k >= 0; --k) {
+    if (running < budget && running + h[k] >= budget) {
+      info[0] = tid * BPT + k;
+      info[1] = running;
+    }
+    running += h[k];
+  }
+  __syncthreads();
+  T = info[0];
+  c_above = info[1];
+  __syncthreads();
+}
+
+// Among the values of a CTA-wide histogram `rh` of `nbins` bins (counts of one
+// digit), the digit U such that count(digit > U) < need <= count(digit >= U),
+// and count(digit > U).
+template <int NBINS>
+__device__ __forceinline__ void digit_from_top(const int* rh, int need, int* scan, int* info, int& U, int& above_U) {
+  constexpr int PER = NBINS / kSelThreads;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    info[2] = 0;
+    info[3] = 0;
+  }
+  int own = 0;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) own += rh[tid * PER + k];
+  int total;
+  const int excl = cta_exclusive_scan<kSelThreads>(own, scan, total);
+  int running = total - excl - own;
+#pragma unroll
+  for (int k = PER - 1; k >= 0; --k) {
+    const int c = rh[tid * PER + k];
+    if (running < need && running + c >= need) {
+      info[2] = tid * PER + k;
+      info[3] = running;
+    }
+    running += c;
+  }
+  __syncthreads();
+  U = info[2];
+  above_U = info[3];
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const SelectArgs a) {
-  __shared__ int red[2 * kSelThreads / 32];
   __shared__ int scan[kSelThreads / 32];
   __shared__ int info[8];
-  __shared__ int buf_s[kMaxSelect];            // filter: sure ids | final: kept ids to sort
-  __shared__ uint32_t tkey_s[kSliceBlocks];    // filter: this slice's ties
-  __shared__ int tid_s[kSliceBlocks];
+  __shared__ int wcnt[kSelThreads / 32];
+  __shared__ int sbase[kMaxSlices + 1];
+  __shared__ int rh[1024];
+  __shared__ uint32_t ck_s[kStageCand];
+  __shared__ int ci_s[kStageCand];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int s = blockIdx.x, b = blockIdx.y;
   const int L = max(0, min(a.ctx[b], a.maxPagesPerSeq * kTokensPerPage));
@@ -443,7 +526,6 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
   const int n_c = L / a.ratio;
   int32_t* out = a.indices + static_cast<size_t>(b) * a.topK;
   int32_t* hrow = a.hist + static_cast<size_t>(b) * kNumBins;
-  int32_t* ctr = a.counters + static_cast<size_t>(b) * 3;
   if (L == 0) {
     if (s == 0)
       for (int i = tid; i < a.topK; i += kSelThreads) out[i] = -1;
@@ -459,215 +541,164 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
   const int nsplit = (n_c + kSliceBlocks - 1) / kSliceBlocks;
   if (s >= nsplit) return;
 
-  // ---- the bin holding the budget-th largest score
-  constexpr int BPT = kNumBins / kSelThreads;  // 16 bins per thread
-  int h[BPT];
-  int own = 0;
-#pragma unroll
-  for (int k = 0; k < BPT; ++k) {
-    h[k] = __ldcg(hrow + tid * BPT + k);
-    own += h[k];
-  }
-  if (tid == 0) {
-    info[0] = 0;  // threshold bin
-    info[1] = 0;  // blocks in higher bins
-    info[2] = 0;  // sure blocks gathered by this CTA
-    info[3] = 0;  // ties gathered by this CTA
-  }
-  int total;
-  const int excl = cta_exclusive_scan<kSelThreads>(own, scan, total);
-  int running = total - excl - own;  // blocks in bins of higher threads
-#pragma unroll
-  for (int k = BPT - 1; k >= 0; --k) {
-    if (running < a.budget && running + h[k] >= a.budget) {
-      info[0] = tid * BPT + k;
-      info[1] = running;
-    }
-    running += h[k];
-  }
-  __syncthreads();
-  const int T = info[0], c_above = info[1];
+  int T, c_above;
+  threshold_bin(hrow, a.budget, scan, info, T, c_above);
 
-  // ---- classify this slice: above the bin (kept) or inside it (tie)
+  // ---- candidates of this slice (bin >= T), compacted in ascending id order:
+  // warp w covers blocks g0 + 256 w + [0, 256), visited as lane + 32 m
   const float* srow = a.scores + static_cast<size_t>(b) * a.nbmax;
   const int g0 = s * kSliceBlocks, g1 = min(g0 + kSliceBlocks, n_c);
-  constexpr int U = kSliceBlocks / kSelThreads;
-  uint32_t keys[U];
+  constexpr int M = kSliceBlocks / kSelThreads;
+  uint32_t keys[M];
+  unsigned cm[M];
+  int wc = 0;
 #pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int g = g0 + u * kSelThreads + tid;
-    keys[u] = g < g1 ? __float_as_uint(__ldcg(srow + g)) : 0u;
+  for (int m = 0; m < M; ++m) {
+    const int g = g0 + warp * 32 * M + m * 32 + lane;
+    keys[m] = g < g1 ? __float_as_uint(__ldcg(srow + g)) : 0u;
   }
 #pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int g = g0 + u * kSelThreads + tid;
-    const bool valid = g < g1;
-    const int bin = static_cast<int>(keys[u] >> kBinShift);
-    const bool sure = valid && bin > T, tie = valid && bin == T;
-    const unsigned sm = __ballot_sync(kFull, sure), tm = __ballot_sync(kFull, tie);
-    const unsigned lt = (1u << lane) - 1u;
-    if (sm) {
-      int p0 = 0;
-      if (lane == 0) p0 = atomicAdd(&info[2], __popc(sm));
-      p0 = __shfl_sync(kFull, p0, 0);
-      if (sure) {
-        const int at = p0 + __popc(sm & lt);
-        if (at < kMaxSelect) buf_s[at] = g;
-      }
-    }
-    if (tm) {
-      int p0 = 0;
-      if (lane == 0) p0 = atomicAdd(&info[3], __popc(tm));
-      p0 = __shfl_sync(kFull, p0, 0);
-      if (tie) {
-        const int at = p0 + __popc(tm & lt);
-        tkey_s[at] = keys[u];
-        tid_s[at] = g;
-      }
-    }
+  for (int m = 0; m < M; ++m) {
+    const int g = g0 + warp * 32 * M + m * 32 + lane;
+    cm[m] = __ballot_sync(kFull, g < g1 && static_cast<int>(keys[m] >> kBinShift) >= T);
+    wc += __popc(cm[m]);
   }
+  if (lane == 0) wcnt[warp] = wc;
   __syncthreads();
-  {  // one global reservation per list per CTA
-    const int ns = min(info[2], kMaxSelect), nts = info[3];
-    if (tid == 0) {
-      info[4] = ns ? atomicAdd(ctr + 0, ns) : 0;
-      info[5] = nts ? atomicAdd(ctr + 1, nts) : 0;
-    }
-    __syncthreads();
-    const int as = info[4], at = info[5];
-    for (int e = tid; e < ns; e += kSelThreads)
-      if (as + e < a.budget) a.sureId[static_cast<size_t>(b) * a.budget + as + e] = buf_s[e];
-    for (int e = tid; e < nts; e += kSelThreads) {
-      a.tieKey[static_cast<size_t>(b) * a.nbmax + at + e] = tkey_s[e];
-      a.tieId[static_cast<size_t>(b) * a.nbmax + at + e] = tid_s[e];
-    }
+  int off = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kSelThreads / 32; ++w) {
+    off += w < warp ? wcnt[w] : 0;
+    tot += wcnt[w];
   }
+  uint32_t* ckey = a.candKey + static_cast<size_t>(b) * a.nbmax;
+  int32_t* cid = a.candId + static_cast<size_t>(b) * a.nbmax;
+  const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    if ((cm[m] >> lane) & 1u) {
+      const int at = g0 + off + __popc(cm[m] & below);
+      ckey[at] = keys[m];
+      cid[at] = g0 + warp * 32 * M + m * 32 + lane;
+    }
+    off += __popc(cm[m]);
+  }
+  if (tid == 0) a.sliceCnt[static_cast<size_t>(b) * a.nsplitmax + s] = tot;
   __threadfence();
   __syncthreads();
-  if (tid == 0) info[6] = atomicAdd(ctr + 2, 1) == nsplit - 1;
+  if (tid == 0) info[6] = atomicAdd(a.ticket + b, 1) == nsplit - 1;
   __syncthreads();
   if (!info[6]) return;
   __threadfence();
 
-  // ---- last CTA: kept blocks = the sure ones + the top of the tie bin by (score desc, id asc)
-  const int need = a.budget - c_above;
-  const int nt = __ldcg(ctr + 1);
-  const uint32_t* tk = a.tieKey + static_cast<size_t>(b) * a.nbmax;
-  const int32_t* ti = a.tieId + static_cast<size_t>(b) * a.nbmax;
-  for (int e = tid; e < c_above; e += kSelThreads) buf_s[e] = __ldcg(a.sureId + static_cast<size_t>(b) * a.budget + e);
-  if (tid == 0) info[7] = c_above;  // next free slot of buf_s
-  __syncthreads();
-  auto keep = [&](int id) {
-    const int at = atomicAdd(&info[7], 1);
-    if (at < kMaxSelect) buf_s[at] = id;
-  };
-  if (nt <= need) {
-    for (int e = tid; e < nt; e += kSelThreads) keep(__ldcg(ti + e));
-  } else {
-    // bisection on the score bits inside bin T, then on the id among exact ties at the cut
-    const bool regs = nt <= kTieVPT * kSelThreads;
-    uint32_t key[kTieVPT];
-    int id[kTieVPT];
-    const int nv = regs ? max(0, min(kTieVPT, nt - tid * kTieVPT)) : 0;
+  // ---- last CTA of the sequence: the candidates of all slices, in id order
+  {
+    constexpr int PER = kMaxSlices / kSelThreads;
+    int v[PER], own = 0;
 #pragma unroll
-    for (int v = 0; v < kTieVPT; ++v) {
-      key[v] = v < nv ? __ldcg(tk + tid * kTieVPT + v) : 0u;
-      id[v] = v < nv ? __ldcg(ti + tid * kTieVPT + v) : 0;
+    for (int k = 0; k < PER; ++k) {
+      const int sl = tid * PER + k;
+      v[k] = sl < nsplit ? __ldcg(a.sliceCnt + static_cast<size_t>(b) * a.nsplitmax + sl) : 0;
+      own += v[k];
     }
-    auto count_ge = [&](uint32_t x) {
-      int c = 0;
-      if (regs) {
+    int total;
+    int run = cta_exclusive_scan<kSelThreads>(own, scan, total);
 #pragma unroll
-        for (int v = 0; v < kTieVPT; ++v) c += (v < nv && key[v] >= x) ? 1 : 0;
-      } else {
-        for (int e = tid; e < nt; e += kSelThreads) c += __ldcg(tk + e) >= x ? 1 : 0;
-      }
-      return c;
-    };
-    auto count_eq_le = [&](uint32_t x, int y) {
-      int c = 0;
-      if (regs) {
-#pragma unroll
-        for (int v = 0; v < kTieVPT; ++v) c += (v < nv && key[v] == x && id[v] <= y) ? 1 : 0;
-      } else {
-        for (int e = tid; e < nt; e += kSelThreads) c += (__ldcg(tk + e) == x && __ldcg(ti + e) <= y) ? 1 : 0;
-      }
-      return c;
-    };
-    int phase = 0;
-    uint32_t lo = static_cast<uint32_t>(T) << kBinShift, hi = static_cast<uint32_t>(T + 1) << kBinShift;
-    int cnt_lo = nt, cnt_hi = 0;  // count(>= lo) >= need > count(>= hi)
-    while (hi - lo > 1u) {
-      const uint32_t mid = lo + ((hi - lo) >> 1);
-      const int tot = cta_sum<kSelThreads>(count_ge(mid), red, phase);
-      if (tot >= need) {
+    for (int k = 0; k < PER; ++k) {
+      sbase[tid * PER + k] = run;
+      run += v[k];
+    }
+    if (tid == 0) sbase[kMaxSlices] = total;
+    __syncthreads();
+  }
+  const int ncand = sbase[kMaxSlices];
+  auto locate = [&](int e) {  // flat candidate index -> position in the slice-major arrays
+    int lo = 0, hi = nsplit;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (sbase[mid] <= e)
         lo = mid;
-        cnt_lo = tot;
-      } else {
+      else
         hi = mid;
-        cnt_hi = tot;
-      }
     }
-    const uint32_t Tk = lo;
-    const int n_eq = need - cnt_hi;  // keys equal to Tk to keep, lowest ids first
-    int ilo = -1, ihi = a.nbmax;
-    if (cnt_lo - cnt_hi != n_eq) {
-      while (ihi - ilo > 1) {
-        const int mid = ilo + ((ihi - ilo) >> 1);
-        if (cta_sum<kSelThreads>(count_eq_le(Tk, mid), red, phase) >= n_eq)
-          ihi = mid;
-        else
-          ilo = mid;
-      }
+    return lo * kSliceBlocks + (e - sbase[lo]);
+  };
+  const bool staged = ncand <= kStageCand;
+  if (staged) {
+    for (int e = tid; e < ncand; e += kSelThreads) {
+      const int at = locate(e);
+      ck_s[e] = __ldcg(ckey + at);
+      ci_s[e] = __ldcg(cid + at);
     }
-    if (regs) {
-#pragma unroll
-      for (int v = 0; v < kTieVPT; ++v)
-        if (v < nv && (key[v] > Tk || (key[v] == Tk && id[v] <= ihi))) keep(id[v]);
-    } else {
-      for (int e = tid; e < nt; e += kSelThreads) {
-        const uint32_t k = __ldcg(tk + e);
-        const int i2 = __ldcg(ti + e);
-        if (k > Tk || (k == Tk && i2 <= ihi)) keep(i2);
-      }
-    }
+    __syncthreads();
+  }
+  auto key_at = [&](int e) { return staged ? ck_s[e] : __ldcg(ckey + locate(e)); };
+  auto id_at = [&](int e) { return staged ? ci_s[e] : __ldcg(cid + locate(e)); };
+
+  // ---- the cut inside bin T: two radix digits (bits 18..9, then 8..0)
+  const int need = a.budget - c_above;  // >= 1 blocks of bin T to keep
+  for (int i = tid; i < 1024; i += kSelThreads) rh[i] = 0;
+  __syncthreads();
+  for (int e = tid; e < ncand; e += kSelThreads) {
+    const uint32_t k = key_at(e);
+    if (static_cast<int>(k >> kBinShift) == T) atomicAdd(&rh[(k >> 9) & 1023], 1);
   }
   __syncthreads();
-  // ---- sort the kept ids ascending (bitonic, padded to a power of two), expand with the tail
-  const int nk = min(info[7], kMaxSelect);
-  int np2 = 1;
-  while (np2 < nk) np2 <<= 1;
-  for (int e = nk + tid; e < np2; e += kSelThreads) buf_s[e] = 0x7fffffff;
+  int U, above_U;
+  digit_from_top<1024>(rh, need, scan, info, U, above_U);
+  for (int i = tid; i < 512; i += kSelThreads) rh[i] = 0;
   __syncthreads();
-  for (int k = 2; k <= np2; k <<= 1) {
-    for (int jb = k >> 1; jb > 0; jb >>= 1) {
-      for (int e = tid; e < np2; e += kSelThreads) {
-        const int f = e ^ jb;
-        if (f > e) {
-          const int x = buf_s[e], y = buf_s[f];
-          const bool up = (e & k) == 0;
-          if ((x > y) == up) {
-            buf_s[e] = y;
-            buf_s[f] = x;
-          }
-        }
-      }
-      __syncthreads();
+  const uint32_t hiU = (static_cast<uint32_t>(T) << 10) | static_cast<uint32_t>(U);
+  for (int e = tid; e < ncand; e += kSelThreads) {
+    const uint32_t k = key_at(e);
+    if ((k >> 9) == hiU) atomicAdd(&rh[k & 511], 1);
+  }
+  __syncthreads();
+  int V, above_V;
+  digit_from_top<512>(rh, need - above_U, scan, info, V, above_V);
+  const uint32_t Tk = (hiU << 9) | static_cast<uint32_t>(V);
+  const int n_eq = need - above_U - above_V;  // keys equal to Tk to keep, lowest ids first
+
+  // ---- keep: key > Tk, or key == Tk among the first n_eq such in id order;
+  // each thread filters a contiguous run of the (ascending) candidates
+  const int C = (ncand + kSelThreads - 1) / kSelThreads;
+  const int e0 = min(tid * C, ncand), e1 = min(e0 + C, ncand);
+  int ceq = 0;
+  for (int e = e0; e < e1; ++e) ceq += key_at(e) == Tk ? 1 : 0;
+  int tmp;
+  const int eq_before = cta_exclusive_scan<kSelThreads>(ceq, scan, tmp);
+  int nk = 0;
+  {
+    int r = eq_before;
+    for (int e = e0; e < e1; ++e) {
+      const uint32_t k = key_at(e);
+      nk += (k > Tk || (k == Tk && r < n_eq)) ? 1 : 0;
+      r += k == Tk ? 1 : 0;
     }
   }
-  for (int e = tid; e < nk * a.ratio && e < a.topK; e += kSelThreads) out[e] = buf_s[e / a.ratio] * a.ratio + e % a.ratio;
-  const int head = nk * a.ratio;
+  int kept;
+  int pos = cta_exclusive_scan<kSelThreads>(nk, scan, kept);
+  {
+    int r = eq_before;
+    for (int e = e0; e < e1; ++e) {
+      const uint32_t k = key_at(e);
+      if (k > Tk || (k == Tk && r < n_eq)) {
+        const int g = id_at(e);
+        if ((pos + 1) * a.ratio <= a.topK)
+          for (int j = 0; j < a.ratio; ++j) out[pos * a.ratio + j] = g * a.ratio + j;
+        ++pos;
+      }
+      r += k == Tk ? 1 : 0;
+    }
+  }
+  const int head = min(kept * a.ratio, a.topK);
   for (int i = head + tid; i < a.topK; i += kSelThreads) {
     const int j = n_c * a.ratio + (i - head);
     out[i] = j <= t ? j : -1;
   }
   // re-arm for the next call
   for (int i = tid; i < kNumBins; i += kSelThreads) hrow[i] = 0;
-  if (tid == 0) {
-    ctr[0] = 0;
-    ctr[1] = 0;
-    ctr[2] = 0;
-  }
+  if (tid == 0) a.ticket[b] = 0;
 }
 
 int sm_count() {
@@ -686,7 +717,8 @@ int sm_count() {
 
 size_t indexer_decode_workspace_bytes(int B, int maxPagesPerSeq, int ratio, int budget) {
   const int nbmax = maxPagesPerSeq * (kTokensPerPageHost / ratio);
-  return ws_layout(B, nbmax, budget).total;
+  (void)budget;
+  return ws_layout(B, nbmax).total;
 }
 
 cudaError_t launch_indexer_decode(const QsaIndexerDecodeParams& p, const RopeFreqs& rf,
@@ -694,13 +726,12 @@ cudaError_t launch_indexer_decode(const QsaIndexerDecodeParams& p, const RopeFre
   const int B = p.batchSize;
   const int bpp = kTokensPerPageHost / p.compressRatio;
   const int nbmax = p.maxPagesPerSeq * bpp;
-  const WsLayout l = ws_layout(B, nbmax, p.budget);
+  const WsLayout l = ws_layout(B, nbmax);
   uint8_t* ws = static_cast<uint8_t*>(p.workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
   float* q = reinterpret_cast<float*>(ws + l.q);
   float* scores = reinterpret_cast<float*>(ws + l.scores);
   int32_t* hist = reinterpret_cast<int32_t*>(ws + l.hist);
-  int32_t* counters = reinterpret_cast<int32_t*>(ws + l.counters);
   cudaStream_t st = static_cast<cudaStream_t>(p.stream);
 
   PrepArgs pa;
@@ -724,9 +755,9 @@ cudaError_t launch_indexer_decode(const QsaIndexerDecodeParams& p, const RopeFre
   pa.eps = p.rmsNormEps;
   pa.rf = rf;
   if (p.headDim == 64)
-    decode_prep_kernel<64><<<B, 256, 0, st>>>(pa);
+    decode_prep_kernel<64><<<B, 256 + 64, 0, st>>>(pa);
   else
-    decode_prep_kernel<128><<<B, 256, 0, st>>>(pa);
+    decode_prep_kernel<128><<<B, 256 + 128, 0, st>>>(pa);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -764,17 +795,19 @@ cudaError_t launch_indexer_decode(const QsaIndexerDecodeParams& p, const RopeFre
   se.ctx = p.contextLengths;
   se.scores = scores;
   se.hist = hist;
-  se.sureId = reinterpret_cast<int32_t*>(ws + l.sureId);
-  se.tieKey = reinterpret_cast<uint32_t*>(ws + l.tieKey);
-  se.tieId = reinterpret_cast<int32_t*>(ws + l.tieId);
-  se.counters = counters;
+  se.candKey = reinterpret_cast<uint32_t*>(ws + l.candKey);
+  se.candId = reinterpret_cast<int32_t*>(ws + l.candId);
+  se.sliceCnt = reinterpret_cast<int32_t*>(ws + l.sliceCnt);
+  se.ticket = reinterpret_cast<int32_t*>(ws + l.ticket);
   se.indices = p.indices;
   se.maxPagesPerSeq = p.maxPagesPerSeq;
   se.ratio = p.compressRatio;
   se.budget = p.budget;
   se.topK = p.topK;
   se.nbmax = nbmax;
-  dim3 sgrid((nbmax + kSliceBlocks - 1) / kSliceBlocks, B);
+  se.nsplitmax = (nbmax + kSliceBlocks - 1) / kSliceBlocks;
+  if (se.nsplitmax > kMaxSlices) return cudaErrorInvalidValue;
+  dim3 sgrid(se.nsplitmax, B);
   decode_select_kernel<<<sgrid, kSelThreads, 0, st>>>(se);
   return cudaGetLastError();
 }

@@ -119,6 +119,18 @@ def test_indexer_decode_edges():
     ind, _ = _gpu_indexer(d_dev, cfg0)
     ref, _ = _oracle_indexer(d_np, pool_np, cfg0)
     assert np.array_equal(to_np(ind)[:, 0], ref)
+    # the same ties over more candidates than the selection stages on chip (n_c = 6000 and 5120 blocks,
+    # several slices): the final pass reads them back from the workspace
+    cfg1 = dataclasses.replace(cfg0, B=2, ctx_list=(24000, 20483), max_ctx=24576, seed=22)
+    d = syn.make_decode(cfg1)
+    pool = d["pool"]
+    pool[:, :, 0, cfg1.D:] = pool[0, 0, 0, cfg1.D:]
+    d_np = _np(d)
+    pool_np = d_np["pool"].copy()
+    d_dev = _to_dev(d)
+    ind, _ = _gpu_indexer(d_dev, cfg1)
+    ref, _ = _oracle_indexer(d_np, pool_np, cfg1)
+    assert np.array_equal(to_np(ind)[:, 0], ref)
 
 
 def _state(pool, pt, b, L, cfg):
