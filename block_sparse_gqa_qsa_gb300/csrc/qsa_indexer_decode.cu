@@ -15,12 +15,13 @@
 //       a producer warp streams the key tails of every page that holds
 //       complete blocks (3-D TMA copies, box {64, 128/r, 1} with the 128-byte
 //       swizzle over a strided view of the pool, page ids fetched 32 at a time)
-//       into a 24-stage ring; 15 consumer warps score one page each: 16 lanes
-//       per key, 8 dims x 8 heads per lane (dims paired in fp32x2 FMAs), then
-//       a transposing shuffle reduction whose head order is pre-permuted per
-//       lane (h ^ m) so that every step is one add of one shuffle; they write
-//       the scores and add them to a 4096-bin histogram of the score bits per
-//       sequence.  Pages are split evenly over the CTAs.
+//       into a 16-stage ring; 15 consumer warps score one page each: two lanes
+//       per key (one per half of the dims), two keys per lane, the warp's
+//       queries read from shared memory by broadcast, dims paired in fp32x2
+//       FMAs; one transposing shuffle exchange joins the halves, then relu
+//       per head and the head sum.  They write the scores and add them to a
+//       4096-bin histogram of the score bits per sequence.  Pages are split
+//       evenly over the CTAs.
 //   decode_select_kernel  (B3) per sequence: the histogram gives the bin T that
 //       holds the budget-th largest score; one CTA per 2048-block slice writes
 //       the slice's candidates (blocks in bins >= T) in ascending id order
@@ -46,7 +47,7 @@ constexpr int kMaxSlices = 1024;     // slices per sequence (blocks <= 2M): thei
 constexpr int kStageCand = 4096;     // candidates the final CTA stages in shared memory (more: read from L2)
 constexpr int kConsumerWarps = 15;  // + 1 producer warp = 16 warps, up to 128 registers each
 constexpr int kScoreThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 24;
+constexpr int kStages = 16;
 constexpr int kSelThreads = 256;
 constexpr int kPrepThreads = 256 + 128;  // 8 query-prep warps + up to 4 state-update warps
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;  // 0.2 s
@@ -249,7 +250,8 @@ struct ScoreArgs {
 
 __host__ __device__ __forceinline__ int score_smem_bytes(int di, int ratio, int B) {
   const int stage = (kTokensPerPage / ratio) * di * 2;
-  return kStages * stage + 2 * kStages * 8 + ((B + 1 + 3) / 4) * 16 + kConsumerWarps * 128 * 4;
+  return kStages * stage + 2 * kStages * 8 + ((B + 1 + 3) / 4) * 16 + kConsumerWarps * 128 * 4 +
+         kConsumerWarps * 2 * ((di / 16) * 64 + 4) * 4;
 }
 
 // One lane per key row: byte offset of 16-byte chunk c (dims 8c..8c+7 of a
@@ -357,29 +359,33 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
     return;
   }
 
-  // ---- consumers: warp w takes pages lo + w, lo + w + kConsumerWarps, ...; 16 lanes per key
-  constexpr int LPB = DI / 8, BPW = 32 / LPB, LOGL = LPB == 16 ? 4 : 3;
-  const int sub = lane % LPB;
-  const int m = (sub >> (LOGL - 3)) & 7;
-  uint64_t q2[8][4];
+  // ---- consumers: warp w scores pages lo + w, lo + w + kConsumerWarps, ...
+  // Lane (kk, hh) = (lane & 15, lane >> 4) holds keys kk and kk + 16 of the
+  // page and dims [hh*DI/2, (hh+1)*DI/2) of them; q comes from the warp's own
+  // shared-memory copy of its sequence's queries (broadcast reads), stored
+  // with the head order h ^ 4hh so that each lane's heads 0..3 are the ones
+  // it keeps after one transposing exchange with the other half (lane ^ 16).
+  constexpr int NCH = DI / 16;                // 8-dim chunks per lane
+  constexpr int QS = NCH * 64 + 4;            // floats per half, padded so the halves use other banks
+  const int kk = lane & 15, hh = lane >> 4;
+  float* qw = reinterpret_cast<float*>(pref + (a.B + 1 + 3) / 4 * 4) + kConsumerWarps * 128 + warp * 2 * QS;
+  float* myscr = reinterpret_cast<float*>(pref + (a.B + 1 + 3) / 4 * 4) + warp * 128;
   int cached_b = -1, n_c = 0;
   int b = 0;
-  float* myscr = reinterpret_cast<float*>(pref + (a.B + 1 + 3) / 4 * 4) + warp * 128;
   for (long long i = lo + warp; i < hi; i += kConsumerWarps) {
     while (i >= pref[b + 1]) ++b;
     const int p = static_cast<int>(i - pref[b]);
     const int jx = static_cast<int>(i - lo), s = jx % kStages, n = jx / kStages;
     if (b != cached_b) {
-      const float* qb = a.q + static_cast<size_t>(b) * 8 * 128;
-#pragma unroll
-      for (int h = 0; h < 8; ++h) {
-        const float4 x0 = *reinterpret_cast<const float4*>(qb + (h ^ m) * 128 + sub * 8);
-        const float4 x1 = *reinterpret_cast<const float4*>(qb + (h ^ m) * 128 + sub * 8 + 4);
-        q2[h][0] = pack_f2(x0.x, x0.y);
-        q2[h][1] = pack_f2(x0.z, x0.w);
-        q2[h][2] = pack_f2(x1.x, x1.y);
-        q2[h][3] = pack_f2(x1.z, x1.w);
+      __syncwarp();
+      const float4* qg = reinterpret_cast<const float4*>(a.q + static_cast<size_t>(b) * 8 * 128);
+      for (int e = lane; e < 8 * DI / 4; e += 32) {  // q[h][d .. d+3]
+        const float4 v = __ldcg(qg + (e / (DI / 4)) * 32 + (e % (DI / 4)));
+        const int h = e / (DI / 4), d = 4 * (e % (DI / 4));
+        const int half = d / (DI / 2), c = (d % (DI / 2)) / 8, i4 = d % 8;
+        *reinterpret_cast<float4*>(qw + half * QS + c * 64 + (h ^ (4 * half)) * 8 + i4) = v;
       }
+      __syncwarp();
       n_c = max(0, min(a.ctx[b], MAXL)) / a.ratio;
       cached_b = b;
     }
@@ -388,40 +394,64 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
       break;
     }
     const uint8_t* tile = ring + s * stage_bytes;
-#pragma unroll 2
-    for (int pass = 0; pass < bpp / BPW; ++pass) {
-      const int blk = pass * BPW + lane / LPB;
-      const uint4 raw = *reinterpret_cast<const uint4*>(tile + (sub >> 3) * bpp * 128 + swz128(blk, sub & 7));
-      const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
-      uint64_t kp[4];
+    const int r0 = kk & (bpp - 1), r1 = (kk + 16) & (bpp - 1);  // rows past the page repeat (discarded)
+    uint64_t acc0[8], acc1[8];
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const float2 f = __half22float2(h2[jj]);
-        kp[jj] = pack_f2(f.x, f.y);
+    for (int h = 0; h < 8; ++h) acc0[h] = acc1[h] = 0ull;
+    const float* qh = qw + hh * QS;
+#pragma unroll 2
+    for (int c = 0; c < NCH; ++c) {
+      const int cg = hh * NCH + c;  // chunk of the 64-dim half cg >> 3, at cg & 7
+      const uint4 kr0 = *reinterpret_cast<const uint4*>(tile + (cg >> 3) * bpp * 128 + swz128(r0, cg & 7));
+      const uint4 kr1 = *reinterpret_cast<const uint4*>(tile + (cg >> 3) * bpp * 128 + swz128(r1, cg & 7));
+      uint64_t k0[4], k1[4];
+      {
+        const __half2* h0 = reinterpret_cast<const __half2*>(&kr0);
+        const __half2* h1 = reinterpret_cast<const __half2*>(&kr1);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const float2 f0 = __half22float2(h0[jj]), f1 = __half22float2(h1[jj]);
+          k0[jj] = pack_f2(f0.x, f0.y);
+          k1[jj] = pack_f2(f1.x, f1.y);
+        }
       }
-      float d[8];
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
-        uint64_t acc = ffma2(q2[h][0], kp[0], 0ull);
-        acc = ffma2(q2[h][1], kp[1], acc);
-        acc = ffma2(q2[h][2], kp[2], acc);
-        acc = ffma2(q2[h][3], kp[3], acc);
-        d[h] = lo_f2(acc) + hi_f2(acc);
+        const float4 qa = *reinterpret_cast<const float4*>(qh + c * 64 + h * 8);
+        const float4 qb = *reinterpret_cast<const float4*>(qh + c * 64 + h * 8 + 4);
+        const uint64_t q0 = pack_f2(qa.x, qa.y), q1 = pack_f2(qa.z, qa.w);
+        const uint64_t q2 = pack_f2(qb.x, qb.y), q3 = pack_f2(qb.z, qb.w);
+        acc0[h] = ffma2(q0, k0[0], acc0[h]);
+        acc1[h] = ffma2(q0, k1[0], acc1[h]);
+        acc0[h] = ffma2(q1, k0[1], acc0[h]);
+        acc1[h] = ffma2(q1, k1[1], acc1[h]);
+        acc0[h] = ffma2(q2, k0[2], acc0[h]);
+        acc1[h] = ffma2(q2, k1[2], acc1[h]);
+        acc0[h] = ffma2(q3, k0[3], acc0[h]);
+        acc1[h] = ffma2(q3, k1[3], acc1[h]);
       }
-#pragma unroll
-      for (int i2 = 0; i2 < 4; ++i2) d[i2] += __shfl_xor_sync(kFull, d[i2 + 4], LPB / 2);
-#pragma unroll
-      for (int i2 = 0; i2 < 2; ++i2) d[i2] += __shfl_xor_sync(kFull, d[i2 + 2], LPB / 4);
-      d[0] += __shfl_xor_sync(kFull, d[1], LPB / 8);
-      if (LPB == 16) d[0] += __shfl_xor_sync(kFull, d[0], 1);
-      float sc = d[0] > 0.f ? d[0] : 0.f;
-      sc += __shfl_xor_sync(kFull, sc, LPB / 8);
-      sc += __shfl_xor_sync(kFull, sc, LPB / 4);
-      sc += __shfl_xor_sync(kFull, sc, LPB / 2);
-      if (sub == 0) myscr[blk] = sc;
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    if (lane == 0) mbar_arrive(&empty[s]);  // every lane's tile reads are done
+    float sc[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float d[8];
+#pragma unroll
+      for (int h = 0; h < 8; ++h) d[h] = j == 0 ? lo_f2(acc0[h]) + hi_f2(acc0[h]) : lo_f2(acc1[h]) + hi_f2(acc1[h]);
+      float t4 = 0.f;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const float full = d[h] + __shfl_xor_sync(kFull, d[h + 4], 16);  // head (h ^ 4hh), both halves of dims
+        t4 += full > 0.f ? full : 0.f;
+      }
+      sc[j] = t4 + __shfl_xor_sync(kFull, t4, 16);
+    }
+    if (hh == 0) {
+      myscr[kk] = sc[0];
+      myscr[kk + 16] = sc[1];
+    }
+    __syncwarp();
     page_epilogue(a, b, p, n_c, bpp, myscr[lane < bpp ? lane : 0]);
     __syncwarp();
   }
