@@ -15,13 +15,13 @@
 //       a producer warp streams the key tails of every page that holds
 //       complete blocks (3-D TMA copies, box {64, 128/r, 1} with the 128-byte
 //       swizzle over a strided view of the pool, page ids fetched 32 at a time)
-//       into a 16-stage ring; 15 consumer warps score one page each: two lanes
-//       per key (one per half of the dims), two keys per lane, the warp's
-//       queries read from shared memory by broadcast, dims paired in fp32x2
-//       FMAs; one transposing shuffle exchange joins the halves, then relu
-//       per head and the head sum.  They write the scores and add them to a
-//       4096-bin histogram of the score bits per sequence.  Pages are split
-//       evenly over the CTAs.
+//       into a 22-stage ring; 15 consumer warps score one page each: four
+//       lanes per key (a quarter of the dims each), four keys per lane, the
+//       queries read by broadcast from the CTA's shared-memory copy (written
+//       by B1 in that layout), dims paired in fp32x2 FMAs; two transposing
+//       shuffle exchanges join the quarters, then relu per head and the head
+//       sum.  They write the scores and add them to a 4096-bin histogram of
+//       the score bits per sequence.  Pages are split evenly over the CTAs.
 //   decode_select_kernel  (B3) per sequence: the histogram gives the bin T that
 //       holds the budget-th largest score; one CTA per 2048-block slice writes
 //       the slice's candidates (blocks in bins >= T) in ascending id order
@@ -47,7 +47,13 @@ constexpr int kMaxSlices = 1024;     // slices per sequence (blocks <= 2M): thei
 constexpr int kStageCand = 4096;     // candidates the final CTA stages in shared memory (more: read from L2)
 constexpr int kConsumerWarps = 15;  // + 1 producer warp = 16 warps, up to 128 registers each
 constexpr int kScoreThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 16;
+constexpr int kStages = 22;
+constexpr int kQSlots = 8;            // sequences whose queries a scorer CTA keeps in shared memory
+// Queries as the scorer reads them: per sequence 4 quarters of the dims, each
+// [chunk][head slot][8 dims] plus 4 floats of padding (the quarters then start
+// in different banks); in quarter t, slot p holds head p ^ (4*(t>>1) + 2*(t&1)).
+constexpr int kQS128 = (128 / 32) * 64 + 4;
+constexpr int kQPerSeq = 4 * kQS128;  // floats per sequence in the workspace (the 128-dim layout)
 constexpr int kSelThreads = 256;
 constexpr int kPrepThreads = 256 + 128;  // 8 query-prep warps + up to 4 state-update warps
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;  // 0.2 s
@@ -63,7 +69,7 @@ WsLayout ws_layout(int B, int nbmax) {
   WsLayout l;
   size_t off = kStatusBytes;
   l.q = off;
-  off += up256(static_cast<size_t>(B) * 8 * 128 * 4);  // prepared queries fp32 [B][8][128]
+  off += up256(static_cast<size_t>(B) * kQPerSeq * 4);  // prepared queries fp32, scorer layout [B][kQPerSeq]
   l.scores = off;
   off += up256(static_cast<size_t>(B) * nbmax * 4);     // block scores fp32 [B][nbmax]
   l.hist = off;
@@ -129,7 +135,12 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const PrepArg
   // warps 8..: the state update, concurrently (named barrier 1 among them)
   if (warp < 8) {
     const int h = warp;
-    float* qo = a.q + (static_cast<size_t>(b) * 8 + h) * 128;
+    float* qo = a.q + static_cast<size_t>(b) * kQPerSeq;
+    constexpr int QS = (DI / 32) * 64 + 4;
+    auto qpos = [&](int i) {  // scorer layout position of (head h, dim i)
+      const int qt = i / (DI / 4), c = (i % (DI / 4)) / 8;
+      return qt * QS + c * 64 + (h ^ (4 * (qt >> 1) + 2 * (qt & 1))) * 8 + (i % 8);
+    };
     if (h < a.Hi) {
       const __half* x = a.idxQ + (static_cast<size_t>(b) * a.Hi + h) * DI;
       float y[PER];
@@ -164,11 +175,11 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const PrepArg
           rope_cos_sin_f32(static_cast<double>(t), a.rf.inv_freq[k], cs, sn);
           v = y[p] * cs + y_s[h][k] * sn;
         }
-        qo[i] = v;
+        qo[qpos(i)] = v;
       }
     } else {
 #pragma unroll
-      for (int p = 0; p < PER; ++p) qo[lane + 32 * p] = 0.f;
+      for (int p = 0; p < PER; ++p) qo[qpos(lane + 32 * p)] = 0.f;
     }
     return;
   }
@@ -251,7 +262,7 @@ struct ScoreArgs {
 __host__ __device__ __forceinline__ int score_smem_bytes(int di, int ratio, int B) {
   const int stage = (kTokensPerPage / ratio) * di * 2;
   return kStages * stage + 2 * kStages * 8 + ((B + 1 + 3) / 4) * 16 + kConsumerWarps * 128 * 4 +
-         kConsumerWarps * 2 * ((di / 16) * 64 + 4) * 4;
+         kQSlots * 4 * ((di / 32) * 64 + 4) * 4;
 }
 
 // One lane per key row: byte offset of 16-byte chunk c (dims 8c..8c+7 of a
@@ -270,6 +281,70 @@ __device__ __forceinline__ void page_epilogue(const ScoreArgs& a, int b, int p, 
   if (valid) {
     const unsigned peers = __match_any_sync(act, bin);
     if (lane == __ffs(peers) - 1) atomicAdd(a.hist + static_cast<size_t>(b) * kNumBins + bin, __popc(peers));
+  }
+}
+
+// Scores one page (bpp <= 32 block keys in a swizzled stage) for one warp.
+// Lane (kk, hh) = (lane & 7, lane >> 3) holds keys kk + 8j (j < 4) and their
+// dims [hh*DI/4, (hh+1)*DI/4); its quarter of the queries (qh, scorer layout)
+// is read by broadcast, dims are paired in fp32x2 FMAs, and two transposing
+// exchanges (lane ^ 16, then ^ 8) leave each lane the full dot products of its
+// head slots 0 and 1 -- every step one shuffle and one add.  Writes the page's
+// scores to myscr[0, 32).  kSmemQ: qh points to shared memory (else global).
+template <int DI, bool kSmemQ>
+__device__ __forceinline__ void score_page(const uint8_t* tile, int bpp, const float* qh, float* myscr) {
+  constexpr int NCH = DI / 32;
+  const int lane = threadIdx.x & 31, kk = lane & 7, hh = lane >> 3;
+  uint64_t acc[4][8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int h = 0; h < 8; ++h) acc[j][h] = 0ull;
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    const int cg = hh * NCH + c;  // this lane's chunk: half cg >> 3 of the row, 16-byte slot cg & 7
+    uint64_t kp[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = (kk + 8 * j) & (bpp - 1);  // rows past a short page repeat (discarded)
+      const uint4 raw = *reinterpret_cast<const uint4*>(tile + (cg >> 3) * bpp * 128 + swz128(r, cg & 7));
+      const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const float2 f = __half22float2(h2[jj]);
+        kp[j][jj] = pack_f2(f.x, f.y);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      const float4* q4 = reinterpret_cast<const float4*>(qh + c * 64 + h * 8);
+      const float4 qa = kSmemQ ? q4[0] : __ldg(q4);
+      const float4 qb = kSmemQ ? q4[1] : __ldg(q4 + 1);
+      const uint64_t q0 = pack_f2(qa.x, qa.y), q1 = pack_f2(qa.z, qa.w);
+      const uint64_t q2 = pack_f2(qb.x, qb.y), q3 = pack_f2(qb.z, qb.w);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        acc[j][h] = ffma2(q0, kp[j][0], acc[j][h]);
+        acc[j][h] = ffma2(q1, kp[j][1], acc[j][h]);
+        acc[j][h] = ffma2(q2, kp[j][2], acc[j][h]);
+        acc[j][h] = ffma2(q3, kp[j][3], acc[j][h]);
+      }
+    }
+  }
+  __syncwarp();  // every lane's reads of the stage are done
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float d[8];
+#pragma unroll
+    for (int h = 0; h < 8; ++h) d[h] = lo_f2(acc[j][h]) + hi_f2(acc[j][h]);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) d[h] += __shfl_xor_sync(kFull, d[h + 4], 16);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) d[h] += __shfl_xor_sync(kFull, d[h + 2], 8);
+    float t = (d[0] > 0.f ? d[0] : 0.f) + (d[1] > 0.f ? d[1] : 0.f);
+    t += __shfl_xor_sync(kFull, t, 8);
+    t += __shfl_xor_sync(kFull, t, 16);
+    if (hh == 0) myscr[kk + 8 * j] = t;
   }
 }
 
@@ -317,6 +392,29 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
   const long long W = pref[a.B];
   const long long lo = W * blockIdx.x / gridDim.x, hi = W * (blockIdx.x + 1) / gridDim.x;
   if (lo >= hi) return;
+  // queries of the first kQSlots sequences this CTA's pages belong to
+  constexpr int QS = (DI / 32) * 64 + 4;
+  float* myscr0 = reinterpret_cast<float*>(pref + (a.B + 1 + 3) / 4 * 4);
+  float* qcache = myscr0 + kConsumerWarps * 128;
+  auto seq_of = [&](long long page) {  // largest b with pref[b] <= page
+    int l = 0, h = a.B;
+    while (h - l > 1) {
+      const int m = (l + h) >> 1;
+      if (pref[m] <= page)
+        l = m;
+      else
+        h = m;
+    }
+    return l;
+  };
+  const int b_first = seq_of(lo);
+  const int nslot = min(kQSlots, seq_of(hi - 1) - b_first + 1);
+  for (int e = tid; e < nslot * QS; e += blockDim.x) {  // float4 units: 4*QS floats per sequence
+    const int bi = e / QS, w4 = e % QS;
+    reinterpret_cast<float4*>(qcache)[e] =
+        __ldcg(reinterpret_cast<const float4*>(a.q + static_cast<size_t>(b_first + bi) * kQPerSeq) + w4);
+  }
+  __syncthreads();
 
   if (warp == kConsumerWarps) {  // ---- producer: page ids 32 at a time, one TMA per 64-dim half
     int bw = 0;  // sequence of the batch's first page
@@ -360,16 +458,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
   }
 
   // ---- consumers: warp w scores pages lo + w, lo + w + kConsumerWarps, ...
-  // Lane (kk, hh) = (lane & 15, lane >> 4) holds keys kk and kk + 16 of the
-  // page and dims [hh*DI/2, (hh+1)*DI/2) of them; q comes from the warp's own
-  // shared-memory copy of its sequence's queries (broadcast reads), stored
-  // with the head order h ^ 4hh so that each lane's heads 0..3 are the ones
-  // it keeps after one transposing exchange with the other half (lane ^ 16).
-  constexpr int NCH = DI / 16;                // 8-dim chunks per lane
-  constexpr int QS = NCH * 64 + 4;            // floats per half, padded so the halves use other banks
-  const int kk = lane & 15, hh = lane >> 4;
-  float* qw = reinterpret_cast<float*>(pref + (a.B + 1 + 3) / 4 * 4) + kConsumerWarps * 128 + warp * 2 * QS;
-  float* myscr = reinterpret_cast<float*>(pref + (a.B + 1 + 3) / 4 * 4) + warp * 128;
+  float* myscr = myscr0 + warp * 128;
+  const int hh = lane >> 3;
   int cached_b = -1, n_c = 0;
   int b = 0;
   for (long long i = lo + warp; i < hi; i += kConsumerWarps) {
@@ -377,80 +467,25 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
     const int p = static_cast<int>(i - pref[b]);
     const int jx = static_cast<int>(i - lo), s = jx % kStages, n = jx / kStages;
     if (b != cached_b) {
-      __syncwarp();
-      const float4* qg = reinterpret_cast<const float4*>(a.q + static_cast<size_t>(b) * 8 * 128);
-      for (int e = lane; e < 8 * DI / 4; e += 32) {  // q[h][d .. d+3]
-        const float4 v = __ldcg(qg + (e / (DI / 4)) * 32 + (e % (DI / 4)));
-        const int h = e / (DI / 4), d = 4 * (e % (DI / 4));
-        const int half = d / (DI / 2), c = (d % (DI / 2)) / 8, i4 = d % 8;
-        *reinterpret_cast<float4*>(qw + half * QS + c * 64 + (h ^ (4 * half)) * 8 + i4) = v;
-      }
-      __syncwarp();
       n_c = max(0, min(a.ctx[b], MAXL)) / a.ratio;
       cached_b = b;
     }
-    if (!mbar_wait_bounded(&full[s], n & 1, kWaitLimitNs)) {
+    // Warps take pages round-robin, so this warp can reach page jx while the
+    // stage's previous page (jx - kStages, another warp's) is still landing;
+    // its full phase would then look complete to a parity wait.  Waiting first
+    // for that page to be consumed (empty phase n-1) leaves the full barrier
+    // exactly one phase short of page jx's, so the parity wait is exact.
+    if ((n > 0 && !mbar_wait_bounded(&empty[s], (n - 1) & 1, kWaitLimitNs)) ||
+        !mbar_wait_bounded(&full[s], n & 1, kWaitLimitNs)) {
       if (lane == 0) atomicOr(a.status, kErrWaitTimeout);
       break;
     }
     const uint8_t* tile = ring + s * stage_bytes;
-    const int r0 = kk & (bpp - 1), r1 = (kk + 16) & (bpp - 1);  // rows past the page repeat (discarded)
-    uint64_t acc0[8], acc1[8];
-#pragma unroll
-    for (int h = 0; h < 8; ++h) acc0[h] = acc1[h] = 0ull;
-    const float* qh = qw + hh * QS;
-#pragma unroll 2
-    for (int c = 0; c < NCH; ++c) {
-      const int cg = hh * NCH + c;  // chunk of the 64-dim half cg >> 3, at cg & 7
-      const uint4 kr0 = *reinterpret_cast<const uint4*>(tile + (cg >> 3) * bpp * 128 + swz128(r0, cg & 7));
-      const uint4 kr1 = *reinterpret_cast<const uint4*>(tile + (cg >> 3) * bpp * 128 + swz128(r1, cg & 7));
-      uint64_t k0[4], k1[4];
-      {
-        const __half2* h0 = reinterpret_cast<const __half2*>(&kr0);
-        const __half2* h1 = reinterpret_cast<const __half2*>(&kr1);
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const float2 f0 = __half22float2(h0[jj]), f1 = __half22float2(h1[jj]);
-          k0[jj] = pack_f2(f0.x, f0.y);
-          k1[jj] = pack_f2(f1.x, f1.y);
-        }
-      }
-#pragma unroll
-      for (int h = 0; h < 8; ++h) {
-        const float4 qa = *reinterpret_cast<const float4*>(qh + c * 64 + h * 8);
-        const float4 qb = *reinterpret_cast<const float4*>(qh + c * 64 + h * 8 + 4);
-        const uint64_t q0 = pack_f2(qa.x, qa.y), q1 = pack_f2(qa.z, qa.w);
-        const uint64_t q2 = pack_f2(qb.x, qb.y), q3 = pack_f2(qb.z, qb.w);
-        acc0[h] = ffma2(q0, k0[0], acc0[h]);
-        acc1[h] = ffma2(q0, k1[0], acc1[h]);
-        acc0[h] = ffma2(q1, k0[1], acc0[h]);
-        acc1[h] = ffma2(q1, k1[1], acc1[h]);
-        acc0[h] = ffma2(q2, k0[2], acc0[h]);
-        acc1[h] = ffma2(q2, k1[2], acc1[h]);
-        acc0[h] = ffma2(q3, k0[3], acc0[h]);
-        acc1[h] = ffma2(q3, k1[3], acc1[h]);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);  // every lane's tile reads are done
-    float sc[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      float d[8];
-#pragma unroll
-      for (int h = 0; h < 8; ++h) d[h] = j == 0 ? lo_f2(acc0[h]) + hi_f2(acc0[h]) : lo_f2(acc1[h]) + hi_f2(acc1[h]);
-      float t4 = 0.f;
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const float full = d[h] + __shfl_xor_sync(kFull, d[h + 4], 16);  // head (h ^ 4hh), both halves of dims
-        t4 += full > 0.f ? full : 0.f;
-      }
-      sc[j] = t4 + __shfl_xor_sync(kFull, t4, 16);
-    }
-    if (hh == 0) {
-      myscr[kk] = sc[0];
-      myscr[kk + 16] = sc[1];
-    }
+    if (b - b_first < kQSlots)
+      score_page<DI, true>(tile, bpp, qcache + (b - b_first) * 4 * QS + hh * QS, myscr);
+    else
+      score_page<DI, false>(tile, bpp, a.q + static_cast<size_t>(b) * kQPerSeq + hh * QS, myscr);
+    if (lane == 0) mbar_arrive(&empty[s]);
     __syncwarp();
     page_epilogue(a, b, p, n_c, bpp, myscr[lane < bpp ? lane : 0]);
     __syncwarp();
