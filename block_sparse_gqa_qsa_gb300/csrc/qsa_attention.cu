@@ -34,6 +34,14 @@ constexpr int kOStride = 132;  // padded fp32 row of the warp-merge buffer
 // over 8-row groups so ldmatrix reads are bank-conflict free).
 __device__ __forceinline__ uint32_t swz(int r, int c) { return r * 256 + ((c ^ (r & 7)) << 4); }
 
+// 2^x by the hardware approximation, results below the normal range flushed
+// to zero (probabilities that small do not change an fp16 output).
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <int NT>
 struct WarpAcc {
   float o[8][NT][4];  // O^T fragments: dims 16*mt + (g, g+8), heads 8*nt + (2q, 2q+1)
@@ -102,10 +110,10 @@ __device__ __forceinline__ void attend16(WarpAcc<NT>& A, uint32_t k_tile, uint32
     }
     const float mn0 = fmaxf(A.m[nt][0], mx0), mn1 = fmaxf(A.m[nt][1], mx1);
     const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = exp2f(A.m[nt][0] - mu0), al1 = exp2f(A.m[nt][1] - mu1);
+    const float al0 = ex2_ftz(A.m[nt][0] - mu0), al1 = ex2_ftz(A.m[nt][1] - mu1);
     A.m[nt][0] = mn0;
     A.m[nt][1] = mn1;
-    const float p0 = exp2f(x0 - mu0), p1 = exp2f(x1 - mu1), p2 = exp2f(x2 - mu0), p3 = exp2f(x3 - mu1);
+    const float p0 = ex2_ftz(x0 - mu0), p1 = ex2_ftz(x1 - mu1), p2 = ex2_ftz(x2 - mu0), p3 = ex2_ftz(x3 - mu1);
     A.l[nt][0] = A.l[nt][0] * al0 + (p0 + p2);
     A.l[nt][1] = A.l[nt][1] * al1 + (p1 + p3);
 #pragma unroll

@@ -15,7 +15,7 @@
 //       a producer warp streams the key tails of every page that holds
 //       complete blocks (3-D TMA copies, box {64, 128/r, 1} with the 128-byte
 //       swizzle over a strided view of the pool, page ids fetched 32 at a time)
-//       into a 22-stage ring; 15 consumer warps score one page each: four
+//       into a 22-stage ring; 11 consumer warps score one page each: four
 //       lanes per key (a quarter of the dims each), four keys per lane, the
 //       queries read by broadcast from the CTA's shared-memory copy (written
 //       by B1 in that layout), dims paired in fp32x2 FMAs; two transposing
@@ -45,7 +45,7 @@ constexpr int kBinShift = 19;
 constexpr int kSliceBlocks = 2048;   // blocks one select CTA filters (8 per thread, one round of loads)
 constexpr int kMaxSlices = 1024;     // slices per sequence (blocks <= 2M): their bases live in shared memory
 constexpr int kStageCand = 4096;     // candidates the final CTA stages in shared memory (more: read from L2)
-constexpr int kConsumerWarps = 15;  // + 1 producer warp = 16 warps, up to 128 registers each
+constexpr int kConsumerWarps = 11;  // + 1 producer warp: 12 warps (3 per SM sub-partition), up to 168 registers
 constexpr int kScoreThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 22;
 constexpr int kQSlots = 8;            // sequences whose queries a scorer CTA keeps in shared memory
