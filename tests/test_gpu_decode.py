@@ -68,8 +68,19 @@ def _np(d):
     return {k: (v.numpy() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
 
 
-def test_indexer_decode_parity_and_state_update():
-    cfg = syn.DECODE_PARITY
+DECODE_SHAPES = [
+    syn.DECODE_PARITY,
+    # 16 and 8 block keys per page (a short swizzled tile), blocks completed at L % r == 0
+    dataclasses.replace(syn.DECODE_PARITY, name="ratio8", ratio=8, ctx_list=(1, 8, 1031, 2048, 4103, 6000), seed=31),
+    dataclasses.replace(syn.DECODE_PARITY, name="ratio16", ratio=16, ctx_list=(1, 16, 2063, 4096, 4111, 6000),
+                        seed=32),
+    # 64-dim index keys (one 64-dim TMA box per page row), fewer index heads
+    dataclasses.replace(syn.DECODE_PARITY, name="di64", di=64, rot=32, Hi=4, seed=33),
+]
+
+
+@pytest.mark.parametrize("cfg", DECODE_SHAPES, ids=lambda c: c.name)
+def test_indexer_decode_parity_and_state_update(cfg):
     d = syn.make_decode(cfg)
     d_np = _np(d)
     pool_np = d_np["pool"].copy()
