@@ -194,7 +194,7 @@ struct PrefillArgs {
 };
 
 template <int NT, int STAGES>
-__global__ void __launch_bounds__(kThreads, 3) sparse_prefill_kernel(const PrefillArgs a) {
+__global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_kernel(const PrefillArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t ring = smem_addr(smem);                       // [STAGES][K 16 KB | V 16 KB]
   const uint32_t q_tile = ring + STAGES * 2 * kTileBytes;      // [8*NT][256 B]
@@ -253,27 +253,43 @@ __global__ void __launch_bounds__(kThreads, 3) sparse_prefill_kernel(const Prefi
       cp_async16(vdst + swz(key, ch), a.v + row + ch * 8, ok);
     }
   };
-#pragma unroll
-  for (int s = 0; s < STAGES - 1; ++s) {
-    if (s < ntiles) issue(s, s);
-    cp_async_commit();
-  }
-  cp_async_wait<STAGES - 1>();  // the Q group (oldest) has landed
-  __syncthreads();
   uint32_t qf[NT][8][2];
-  load_q_frags<NT>(q_tile, qf);
-
   WarpAcc<NT> A;
   acc_init(A);
-  for (int i = 0; i < ntiles; ++i) {
-    cp_async_wait<STAGES - 2>();
+  if constexpr (STAGES == 1) {
+    // One tile in shared memory per CTA: a small CTA (42 KB), so 5 share an
+    // SM and each one's gather latency is covered by the others' arithmetic.
+    cp_async_wait<0>();  // Q
     __syncthreads();
-    if (i + STAGES - 1 < ntiles) issue(i + STAGES - 1, (i + STAGES - 1) % STAGES);
-    cp_async_commit();
-    const int stage = i % STAGES;
-    const int slot = i * kKeys + warp * 16 + (lane >> 2);
-    attend16<NT>(A, ring + stage * 2 * kTileBytes, ring + stage * 2 * kTileBytes + kTileBytes, qf,
-                 idx_s[slot] >= 0, idx_s[slot + 8] >= 0, a.sl2);
+    load_q_frags<NT>(q_tile, qf);
+    for (int i = 0; i < ntiles; ++i) {
+      __syncthreads();  // every warp is done with tile i-1
+      issue(i, 0);
+      cp_async_commit();
+      cp_async_wait<0>();
+      __syncthreads();
+      const int slot = i * kKeys + warp * 16 + (lane >> 2);
+      attend16<NT>(A, ring, ring + kTileBytes, qf, idx_s[slot] >= 0, idx_s[slot + 8] >= 0, a.sl2);
+    }
+  } else {
+#pragma unroll
+    for (int s = 0; s < STAGES - 1; ++s) {
+      if (s < ntiles) issue(s, s);
+      cp_async_commit();
+    }
+    cp_async_wait<STAGES - 1>();  // the Q group (oldest) has landed
+    __syncthreads();
+    load_q_frags<NT>(q_tile, qf);
+    for (int i = 0; i < ntiles; ++i) {
+      cp_async_wait<STAGES - 2>();
+      __syncthreads();
+      if (i + STAGES - 1 < ntiles) issue(i + STAGES - 1, (i + STAGES - 1) % STAGES);
+      cp_async_commit();
+      const int stage = i % STAGES;
+      const int slot = i * kKeys + warp * 16 + (lane >> 2);
+      attend16<NT>(A, ring + stage * 2 * kTileBytes, ring + stage * 2 * kTileBytes + kTileBytes, qf,
+                   idx_s[slot] >= 0, idx_s[slot + 8] >= 0, a.sl2);
+    }
   }
   cp_async_wait<0>();
   __syncthreads();
@@ -313,7 +329,7 @@ struct DecodeArgs {
 };
 
 template <int NT, int STAGES>
-__global__ void __launch_bounds__(kThreads, 3) sparse_decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t ring = smem_addr(smem);
   const uint32_t q_tile = ring + STAGES * 2 * kTileBytes;
@@ -373,26 +389,41 @@ __global__ void __launch_bounds__(kThreads, 3) sparse_decode_kernel(const Decode
       cp_async16(vdst + swz(key, ch), a.pool + (ok ? vo : 0) + ch * 8, ok);
     }
   };
-#pragma unroll
-  for (int s = 0; s < STAGES - 1; ++s) {
-    if (s < ntiles) issue(s, s);
-    cp_async_commit();
-  }
-  cp_async_wait<STAGES - 1>();
-  __syncthreads();
   uint32_t qf[NT][8][2];
-  load_q_frags<NT>(q_tile, qf);
   WarpAcc<NT> A;
   acc_init(A);
-  for (int i = 0; i < ntiles; ++i) {
-    cp_async_wait<STAGES - 2>();
+  if constexpr (STAGES == 1) {  // one tile per CTA, 5 CTAs per SM (as in prefill)
+    cp_async_wait<0>();
     __syncthreads();
-    if (i + STAGES - 1 < ntiles) issue(i + STAGES - 1, (i + STAGES - 1) % STAGES);
-    cp_async_commit();
-    const int stage = i % STAGES;
-    const int slot = i * kKeys + warp * 16 + (lane >> 2);
-    attend16<NT>(A, ring + stage * 2 * kTileBytes, ring + stage * 2 * kTileBytes + kTileBytes, qf,
-                 kofs[slot] >= 0, kofs[slot + 8] >= 0, a.sl2);
+    load_q_frags<NT>(q_tile, qf);
+    for (int i = 0; i < ntiles; ++i) {
+      __syncthreads();
+      issue(i, 0);
+      cp_async_commit();
+      cp_async_wait<0>();
+      __syncthreads();
+      const int slot = i * kKeys + warp * 16 + (lane >> 2);
+      attend16<NT>(A, ring, ring + kTileBytes, qf, kofs[slot] >= 0, kofs[slot + 8] >= 0, a.sl2);
+    }
+  } else {
+#pragma unroll
+    for (int s = 0; s < STAGES - 1; ++s) {
+      if (s < ntiles) issue(s, s);
+      cp_async_commit();
+    }
+    cp_async_wait<STAGES - 1>();
+    __syncthreads();
+    load_q_frags<NT>(q_tile, qf);
+    for (int i = 0; i < ntiles; ++i) {
+      cp_async_wait<STAGES - 2>();
+      __syncthreads();
+      if (i + STAGES - 1 < ntiles) issue(i + STAGES - 1, (i + STAGES - 1) % STAGES);
+      cp_async_commit();
+      const int stage = i % STAGES;
+      const int slot = i * kKeys + warp * 16 + (lane >> 2);
+      attend16<NT>(A, ring + stage * 2 * kTileBytes, ring + stage * 2 * kTileBytes + kTileBytes, qf,
+                   kofs[slot] >= 0, kofs[slot + 8] >= 0, a.sl2);
+    }
   }
   cp_async_wait<0>();
   __syncthreads();
@@ -455,16 +486,21 @@ __global__ void __launch_bounds__(kThreads, 3) sparse_decode_kernel(const Decode
   if (tid == 0) a.counters[b * a.Hkv + kvh] = 0;
 }
 
-constexpr int kPrefillStages = 2;  // 74 KB of shared memory: 3 CTAs per SM
-constexpr int kDecodeStages = 2;
+// Ring depth of both kernels: one 64-key tile (42 KB of shared memory, 5 CTAs
+// per SM, each CTA's gather latency covered by the others) for a head group
+// of up to 8; two (3 CTAs per SM, the register budget of the 16-head group)
+// otherwise.
+template <int NT>
+constexpr int kRingStagesFor = NT == 1 ? 1 : 2;
 
 template <int NT>
 size_t prefill_smem(int topKpad) {
-  return static_cast<size_t>(kPrefillStages) * 2 * kTileBytes + NT * 8 * 256 + static_cast<size_t>(topKpad) * 4 + 64;
+  return static_cast<size_t>(kRingStagesFor<NT>) * 2 * kTileBytes + NT * 8 * 256 +
+         static_cast<size_t>(topKpad) * 4 + 64;
 }
 template <int NT>
 size_t decode_smem(int slicePad) {
-  return static_cast<size_t>(kDecodeStages) * 2 * kTileBytes + NT * 8 * 256 + static_cast<size_t>(slicePad) * 16 + 64;
+  return static_cast<size_t>(kRingStagesFor<NT>) * 2 * kTileBytes + NT * 8 * 256 + static_cast<size_t>(slicePad) * 16 + 64;
 }
 
 constexpr int kMaxDynSmem = 227 * 1024;  // per-CTA opt-in limit; the launch asks only for what it uses
@@ -472,21 +508,21 @@ constexpr int kMaxDynSmem = 227 * 1024;  // per-CTA opt-in limit; the launch ask
 template <int NT>
 cudaError_t prefill_nt(const PrefillArgs& a, long long nblocks, cudaStream_t st) {
   const size_t smem = prefill_smem<NT>(a.topKpad);
-  static const cudaError_t attr = cudaFuncSetAttribute(sparse_prefill_kernel<NT, kPrefillStages>,
+  static const cudaError_t attr = cudaFuncSetAttribute(sparse_prefill_kernel<NT, kRingStagesFor<NT>>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
   if (attr != cudaSuccess) return attr;
-  sparse_prefill_kernel<NT, kPrefillStages><<<static_cast<unsigned>(nblocks), kThreads, smem, st>>>(a);
+  sparse_prefill_kernel<NT, kRingStagesFor<NT>><<<static_cast<unsigned>(nblocks), kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
 template <int NT>
 cudaError_t decode_nt(const DecodeArgs& a, int B, cudaStream_t st) {
   const size_t smem = decode_smem<NT>(a.slicePad);
-  static const cudaError_t attr = cudaFuncSetAttribute(sparse_decode_kernel<NT, kDecodeStages>,
+  static const cudaError_t attr = cudaFuncSetAttribute(sparse_decode_kernel<NT, kRingStagesFor<NT>>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
   if (attr != cudaSuccess) return attr;
   dim3 grid(kMaxSplits, a.Hkv, B);
-  sparse_decode_kernel<NT, kDecodeStages><<<grid, kThreads, smem, st>>>(a);
+  sparse_decode_kernel<NT, kRingStagesFor<NT>><<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
