@@ -49,10 +49,10 @@ def f32(x):
 
 
 # DRAM read+write bytes of one sparse_prefill_kernel launch on the 8K prefill workload, from the ncu
-# capture summarised in profiles/sparse_prefill_kernel__prefill_S8192.md.  Reported only while the
+# capture summarised in profiles/prefill_kernels__prefill_S8192.md.  Reported only while the
 # kernel's sources hash to the value they had when the counters were taken.
-PROFILED_TRAFFIC = {"bytes": 202_572_288, "sources": ("qsa_attention.cu", "qsa_device.cuh"),
-                    "sha256": "7a2c07ecc7756744b1000c04237f80c7042476f88da966c0ee462e75e429b35f"}
+PROFILED_TRAFFIC = {"bytes": 202_220_288, "sources": ("qsa_attention.cu", "qsa_device.cuh"),
+                    "sha256": "2271e5302ecd7e75b266165a405f38ecca2c044b79237f5255fa76487e4d4a89"}
 
 
 def profiled_traffic():
