@@ -126,22 +126,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
 }
 
 // -------------------------------------------------------- CTA reductions
-// Sum of one int per thread over a CTA of NT threads.  `red` holds 2*NT/32
-// ints; `phase` alternates so that one barrier per call suffices.
-template <int NT>
-__device__ __forceinline__ int cta_sum(int v, int* red, int& phase) {
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  v = __reduce_add_sync(kFull, v);
-  int* r = red + phase * (NT / 32);
-  if (lane == 0) r[w] = v;
-  __syncthreads();
-  int s = 0;
-#pragma unroll
-  for (int i = 0; i < NT / 32; ++i) s += r[i];
-  phase ^= 1;
-  return s;
-}
-
 // Exclusive prefix sum over the CTA in thread order; `total` gets the sum.
 template <int NT>
 __device__ __forceinline__ int cta_exclusive_scan(int v, int* scratch, int& total) {
