@@ -52,6 +52,14 @@ class QsaIndexerDecodeParams(ctypes.Structure):
                 ("ropeTheta", _f32), ("rmsNormEps", _f32), ("stream", _vp)]
 
 
+class QsaIndexerHandoffParams(ctypes.Structure):
+    _fields_ = [("idxK", ctypes.c_void_p), ("contextLengths", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("workspaceBytes", ctypes.c_size_t), ("kvPool", ctypes.c_void_p), ("pageTable", ctypes.c_void_p),
+                ("batchSize", _i32), ("seqLen", _i32), ("headDim", _i32), ("compressRatio", _i32),
+                ("numKVHeads", _i32), ("kvHeadDim", _i32), ("poolHeadDim", _i32), ("numFlatPages", _i32),
+                ("maxPagesPerSeq", _i32), ("stream", ctypes.c_void_p)]
+
+
 class QsaSparsePrefillParams(ctypes.Structure):
     _fields_ = [("qPtr", _vp), ("kPtr", _vp), ("vPtr", _vp), ("oPtr", _vp), ("indices", _vp),
                 ("contextLengths", _vp), ("batchSize", _i32), ("seqLen", _i32), ("numQHeads", _i32),
@@ -84,7 +92,8 @@ def lib() -> ctypes.CDLL:
                              ("qsa_indexer_decode", QsaIndexerDecodeParams),
                              ("qsa_sparse_prefill", QsaSparsePrefillParams),
                              ("qsa_sparse_decode", QsaSparseDecodeParams),
-                             ("qsa_sparse_decode_noalloc", QsaSparseDecodeParams)):
+                             ("qsa_sparse_decode_noalloc", QsaSparseDecodeParams),
+                             ("qsa_indexer_prefill_handoff", QsaIndexerHandoffParams)):
                 f = getattr(L, name)
                 f.argtypes = [ctypes.POINTER(st)]
                 f.restype = ctypes.c_int
@@ -191,6 +200,21 @@ def indexer_decode(idxQ, idxK, wq, wk, pool, page_table, ctx, indices, workspace
     if tpp != 128 or tuple(page_table.shape[:2]) != (B, 2) or indices.numel() != B * topK:
         raise ValueError("indexer_decode: shape mismatch")
     _check(lib().qsa_indexer_decode(ctypes.byref(p)))
+
+
+def indexer_prefill_handoff(idxK, ctx, workspace, pool, page_table, *, D, ratio, stream=None):
+    """qsa_indexer_prefill_handoff: the prefill call's block keys and trailing raw keys into the pool tails."""
+    B, S, di = idxK.shape
+    nflat, tpp, Hkv, phd = pool.shape
+    if tpp != 128 or tuple(page_table.shape[:2]) != (B, 2):
+        raise ValueError("indexer_prefill_handoff: shape mismatch")
+    p = QsaIndexerHandoffParams(
+        idxK=_ptr(idxK, torch.float16, "idxK"), contextLengths=_ptr(ctx, torch.int32, "contextLengths"),
+        workspace=_ptr(workspace, None, "workspace"), workspaceBytes=workspace.numel() * workspace.element_size(),
+        kvPool=_ptr(pool, torch.float16, "kvPool"), pageTable=_ptr(page_table, torch.int32, "pageTable"),
+        batchSize=B, seqLen=S, headDim=di, compressRatio=ratio, numKVHeads=Hkv, kvHeadDim=D, poolHeadDim=phd,
+        numFlatPages=nflat, maxPagesPerSeq=page_table.shape[-1], stream=_stream(stream))
+    _check(lib().qsa_indexer_prefill_handoff(ctypes.byref(p)))
 
 
 def sparse_prefill(q, k, v, indices, ctx, out, scale, stream=None):

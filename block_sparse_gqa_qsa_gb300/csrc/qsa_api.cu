@@ -230,6 +230,32 @@ qsa_status_t qsa_sparse_prefill(const QsaSparsePrefillParams* p) {
   return e == cudaSuccess ? ok() : cuda_fail(e, "qsa_sparse_prefill");
 }
 
+qsa_status_t qsa_indexer_prefill_handoff(const QsaIndexerHandoffParams* p) {
+  if (!p) return fail(QSA_ERR_INVALID_ARG, "qsa_indexer_prefill_handoff: params is NULL");
+  if (!p->idxK || !p->contextLengths || !p->workspace || !p->kvPool || !p->pageTable)
+    return fail(QSA_ERR_INVALID_ARG, "qsa_indexer_prefill_handoff: a pointer is NULL");
+  if (p->batchSize < 1 || p->seqLen < 1 || p->compressRatio < 1 || p->numKVHeads < 1 || p->kvHeadDim < 1 ||
+      p->numFlatPages < 1 || p->maxPagesPerSeq < 1)
+    return fail(QSA_ERR_INVALID_ARG, "qsa_indexer_prefill_handoff: sizes must be >= 1");
+  if (p->headDim != 64 && p->headDim != 128)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_prefill_handoff: headDim %d not 64 or 128", p->headDim);
+  if (p->poolHeadDim < p->kvHeadDim + p->headDim)
+    return fail(QSA_ERR_INVALID_ARG, "qsa_indexer_prefill_handoff: poolHeadDim %d < kvHeadDim + headDim",
+                p->poolHeadDim);
+  if (p->kvHeadDim % 8 || p->poolHeadDim % 8 || !aligned(p->kvPool, 16) || !aligned(p->idxK, 16))
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_prefill_handoff: kvHeadDim and poolHeadDim must be multiples of 8 "
+                                     "and idxK / kvPool 16-byte aligned (16-byte copies)");
+  if (static_cast<long long>(p->maxPagesPerSeq) * qsa::kTokensPerPageHost < p->seqLen ||
+      static_cast<long long>(p->maxPagesPerSeq) * qsa::kTokensPerPageHost > 0x7fffffffLL)
+    return fail(QSA_ERR_INVALID_ARG, "qsa_indexer_prefill_handoff: maxPagesPerSeq must cover seqLen");
+  const size_t need = qsa::indexer_prefill_workspace_bytes(p->batchSize, p->seqLen, p->headDim, p->compressRatio);
+  if (p->workspaceBytes < need || !aligned(p->workspace, 256))
+    return fail(QSA_ERR_WORKSPACE, "qsa_indexer_prefill_handoff: the prefill workspace has %zu bytes, 256-byte "
+                                   "aligned, for this shape", need);
+  const cudaError_t e = qsa::launch_indexer_handoff(*p);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "qsa_indexer_prefill_handoff");
+}
+
 qsa_status_t qsa_sparse_decode(const QsaSparseDecodeParams* p) {
   if (!p) return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_decode: params is NULL");
   if (!p->qPtr || !p->kvPoolPtr || !p->pageTable || !p->indices || !p->contextLengths || !p->oPtr)

@@ -358,6 +358,59 @@ cudaError_t launch_select_di(const SelArgs& a, int B, cudaStream_t st) {
 
 }  // namespace
 
+// ------------------------------------------------ prefill -> decode hand-off
+struct HandoffArgs {
+  const __half* idxK;
+  const int32_t* ctx;
+  const __half* kbar;
+  int32_t* status;
+  __half* pool;
+  const int32_t* pageTable;
+  int S, nbmax, ratio, Hkv, D, poolHeadDim, numFlatPages, maxPagesPerSeq;
+};
+
+// One warp per item of a sequence: items g < n_c copy block g's key into the
+// V-row tail of token r*g; item n_c copies the raw keys of the trailing
+// incomplete block into their K-row tails.  16-byte copies.
+template <int DI>
+__global__ void __launch_bounds__(256) handoff_kernel(const HandoffArgs a) {
+  constexpr int CH = DI / 8;  // 16-byte chunks of a key
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.y;
+  const int g = blockIdx.x * 8 + warp;
+  const int L = max(0, min(a.ctx[b], min(a.S, a.maxPagesPerSeq * kTokensPerPageHost)));
+  const int n_c = L / a.ratio;
+  if (g > n_c) return;
+  const int32_t* ptK = a.pageTable + static_cast<size_t>(b) * 2 * a.maxPagesPerSeq;
+  const int32_t* ptV = ptK + a.maxPagesPerSeq;
+  auto tail_row = [&](int page, int tok) {
+    return a.pool + ((static_cast<size_t>(page) * kTokensPerPageHost + (tok & 127)) * a.Hkv) * a.poolHeadDim + a.D;
+  };
+  if (g < n_c) {
+    const int tok = g * a.ratio;
+    const int vp = __ldg(ptV + (tok >> 7));
+    if (static_cast<unsigned>(vp) >= static_cast<unsigned>(a.numFlatPages)) {
+      if (lane == 0) atomicOr(a.status, kErrBadPage);
+      return;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(a.kbar + (static_cast<size_t>(b) * a.nbmax + g) * DI);
+    uint4* dst = reinterpret_cast<uint4*>(tail_row(vp, tok));
+    if (lane < CH) dst[lane] = __ldg(src + lane);
+    return;
+  }
+  // g == n_c: raw keys of tokens r*n_c .. L-1
+  for (int e = lane; e < (L - n_c * a.ratio) * CH; e += 32) {
+    const int tok = n_c * a.ratio + e / CH, c = e % CH;
+    const int kp = __ldg(ptK + (tok >> 7));
+    if (static_cast<unsigned>(kp) >= static_cast<unsigned>(a.numFlatPages)) {
+      atomicOr(a.status, kErrBadPage);
+      continue;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(a.idxK + (static_cast<size_t>(b) * a.S + tok) * DI);
+    reinterpret_cast<uint4*>(tail_row(kp, tok))[c] = __ldg(src + c);
+  }
+}
+
 size_t indexer_prefill_workspace_bytes(int B, int S, int di, int ratio) {
   return kStatusBytes + static_cast<size_t>(B) * (S / ratio) * di * sizeof(__half);
 }
@@ -402,6 +455,31 @@ cudaError_t launch_indexer_prefill(const QsaIndexerPrefillParams& p, const RopeF
   sa.eps = p.rmsNormEps;
   sa.rf = rf;
   return p.headDim == 64 ? launch_select_di<64>(sa, p.batchSize, st) : launch_select_di<128>(sa, p.batchSize, st);
+}
+
+cudaError_t launch_indexer_handoff(const QsaIndexerHandoffParams& p) {
+  HandoffArgs a;
+  a.idxK = static_cast<const __half*>(p.idxK);
+  a.ctx = p.contextLengths;
+  a.kbar = reinterpret_cast<const __half*>(static_cast<const char*>(p.workspace) + kStatusBytes);
+  a.status = static_cast<int32_t*>(p.workspace);
+  a.pool = static_cast<__half*>(p.kvPool);
+  a.pageTable = p.pageTable;
+  a.S = p.seqLen;
+  a.nbmax = p.seqLen / p.compressRatio;
+  a.ratio = p.compressRatio;
+  a.Hkv = p.numKVHeads;
+  a.D = p.kvHeadDim;
+  a.poolHeadDim = p.poolHeadDim;
+  a.numFlatPages = p.numFlatPages;
+  a.maxPagesPerSeq = p.maxPagesPerSeq;
+  dim3 grid((a.nbmax + 1 + 7) / 8, p.batchSize);  // items 0..nbmax (the last one: the raw tail)
+  cudaStream_t st = static_cast<cudaStream_t>(p.stream);
+  if (p.headDim == 64)
+    handoff_kernel<64><<<grid, 256, 0, st>>>(a);
+  else
+    handoff_kernel<128><<<grid, 256, 0, st>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace qsa

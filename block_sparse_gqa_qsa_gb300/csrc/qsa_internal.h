@@ -23,6 +23,7 @@ constexpr int kPrefillRowsPerCta = 8;      // query rows sharing one CTA's block
 constexpr int kPrefillMaxBlocks = 4096;    // block scores of a row group kept in shared memory
 size_t indexer_prefill_workspace_bytes(int B, int S, int di, int ratio);
 cudaError_t launch_indexer_prefill(const QsaIndexerPrefillParams& p, const RopeFreqs& rf);
+cudaError_t launch_indexer_handoff(const QsaIndexerHandoffParams& p);
 
 // Decode indexer ------------------------------------------------------------
 constexpr int kDecodeMaxBatch = 1024;   // the streaming scorer keeps a per-sequence page prefix on chip

@@ -145,6 +145,40 @@ typedef struct {
   void* stream;
 } QsaIndexerDecodeParams;
 
+/* Prefill -> decode hand-off of the indexer state ("Qsa Attention Plugin",
+ * "KV pool contract").  After qsa_indexer_prefill has run on a batch, this
+ * call writes that batch's indexer state into a paged KV pool, so that
+ * qsa_indexer_decode can continue each sequence at position L =
+ * contextLengths[b]:
+ *   - the key of every complete block g < floor(L/r) (the fp16 key the
+ *     prefill call left in its workspace) goes to the V-row tail of token r*g;
+ *   - the raw index key of every token of the trailing incomplete block
+ *     (r*floor(L/r) .. L-1) goes to that token's K-row tail.
+ * Tails are head 0, columns [kvHeadDim, kvHeadDim + headDim) of a pool row; no
+ * other pool byte is written.  A decode step at t = L then selects what the
+ * prefill indexer selects for row t of the same sequence extended by one token.
+ * Pages are read from pageTable rows 0 (K) and 1 (V) for tokens < L; a page id
+ * outside [0, numFlatPages) is skipped and sets bit 1 of the status word at the
+ * head of the workspace. */
+typedef struct {
+  const void* idxK;              /* fp16 [B, S, headDim] raw index keys (the prefill call's input)   */
+  const int32_t* contextLengths; /* int32 [B], as given to the prefill call                           */
+  void* workspace;               /* the qsa_indexer_prefill workspace after that call                 */
+  size_t workspaceBytes;
+  void* kvPool;                  /* fp16 [numFlatPages, 128, numKVHeads, poolHeadDim]                 */
+  const int32_t* pageTable;      /* int32 [B, 2, maxPagesPerSeq] (row 1 pre-offset by numPages)       */
+  int32_t batchSize;             /* B                                                                 */
+  int32_t seqLen;                /* S of the prefill call                                             */
+  int32_t headDim;               /* indexer head dim di (64 or 128)                                   */
+  int32_t compressRatio;         /* r of the prefill call                                             */
+  int32_t numKVHeads;            /* Hkv of the pool                                                   */
+  int32_t kvHeadDim;             /* attention head dim D: the tail starts at column D                 */
+  int32_t poolHeadDim;           /* >= kvHeadDim + headDim                                            */
+  int32_t numFlatPages;
+  int32_t maxPagesPerSeq;        /* 128 * maxPagesPerSeq >= S                                         */
+  void* stream;
+} QsaIndexerHandoffParams;
+
 /* --------------------------------------------------------------- attention */
 
 /* Sparse GQA prefill ("Cute Dsl Qsa Sparse Runner", struct
@@ -209,6 +243,7 @@ QSA_API qsa_status_t qsa_indexer_prefill(const QsaIndexerPrefillParams* params);
 QSA_API qsa_status_t qsa_indexer_decode(const QsaIndexerDecodeParams* params);
 QSA_API qsa_status_t qsa_sparse_prefill(const QsaSparsePrefillParams* params);
 QSA_API qsa_status_t qsa_sparse_decode(const QsaSparseDecodeParams* params);
+QSA_API qsa_status_t qsa_indexer_prefill_handoff(const QsaIndexerHandoffParams* params);
 
 /* Split-K sparse decode with no caller workspace.  The pages have no
  * counterpart to this entry point.  It serves callers that cannot hand device

@@ -44,7 +44,8 @@ def test_struct_layouts_match_c(binding, tmp_path):
     structs = {"QsaIndexerPrefillParams": binding.QsaIndexerPrefillParams,
                "QsaIndexerDecodeParams": binding.QsaIndexerDecodeParams,
                "QsaSparsePrefillParams": binding.QsaSparsePrefillParams,
-               "QsaSparseDecodeParams": binding.QsaSparseDecodeParams}
+               "QsaSparseDecodeParams": binding.QsaSparseDecodeParams,
+               "QsaIndexerHandoffParams": binding.QsaIndexerHandoffParams}
     lines = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', "int main(void) {"]
     for s, cls in structs.items():
         lines.append(f'printf("{s} size %zu\\n", sizeof({s}));')
@@ -90,7 +91,8 @@ def _call(binding, fn, params):
 
 def test_validation_rejects_before_launch(binding):
     L = binding.lib()
-    for fn in ("qsa_indexer_prefill", "qsa_indexer_decode", "qsa_sparse_prefill", "qsa_sparse_decode"):
+    for fn in ("qsa_indexer_prefill", "qsa_indexer_decode", "qsa_sparse_prefill", "qsa_sparse_decode",
+               "qsa_indexer_prefill_handoff"):
         assert getattr(L, fn)(None) == binding.QSA_ERR_INVALID_ARG
     fake = 1 << 20  # never dereferenced: every case below fails validation first
     sp = binding.QsaSparsePrefillParams(qPtr=fake, kPtr=fake, vPtr=fake, oPtr=fake, indices=fake,
@@ -139,6 +141,19 @@ def test_validation_rejects_before_launch(binding):
     assert _call(binding, "qsa_indexer_decode", dp) == binding.QSA_ERR_UNSUPPORTED
     dp.compressRatio, dp.topK, dp.batchSize = 4, 2051, 5000
     assert _call(binding, "qsa_indexer_decode", dp) == binding.QSA_ERR_UNSUPPORTED
+
+    hp = binding.QsaIndexerHandoffParams(idxK=fake, contextLengths=fake, workspace=fake, workspaceBytes=16,
+                                         kvPool=fake, pageTable=fake, batchSize=2, seqLen=1000, headDim=128,
+                                         compressRatio=4, numKVHeads=2, kvHeadDim=128, poolHeadDim=256, numFlatPages=8,
+                                         maxPagesPerSeq=8)
+    assert _call(binding, "qsa_indexer_prefill_handoff", hp) == binding.QSA_ERR_WORKSPACE  # 16 bytes
+    hp.maxPagesPerSeq = 7  # 896 tokens < seqLen
+    assert _call(binding, "qsa_indexer_prefill_handoff", hp) == binding.QSA_ERR_INVALID_ARG
+    hp.maxPagesPerSeq, hp.headDim = 8, 96
+    assert _call(binding, "qsa_indexer_prefill_handoff", hp) == binding.QSA_ERR_UNSUPPORTED
+    hp.headDim, hp.poolHeadDim = 128, 200
+    assert _call(binding, "qsa_indexer_prefill_handoff", hp) == binding.QSA_ERR_INVALID_ARG
+    assert L.qsa_indexer_prefill_handoff(None) == binding.QSA_ERR_INVALID_ARG
 
     sd = binding.QsaSparseDecodeParams(qPtr=fake, kvPoolPtr=fake, pageTable=fake, indices=fake,
                                        contextLengths=fake, oPtr=fake, partialO=None, partialStats=fake,
