@@ -76,6 +76,14 @@ def lib():
             L.qsa_oracle_sparse_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                                    i32, dbl, vp, i32]
             L.qsa_oracle_sparse_decode.restype = i32
+            L.qsa_oracle_sparse_prefill_bf16.argtypes = L.qsa_oracle_sparse_prefill.argtypes
+            L.qsa_oracle_sparse_prefill_bf16.restype = i32
+            L.qsa_oracle_attend_rows_bf16.argtypes = L.qsa_oracle_attend_rows.argtypes
+            L.qsa_oracle_attend_rows_bf16.restype = i32
+            L.qsa_oracle_sparse_decode_bf16.argtypes = L.qsa_oracle_sparse_decode.argtypes
+            L.qsa_oracle_sparse_decode_bf16.restype = i32
+            L.qsa_oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+            L.qsa_oracle_bf16_to_double.restype = dbl
             _lib = L
     return _lib
 
@@ -98,6 +106,10 @@ def _check(rc, what):
 
 
 # ---------------------------------------------------------------- fp16 bits
+def bf16_to_double(bits: int) -> float:
+    return lib().qsa_oracle_bf16_to_double(bits)
+
+
 def half_to_double(bits: int) -> float:
     return lib().qsa_oracle_half_to_double(int(bits) & 0xFFFF)
 
@@ -187,11 +199,13 @@ def indexer_prefill(idxQ, idxK, wq, wk, ctx, *, rot, ratio, budget, topK, theta,
     return out[0] if len(out) == 1 else tuple(out)
 
 
-def sparse_prefill(q, k, v, indices, ctx, scale, rows=None, nthreads=0):
-    """f64 attention output ([B,S,Hq,D], or [len(rows),Hq,D] with row-compact indices)."""
-    q, qp = _arr(q, np.float16)
-    k, kp = _arr(k, np.float16)
-    v, vp = _arr(v, np.float16)
+def sparse_prefill(q, k, v, indices, ctx, scale, rows=None, nthreads=0, bf16=False):
+    """f64 attention output ([B,S,Hq,D], or [len(rows),Hq,D] with row-compact indices).
+    bf16=True: q/k/v are bfloat16 bit patterns (np.uint16)."""
+    et = np.uint16 if bf16 else np.float16
+    q, qp = _arr(q, et)
+    k, kp = _arr(k, et)
+    v, vp = _arr(v, et)
     ctx, cp = _arr(ctx, np.int32)
     B, S, Hq, D = q.shape
     Hkv = k.shape[2]
@@ -200,8 +214,9 @@ def sparse_prefill(q, k, v, indices, ctx, scale, rows=None, nthreads=0):
     rows_a, rp = _opt(rows, np.int64)
     nrows = B * S if rows is None else len(rows_a)
     out = np.empty((nrows, Hq, D), np.float64)
-    rc = lib().qsa_oracle_sparse_prefill(qp, kp, vp, ip, cp, B, S, Hq, Hkv, D, topK, scale, rp, nrows,
-                                         out.ctypes.data_as(ctypes.c_void_p), nthreads)
+    fn = lib().qsa_oracle_sparse_prefill_bf16 if bf16 else lib().qsa_oracle_sparse_prefill
+    rc = fn(qp, kp, vp, ip, cp, B, S, Hq, Hkv, D, topK, scale, rp, nrows, out.ctypes.data_as(ctypes.c_void_p),
+            nthreads)
     if rc == -2:
         raise ValueError("oracle sparse_prefill: an index list names a token at or past the live length")
     _check(rc, "sparse_prefill")
@@ -252,23 +267,27 @@ def indexer_decode(idxQ, idxK, wq, wk, pool, page_table, ctx, *, D, rot, ratio, 
     return (ind, sc) if want_scores else ind
 
 
-def attend_rows(q, krows, vrows, scale):
-    """Attention of one token (q fp16 [Hq,D]) over gathered rows (fp16 [n,Hkv,D]) -> f64 [Hq,D]."""
-    q, qp = _arr(q, np.float16)
-    krows, kp = _arr(krows, np.float16)
-    vrows, vp = _arr(vrows, np.float16)
+def attend_rows(q, krows, vrows, scale, bf16=False):
+    """Attention of one token (q [Hq,D]) over gathered rows ([n,Hkv,D]) -> f64 [Hq,D]; fp16, or bfloat16
+    bit patterns (np.uint16) with bf16=True."""
+    et = np.uint16 if bf16 else np.float16
+    q, qp = _arr(q, et)
+    krows, kp = _arr(krows, et)
+    vrows, vp = _arr(vrows, et)
     Hq, D = q.shape
     n, Hkv, _ = krows.shape
     out = np.empty((Hq, D), np.float64)
-    _check(lib().qsa_oracle_attend_rows(qp, kp, vp, n, Hq, Hkv, D, scale,
-                                        out.ctypes.data_as(ctypes.c_void_p)), "attend_rows")
+    fn = lib().qsa_oracle_attend_rows_bf16 if bf16 else lib().qsa_oracle_attend_rows
+    _check(fn(qp, kp, vp, n, Hq, Hkv, D, scale, out.ctypes.data_as(ctypes.c_void_p)), "attend_rows")
     return out
 
 
-def sparse_decode(q, pool, page_table, indices, ctx, *, D, scale, nthreads=0):
-    """Decode attention over the paged pool -> f64 [B,Hq,D]."""
-    q, qp = _arr(q, np.float16)
-    pool, pp = _arr(pool, np.float16)
+def sparse_decode(q, pool, page_table, indices, ctx, *, D, scale, nthreads=0, bf16=False):
+    """Decode attention over the paged pool -> f64 [B,Hq,D]; bf16=True: q and pool are bfloat16 bit
+    patterns (np.uint16)."""
+    et = np.uint16 if bf16 else np.float16
+    q, qp = _arr(q, et)
+    pool, pp = _arr(pool, et)
     page_table, ptp = _arr(page_table, np.int32)
     indices, ip = _arr(indices, np.int32)
     ctx, cp = _arr(ctx, np.int32)
@@ -277,9 +296,9 @@ def sparse_decode(q, pool, page_table, indices, ctx, *, D, scale, nthreads=0):
     maxPages = page_table.shape[-1]
     topK = indices.shape[-1]
     out = np.empty((B, Hq, D), np.float64)
-    rc = lib().qsa_oracle_sparse_decode(qp, pp, ptp, ip, cp, B, Hq, Hkv, D, poolHeadDim, numFlatPages,
-                                        maxPages, topK, scale, out.ctypes.data_as(ctypes.c_void_p),
-                                        nthreads)
+    fn = lib().qsa_oracle_sparse_decode_bf16 if bf16 else lib().qsa_oracle_sparse_decode
+    rc = fn(qp, pp, ptp, ip, cp, B, Hq, Hkv, D, poolHeadDim, numFlatPages, maxPages, topK, scale,
+            out.ctypes.data_as(ctypes.c_void_p), nthreads)
     if rc == -2:
         raise ValueError("oracle sparse_decode: an index list names a token at or past the live length")
     _check(rc, "sparse_decode")

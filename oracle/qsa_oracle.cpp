@@ -82,6 +82,24 @@ const double* half_table() {
   return tab.data();
 }
 
+// bfloat16: the upper 16 bits of a binary32 (1 sign, 8 exponent, 7 fraction
+// bits), so widening is exact: place the bits on top of a float.
+double bf16_to_double(uint16_t h) {
+  const uint32_t u = static_cast<uint32_t>(h) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof(f));
+  return static_cast<double>(f);
+}
+
+const double* bf16_table() {
+  static const std::vector<double> tab = [] {
+    std::vector<double> t(65536);
+    for (int h = 0; h < 65536; ++h) t[h] = bf16_to_double(static_cast<uint16_t>(h));
+    return t;
+  }();
+  return tab.data();
+}
+
 // Round-to-nearest-even of a double to binary16.
 uint16_t double_to_half(double x) {
   if (std::isnan(x)) return 0x7e00;
@@ -201,11 +219,11 @@ int expand(const int32_t* sel, int nsel, int n_c, int64_t t, int r, int topK, in
 
 // Softmax attention of one query head over n rows: o = sum_j p_j v_j,
 // p = softmax(scale * q . k_j).  Empty -> zeros.  ([SR] QsaSparsePrefillParams)
+// H widens the 16-bit inputs to f64: half_table() or bf16_table().
 void attend_head(const uint16_t* q, const uint16_t* const* krows, const uint16_t* const* vrows,
-                 int64_t n, int D, double scale, double* o) {
+                 int64_t n, int D, double scale, double* o, const double* H) {
   for (int d = 0; d < D; ++d) o[d] = 0.0;
   if (n == 0) return;
-  const double* H = half_table();
   std::vector<double> qd(D), s(n);
   for (int d = 0; d < D; ++d) qd[d] = H[q[d]];
   double m = -std::numeric_limits<double>::infinity();
@@ -337,10 +355,10 @@ int32_t qsa_oracle_indexer_prefill(const uint16_t* idxQ, const uint16_t* idxK, c
   return 0;
 }
 
-int32_t qsa_oracle_sparse_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                                  const int32_t* indices, const int32_t* ctx, int32_t B, int32_t S,
-                                  int32_t Hq, int32_t Hkv, int32_t D, int32_t topK, double scale,
-                                  const int64_t* rows, int64_t nrows, double* out, int32_t nthreads) {
+int32_t sparse_prefill_impl(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* indices,
+                            const int32_t* ctx, int32_t B, int32_t S, int32_t Hq, int32_t Hkv, int32_t D,
+                            int32_t topK, double scale, const int64_t* rows, int64_t nrows, double* out,
+                            int32_t nthreads, const double* H) {
   if (!q || !k || !v || !indices || !ctx || !out) return -1;
   if (B <= 0 || S <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || topK <= 0 || Hq % Hkv != 0) return -1;
   for (int b = 0; b < B; ++b)
@@ -375,7 +393,7 @@ int32_t qsa_oracle_sparse_prefill(const uint16_t* q, const uint16_t* k, const ui
       vr.push_back(v + ((static_cast<size_t>(b) * S + j) * Hkv + g) * D);
     }
     attend_head(q + ((static_cast<size_t>(b) * S + t) * Hq + h) * D, kr.data(), vr.data(),
-                static_cast<int64_t>(kr.size()), D, scale, o);
+                static_cast<int64_t>(kr.size()), D, scale, o, H);
   });
   return bad ? -2 : 0;
 }
@@ -486,8 +504,8 @@ int32_t qsa_oracle_indexer_decode(const uint16_t* idxQ, const uint16_t* idxK, co
   return 0;
 }
 
-int32_t qsa_oracle_attend_rows(const uint16_t* q, const uint16_t* krows, const uint16_t* vrows, int64_t n,
-                               int32_t Hq, int32_t Hkv, int32_t D, double scale, double* out) {
+int32_t attend_rows_impl(const uint16_t* q, const uint16_t* krows, const uint16_t* vrows, int64_t n, int32_t Hq,
+                         int32_t Hkv, int32_t D, double scale, double* out, const double* H) {
   if (!q || !out || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0 || n < 0 || (n > 0 && (!krows || !vrows)))
     return -1;
   const int group = Hq / Hkv;
@@ -498,16 +516,16 @@ int32_t qsa_oracle_attend_rows(const uint16_t* q, const uint16_t* krows, const u
       kr[j] = krows + (j * Hkv + g) * D;
       vr[j] = vrows + (j * Hkv + g) * D;
     }
-    attend_head(q + static_cast<size_t>(h) * D, kr.data(), vr.data(), n, D, scale, out + static_cast<size_t>(h) * D);
+    attend_head(q + static_cast<size_t>(h) * D, kr.data(), vr.data(), n, D, scale, out + static_cast<size_t>(h) * D,
+                H);
   }
   return 0;
 }
 
-int32_t qsa_oracle_sparse_decode(const uint16_t* q, const uint16_t* pool, const int32_t* pageTable,
-                                 const int32_t* indices, const int32_t* ctx, int32_t B, int32_t Hq,
-                                 int32_t Hkv, int32_t D, int32_t poolHeadDim, int32_t numFlatPages,
-                                 int32_t maxPagesPerSeq, int32_t topK, double scale, double* out,
-                                 int32_t nthreads) {
+int32_t sparse_decode_impl(const uint16_t* q, const uint16_t* pool, const int32_t* pageTable,
+                           const int32_t* indices, const int32_t* ctx, int32_t B, int32_t Hq, int32_t Hkv,
+                           int32_t D, int32_t poolHeadDim, int32_t numFlatPages, int32_t maxPagesPerSeq,
+                           int32_t topK, double scale, double* out, int32_t nthreads, const double* H) {
   if (!q || !pool || !pageTable || !indices || !ctx || !out) return -1;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0 || poolHeadDim < D || topK <= 0) return -1;
   const int group = Hq / Hkv;
@@ -533,9 +551,49 @@ int32_t qsa_oracle_sparse_decode(const uint16_t* q, const uint16_t* pool, const 
       kr.push_back(pool + ((static_cast<size_t>(kp) * kTokensPerPage + j % kTokensPerPage) * Hkv + g) * poolHeadDim);
       vr.push_back(pool + ((static_cast<size_t>(vp) * kTokensPerPage + j % kTokensPerPage) * Hkv + g) * poolHeadDim);
     }
-    attend_head(q + bh * D, kr.data(), vr.data(), static_cast<int64_t>(kr.size()), D, scale, o);
+    attend_head(q + bh * D, kr.data(), vr.data(), static_cast<int64_t>(kr.size()), D, scale, o, H);
   });
   return bad ? -2 : 0;
 }
+
+int32_t qsa_oracle_sparse_prefill(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                  const int32_t* indices, const int32_t* ctx, int32_t B, int32_t S,
+                                  int32_t Hq, int32_t Hkv, int32_t D, int32_t topK, double scale,
+                                  const int64_t* rows, int64_t nrows, double* out, int32_t nthreads) {
+  return sparse_prefill_impl(q, k, v, indices, ctx, B, S, Hq, Hkv, D, topK, scale, rows, nrows, out, nthreads,
+                             half_table());
+}
+int32_t qsa_oracle_sparse_prefill_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                       const int32_t* indices, const int32_t* ctx, int32_t B, int32_t S,
+                                       int32_t Hq, int32_t Hkv, int32_t D, int32_t topK, double scale,
+                                       const int64_t* rows, int64_t nrows, double* out, int32_t nthreads) {
+  return sparse_prefill_impl(q, k, v, indices, ctx, B, S, Hq, Hkv, D, topK, scale, rows, nrows, out, nthreads,
+                             bf16_table());
+}
+int32_t qsa_oracle_attend_rows(const uint16_t* q, const uint16_t* krows, const uint16_t* vrows, int64_t n,
+                               int32_t Hq, int32_t Hkv, int32_t D, double scale, double* out) {
+  return attend_rows_impl(q, krows, vrows, n, Hq, Hkv, D, scale, out, half_table());
+}
+int32_t qsa_oracle_attend_rows_bf16(const uint16_t* q, const uint16_t* krows, const uint16_t* vrows, int64_t n,
+                                    int32_t Hq, int32_t Hkv, int32_t D, double scale, double* out) {
+  return attend_rows_impl(q, krows, vrows, n, Hq, Hkv, D, scale, out, bf16_table());
+}
+int32_t qsa_oracle_sparse_decode(const uint16_t* q, const uint16_t* pool, const int32_t* pageTable,
+                                 const int32_t* indices, const int32_t* ctx, int32_t B, int32_t Hq,
+                                 int32_t Hkv, int32_t D, int32_t poolHeadDim, int32_t numFlatPages,
+                                 int32_t maxPagesPerSeq, int32_t topK, double scale, double* out,
+                                 int32_t nthreads) {
+  return sparse_decode_impl(q, pool, pageTable, indices, ctx, B, Hq, Hkv, D, poolHeadDim, numFlatPages,
+                            maxPagesPerSeq, topK, scale, out, nthreads, half_table());
+}
+int32_t qsa_oracle_sparse_decode_bf16(const uint16_t* q, const uint16_t* pool, const int32_t* pageTable,
+                                      const int32_t* indices, const int32_t* ctx, int32_t B, int32_t Hq,
+                                      int32_t Hkv, int32_t D, int32_t poolHeadDim, int32_t numFlatPages,
+                                      int32_t maxPagesPerSeq, int32_t topK, double scale, double* out,
+                                      int32_t nthreads) {
+  return sparse_decode_impl(q, pool, pageTable, indices, ctx, B, Hq, Hkv, D, poolHeadDim, numFlatPages,
+                            maxPagesPerSeq, topK, scale, out, nthreads, bf16_table());
+}
+double qsa_oracle_bf16_to_double(uint16_t h) { return bf16_to_double(h); }
 
 }  // extern "C"

@@ -122,6 +122,26 @@ int32_t qsa_oracle_sparse_decode(const uint16_t* q, const uint16_t* pool, const 
                                  int32_t numFlatPages, int32_t maxPagesPerSeq, int32_t topK,
                                  double scale, double* out, int32_t nthreads);
 
+/* bf16 variants of the three attention passes: the same arguments, with every
+ * 16-bit tensor (q, k, v, krows, vrows, pool) read as bfloat16 bit patterns
+ * ("Cute Dsl Qsa Sparse Runner": Q/K/V are fp16 or bf16). */
+int32_t qsa_oracle_sparse_prefill_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                       const int32_t* indices, const int32_t* ctx,
+                                       int32_t B, int32_t S, int32_t Hq, int32_t Hkv, int32_t D,
+                                       int32_t topK, double scale,
+                                       const int64_t* rows, int64_t nrows, double* out,
+                                       int32_t nthreads);
+int32_t qsa_oracle_attend_rows_bf16(const uint16_t* q, const uint16_t* krows, const uint16_t* vrows,
+                                    int64_t n, int32_t Hq, int32_t Hkv, int32_t D, double scale,
+                                    double* out);
+int32_t qsa_oracle_sparse_decode_bf16(const uint16_t* q, const uint16_t* pool, const int32_t* pageTable,
+                                      const int32_t* indices, const int32_t* ctx,
+                                      int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t poolHeadDim,
+                                      int32_t numFlatPages, int32_t maxPagesPerSeq, int32_t topK,
+                                      double scale, double* out, int32_t nthreads);
+/* bfloat16 -> binary64 (exact widening). */
+double qsa_oracle_bf16_to_double(uint16_t h);
+
 #ifdef __cplusplus
 }
 #endif

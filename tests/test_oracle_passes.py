@@ -283,3 +283,66 @@ def test_decode_pool_passes_match_prefill(oracle_mod):
     pool2, pt2 = _pool_from_dense(t["idxK"], t["k"], t["v"], L_list, Hkv, D, di, maxPages, seed=10)
     out2 = oracle_mod.sparse_decode(q_tok, pool2, pt2, ind, ctx, D=D, scale=0.088)
     np.testing.assert_array_equal(out2, out)
+
+
+# ---------------------------------------------------------------- bf16 inputs
+# ("Cute Dsl Qsa Sparse Runner": Q/K/V are fp16 or bf16.)  The bf16 passes
+# are pinned to the fp16 ones: on values that both formats hold exactly the
+# two must agree to the last bit, and widening must match torch's.
+
+def _bf16_bits(x: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy() \
+        .view(np.uint16)
+
+
+def _shared_values(shape, rng):
+    """Values exact in fp16 and bf16: k/8 with |k| <= 31 (5 significant bits)."""
+    return (rng.integers(-31, 32, size=shape) / 8.0).astype(np.float32)
+
+
+def test_bf16_widening_all_patterns(oracle_mod):
+    bits = np.arange(65536, dtype=np.uint16)
+    want = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([oracle_mod.bf16_to_double(int(b)) for b in bits])
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+def test_bf16_attention_equals_fp16_on_shared_values(oracle_mod):
+    rng = np.random.default_rng(5)
+    B, S, Hq, Hkv, D, topK = 2, 40, 4, 2, 16, 24
+    q, k, v = (_shared_values(s, rng) for s in ((B, S, Hq, D), (B, S, Hkv, D), (B, S, Hkv, D)))
+    ctx = np.array([40, 29], np.int32)
+    ind = np.full((B, S, topK), -1, np.int32)
+    for b in range(B):
+        for t in range(int(ctx[b])):
+            n = min(t + 1, topK)
+            ind[b, t, :n] = rng.choice(t + 1, size=n, replace=False)
+    o16 = oracle_mod.sparse_prefill(q.astype(np.float16), k.astype(np.float16), v.astype(np.float16), ind, ctx, 0.25)
+    ob = oracle_mod.sparse_prefill(_bf16_bits(q), _bf16_bits(k), _bf16_bits(v), ind, ctx, 0.25, bf16=True)
+    assert np.array_equal(o16, ob)
+    # one index: the (bf16) value row itself
+    one = np.full((B, S, topK), -1, np.int32)
+    one[:, :, 0] = 3
+    v2 = rng.standard_normal((B, S, Hkv, D)).astype(np.float32)
+    ob1 = oracle_mod.sparse_prefill(_bf16_bits(q), _bf16_bits(k), _bf16_bits(v2), one, np.array([S, S], np.int32),
+                                    0.25, bf16=True)
+    vb = torch.from_numpy(v2).to(torch.bfloat16).to(torch.float64).numpy()
+    for h in range(Hq):
+        assert np.array_equal(ob1[:, 10, h], vb[:, 3, h // (Hq // Hkv)])
+
+
+def test_bf16_decode_equals_fp16_on_shared_values(oracle_mod):
+    rng = np.random.default_rng(6)
+    B, Hq, Hkv, D, phd, npg, topK = 2, 8, 2, 16, 24, 6, 40
+    pool = _shared_values((npg, 128, Hkv, phd), rng)
+    pt = np.stack([np.stack([np.arange(3), np.arange(3) + 3]) for _ in range(B)]).astype(np.int32)
+    q = _shared_values((B, Hq, D), rng)
+    ctx = np.array([300, 57], np.int32)
+    ind = np.full((B, topK), -1, np.int32)
+    for b in range(B):
+        ind[b, :topK - 5] = rng.choice(int(ctx[b]), size=topK - 5, replace=False)
+    o16 = oracle_mod.sparse_decode(q.astype(np.float16), pool.astype(np.float16), pt, ind, ctx, D=D, scale=0.3)
+    ob = oracle_mod.sparse_decode(_bf16_bits(q), _bf16_bits(pool), pt, ind, ctx, D=D, scale=0.3, bf16=True)
+    assert np.array_equal(o16, ob)
