@@ -380,6 +380,27 @@ def run_ours(args, rank, world, dev):
                    "blocks": nb}
         del pool
 
+    # bf16 surface of the prefill attention: the same workload and lists with bfloat16 Q/K/V/O
+    t16 = {n: pf.t[n].to(torch.bfloat16) for n in ("q", "k", "v")}
+    out16 = torch.empty(pf.out.shape, dtype=torch.bfloat16, device=dev)
+    pf.indexer()
+    ts = []
+    with clk.window():
+        for i in range(args.steps + 3):
+            flush.add_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            pf.qb.sparse_prefill(t16["q"], t16["k"], t16["v"], pf.ind, pf.t["ctx"], out16, f32(cfg.scale))
+            e1.record()
+            e1.synchronize()
+            if i >= 3:
+                ts.append(e0.elapsed_time(e1))
+    bf16_ms = statistics.mean(ts)
+    bf16 = {"workload": cfg.name, "kernel": "sparse_prefill_kernel (bf16)", "ms": round(bf16_ms, 4),
+            "achieved_gbs": round(gbytes / (bf16_ms / 1000.0) / 1e9, 1),
+            "frac": round(gbytes / (bf16_ms / 1000.0) / 1e9 / hbm_peak, 4)}
+    del t16, out16
+
     # decode workloads: one graph replay per step
     decode = []
     for dc in DECODES:
@@ -396,7 +417,7 @@ def run_ours(args, rank, world, dev):
         "value": value, "ms": ms, "tok": tok, "t_idx": statistics.mean(t_idx), "t_att": att_ms,
         "achieved": achieved, "gbytes": gbytes, "flops": flops, "cnt": cnt, "hbm_peak": hbm_peak,
         "peak_kind": peak_kind, "e2e": e2e_value, "h2d": h2d, "d2h": d2h, "clocks": clk.summary(),
-        "decode": decode, "handoff": handoff, "launches": 3 * args.steps,
+        "decode": decode, "handoff": handoff, "bf16_prefill_attention": bf16, "launches": 3 * args.steps,
     }
 
 
@@ -496,6 +517,7 @@ def main():
                          "note": "achieved counts every gathered K/V row of every (row, KV head) list; one sequence's K/V (16.8 MB) stays in L2, which serves >99% of those rows (ncu), so frac above 1 is expected and traffic (DRAM bytes per launch) is far below the algorithmic bytes"},
             "decode": r["decode"],
             "handoff": r["handoff"],
+            "bf16_prefill_attention": r["bf16_prefill_attention"],
             "e2e": {"value": r["e2e"], "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                     "note": "each step copies its inputs from pinned host memory and its output back; a second "
                             "stream overlaps step i+1's input copy and step i's output copy with step i's kernels"},

@@ -93,7 +93,9 @@ def lib() -> ctypes.CDLL:
                              ("qsa_sparse_prefill", QsaSparsePrefillParams),
                              ("qsa_sparse_decode", QsaSparseDecodeParams),
                              ("qsa_sparse_decode_noalloc", QsaSparseDecodeParams),
-                             ("qsa_indexer_prefill_handoff", QsaIndexerHandoffParams)):
+                             ("qsa_indexer_prefill_handoff", QsaIndexerHandoffParams),
+                             ("qsa_sparse_prefill_bf16", QsaSparsePrefillParams),
+                             ("qsa_sparse_decode_bf16", QsaSparseDecodeParams)):
                 f = getattr(L, name)
                 f.argtypes = [ctypes.POINTER(st)]
                 f.restype = ctypes.c_int
@@ -218,7 +220,11 @@ def indexer_prefill_handoff(idxK, ctx, workspace, pool, page_table, *, D, ratio,
 
 
 def sparse_prefill(q, k, v, indices, ctx, out, scale, stream=None):
-    """qsa_sparse_prefill: q/out fp16 [B,S,Hq,D], k/v fp16 [B,S,Hkv,D], indices int32 [B,S,topK]."""
+    """qsa_sparse_prefill (fp16 tensors) or qsa_sparse_prefill_bf16 (bfloat16 tensors):
+    q/out [B,S,Hq,D], k/v [B,S,Hkv,D], indices int32 [B,S,topK]."""
+    et = q.dtype
+    if et not in (torch.float16, torch.bfloat16):
+        raise ValueError("sparse_prefill: q must be float16 or bfloat16")
     B, S, Hq, D = q.shape
     Hkv = k.shape[2]
     topK = indices.shape[-1]
@@ -226,16 +232,21 @@ def sparse_prefill(q, k, v, indices, ctx, out, scale, stream=None):
             or indices.numel() != B * S * topK:
         raise ValueError("sparse_prefill: shape mismatch")
     p = QsaSparsePrefillParams(
-        qPtr=_ptr(q, torch.float16, "q"), kPtr=_ptr(k, torch.float16, "k"), vPtr=_ptr(v, torch.float16, "v"),
-        oPtr=_ptr(out, torch.float16, "out"), indices=_ptr(indices, torch.int32, "indices"),
+        qPtr=_ptr(q, et, "q"), kPtr=_ptr(k, et, "k"), vPtr=_ptr(v, et, "v"),
+        oPtr=_ptr(out, et, "out"), indices=_ptr(indices, torch.int32, "indices"),
         contextLengths=_ptr(ctx, torch.int32, "contextLengths"), batchSize=B, seqLen=S, numQHeads=Hq,
         numKVHeads=Hkv, headDim=D, topK=topK, attentionScale=scale, stream=_stream(stream))
-    _check(lib().qsa_sparse_prefill(ctypes.byref(p)))
+    fn = lib().qsa_sparse_prefill_bf16 if et == torch.bfloat16 else lib().qsa_sparse_prefill
+    _check(fn(ctypes.byref(p)))
 
 
 def sparse_decode(q, pool, page_table, indices, ctx, out, partial_o, partial_stats, counters, *, D, scale,
                   stream=None):
-    """qsa_sparse_decode: q/out fp16 [B,1,Hq,D]; split-K over the pool through the page table."""
+    """qsa_sparse_decode (fp16) or qsa_sparse_decode_bf16 (bfloat16 q/pool/out): q/out [B,1,Hq,D]; split-K
+    over the pool through the page table."""
+    et = q.dtype
+    if et not in (torch.float16, torch.bfloat16):
+        raise ValueError("sparse_decode: q must be float16 or bfloat16")
     B = q.shape[0]
     Hq = q.shape[-2]
     nflat, tpp, Hkv, phd = pool.shape
@@ -243,15 +254,16 @@ def sparse_decode(q, pool, page_table, indices, ctx, out, partial_o, partial_sta
     if q.numel() != B * Hq * D or out.numel() != B * Hq * D or indices.numel() != B * topK or tpp != 128:
         raise ValueError("sparse_decode: shape mismatch")
     p = QsaSparseDecodeParams(
-        qPtr=_ptr(q, torch.float16, "q"), kvPoolPtr=_ptr(pool, torch.float16, "kvPool"),
+        qPtr=_ptr(q, et, "q"), kvPoolPtr=_ptr(pool, et, "kvPool"),
         pageTable=_ptr(page_table, torch.int32, "pageTable"), indices=_ptr(indices, torch.int32, "indices"),
-        contextLengths=_ptr(ctx, torch.int32, "contextLengths"), oPtr=_ptr(out, torch.float16, "out"),
+        contextLengths=_ptr(ctx, torch.int32, "contextLengths"), oPtr=_ptr(out, et, "out"),
         partialO=_ptr(partial_o, torch.float32, "partialO"),
         partialStats=_ptr(partial_stats, torch.float32, "partialStats"),
         splitCounters=_ptr(counters, torch.int32, "splitCounters"), batchSize=B, numQHeads=Hq, numKVHeads=Hkv,
         headDim=D, poolHeadDim=phd, numFlatPages=nflat, maxPagesPerSeq=page_table.shape[-1], topK=topK,
         attentionScale=scale, stream=_stream(stream))
-    _check(lib().qsa_sparse_decode(ctypes.byref(p)))
+    fn = lib().qsa_sparse_decode_bf16 if et == torch.bfloat16 else lib().qsa_sparse_decode
+    _check(fn(ctypes.byref(p)))
 
 
 def sparse_decode_noalloc(q, pool, page_table, indices, ctx, out, *, D, scale, stream=None):

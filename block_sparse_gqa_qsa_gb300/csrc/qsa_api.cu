@@ -86,6 +86,59 @@ EncodeTiledFn encode_tiled() {
 
 }  // namespace
 
+namespace {
+
+// The attention entry points share their checks; fn names the caller in messages.
+qsa_status_t sparse_prefill_entry(const QsaSparsePrefillParams* p, const char* fn, bool bf16) {
+  if (!p) return fail(QSA_ERR_INVALID_ARG, "%s: params is NULL", fn);
+  if (!p->qPtr || !p->kPtr || !p->vPtr || !p->oPtr || !p->indices || !p->contextLengths)
+    return fail(QSA_ERR_INVALID_ARG, "%s: a tensor pointer is NULL", fn);
+  if (p->batchSize < 1 || p->seqLen < 1 || p->numQHeads < 1 || p->numKVHeads < 1 || p->headDim < 1 || p->topK < 1)
+    return fail(QSA_ERR_INVALID_ARG, "%s: sizes must be >= 1", fn);
+  if (p->numQHeads % p->numKVHeads)
+    return fail(QSA_ERR_INVALID_ARG, "%s: numQHeads %% numKVHeads != 0", fn);
+  if (!qsa_sparse_prefill_can_implement(p->numQHeads, p->numKVHeads, p->headDim))
+    return fail(QSA_ERR_UNSUPPORTED, "%s: needs headDim 128 and a GQA group of at most 16", fn);
+  if (p->topK > kMaxAttnListWidth)
+    return fail(QSA_ERR_UNSUPPORTED, "%s: topK > %d", fn, kMaxAttnListWidth);
+  if (static_cast<long long>(p->batchSize) * p->seqLen * p->numKVHeads > 0x7fffffffLL)
+    return fail(QSA_ERR_UNSUPPORTED, "%s: batchSize*seqLen*numKVHeads exceeds the grid", fn);
+  if (!aligned(p->qPtr, 16) || !aligned(p->kPtr, 16) || !aligned(p->vPtr, 16) || !aligned(p->oPtr, 16))
+    return fail(QSA_ERR_INVALID_ARG, "%s: Q/K/V/O must be 16-byte aligned", fn);
+  const cudaError_t e = qsa::launch_sparse_prefill(*p, bf16);
+  return e == cudaSuccess ? ok() : cuda_fail(e, fn);
+}
+
+
+qsa_status_t sparse_decode_entry(const QsaSparseDecodeParams* p, const char* fn, bool bf16) {
+  if (!p) return fail(QSA_ERR_INVALID_ARG, "%s: params is NULL", fn);
+  if (!p->qPtr || !p->kvPoolPtr || !p->pageTable || !p->indices || !p->contextLengths || !p->oPtr)
+    return fail(QSA_ERR_INVALID_ARG, "%s: a tensor pointer is NULL", fn);
+  if (!p->partialO || !p->partialStats || !p->splitCounters)
+    return fail(QSA_ERR_WORKSPACE, "%s: partialO/partialStats/splitCounters is NULL", fn);
+  if (p->batchSize < 1 || p->numQHeads < 1 || p->numKVHeads < 1 || p->headDim < 1 || p->topK < 1 ||
+      p->numFlatPages < 1 || p->maxPagesPerSeq < 1)
+    return fail(QSA_ERR_INVALID_ARG, "%s: sizes must be >= 1", fn);
+  if (p->numQHeads % p->numKVHeads)
+    return fail(QSA_ERR_INVALID_ARG, "%s: numQHeads %% numKVHeads != 0", fn);
+  if (p->poolHeadDim < p->headDim) return fail(QSA_ERR_INVALID_ARG, "%s: poolHeadDim < headDim", fn);
+  if (!qsa_sparse_decode_can_implement(p->numQHeads, p->numKVHeads, p->headDim, p->poolHeadDim))
+    return fail(QSA_ERR_UNSUPPORTED,
+                "%s: needs headDim 128, a GQA group of at most 16, poolHeadDim a multiple of 8", fn);
+  if (p->topK > kMaxAttnListWidth) return fail(QSA_ERR_UNSUPPORTED, "%s: topK > %d", fn, kMaxAttnListWidth);
+  if (p->batchSize > 65535 || p->numKVHeads > 65535)
+    return fail(QSA_ERR_UNSUPPORTED, "%s: batchSize/numKVHeads > 65535", fn);
+  if (static_cast<long long>(p->maxPagesPerSeq) * 128 > 0x7fffffffLL)
+    return fail(QSA_ERR_UNSUPPORTED, "%s: maxPagesPerSeq too large", fn);
+  if (!aligned(p->qPtr, 16) || !aligned(p->kvPoolPtr, 16) || !aligned(p->oPtr, 16) || !aligned(p->partialO, 16) ||
+      !aligned(p->partialStats, 4) || !aligned(p->splitCounters, 4))
+    return fail(QSA_ERR_INVALID_ARG, "%s: q/pool/o/partialO must be 16-byte aligned", fn);
+  const cudaError_t e = qsa::launch_sparse_decode(*p, bf16);
+  return e == cudaSuccess ? ok() : cuda_fail(e, fn);
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* qsa_status_string(qsa_status_t s) {
@@ -211,23 +264,10 @@ qsa_status_t qsa_indexer_decode(const QsaIndexerDecodeParams* p) {
 }
 
 qsa_status_t qsa_sparse_prefill(const QsaSparsePrefillParams* p) {
-  if (!p) return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_prefill: params is NULL");
-  if (!p->qPtr || !p->kPtr || !p->vPtr || !p->oPtr || !p->indices || !p->contextLengths)
-    return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_prefill: a tensor pointer is NULL");
-  if (p->batchSize < 1 || p->seqLen < 1 || p->numQHeads < 1 || p->numKVHeads < 1 || p->headDim < 1 || p->topK < 1)
-    return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_prefill: sizes must be >= 1");
-  if (p->numQHeads % p->numKVHeads)
-    return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_prefill: numQHeads %% numKVHeads != 0");
-  if (!qsa_sparse_prefill_can_implement(p->numQHeads, p->numKVHeads, p->headDim))
-    return fail(QSA_ERR_UNSUPPORTED, "qsa_sparse_prefill: needs headDim 128 and a GQA group of at most 16");
-  if (p->topK > kMaxAttnListWidth)
-    return fail(QSA_ERR_UNSUPPORTED, "qsa_sparse_prefill: topK > %d", kMaxAttnListWidth);
-  if (static_cast<long long>(p->batchSize) * p->seqLen * p->numKVHeads > 0x7fffffffLL)
-    return fail(QSA_ERR_UNSUPPORTED, "qsa_sparse_prefill: batchSize*seqLen*numKVHeads exceeds the grid");
-  if (!aligned(p->qPtr, 16) || !aligned(p->kPtr, 16) || !aligned(p->vPtr, 16) || !aligned(p->oPtr, 16))
-    return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_prefill: Q/K/V/O must be 16-byte aligned");
-  const cudaError_t e = qsa::launch_sparse_prefill(*p);
-  return e == cudaSuccess ? ok() : cuda_fail(e, "qsa_sparse_prefill");
+  return sparse_prefill_entry(p, "qsa_sparse_prefill", false);
+}
+qsa_status_t qsa_sparse_prefill_bf16(const QsaSparsePrefillParams* p) {
+  return sparse_prefill_entry(p, "qsa_sparse_prefill_bf16", true);
 }
 
 qsa_status_t qsa_indexer_prefill_handoff(const QsaIndexerHandoffParams* p) {
@@ -257,30 +297,10 @@ qsa_status_t qsa_indexer_prefill_handoff(const QsaIndexerHandoffParams* p) {
 }
 
 qsa_status_t qsa_sparse_decode(const QsaSparseDecodeParams* p) {
-  if (!p) return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_decode: params is NULL");
-  if (!p->qPtr || !p->kvPoolPtr || !p->pageTable || !p->indices || !p->contextLengths || !p->oPtr)
-    return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_decode: a tensor pointer is NULL");
-  if (!p->partialO || !p->partialStats || !p->splitCounters)
-    return fail(QSA_ERR_WORKSPACE, "qsa_sparse_decode: partialO/partialStats/splitCounters is NULL");
-  if (p->batchSize < 1 || p->numQHeads < 1 || p->numKVHeads < 1 || p->headDim < 1 || p->topK < 1 ||
-      p->numFlatPages < 1 || p->maxPagesPerSeq < 1)
-    return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_decode: sizes must be >= 1");
-  if (p->numQHeads % p->numKVHeads)
-    return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_decode: numQHeads %% numKVHeads != 0");
-  if (p->poolHeadDim < p->headDim) return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_decode: poolHeadDim < headDim");
-  if (!qsa_sparse_decode_can_implement(p->numQHeads, p->numKVHeads, p->headDim, p->poolHeadDim))
-    return fail(QSA_ERR_UNSUPPORTED,
-                "qsa_sparse_decode: needs headDim 128, a GQA group of at most 16, poolHeadDim a multiple of 8");
-  if (p->topK > kMaxAttnListWidth) return fail(QSA_ERR_UNSUPPORTED, "qsa_sparse_decode: topK > %d", kMaxAttnListWidth);
-  if (p->batchSize > 65535 || p->numKVHeads > 65535)
-    return fail(QSA_ERR_UNSUPPORTED, "qsa_sparse_decode: batchSize/numKVHeads > 65535");
-  if (static_cast<long long>(p->maxPagesPerSeq) * 128 > 0x7fffffffLL)
-    return fail(QSA_ERR_UNSUPPORTED, "qsa_sparse_decode: maxPagesPerSeq too large");
-  if (!aligned(p->qPtr, 16) || !aligned(p->kvPoolPtr, 16) || !aligned(p->oPtr, 16) || !aligned(p->partialO, 16) ||
-      !aligned(p->partialStats, 4) || !aligned(p->splitCounters, 4))
-    return fail(QSA_ERR_INVALID_ARG, "qsa_sparse_decode: q/pool/o/partialO must be 16-byte aligned");
-  const cudaError_t e = qsa::launch_sparse_decode(*p);
-  return e == cudaSuccess ? ok() : cuda_fail(e, "qsa_sparse_decode");
+  return sparse_decode_entry(p, "qsa_sparse_decode", false);
+}
+qsa_status_t qsa_sparse_decode_bf16(const QsaSparseDecodeParams* p) {
+  return sparse_decode_entry(p, "qsa_sparse_decode_bf16", true);
 }
 
 }  // extern "C"

@@ -34,6 +34,24 @@ constexpr int kOStride = 132;  // padded fp32 row of the warp-merge buffer
 // over 8-row groups so ldmatrix reads are bank-conflict free).
 __device__ __forceinline__ uint32_t swz(int r, int c) { return r * 256 + ((c ^ (r & 7)) << 4); }
 
+// The element type of Q/K/V/O: fp16, or bf16 (kBf16).  Copies move the 16-bit
+// values as they are; only the MMA, the rounding of P and the output differ.
+template <bool kBf16>
+__device__ __forceinline__ void mma_tile(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (kBf16)
+    mma16816_bf16(d, a, b0, b1);
+  else
+    mma16816(d, a, b0, b1);
+}
+template <bool kBf16>
+__device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
+  return kBf16 ? pack_bf162(lo, hi) : pack_half2(lo, hi);
+}
+template <bool kBf16>
+__device__ __forceinline__ void store_pair(__half* dst, float x, float y) {
+  *reinterpret_cast<uint32_t*>(dst) = pack_p<kBf16>(x, y);
+}
+
 // 2^x by the hardware approximation, results below the normal range flushed
 // to zero (probabilities that small do not change an fp16 output).
 __device__ __forceinline__ float ex2_ftz(float x) {
@@ -79,7 +97,7 @@ __device__ __forceinline__ void load_q_frags(uint32_t q_tile, uint32_t (&qf)[NT]
 }
 
 // One warp, 16 keys (tile rows 16*warp ..): S^T = K Q^T, online softmax, O^T += V^T P^T.
-template <int NT>
+template <int NT, bool kBf16>
 __device__ __forceinline__ void attend16(WarpAcc<NT>& A, uint32_t k_tile, uint32_t v_tile,
                                          const uint32_t (&qf)[NT][8][2], bool valid0, bool valid1, float sl2) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -93,7 +111,7 @@ __device__ __forceinline__ void attend16(WarpAcc<NT>& A, uint32_t k_tile, uint32
     uint32_t a[4];
     ldsm_x4(k_tile + swz(kr0 + (lane & 7) + 8 * (mi & 1), 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) mma16816(s[nt], a, qf[nt][ks][0], qf[nt][ks][1]);
+    for (int nt = 0; nt < NT; ++nt) mma_tile<kBf16>(s[nt], a, qf[nt][ks][0], qf[nt][ks][1]);
   }
   uint32_t pb[NT][2];
 #pragma unroll
@@ -123,15 +141,15 @@ __device__ __forceinline__ void attend16(WarpAcc<NT>& A, uint32_t k_tile, uint32
       A.o[mt][nt][2] *= al0;
       A.o[mt][nt][3] *= al1;
     }
-    pb[nt][0] = movmatrix_t(pack_half2(p0, p1));  // keys 0..7  -> (k = 2q..2q+1, n = g)
-    pb[nt][1] = movmatrix_t(pack_half2(p2, p3));  // keys 8..15
+    pb[nt][0] = movmatrix_t(pack_p<kBf16>(p0, p1));  // keys 0..7  -> (k = 2q..2q+1, n = g)
+    pb[nt][1] = movmatrix_t(pack_p<kBf16>(p2, p3));  // keys 8..15
   }
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
     uint32_t a[4];
     ldsm_x4_t(v_tile + swz(kr0 + (lane & 7) + 8 * (mi >> 1), 2 * mt + (mi & 1)), a[0], a[1], a[2], a[3]);
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) mma16816(A.o[mt][nt], a, pb[nt][0], pb[nt][1]);
+    for (int nt = 0; nt < NT; ++nt) mma_tile<kBf16>(A.o[mt][nt], a, pb[nt][0], pb[nt][1]);
   }
 }
 
@@ -193,7 +211,7 @@ struct PrefillArgs {
   float sl2;  // attentionScale * log2(e)
 };
 
-template <int NT, int STAGES>
+template <int NT, int STAGES, bool kBf16>
 __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_kernel(const PrefillArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t ring = smem_addr(smem);                       // [STAGES][K 16 KB | V 16 KB]
@@ -269,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_
       cp_async_wait<0>();
       __syncthreads();
       const int slot = i * kKeys + warp * 16 + (lane >> 2);
-      attend16<NT>(A, ring, ring + kTileBytes, qf, idx_s[slot] >= 0, idx_s[slot + 8] >= 0, a.sl2);
+      attend16<NT, kBf16>(A, ring, ring + kTileBytes, qf, idx_s[slot] >= 0, idx_s[slot + 8] >= 0, a.sl2);
     }
   } else {
 #pragma unroll
@@ -287,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_
       cp_async_commit();
       const int stage = i % STAGES;
       const int slot = i * kKeys + warp * 16 + (lane >> 2);
-      attend16<NT>(A, ring + stage * 2 * kTileBytes, ring + stage * 2 * kTileBytes + kTileBytes, qf,
+      attend16<NT, kBf16>(A, ring + stage * 2 * kTileBytes, ring + stage * 2 * kTileBytes + kTileBytes, qf,
                    idx_s[slot] >= 0, idx_s[slot + 8] >= 0, a.sl2);
     }
   }
@@ -309,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_
       o1 += f[w] * ow[(w * 16 + h) * kOStride + d + 1];
     }
     const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-    reinterpret_cast<__half2*>(out + h * kD)[d / 2] = __floats2half2_rn(o0 * inv, o1 * inv);
+    store_pair<kBf16>(out + h * kD + d, o0 * inv, o1 * inv);
   }
 }
 
@@ -328,7 +346,7 @@ struct DecodeArgs {
   float sl2;
 };
 
-template <int NT, int STAGES>
+template <int NT, int STAGES, bool kBf16>
 __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t ring = smem_addr(smem);
@@ -403,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_k
       cp_async_wait<0>();
       __syncthreads();
       const int slot = i * kKeys + warp * 16 + (lane >> 2);
-      attend16<NT>(A, ring, ring + kTileBytes, qf, kofs[slot] >= 0, kofs[slot + 8] >= 0, a.sl2);
+      attend16<NT, kBf16>(A, ring, ring + kTileBytes, qf, kofs[slot] >= 0, kofs[slot + 8] >= 0, a.sl2);
     }
   } else {
 #pragma unroll
@@ -421,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_k
       cp_async_commit();
       const int stage = i % STAGES;
       const int slot = i * kKeys + warp * 16 + (lane >> 2);
-      attend16<NT>(A, ring + stage * 2 * kTileBytes, ring + stage * 2 * kTileBytes + kTileBytes, qf,
+      attend16<NT, kBf16>(A, ring + stage * 2 * kTileBytes, ring + stage * 2 * kTileBytes + kTileBytes, qf,
                    kofs[slot] >= 0, kofs[slot + 8] >= 0, a.sl2);
     }
   }
@@ -481,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_k
       o1 += f * ov.y;
     }
     const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-    reinterpret_cast<__half2*>(out + h * kD)[d / 2] = __floats2half2_rn(o0 * inv, o1 * inv);
+    store_pair<kBf16>(out + h * kD + d, o0 * inv, o1 * inv);
   }
   if (tid == 0) a.counters[b * a.Hkv + kvh] = 0;
 }
@@ -505,30 +523,30 @@ size_t decode_smem(int slicePad) {
 
 constexpr int kMaxDynSmem = 227 * 1024;  // per-CTA opt-in limit; the launch asks only for what it uses
 
-template <int NT>
+template <int NT, bool kBf16>
 cudaError_t prefill_nt(const PrefillArgs& a, long long nblocks, cudaStream_t st) {
   const size_t smem = prefill_smem<NT>(a.topKpad);
-  static const cudaError_t attr = cudaFuncSetAttribute(sparse_prefill_kernel<NT, kRingStagesFor<NT>>,
+  static const cudaError_t attr = cudaFuncSetAttribute(sparse_prefill_kernel<NT, kRingStagesFor<NT>, kBf16>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
   if (attr != cudaSuccess) return attr;
-  sparse_prefill_kernel<NT, kRingStagesFor<NT>><<<static_cast<unsigned>(nblocks), kThreads, smem, st>>>(a);
+  sparse_prefill_kernel<NT, kRingStagesFor<NT>, kBf16><<<static_cast<unsigned>(nblocks), kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
-template <int NT>
+template <int NT, bool kBf16>
 cudaError_t decode_nt(const DecodeArgs& a, int B, cudaStream_t st) {
   const size_t smem = decode_smem<NT>(a.slicePad);
-  static const cudaError_t attr = cudaFuncSetAttribute(sparse_decode_kernel<NT, kRingStagesFor<NT>>,
+  static const cudaError_t attr = cudaFuncSetAttribute(sparse_decode_kernel<NT, kRingStagesFor<NT>, kBf16>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
   if (attr != cudaSuccess) return attr;
   dim3 grid(kMaxSplits, a.Hkv, B);
-  sparse_decode_kernel<NT, kRingStagesFor<NT>><<<grid, kThreads, smem, st>>>(a);
+  sparse_decode_kernel<NT, kRingStagesFor<NT>, kBf16><<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_sparse_prefill(const QsaSparsePrefillParams& p) {
+cudaError_t launch_sparse_prefill(const QsaSparsePrefillParams& p, bool bf16) {
   PrefillArgs a;
   a.q = static_cast<const __half*>(p.qPtr);
   a.k = static_cast<const __half*>(p.kPtr);
@@ -545,10 +563,11 @@ cudaError_t launch_sparse_prefill(const QsaSparsePrefillParams& p) {
   a.sl2 = p.attentionScale * kLog2e;
   const long long nblocks = static_cast<long long>(p.batchSize) * p.seqLen * p.numKVHeads;
   cudaStream_t st = static_cast<cudaStream_t>(p.stream);
-  return a.G <= 8 ? prefill_nt<1>(a, nblocks, st) : prefill_nt<2>(a, nblocks, st);
+  if (bf16) return a.G <= 8 ? prefill_nt<1, true>(a, nblocks, st) : prefill_nt<2, true>(a, nblocks, st);
+  return a.G <= 8 ? prefill_nt<1, false>(a, nblocks, st) : prefill_nt<2, false>(a, nblocks, st);
 }
 
-cudaError_t launch_sparse_decode(const QsaSparseDecodeParams& p) {
+cudaError_t launch_sparse_decode(const QsaSparseDecodeParams& p, bool bf16) {
   DecodeArgs a;
   a.q = static_cast<const __half*>(p.qPtr);
   a.pool = static_cast<const __half*>(p.kvPoolPtr);
@@ -570,7 +589,8 @@ cudaError_t launch_sparse_decode(const QsaSparseDecodeParams& p) {
   a.slicePad = (a.sliceLen + kKeys - 1) / kKeys * kKeys;
   a.sl2 = p.attentionScale * kLog2e;
   cudaStream_t st = static_cast<cudaStream_t>(p.stream);
-  return a.G <= 8 ? decode_nt<1>(a, p.batchSize, st) : decode_nt<2>(a, p.batchSize, st);
+  if (bf16) return a.G <= 8 ? decode_nt<1, true>(a, p.batchSize, st) : decode_nt<2, true>(a, p.batchSize, st);
+  return a.G <= 8 ? decode_nt<1, false>(a, p.batchSize, st) : decode_nt<2, false>(a, p.batchSize, st);
 }
 
 }  // namespace qsa

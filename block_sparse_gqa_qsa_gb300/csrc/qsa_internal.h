@@ -32,8 +32,9 @@ cudaError_t launch_indexer_decode(const QsaIndexerDecodeParams& p, const RopeFre
                                   const CUtensorMap& kbarMap);
 
 // Attention -----------------------------------------------------------------
-cudaError_t launch_sparse_prefill(const QsaSparsePrefillParams& p);
-cudaError_t launch_sparse_decode(const QsaSparseDecodeParams& p);
+// bf16: Q/K/V/O (prefill) or q/pool/o (decode) hold bfloat16 instead of fp16.
+cudaError_t launch_sparse_prefill(const QsaSparsePrefillParams& p, bool bf16 = false);
+cudaError_t launch_sparse_decode(const QsaSparseDecodeParams& p, bool bf16 = false);
 
 // Stores msg as the calling thread's qsa_last_error_message() and returns s.
 qsa_status_t record_error(qsa_status_t s, const char* msg);

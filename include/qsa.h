@@ -245,6 +245,16 @@ QSA_API qsa_status_t qsa_sparse_prefill(const QsaSparsePrefillParams* params);
 QSA_API qsa_status_t qsa_sparse_decode(const QsaSparseDecodeParams* params);
 QSA_API qsa_status_t qsa_indexer_prefill_handoff(const QsaIndexerHandoffParams* params);
 
+/* The two attention calls with bfloat16 tensors ("Cute Dsl Qsa Sparse Runner":
+ * the runners take fp16 or bf16): the same params structs, contract and
+ * checks, with qPtr/kPtr/vPtr/oPtr (prefill) and qPtr/kvPoolPtr/oPtr (decode)
+ * holding bf16 instead of fp16.  Arithmetic: products in fp32, softmax in fp32,
+ * P rounded to bf16 for the PV product, fp32 accumulation, output rounded to
+ * bf16.  The decode indexer keeps its fp16 tails in a bf16 pool's columns
+ * [kvHeadDim, kvHeadDim + headDim): the attention never reads them. */
+QSA_API qsa_status_t qsa_sparse_prefill_bf16(const QsaSparsePrefillParams* params);
+QSA_API qsa_status_t qsa_sparse_decode_bf16(const QsaSparseDecodeParams* params);
+
 /* Split-K sparse decode with no caller workspace.  The pages have no
  * counterpart to this entry point.  It serves callers that cannot hand device
  * memory to a library call on their decode path: an engine whose memory is
