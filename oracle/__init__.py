@@ -82,6 +82,9 @@ def lib():
             L.qsa_oracle_attend_rows_bf16.restype = i32
             L.qsa_oracle_sparse_decode_bf16.argtypes = L.qsa_oracle_sparse_decode.argtypes
             L.qsa_oracle_sparse_decode_bf16.restype = i32
+            L.qsa_oracle_rope_qkv.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, dbl, dbl, vp, vp, vp,
+                                              i32]
+            L.qsa_oracle_rope_qkv.restype = i32
             L.qsa_oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
             L.qsa_oracle_bf16_to_double.restype = dbl
             _lib = L
@@ -303,3 +306,22 @@ def sparse_decode(q, pool, page_table, indices, ctx, *, D, scale, nthreads=0, bf
         raise ValueError("oracle sparse_decode: an index list names a token at or past the live length")
     _check(rc, "sparse_decode")
     return out
+
+
+def rope_qkv(qkv, qw, kw, ctx, *, Hq, Hkv, rot, theta, eps, nthreads=0):
+    """Upstream q/k norm + partial RoPE of packed QKV fp16 [B,S,Hq+2Hkv,D] -> (q [B,S,Hq,D], k, v [B,S,Hkv,D]),
+    fp16 rounded once from f64."""
+    qkv, xp = _arr(qkv, np.float16)
+    qw, qwp = _arr(qw, np.float32)
+    kw, kwp = _arr(kw, np.float32)
+    ctx, cp = _arr(ctx, np.int32)
+    B, S, NH, D = qkv.shape
+    if NH != Hq + 2 * Hkv:
+        raise ValueError("rope_qkv: head count mismatch")
+    q = np.empty((B, S, Hq, D), np.float16)
+    k = np.empty((B, S, Hkv, D), np.float16)
+    v = np.empty((B, S, Hkv, D), np.float16)
+    _check(lib().qsa_oracle_rope_qkv(xp, qwp, kwp, cp, B, S, Hq, Hkv, D, rot, theta, eps,
+                                     q.ctypes.data_as(ctypes.c_void_p), k.ctypes.data_as(ctypes.c_void_p),
+                                     v.ctypes.data_as(ctypes.c_void_p), nthreads), "rope_qkv")
+    return q, k, v

@@ -596,4 +596,42 @@ int32_t qsa_oracle_sparse_decode_bf16(const uint16_t* q, const uint16_t* pool, c
 }
 double qsa_oracle_bf16_to_double(uint16_t h) { return bf16_to_double(h); }
 
+// Upstream step of the attention layer ("Qsa Attention Plugin", fused step 1):
+// split a packed QKV row into heads; q and k heads get the per-head RMSNorm
+// with (1 + w) and the partial RoPE at the row's position (the same two
+// operations as the index-query prep), v heads pass through; every output is
+// rounded once to fp16.  Row s is at position s when S > 1 (prefill from 0) and
+// at L - 1 when S == 1 (one new token); rows at or past L are zeros.
+int32_t qsa_oracle_rope_qkv(const uint16_t* qkv, const float* qw, const float* kw, const int32_t* ctx, int32_t B,
+                            int32_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t rot, double theta, double eps,
+                            uint16_t* qout, uint16_t* kout, uint16_t* vout, int32_t nthreads) {
+  if (!qkv || !qw || !kw || !ctx || !qout || !kout || !vout) return -1;
+  if (B <= 0 || S <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || rot < 0 || rot > D || (rot & 1)) return -1;
+  const int NH = Hq + 2 * Hkv;
+  parallel_for(static_cast<int64_t>(B) * S * NH, nthreads, [&](int64_t i) {
+    const int h = static_cast<int>(i % NH);
+    const int64_t bs = i / NH;
+    const int b = static_cast<int>(bs / S), s = static_cast<int>(bs % S);
+    const int L = ctx[b];
+    const bool live = S == 1 ? L >= 1 : s < L;
+    const int64_t pos = S == 1 ? static_cast<int64_t>(L) - 1 : s;
+    const uint16_t* x = qkv + (bs * NH + h) * D;
+    uint16_t* dst = h < Hq ? qout + (bs * Hq + h) * D
+                  : h < Hq + Hkv ? kout + (bs * Hkv + (h - Hq)) * D
+                                 : vout + (bs * Hkv + (h - Hq - Hkv)) * D;
+    if (!live) {
+      for (int d = 0; d < D; ++d) dst[d] = 0;
+      return;
+    }
+    if (h >= Hq + Hkv) {
+      for (int d = 0; d < D; ++d) dst[d] = x[d];
+      return;
+    }
+    std::vector<double> y(D);
+    index_q(x, h < Hq ? qw : kw, D, rot, pos, theta, eps, y.data());
+    for (int d = 0; d < D; ++d) dst[d] = double_to_half(y[d]);
+  });
+  return 0;
+}
+
 }  // extern "C"

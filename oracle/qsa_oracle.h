@@ -139,6 +139,17 @@ int32_t qsa_oracle_sparse_decode_bf16(const uint16_t* q, const uint16_t* pool, c
                                       int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t poolHeadDim,
                                       int32_t numFlatPages, int32_t maxPagesPerSeq, int32_t topK,
                                       double scale, double* out, int32_t nthreads);
+/* Upstream step of the attention layer: packed QKV fp16 [B][S][Hq + 2*Hkv][D]
+ * (q heads, then k heads, then v heads) -> qout fp16 [B][S][Hq][D] and
+ * kout / vout fp16 [B][S][Hkv][D].  q and k heads: RMSNorm*(1+w) (qw, kw fp32
+ * [D]) then partial RoPE on [0, rot) at the row's position, rounded once to
+ * fp16; v heads copied.  Row s is at position s when S > 1, at ctx[b]-1 when
+ * S == 1; rows at or past the live length are zeros. */
+int32_t qsa_oracle_rope_qkv(const uint16_t* qkv, const float* qw, const float* kw, const int32_t* ctx,
+                            int32_t B, int32_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t rot,
+                            double theta, double eps, uint16_t* qout, uint16_t* kout, uint16_t* vout,
+                            int32_t nthreads);
+
 /* bfloat16 -> binary64 (exact widening). */
 double qsa_oracle_bf16_to_double(uint16_t h);
 

@@ -346,3 +346,37 @@ def test_bf16_decode_equals_fp16_on_shared_values(oracle_mod):
     o16 = oracle_mod.sparse_decode(q.astype(np.float16), pool.astype(np.float16), pt, ind, ctx, D=D, scale=0.3)
     ob = oracle_mod.sparse_decode(_bf16_bits(q), _bf16_bits(pool), pt, ind, ctx, D=D, scale=0.3, bf16=True)
     assert np.array_equal(o16, ob)
+
+
+# ------------------------------------------------ upstream q/k norm + RoPE
+# ("Qsa Attention Plugin", fused step 1: packed-QKV split, per-head qk-norm
+# with (1 + w), partial RoPE.)  Pinned to the index-query prep, which carries
+# the RMSNorm and RoPE pins above, and to fp16 round-to-nearest-even.
+
+def test_rope_qkv_heads_positions_and_padding(oracle_mod):
+    rng = np.random.default_rng(9)
+    B, S, Hq, Hkv, D, rot = 2, 7, 4, 2, 64, 32
+    qkv = rng.standard_normal((B, S, Hq + 2 * Hkv, D)).astype(np.float16)
+    qw = (0.1 * rng.standard_normal(D)).astype(np.float32)
+    kw = (0.1 * rng.standard_normal(D)).astype(np.float32)
+    ctx = np.array([7, 4], np.int32)
+    q, k, v = oracle_mod.rope_qkv(qkv, qw, kw, ctx, Hq=Hq, Hkv=Hkv, rot=rot, theta=1e4, eps=1e-6)
+    for b in range(B):
+        for s in range(S):
+            if s >= ctx[b]:
+                assert not q[b, s].any() and not k[b, s].any() and not v[b, s].any()
+                continue
+            for h in range(Hq):
+                want = oracle_mod.index_q(qkv[b, s, h], qw, rot=rot, pos=s, theta=1e4, eps=1e-6).astype(np.float16)
+                assert np.array_equal(q[b, s, h].view(np.uint16), want.view(np.uint16))
+            for h in range(Hkv):
+                want = oracle_mod.index_q(qkv[b, s, Hq + h], kw, rot=rot, pos=s, theta=1e4, eps=1e-6).astype(np.float16)
+                assert np.array_equal(k[b, s, h].view(np.uint16), want.view(np.uint16))
+                assert np.array_equal(v[b, s, h].view(np.uint16), qkv[b, s, Hq + Hkv + h].view(np.uint16))
+    # one new token (S == 1) sits at position L - 1
+    q1, k1, _ = oracle_mod.rope_qkv(qkv[:, :1], qw, kw, np.array([300, 1], np.int32), Hq=Hq, Hkv=Hkv, rot=rot,
+                                    theta=1e4, eps=1e-6)
+    want = oracle_mod.index_q(qkv[0, 0, 1], qw, rot=rot, pos=299, theta=1e4, eps=1e-6).astype(np.float16)
+    assert np.array_equal(q1[0, 0, 1].view(np.uint16), want.view(np.uint16))
+    want = oracle_mod.index_q(qkv[1, 0, Hq], kw, rot=rot, pos=0, theta=1e4, eps=1e-6).astype(np.float16)
+    assert np.array_equal(k1[1, 0, 0].view(np.uint16), want.view(np.uint16))
