@@ -5,7 +5,9 @@ Headline: prefill tokens/s on the 8K workload (B=1, S=8192, Hq=32, Hkv=4,
 D=128, indexer 8 x 128, rot 64, ratio 4, budget 512, topK 2051): one step is
 qsa_indexer_prefill + qsa_sparse_prefill over one batch already resident in
 HBM, timed with CUDA events per step on the launching stream, L2 flushed
-(a 512 MB write) between steps outside the timed events.  The same line
+between steps outside the timed events (a 512 MB write, then a 256 MB read
+of another buffer, so that L2 holds neither the step's data nor dirty lines
+whose write-back the step would pay).  The same line
 carries the decode us/step of the two decode workloads (one CUDA-graph replay
 of qsa_indexer_decode + qsa_sparse_decode), the roofline of the dominant
 kernel, an end-to-end figure through the C ABI with host buffers, the CPU
@@ -51,8 +53,8 @@ def f32(x):
 # DRAM read+write bytes of one sparse_prefill_kernel launch on the 8K prefill workload, from the ncu
 # capture summarised in profiles/prefill_kernels__prefill_S8192.md.  Reported only while the
 # kernel's sources hash to the value they had when the counters were taken.
-PROFILED_TRAFFIC = {"bytes": 202_220_288, "sources": ("qsa_attention.cu", "qsa_device.cuh"),
-                    "sha256": "883aeec793b2f475f060afb30ece72148d867cd95a5b78d1f4a068e68764343e"}
+PROFILED_TRAFFIC = {"bytes": 201_645_568, "sources": ("qsa_attention.cu", "qsa_device.cuh"),
+                    "sha256": "b0c9cc3ff12db9a45fbbc380793922efd092f99677ac57f3ab3ed78810e534df"}
 
 
 def profiled_traffic():
@@ -240,6 +242,20 @@ class Decode:
                               scale=f32(c.scale))
 
 
+class L2Flush:
+    """Evicts everything from L2 between timed steps: a write of FLUSH_BYTES (> L2), then a read of
+    half as much from a second buffer, which turns the written buffer's dirty lines into clean,
+    unrelated ones."""
+
+    def __init__(self, dev):
+        self.w = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.r = torch.zeros(FLUSH_BYTES // 8, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.add_(1)
+        self.r.sum()
+
+
 def time_decode(dec, flush, clk, reps=50, warm=10):
     for _ in range(3):
         dec.step()
@@ -253,7 +269,7 @@ def time_decode(dec, flush, clk, reps=50, warm=10):
     times = []
     with clk.window():
         for _ in range(reps):
-            flush.add_(1)
+            flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             g.replay()
@@ -269,7 +285,7 @@ def run_ours(args, rank, world, dev):
     hbm_peak, _, peak_kind = peaks()
     cfg = HEADLINE
     pf = Prefill(cfg, dev)
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     clk = ClockSampler(torch.cuda.current_device())
     clk.__enter__()
     for _ in range(max(args.warmup, 3)):
@@ -282,7 +298,7 @@ def run_ours(args, rank, world, dev):
     t_idx, t_att, t_step = [], [], []
     with clk.window():
         for _ in range(args.steps):
-            flush.add_(1)  # L2 flush, outside the timed events
+            flush()  # L2 flush, outside the timed events
             e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
             e[0].record()
             pf.indexer()
@@ -366,7 +382,7 @@ def run_ours(args, rank, world, dev):
         ts = []
         with clk.window():
             for i in range(args.steps + 3):
-                flush.add_(1)
+                flush()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record()
                 pf.qb.indexer_prefill_handoff(pf.t["idxK"], pf.t["ctx"], pf.ws, pool, pt, D=cfg.D, ratio=cfg.ratio)
@@ -387,7 +403,7 @@ def run_ours(args, rank, world, dev):
     ts = []
     with clk.window():
         for i in range(args.steps + 3):
-            flush.add_(1)
+            flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             pf.qb.sparse_prefill(t16["q"], t16["k"], t16["v"], pf.ind, pf.t["ctx"], out16, f32(cfg.scale))
@@ -400,6 +416,29 @@ def run_ours(args, rank, world, dev):
             "achieved_gbs": round(gbytes / (bf16_ms / 1000.0) / 1e9, 1),
             "frac": round(gbytes / (bf16_ms / 1000.0) / 1e9 / hbm_peak, 4)}
     del t16, out16
+
+    # upstream q/k norm + partial RoPE of the workload's packed QKV (dense q/k/v outputs)
+    qkv = torch.cat([pf.t["q"], pf.t["k"], pf.t["v"]], dim=2).contiguous()
+    qo = torch.empty_like(pf.t["q"])
+    ko, vo = torch.empty_like(pf.t["k"]), torch.empty_like(pf.t["v"])
+    ts = []
+    with clk.window():
+        for i in range(args.steps + 3):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            pf.qb.rope_qkv(qkv, pf.t["wq"], pf.t["wk"], pf.t["ctx"], qo, Hq=cfg.Hq, Hkv=cfg.Hkv, rot=cfg.rot,
+                           theta=cfg.theta, eps=cfg.eps, k_out=ko, v_out=vo)
+            e1.record()
+            e1.synchronize()
+            if i >= 3:
+                ts.append(e0.elapsed_time(e1) * 1000.0)
+    rope_bytes = 2 * qkv.numel() * qkv.element_size()  # read once, written once (q, k, v)
+    rope_us = statistics.median(ts)
+    rope = {"workload": f"{cfg.name} packed QKV", "us": round(rope_us, 2), "bytes": rope_bytes,
+            "achieved_gbs": round(rope_bytes / (rope_us * 1e-6) / 1e9, 1),
+            "frac": round(rope_bytes / (rope_us * 1e-6) / 1e9 / hbm_peak, 4)}
+    del qkv, qo, ko, vo
 
     # decode workloads: one graph replay per step
     decode = []
@@ -417,7 +456,8 @@ def run_ours(args, rank, world, dev):
         "value": value, "ms": ms, "tok": tok, "t_idx": statistics.mean(t_idx), "t_att": att_ms,
         "achieved": achieved, "gbytes": gbytes, "flops": flops, "cnt": cnt, "hbm_peak": hbm_peak,
         "peak_kind": peak_kind, "e2e": e2e_value, "h2d": h2d, "d2h": d2h, "clocks": clk.summary(),
-        "decode": decode, "handoff": handoff, "bf16_prefill_attention": bf16, "launches": 3 * args.steps,
+        "decode": decode, "handoff": handoff, "bf16_prefill_attention": bf16, "rope_qkv": rope,
+        "launches": 3 * args.steps,
     }
 
 
@@ -508,7 +548,7 @@ def main():
             "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
             "config": {"workload": cfg.name, "B": cfg.B, "S": cfg.S, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "D": cfg.D,
                        "indexer": f"{cfg.Hi}x{cfg.di} rot {cfg.rot}", "ratio": cfg.ratio, "budget": cfg.budget,
-                       "topK": cfg.topK, "l2": "flushed between steps (512 MB write)", "parallelism": "replicas"},
+                       "topK": cfg.topK, "l2": "flushed between steps (512 MB write, then 256 MB read)", "parallelism": "replicas"},
             "stages_ms": {"indexer_prefill": round(r["t_idx"], 4), "sparse_prefill": round(r["t_att"], 4)},
             "roofline": {"kernel": "sparse_prefill_kernel", "bound": "hbm", "achieved": round(r["achieved"], 1),
                          "peak": r["hbm_peak"], "unit": "GB/s", "frac": round(r["achieved"] / r["hbm_peak"], 4),
@@ -518,6 +558,7 @@ def main():
             "decode": r["decode"],
             "handoff": r["handoff"],
             "bf16_prefill_attention": r["bf16_prefill_attention"],
+            "rope_qkv": r["rope_qkv"],
             "e2e": {"value": r["e2e"], "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                     "note": "each step copies its inputs from pinned host memory and its output back; a second "
                             "stream overlaps step i+1's input copy and step i's output copy with step i's kernels"},

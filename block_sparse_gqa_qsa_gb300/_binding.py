@@ -60,6 +60,16 @@ class QsaIndexerHandoffParams(ctypes.Structure):
                 ("maxPagesPerSeq", _i32), ("stream", ctypes.c_void_p)]
 
 
+class QsaRopeQkvParams(ctypes.Structure):
+    _fields_ = [("qkv", ctypes.c_void_p), ("qNormW", ctypes.c_void_p), ("kNormW", ctypes.c_void_p),
+                ("contextLengths", ctypes.c_void_p), ("qOut", ctypes.c_void_p), ("kOut", ctypes.c_void_p),
+                ("vOut", ctypes.c_void_p), ("kvPool", ctypes.c_void_p), ("pageTable", ctypes.c_void_p),
+                ("batchSize", _i32), ("seqLen", _i32), ("numQHeads", _i32), ("numKVHeads", _i32),
+                ("headDim", _i32), ("rotDim", _i32), ("poolHeadDim", _i32), ("numFlatPages", _i32),
+                ("maxPagesPerSeq", _i32), ("ropeTheta", ctypes.c_float), ("rmsNormEps", ctypes.c_float),
+                ("stream", ctypes.c_void_p)]
+
+
 class QsaSparsePrefillParams(ctypes.Structure):
     _fields_ = [("qPtr", _vp), ("kPtr", _vp), ("vPtr", _vp), ("oPtr", _vp), ("indices", _vp),
                 ("contextLengths", _vp), ("batchSize", _i32), ("seqLen", _i32), ("numQHeads", _i32),
@@ -95,7 +105,8 @@ def lib() -> ctypes.CDLL:
                              ("qsa_sparse_decode_noalloc", QsaSparseDecodeParams),
                              ("qsa_indexer_prefill_handoff", QsaIndexerHandoffParams),
                              ("qsa_sparse_prefill_bf16", QsaSparsePrefillParams),
-                             ("qsa_sparse_decode_bf16", QsaSparseDecodeParams)):
+                             ("qsa_sparse_decode_bf16", QsaSparseDecodeParams),
+                             ("qsa_rope_qkv", QsaRopeQkvParams)):
                 f = getattr(L, name)
                 f.argtypes = [ctypes.POINTER(st)]
                 f.restype = ctypes.c_int
@@ -217,6 +228,33 @@ def indexer_prefill_handoff(idxK, ctx, workspace, pool, page_table, *, D, ratio,
         batchSize=B, seqLen=S, headDim=di, compressRatio=ratio, numKVHeads=Hkv, kvHeadDim=D, poolHeadDim=phd,
         numFlatPages=nflat, maxPagesPerSeq=page_table.shape[-1], stream=_stream(stream))
     _check(lib().qsa_indexer_prefill_handoff(ctypes.byref(p)))
+
+
+def rope_qkv(qkv, wq, wk, ctx, q_out, *, Hq, Hkv, rot, theta, eps, k_out=None, v_out=None, pool=None,
+             page_table=None, stream=None):
+    """qsa_rope_qkv: packed qkv fp16 [B,S,Hq+2Hkv,D] -> q_out [B,S,Hq,D]; optional dense k_out / v_out
+    [B,S,Hkv,D] and pool K/V rows through the page table."""
+    B, S, NH, D = qkv.shape
+    if NH != Hq + 2 * Hkv or tuple(q_out.shape) != (B, S, Hq, D):
+        raise ValueError("rope_qkv: shape mismatch")
+    for t in (k_out, v_out):
+        if t is not None and tuple(t.shape) != (B, S, Hkv, D):
+            raise ValueError("rope_qkv: k_out/v_out shape mismatch")
+    nflat = phd = mpp = 0
+    if pool is not None:
+        nflat, tpp, ph, phd = pool.shape
+        if tpp != 128 or ph != Hkv or page_table is None or tuple(page_table.shape[:2]) != (B, 2):
+            raise ValueError("rope_qkv: pool/page table shape mismatch")
+        mpp = page_table.shape[-1]
+    p = QsaRopeQkvParams(
+        qkv=_ptr(qkv, torch.float16, "qkv"), qNormW=_ptr(wq, torch.float32, "qNormW"),
+        kNormW=_ptr(wk, torch.float32, "kNormW"), contextLengths=_ptr(ctx, torch.int32, "contextLengths"),
+        qOut=_ptr(q_out, torch.float16, "q_out"), kOut=_ptr(k_out, torch.float16, "k_out"),
+        vOut=_ptr(v_out, torch.float16, "v_out"), kvPool=_ptr(pool, torch.float16, "kvPool"),
+        pageTable=_ptr(page_table, torch.int32, "pageTable"), batchSize=B, seqLen=S, numQHeads=Hq,
+        numKVHeads=Hkv, headDim=D, rotDim=rot, poolHeadDim=phd, numFlatPages=nflat, maxPagesPerSeq=mpp,
+        ropeTheta=theta, rmsNormEps=eps, stream=_stream(stream))
+    _check(lib().qsa_rope_qkv(ctypes.byref(p)))
 
 
 def sparse_prefill(q, k, v, indices, ctx, out, scale, stream=None):

@@ -270,6 +270,40 @@ qsa_status_t qsa_sparse_prefill_bf16(const QsaSparsePrefillParams* p) {
   return sparse_prefill_entry(p, "qsa_sparse_prefill_bf16", true);
 }
 
+qsa_status_t qsa_rope_qkv(const QsaRopeQkvParams* p) {
+  if (!p) return fail(QSA_ERR_INVALID_ARG, "qsa_rope_qkv: params is NULL");
+  if (!p->qkv || !p->qNormW || !p->kNormW || !p->contextLengths || !p->qOut)
+    return fail(QSA_ERR_INVALID_ARG, "qsa_rope_qkv: a required pointer is NULL");
+  if (p->batchSize < 1 || p->seqLen < 1 || p->numQHeads < 1 || p->numKVHeads < 1)
+    return fail(QSA_ERR_INVALID_ARG, "qsa_rope_qkv: sizes must be >= 1");
+  if (p->headDim != 64 && p->headDim != 128)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_rope_qkv: headDim %d not 64 or 128", p->headDim);
+  if (p->rotDim < 0 || p->rotDim > p->headDim || (p->rotDim & 1) || !(p->ropeTheta > 0.f) || !(p->rmsNormEps >= 0.f))
+    return fail(QSA_ERR_INVALID_ARG, "qsa_rope_qkv: rotDim must be even and <= headDim; theta > 0, eps >= 0");
+  if (static_cast<long long>(p->numQHeads + 2LL * p->numKVHeads) * p->headDim * 2 > qsa::kRopeMaxRowBytes)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_rope_qkv: (numQHeads + 2 numKVHeads) * headDim * 2 exceeds %d bytes",
+                qsa::kRopeMaxRowBytes);
+  if (p->rotDim % 16)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_rope_qkv: rotDim %d is not a multiple of 16 (rotation partners are "
+                                     "exchanged as whole 8-element chunks)", p->rotDim);
+  if (!aligned(p->qkv, 16) || !aligned(p->qOut, 16) || !aligned(p->kOut, 16) || !aligned(p->vOut, 16) ||
+      !aligned(p->kvPool, 16))
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_rope_qkv: qkv, qOut, kOut, vOut and kvPool must be 16-byte aligned");
+  if (static_cast<long long>(p->batchSize) * p->seqLen > 0x7fffffffLL)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_rope_qkv: batchSize*seqLen exceeds the grid");
+  if (p->kvPool) {
+    if (!p->pageTable || p->poolHeadDim < p->headDim || p->numFlatPages < 1 || p->maxPagesPerSeq < 1)
+      return fail(QSA_ERR_INVALID_ARG, "qsa_rope_qkv: kvPool needs pageTable, poolHeadDim >= headDim and page counts");
+    if (p->poolHeadDim % 8)
+      return fail(QSA_ERR_UNSUPPORTED, "qsa_rope_qkv: poolHeadDim %d is not a multiple of 8 (16-byte row writes)",
+                  p->poolHeadDim);
+    if (static_cast<long long>(p->maxPagesPerSeq) * qsa::kTokensPerPageHost > 0x7fffffffLL)
+      return fail(QSA_ERR_UNSUPPORTED, "qsa_rope_qkv: maxPagesPerSeq too large");
+  }
+  const cudaError_t e = qsa::launch_rope_qkv(*p, rope_freqs(p->ropeTheta, p->rotDim));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "qsa_rope_qkv");
+}
+
 qsa_status_t qsa_indexer_prefill_handoff(const QsaIndexerHandoffParams* p) {
   if (!p) return fail(QSA_ERR_INVALID_ARG, "qsa_indexer_prefill_handoff: params is NULL");
   if (!p->idxK || !p->contextLengths || !p->workspace || !p->kvPool || !p->pageTable)

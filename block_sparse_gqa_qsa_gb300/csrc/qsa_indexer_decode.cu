@@ -766,6 +766,8 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
   if (tid == 0) a.ticket[b] = 0;
 }
 
+}  // namespace
+
 int sm_count() {
   static int cached[64] = {0};
   int dev = 0;
@@ -777,8 +779,6 @@ int sm_count() {
   }
   return cached[dev];
 }
-
-}  // namespace
 
 size_t indexer_decode_workspace_bytes(int B, int maxPagesPerSeq, int ratio, int budget) {
   const int nbmax = maxPagesPerSeq * (kTokensPerPageHost / ratio);

@@ -36,6 +36,13 @@ cudaError_t launch_indexer_decode(const QsaIndexerDecodeParams& p, const RopeFre
 cudaError_t launch_sparse_prefill(const QsaSparsePrefillParams& p, bool bf16 = false);
 cudaError_t launch_sparse_decode(const QsaSparseDecodeParams& p, bool bf16 = false);
 
+// Upstream q/k norm + RoPE ------------------------------------------------------
+cudaError_t launch_rope_qkv(const QsaRopeQkvParams& p, const RopeFreqs& rf);
+constexpr int kRopeMaxRowBytes = 64 * 1024;  // one token's packed heads, staged in shared memory
+
+// SMs of the current device (cached per device).
+int sm_count();
+
 // Stores msg as the calling thread's qsa_last_error_message() and returns s.
 qsa_status_t record_error(qsa_status_t s, const char* msg);
 

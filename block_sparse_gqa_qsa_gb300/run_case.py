@@ -9,6 +9,10 @@ of tens).
 
     python -m block_sparse_gqa_qsa_gb300.run_case prefill_S8192 --steps 2
     python -m block_sparse_gqa_qsa_gb300.run_case decode_long_B8_L512k --B 1 --steps 2
+    python -m block_sparse_gqa_qsa_gb300.run_case prefill_S8192 --op rope --steps 2
+
+`--op rope` runs qsa_rope_qkv on the workload's packed QKV instead (prefill
+workloads: dense q/k/v outputs).
 """
 from __future__ import annotations
 
@@ -32,6 +36,18 @@ def _prefill_steps(cfg, steps):
         qb.indexer_prefill(t["idxQ"], t["idxK"], t["wq"], t["wk"], t["ctx"], ind, ws, rot=cfg.rot, ratio=cfg.ratio,
                            budget=cfg.budget, topK=cfg.topK, theta=cfg.theta, eps=cfg.eps)
         qb.sparse_prefill(t["q"], t["k"], t["v"], ind, t["ctx"], out, scale)
+
+
+def _rope_steps(cfg, steps):
+    t = syn.make_prefill(cfg)
+    qkv = torch.cat([t["q"], t["k"], t["v"]], dim=2).contiguous().cuda()
+    wq, wk, ctx = t["wq"].cuda(), t["wk"].cuda(), t["ctx"].cuda()
+    qo = torch.empty((cfg.B, cfg.S, cfg.Hq, cfg.D), dtype=torch.float16, device="cuda")
+    ko = torch.empty((cfg.B, cfg.S, cfg.Hkv, cfg.D), dtype=torch.float16, device="cuda")
+    vo = torch.empty_like(ko)
+    for _ in range(steps):
+        qb.rope_qkv(qkv, wq, wk, ctx, qo, Hq=cfg.Hq, Hkv=cfg.Hkv, rot=cfg.rot, theta=cfg.theta, eps=cfg.eps,
+                    k_out=ko, v_out=vo)
 
 
 def _decode_steps(cfg, steps):
@@ -58,12 +74,17 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2)
     ap.add_argument("--B", type=int, default=None, help="override the batch size")
     ap.add_argument("--ctx", type=int, default=None, help="decode: every sequence gets this total length")
+    ap.add_argument("--op", choices=("path", "rope"), default="path", help="rope: qsa_rope_qkv of a prefill workload")
     args = ap.parse_args(argv)
     cfg = names[args.workload]
     if args.B is not None:
         cfg = dataclasses.replace(cfg, B=args.B)
     qb.lib()
-    if isinstance(cfg, syn.DecodeConfig):
+    if args.op == "rope":
+        if isinstance(cfg, syn.DecodeConfig):
+            ap.error("--op rope takes a prefill workload")
+        _rope_steps(cfg, args.steps)
+    elif isinstance(cfg, syn.DecodeConfig):
         if args.ctx is not None:
             cfg = dataclasses.replace(cfg, ctx_lo=args.ctx, ctx_hi=args.ctx, max_ctx=max(args.ctx, 1), ctx_list=None)
         _decode_steps(cfg, args.steps)

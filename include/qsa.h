@@ -179,6 +179,50 @@ typedef struct {
   void* stream;
 } QsaIndexerHandoffParams;
 
+/* Upstream step of a QSA attention layer ("Qsa Attention Plugin", fused step
+ * 1: packed-QKV split, per-head qk-norm with (1 + w), partial RoPE, paged-KV
+ * write, dense K/V mirrors).  The projections stay with the caller: this call
+ * takes their packed output.  For every live row and head:
+ *   q/k heads: y = x / sqrt(mean(x^2) + eps) * (1 + w), then the half-split
+ *              RoPE of dims [0, rotDim) at the row's position, rounded to fp16;
+ *   v heads:   copied.
+ * Row s is at position s when seqLen > 1 (a prefill from position 0; rows
+ * s >= contextLengths[b] are padding) and at contextLengths[b] - 1 when
+ * seqLen == 1 (one new token, contextLengths = total length including it).
+ * Outputs: qOut (always; zeros for padding rows), kOut / vOut dense mirrors
+ * when non-NULL (zeros for padding rows), and, when kvPool is non-NULL, the
+ * leading headDim columns of the token's K row (page table row 0) and V row
+ * (row 1) for every KV head.  Pool tails and padding rows' pool rows are not
+ * written; a page id outside [0, numFlatPages) is skipped.
+ * Errors: QSA_ERR_INVALID_ARG for NULL required pointers, sizes < 1, an odd
+ * rotDim or rotDim > headDim, theta <= 0, eps < 0, or a pool without its page
+ * table; QSA_ERR_UNSUPPORTED for headDim not 64/128, rotDim not a multiple of
+ * 16, poolHeadDim not a multiple of 8, a tensor pointer not 16-byte aligned,
+ * or a packed token row (numQHeads + 2 numKVHeads) * headDim * 2 above 64 KiB.  Ownership: every buffer is the caller's; nothing is allocated. */
+typedef struct {
+  const void* qkv;               /* fp16 [B, S, numQHeads + 2*numKVHeads, headDim]: q, then k, then v heads */
+  const float* qNormW;           /* fp32 [headDim]                                                          */
+  const float* kNormW;           /* fp32 [headDim]                                                          */
+  const int32_t* contextLengths; /* int32 [B]                                                               */
+  void* qOut;                    /* out fp16 [B, S, numQHeads, headDim]                                     */
+  void* kOut;                    /* out fp16 [B, S, numKVHeads, headDim], or NULL                           */
+  void* vOut;                    /* out fp16 [B, S, numKVHeads, headDim], or NULL                           */
+  void* kvPool;                  /* fp16 [numFlatPages, 128, numKVHeads, poolHeadDim], or NULL              */
+  const int32_t* pageTable;      /* int32 [B, 2, maxPagesPerSeq] (needed with kvPool)                       */
+  int32_t batchSize;
+  int32_t seqLen;
+  int32_t numQHeads;
+  int32_t numKVHeads;
+  int32_t headDim;               /* 64 or 128                                                               */
+  int32_t rotDim;                /* multiple of 16, <= headDim                                              */
+  int32_t poolHeadDim;           /* >= headDim, multiple of 8 (with kvPool)                                 */
+  int32_t numFlatPages;
+  int32_t maxPagesPerSeq;
+  float ropeTheta;
+  float rmsNormEps;
+  void* stream;
+} QsaRopeQkvParams;
+
 /* --------------------------------------------------------------- attention */
 
 /* Sparse GQA prefill ("Cute Dsl Qsa Sparse Runner", struct
@@ -244,6 +288,7 @@ QSA_API qsa_status_t qsa_indexer_decode(const QsaIndexerDecodeParams* params);
 QSA_API qsa_status_t qsa_sparse_prefill(const QsaSparsePrefillParams* params);
 QSA_API qsa_status_t qsa_sparse_decode(const QsaSparseDecodeParams* params);
 QSA_API qsa_status_t qsa_indexer_prefill_handoff(const QsaIndexerHandoffParams* params);
+QSA_API qsa_status_t qsa_rope_qkv(const QsaRopeQkvParams* params);
 
 /* The two attention calls with bfloat16 tensors ("Cute Dsl Qsa Sparse Runner":
  * the runners take fp16 or bf16): the same params structs, contract and

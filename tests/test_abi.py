@@ -45,7 +45,8 @@ def test_struct_layouts_match_c(binding, tmp_path):
                "QsaIndexerDecodeParams": binding.QsaIndexerDecodeParams,
                "QsaSparsePrefillParams": binding.QsaSparsePrefillParams,
                "QsaSparseDecodeParams": binding.QsaSparseDecodeParams,
-               "QsaIndexerHandoffParams": binding.QsaIndexerHandoffParams}
+               "QsaIndexerHandoffParams": binding.QsaIndexerHandoffParams,
+               "QsaRopeQkvParams": binding.QsaRopeQkvParams}
     lines = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', "int main(void) {"]
     for s, cls in structs.items():
         lines.append(f'printf("{s} size %zu\\n", sizeof({s}));')
@@ -92,7 +93,7 @@ def _call(binding, fn, params):
 def test_validation_rejects_before_launch(binding):
     L = binding.lib()
     for fn in ("qsa_indexer_prefill", "qsa_indexer_decode", "qsa_sparse_prefill", "qsa_sparse_decode",
-               "qsa_indexer_prefill_handoff"):
+               "qsa_indexer_prefill_handoff", "qsa_rope_qkv", "qsa_sparse_prefill_bf16", "qsa_sparse_decode_bf16"):
         assert getattr(L, fn)(None) == binding.QSA_ERR_INVALID_ARG
     fake = 1 << 20  # never dereferenced: every case below fails validation first
     sp = binding.QsaSparsePrefillParams(qPtr=fake, kPtr=fake, vPtr=fake, oPtr=fake, indices=fake,
@@ -154,6 +155,25 @@ def test_validation_rejects_before_launch(binding):
     hp.headDim, hp.poolHeadDim = 128, 200
     assert _call(binding, "qsa_indexer_prefill_handoff", hp) == binding.QSA_ERR_INVALID_ARG
     assert L.qsa_indexer_prefill_handoff(None) == binding.QSA_ERR_INVALID_ARG
+
+    rp = binding.QsaRopeQkvParams(qkv=fake, qNormW=fake, kNormW=fake, contextLengths=fake, qOut=fake, batchSize=1,
+                                  seqLen=16, numQHeads=8, numKVHeads=2, headDim=96, rotDim=32, ropeTheta=1e4,
+                                  rmsNormEps=1e-6)
+    assert _call(binding, "qsa_rope_qkv", rp) == binding.QSA_ERR_UNSUPPORTED  # headDim 96
+    rp.headDim, rp.rotDim = 128, 33
+    assert _call(binding, "qsa_rope_qkv", rp) == binding.QSA_ERR_INVALID_ARG  # odd rotDim
+    rp.rotDim = 24
+    assert _call(binding, "qsa_rope_qkv", rp) == binding.QSA_ERR_UNSUPPORTED  # rotDim not a multiple of 16
+    rp.rotDim, rp.numQHeads = 64, 300
+    assert _call(binding, "qsa_rope_qkv", rp) == binding.QSA_ERR_UNSUPPORTED  # 304 heads * 256 B > 64 KiB row
+    rp.numQHeads, rp.qkv = 8, fake + 2
+    assert _call(binding, "qsa_rope_qkv", rp) == binding.QSA_ERR_UNSUPPORTED  # qkv not 16-byte aligned
+    rp.qkv, rp.kvPool = fake, fake
+    assert _call(binding, "qsa_rope_qkv", rp) == binding.QSA_ERR_INVALID_ARG  # pool without a page table
+    rp.pageTable, rp.poolHeadDim, rp.numFlatPages, rp.maxPagesPerSeq = fake, 132, 4, 2
+    assert _call(binding, "qsa_rope_qkv", rp) == binding.QSA_ERR_UNSUPPORTED  # poolHeadDim not a multiple of 8
+    rp.kvPool, rp.qOut = None, None
+    assert _call(binding, "qsa_rope_qkv", rp) == binding.QSA_ERR_INVALID_ARG
 
     sd = binding.QsaSparseDecodeParams(qPtr=fake, kvPoolPtr=fake, pageTable=fake, indices=fake,
                                        contextLengths=fake, oPtr=fake, partialO=None, partialStats=fake,
