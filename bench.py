@@ -256,13 +256,14 @@ class L2Flush:
         self.r.sum()
 
 
-def time_decode(dec, flush, clk, reps=50, warm=10):
+def time_graph(fn, flush, clk, reps=50, warm=10):
+    """Median us of one CUDA-graph replay of fn(), L2 flushed before each replay (outside the events)."""
     for _ in range(3):
-        dec.step()
+        fn()
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        dec.step()
+        fn()
     for _ in range(warm):
         g.replay()
     torch.cuda.synchronize()
@@ -277,6 +278,41 @@ def time_decode(dec, flush, clk, reps=50, warm=10):
             e1.synchronize()
             times.append(e0.elapsed_time(e1) * 1000.0)
     return statistics.median(times), times
+
+
+def time_decode(dec, flush, clk, reps=50, warm=10):
+    return time_graph(dec.step, flush, clk, reps, warm)
+
+
+def decode_gather_ab(dec, flush, clk):
+    """The attention half of a decode step two ways on the list the step just produced: the split-K decode
+    gathering through the page table (A), and qsa_gather_selected into contiguous scratch followed by the
+    same decode on the scratch (B)."""
+    qb, c, d = dec.qb, dec.cfg, dec.d
+    out_b = torch.empty_like(dec.out)
+    parts_b = tuple(torch.zeros_like(t) for t in dec.parts)
+    sc = qb.gather_scratch(c.B, c.Hkv, c.D, c.topK, device=dec.dev)
+
+    def a():
+        qb.sparse_decode(d["q"], d["pool"], d["page_table"], dec.ind, d["ctx"], dec.out, *dec.parts, D=c.D,
+                         scale=f32(c.scale))
+
+    def gather():
+        qb.gather_selected(d["pool"], d["page_table"], dec.ind, d["ctx"], *sc, D=c.D)
+
+    def b():
+        gather()
+        qb.sparse_decode(d["q"], sc[0], sc[1], sc[2], sc[3], out_b, *parts_b, D=c.D, scale=f32(c.scale))
+
+    ta, _ = time_graph(a, flush, clk)
+    tg, _ = time_graph(gather, flush, clk)
+    tb, _ = time_graph(b, flush, clk)
+    torch.cuda.synchronize()
+    same = bool(torch.equal(out_b.view(torch.int16), dec.out.view(torch.int16)))
+    valid = int((dec.ind >= 0).sum())
+    row = c.Hkv * c.D * 2
+    return {"in_kernel_gather_us": round(ta, 2), "gather_us": round(tg, 2), "gather_then_decode_us": round(tb, 2),
+            "gather_bytes": 4 * valid * row, "outputs_bit_identical": same}
 
 
 def run_ours(args, rank, world, dev):
@@ -446,9 +482,11 @@ def run_ours(args, rank, world, dev):
         dec = Decode(dc, dev)
         us, _ = time_decode(dec, flush, clk)
         kbar, kv, total = decode_work(dc, dec.ctx_host.tolist())
+        ab = decode_gather_ab(dec, flush, clk)
         decode.append({"workload": dc.name, "us_per_step": round(us, 2), "bytes_per_step": total,
                        "roofline_us": round(total / (hbm_peak * 1e9) * 1e6, 2),
-                       "frac": round(total / (hbm_peak * 1e9) * 1e6 / us, 4), "kernels_per_step": 4})
+                       "frac": round(total / (hbm_peak * 1e9) * 1e6 / us, 4), "kernels_per_step": 4,
+                       "attention_gather_ab": ab})
         del dec
         torch.cuda.empty_cache()
     clk.__exit__(None, None, None)

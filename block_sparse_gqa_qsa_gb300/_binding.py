@@ -85,6 +85,13 @@ class QsaSparseDecodeParams(ctypes.Structure):
                 ("topK", _i32), ("attentionScale", _f32), ("stream", _vp)]
 
 
+class QsaGatherParams(ctypes.Structure):
+    _fields_ = [("kvPool", _vp), ("pageTable", _vp), ("indices", _vp), ("contextLengths", _vp), ("scratch", _vp),
+                ("scratchPageTable", _vp), ("scratchIndices", _vp), ("scratchLengths", _vp), ("batchSize", _i32),
+                ("numKVHeads", _i32), ("headDim", _i32), ("poolHeadDim", _i32), ("numFlatPages", _i32),
+                ("maxPagesPerSeq", _i32), ("topK", _i32), ("stream", _vp)]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -106,7 +113,8 @@ def lib() -> ctypes.CDLL:
                              ("qsa_indexer_prefill_handoff", QsaIndexerHandoffParams),
                              ("qsa_sparse_prefill_bf16", QsaSparsePrefillParams),
                              ("qsa_sparse_decode_bf16", QsaSparseDecodeParams),
-                             ("qsa_rope_qkv", QsaRopeQkvParams)):
+                             ("qsa_rope_qkv", QsaRopeQkvParams),
+                             ("qsa_gather_selected", QsaGatherParams)):
                 f = getattr(L, name)
                 f.argtypes = [ctypes.POINTER(st)]
                 f.restype = ctypes.c_int
@@ -120,6 +128,10 @@ def lib() -> ctypes.CDLL:
             L.qsa_sparse_decode_partial_stats_elems.restype = _sz
             L.qsa_sparse_decode_counter_elems.argtypes = [_i32] * 2
             L.qsa_sparse_decode_counter_elems.restype = _sz
+            L.qsa_gather_scratch_elems.argtypes = [_i32] * 4
+            L.qsa_gather_scratch_elems.restype = _sz
+            L.qsa_gather_scratch_pages.argtypes = [_i32]
+            L.qsa_gather_scratch_pages.restype = _i32
             for n in ("qsa_sparse_decode_max_splits", "qsa_sparse_decode_partial_rows",
                       "qsa_indexer_prefill_max_blocks"):
                 getattr(L, n).argtypes = []
@@ -302,6 +314,44 @@ def sparse_decode(q, pool, page_table, indices, ctx, out, partial_o, partial_sta
         attentionScale=scale, stream=_stream(stream))
     fn = lib().qsa_sparse_decode_bf16 if et == torch.bfloat16 else lib().qsa_sparse_decode
     _check(fn(ctypes.byref(p)))
+
+
+def gather_scratch(B: int, Hkv: int, D: int, topK: int, dtype=torch.float16, device="cuda"):
+    """Buffers for gather_selected: (scratch [2*B*P, 128, Hkv, D], page table int32 [B, 2, P],
+    indices int32 [B, 1, topK], lengths int32 [B]), P = ceil(topK / 128)."""
+    P = int(lib().qsa_gather_scratch_pages(topK))
+    n = int(lib().qsa_gather_scratch_elems(B, Hkv, D, topK))
+    if P < 1 or n != 2 * B * P * 128 * Hkv * D:
+        raise ValueError("gather_scratch: invalid sizes")
+    return (torch.empty((2 * B * P, 128, Hkv, D), dtype=dtype, device=device),
+            torch.empty((B, 2, P), dtype=torch.int32, device=device),
+            torch.empty((B, 1, topK), dtype=torch.int32, device=device),
+            torch.empty((B,), dtype=torch.int32, device=device))
+
+
+def gather_selected(pool, page_table, indices, ctx, scratch, scratch_pt, scratch_idx, scratch_len, *, D,
+                    stream=None):
+    """qsa_gather_selected: the K/V rows a decode list names, from the pool [numFlat, 128, Hkv, poolHeadDim]
+    into contiguous scratch described as a paged pool (see gather_scratch)."""
+    et = pool.dtype
+    if et not in (torch.float16, torch.bfloat16) or scratch.dtype != et:
+        raise ValueError("gather_selected: pool and scratch must share a float16 or bfloat16 dtype")
+    nflat, tpp, Hkv, phd = pool.shape
+    B, topK = ctx.shape[0], indices.shape[-1]
+    P = scratch_pt.shape[-1]
+    if tpp != 128 or tuple(page_table.shape[:2]) != (B, 2) or indices.numel() != B * topK \
+            or tuple(scratch.shape) != (2 * B * P, 128, Hkv, D) or tuple(scratch_pt.shape) != (B, 2, P) \
+            or scratch_idx.numel() != B * topK or scratch_len.numel() != B:
+        raise ValueError("gather_selected: shape mismatch")
+    p = QsaGatherParams(
+        kvPool=_ptr(pool, et, "pool"), pageTable=_ptr(page_table, torch.int32, "pageTable"),
+        indices=_ptr(indices, torch.int32, "indices"), contextLengths=_ptr(ctx, torch.int32, "contextLengths"),
+        scratch=_ptr(scratch, et, "scratch"), scratchPageTable=_ptr(scratch_pt, torch.int32, "scratchPageTable"),
+        scratchIndices=_ptr(scratch_idx, torch.int32, "scratchIndices"),
+        scratchLengths=_ptr(scratch_len, torch.int32, "scratchLengths"), batchSize=B, numKVHeads=Hkv, headDim=D,
+        poolHeadDim=phd, numFlatPages=nflat, maxPagesPerSeq=page_table.shape[-1], topK=topK,
+        stream=_stream(stream))
+    _check(lib().qsa_gather_selected(ctypes.byref(p)))
 
 
 def sparse_decode_noalloc(q, pool, page_table, indices, ctx, out, *, D, scale, stream=None):

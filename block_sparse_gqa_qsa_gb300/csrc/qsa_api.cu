@@ -330,6 +330,34 @@ qsa_status_t qsa_indexer_prefill_handoff(const QsaIndexerHandoffParams* p) {
   return e == cudaSuccess ? ok() : cuda_fail(e, "qsa_indexer_prefill_handoff");
 }
 
+int32_t qsa_gather_scratch_pages(int32_t topK) { return topK < 1 ? 0 : qsa::gather_scratch_pages(topK); }
+
+size_t qsa_gather_scratch_elems(int32_t B, int32_t Hkv, int32_t D, int32_t topK) {
+  if (B < 1 || Hkv < 1 || D < 1 || topK < 1) return 0;
+  return 2 * static_cast<size_t>(B) * qsa::gather_scratch_pages(topK) * qsa::kTokensPerPageHost * Hkv * D;
+}
+
+qsa_status_t qsa_gather_selected(const QsaGatherParams* p) {
+  if (!p) return fail(QSA_ERR_INVALID_ARG, "qsa_gather_selected: params is NULL");
+  if (!p->kvPool || !p->pageTable || !p->indices || !p->contextLengths || !p->scratch || !p->scratchPageTable ||
+      !p->scratchIndices || !p->scratchLengths)
+    return fail(QSA_ERR_INVALID_ARG, "qsa_gather_selected: a pointer is NULL");
+  if (p->batchSize < 1 || p->numKVHeads < 1 || p->headDim < 1 || p->poolHeadDim < 1 || p->numFlatPages < 1 ||
+      p->maxPagesPerSeq < 1 || p->topK < 1)
+    return fail(QSA_ERR_INVALID_ARG, "qsa_gather_selected: sizes must be >= 1");
+  if (p->poolHeadDim < p->headDim) return fail(QSA_ERR_INVALID_ARG, "qsa_gather_selected: poolHeadDim < headDim");
+  if (p->headDim % 8 || p->poolHeadDim % 8 || p->numKVHeads * (p->headDim / 8) > qsa::gather_max_row_chunks())
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_gather_selected: headDim and poolHeadDim must be multiples of 8 and "
+                                     "numKVHeads * headDim at most %d", qsa::gather_max_row_chunks() * 8);
+  if (!aligned(p->kvPool, 16) || !aligned(p->scratch, 16))
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_gather_selected: kvPool and scratch must be 16-byte aligned");
+  if (static_cast<long long>(p->maxPagesPerSeq) * qsa::kTokensPerPageHost > 0x7fffffffLL ||
+      static_cast<long long>(p->batchSize) * p->topK > 0x7fffffffLL)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_gather_selected: maxPagesPerSeq or batchSize * topK too large");
+  const cudaError_t e = qsa::launch_gather(*p);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "qsa_gather_selected");
+}
+
 qsa_status_t qsa_sparse_decode(const QsaSparseDecodeParams* p) {
   return sparse_decode_entry(p, "qsa_sparse_decode", false);
 }

@@ -40,6 +40,10 @@ cudaError_t launch_sparse_decode(const QsaSparseDecodeParams& p, bool bf16 = fal
 cudaError_t launch_rope_qkv(const QsaRopeQkvParams& p, const RopeFreqs& rf);
 constexpr int kRopeMaxRowBytes = 64 * 1024;  // one token's packed heads, staged in shared memory
 
+cudaError_t launch_gather(const QsaGatherParams& p);
+int gather_scratch_pages(int topK);
+int gather_max_row_chunks();  // 16-byte chunks of one K (or V) token row a warp copies
+
 // SMs of the current device (cached per device).
 int sm_count();
 

@@ -323,6 +323,52 @@ QSA_API qsa_status_t qsa_sparse_decode_bf16(const QsaSparseDecodeParams* params)
  *     one stream. */
 QSA_API qsa_status_t qsa_sparse_decode_noalloc(const QsaSparseDecodeParams* params);
 
+/* Gather-to-scratch form of the decode (qsa.rs, "qsa_gather" and the
+ * scratch-as-paged-cache note): copies the K and V rows of the tokens that a
+ * decode list names out of the paged pool into contiguous scratch, and
+ * describes the scratch as a paged pool of its own, so that an unchanged
+ * qsa_sparse_decode can consume it.  It is the A/B counterpart of the
+ * decode's in-kernel page-table gathers: qsa_sparse_decode on
+ * (scratch, scratchPageTable, scratchIndices, scratchLengths) with
+ * numFlatPages = 2 * batchSize * P, maxPagesPerSeq = P, poolHeadDim = headDim
+ * returns exactly, bit for bit, what qsa_sparse_decode returns on the pool
+ * with the original list.
+ *
+ * P = qsa_gather_scratch_pages(topK) = ceil(topK / 128).  Slot n of sequence
+ * b holds list entry n: its K row at scratch page b * P + n / 128, row n % 128,
+ * and its V row at page (batchSize + b) * P + n / 128.  An entry outside
+ * [0, contextLengths[b]) or on a page outside [0, numFlatPages) leaves its
+ * slot unwritten (it is never read) and is -1 in scratchIndices.
+ *
+ * Errors: QSA_ERR_INVALID_ARG for a NULL pointer, sizes < 1 or
+ * poolHeadDim < headDim; QSA_ERR_UNSUPPORTED for headDim not a multiple of 8,
+ * numKVHeads * headDim above 1024, poolHeadDim not a multiple of 8, or kvPool
+ * / scratch not 16-byte aligned.  Every buffer is the caller's; nothing is
+ * allocated. */
+typedef struct {
+  const void* kvPool;            /* fp16 or bf16 [numFlatPages, 128, numKVHeads, poolHeadDim]               */
+  const int32_t* pageTable;      /* int32 [B, 2, maxPagesPerSeq]                                            */
+  const int32_t* indices;        /* int32 [B, 1, topK], -1 padded                                           */
+  const int32_t* contextLengths; /* int32 [B]                                                               */
+  void* scratch;                 /* out, same element type: [2 * B * P, 128, numKVHeads, headDim]           */
+  int32_t* scratchPageTable;     /* out int32 [B, 2, P]                                                     */
+  int32_t* scratchIndices;       /* out int32 [B, 1, topK]: n where entry n names a row, else -1            */
+  int32_t* scratchLengths;       /* out int32 [B]: topK                                                     */
+  int32_t batchSize;
+  int32_t numKVHeads;
+  int32_t headDim;               /* columns [0, headDim) of each pool row are copied                        */
+  int32_t poolHeadDim;
+  int32_t numFlatPages;
+  int32_t maxPagesPerSeq;
+  int32_t topK;
+  void* stream;
+} QsaGatherParams;
+
+QSA_API qsa_status_t qsa_gather_selected(const QsaGatherParams* params);
+QSA_API int32_t qsa_gather_scratch_pages(int32_t topK);
+/* Elements (halves) of the scratch: 2 * batchSize * P * 128 * numKVHeads * headDim (0 when invalid). */
+QSA_API size_t qsa_gather_scratch_elems(int32_t batchSize, int32_t numKVHeads, int32_t headDim, int32_t topK);
+
 /* Workspace bytes of the indexers (0 when the sizes are invalid). */
 QSA_API size_t qsa_indexer_prefill_workspace_size(int32_t batchSize, int32_t seqLen, int32_t headDim,
                                           int32_t compressRatio);

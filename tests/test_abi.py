@@ -46,7 +46,8 @@ def test_struct_layouts_match_c(binding, tmp_path):
                "QsaSparsePrefillParams": binding.QsaSparsePrefillParams,
                "QsaSparseDecodeParams": binding.QsaSparseDecodeParams,
                "QsaIndexerHandoffParams": binding.QsaIndexerHandoffParams,
-               "QsaRopeQkvParams": binding.QsaRopeQkvParams}
+               "QsaRopeQkvParams": binding.QsaRopeQkvParams,
+               "QsaGatherParams": binding.QsaGatherParams}
     lines = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', "int main(void) {"]
     for s, cls in structs.items():
         lines.append(f'printf("{s} size %zu\\n", sizeof({s}));')
@@ -82,6 +83,9 @@ def test_constants_and_sizes(binding):
     assert L.qsa_sparse_prefill_can_implement(64, 2, 128) == 0  # group 32 > 16
     assert L.qsa_sparse_prefill_can_implement(32, 4, 64) == 0
     assert L.qsa_sparse_decode_can_implement(64, 8, 128, 256) == 1
+    assert L.qsa_gather_scratch_pages(2051) == 17 and L.qsa_gather_scratch_pages(128) == 1
+    assert L.qsa_gather_scratch_elems(3, 4, 128, 2051) == 2 * 3 * 17 * 128 * 4 * 128
+    assert L.qsa_gather_scratch_elems(0, 4, 128, 2051) == 0
     assert L.qsa_sparse_decode_can_implement(64, 8, 128, 100) == 0
     assert L.qsa_status_string(2) == b"QSA_ERR_UNSUPPORTED"
 
@@ -93,7 +97,8 @@ def _call(binding, fn, params):
 def test_validation_rejects_before_launch(binding):
     L = binding.lib()
     for fn in ("qsa_indexer_prefill", "qsa_indexer_decode", "qsa_sparse_prefill", "qsa_sparse_decode",
-               "qsa_indexer_prefill_handoff", "qsa_rope_qkv", "qsa_sparse_prefill_bf16", "qsa_sparse_decode_bf16"):
+               "qsa_indexer_prefill_handoff", "qsa_rope_qkv", "qsa_sparse_prefill_bf16", "qsa_sparse_decode_bf16",
+               "qsa_gather_selected"):
         assert getattr(L, fn)(None) == binding.QSA_ERR_INVALID_ARG
     fake = 1 << 20  # never dereferenced: every case below fails validation first
     sp = binding.QsaSparsePrefillParams(qPtr=fake, kPtr=fake, vPtr=fake, oPtr=fake, indices=fake,
@@ -174,6 +179,20 @@ def test_validation_rejects_before_launch(binding):
     assert _call(binding, "qsa_rope_qkv", rp) == binding.QSA_ERR_UNSUPPORTED  # poolHeadDim not a multiple of 8
     rp.kvPool, rp.qOut = None, None
     assert _call(binding, "qsa_rope_qkv", rp) == binding.QSA_ERR_INVALID_ARG
+
+    gp = binding.QsaGatherParams(kvPool=fake, pageTable=fake, indices=fake, contextLengths=fake, scratch=fake,
+                                 scratchPageTable=fake, scratchIndices=fake, scratchLengths=None, batchSize=2,
+                                 numKVHeads=4, headDim=128, poolHeadDim=256, numFlatPages=8, maxPagesPerSeq=4,
+                                 topK=2051)
+    assert _call(binding, "qsa_gather_selected", gp) == binding.QSA_ERR_INVALID_ARG  # no scratchLengths
+    gp.scratchLengths, gp.poolHeadDim = fake, 100
+    assert _call(binding, "qsa_gather_selected", gp) == binding.QSA_ERR_INVALID_ARG  # poolHeadDim < headDim
+    gp.poolHeadDim, gp.numKVHeads = 256, 16
+    assert _call(binding, "qsa_gather_selected", gp) == binding.QSA_ERR_UNSUPPORTED  # 16 x 128 > 1024 per row
+    gp.numKVHeads, gp.scratch = 4, fake + 8
+    assert _call(binding, "qsa_gather_selected", gp) == binding.QSA_ERR_UNSUPPORTED  # scratch not 16-byte aligned
+    gp.scratch, gp.topK = fake, 0
+    assert _call(binding, "qsa_gather_selected", gp) == binding.QSA_ERR_INVALID_ARG
 
     sd = binding.QsaSparseDecodeParams(qPtr=fake, kvPoolPtr=fake, pageTable=fake, indices=fake,
                                        contextLengths=fake, oPtr=fake, partialO=None, partialStats=fake,
