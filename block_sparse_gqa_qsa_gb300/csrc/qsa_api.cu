@@ -44,7 +44,18 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 qsa::RopeFreqs rope_freqs(float theta, int rot) {
   qsa::RopeFreqs r;
   std::memset(&r, 0, sizeof(r));
-  for (int i = 0; i < rot / 2; ++i) r.inv_freq[i] = std::pow(static_cast<double>(theta), -2.0 * i / rot);
+  for (int i = 0; i < rot / 2; ++i) {
+    r.inv_freq[i] = std::pow(static_cast<double>(theta), -2.0 * i / rot);
+    double x = r.inv_freq[i] / 6.283185307179586;
+    x -= std::floor(x);
+    r.turn[i] = static_cast<unsigned long long>(std::ldexp(x, 64));  // x < 1, so this stays below 2^64
+  }
+  const double pi = 3.14159265358979323846;
+  for (int j = 0; j <= 32; ++j) {  // cos(pi j / 64); past pi / 4 as sin of the complement, so j = 32 is exactly 0
+    const double c = j <= 16 ? std::cos(pi * j / 64.0) : std::sin(pi * (32 - j) / 64.0);
+    r.qcos_hi[j] = static_cast<float>(c);
+    r.qcos_lo[j] = static_cast<float>(c - static_cast<double>(r.qcos_hi[j]));
+  }
   return r;
 }
 

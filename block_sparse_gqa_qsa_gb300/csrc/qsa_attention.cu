@@ -342,7 +342,9 @@ struct DecodeArgs {
   float* partialO;
   float* partialStats;
   int32_t* counters;
-  int Hq, Hkv, G, poolHeadDim, numFlatPages, maxPagesPerSeq, topK, sliceLen, slicePad;
+  int Hq, Hkv, G, poolHeadDim, numFlatPages, maxPagesPerSeq, topK;
+  int tilesPerSplit, extraTiles;  // split s owns tilesPerSplit (+1 for s < extraTiles) whole 64-key tiles
+  int slicePad;                   // slots of the longest slice
   float sl2;
 };
 
@@ -358,8 +360,11 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_k
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int L = max(0, min(a.ctx[b], a.maxPagesPerSeq * kTokensPerPage));
-  const int s0 = split * a.sliceLen;
-  const int s1 = min(a.topK, s0 + a.sliceLen);
+  // Slices are whole 64-key tiles of the list, so no split ends on a nearly
+  // empty tile: the ceil(topK / 64) tiles are dealt out evenly, the first
+  // extraTiles splits taking one more.
+  const int s0 = kKeys * (split * a.tilesPerSplit + min(split, a.extraTiles));
+  const int s1 = min(a.topK, s0 + kKeys * (a.tilesPerSplit + (split < a.extraTiles ? 1 : 0)));
   const int32_t* lst = a.indices + static_cast<size_t>(b) * a.topK;
   const int32_t* ptK = a.pageTable + static_cast<size_t>(b) * 2 * a.maxPagesPerSeq;
   const int32_t* ptV = ptK + a.maxPagesPerSeq;
@@ -585,8 +590,10 @@ cudaError_t launch_sparse_decode(const QsaSparseDecodeParams& p, bool bf16) {
   a.numFlatPages = p.numFlatPages;
   a.maxPagesPerSeq = p.maxPagesPerSeq;
   a.topK = p.topK;
-  a.sliceLen = (p.topK + kMaxSplits - 1) / kMaxSplits;
-  a.slicePad = (a.sliceLen + kKeys - 1) / kKeys * kKeys;
+  const int tiles = (p.topK + kKeys - 1) / kKeys;
+  a.tilesPerSplit = tiles / kMaxSplits;
+  a.extraTiles = tiles % kMaxSplits;
+  a.slicePad = kKeys * (a.tilesPerSplit + (a.extraTiles > 0 ? 1 : 0));
   a.sl2 = p.attentionScale * kLog2e;
   cudaStream_t st = static_cast<cudaStream_t>(p.stream);
   if (bf16) return a.G <= 8 ? decode_nt<1, true>(a, p.batchSize, st) : decode_nt<2, true>(a, p.batchSize, st);

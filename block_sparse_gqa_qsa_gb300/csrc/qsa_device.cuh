@@ -169,26 +169,13 @@ __device__ __forceinline__ int cta_exclusive_scan(int v, int* scratch, int& tota
 }
 
 // ------------------------------------------------------------------- RoPE
-// cos/sin of the f64 angle pos * inv_freq, reduced to [-pi, pi] first (2 pi in
-// two parts, each product taken with one rounding by fma) so that the f64
-// sincos stays on its short path even at positions ~5e5.
-__device__ __forceinline__ void rope_cos_sin_f64(double pos, double inv_freq, double& c, double& s) {
-  const double a = __dmul_rn(pos, inv_freq);
-  const double k = rint(a * 0.15915494309189535);
-  double r = fma(-k, 6.283185307179586, a);
-  r = fma(-k, 2.4492935982947064e-16, r);
-  sincos(r, &s, &c);
-}
-
-// cos/sin of pos * inv_freq with the angle formed and reduced modulo 2*pi in
-// f64, then evaluated in fp32 (|r| <= pi): an fp32 product pos * inv_freq
-// would be off by up to 0.03 rad at pos ~ 5e5.
-__device__ __forceinline__ void rope_cos_sin_f32(double pos, double inv_freq, float& c, float& s) {
-  const double a = pos * inv_freq;
-  const double k = rint(a * 0.15915494309189535);           // 1 / (2 pi)
-  double r = fma(-k, 6.283185307179586, a);                   // 2 pi, high part
-  r = fma(-k, 2.4492935982947064e-16, r);                     // 2 pi - high part
-  sincosf(static_cast<float>(r), &s, &c);
+// cos / sin of the angle pos * inv_freq, with inv_freq given as turn = frac(inv_freq / (2 pi)) * 2^64:
+// pos * turn mod 2^64 is the angle's fraction of a full turn, exact in integer arithmetic, and its top
+// 32 bits, read as signed, place it in [-pi, pi).  The only roundings are those of the fp32 argument.
+__device__ __forceinline__ void rope_cos_sin_turns(unsigned pos, unsigned long long turn, float& c, float& s) {
+  const unsigned long long t = turn * pos;
+  const float r = static_cast<float>(static_cast<int>(static_cast<unsigned>(t >> 32))) * 1.4629180792671596e-09f;
+  sincosf(r, &s, &c);
 }
 
 }  // namespace qsa

@@ -5,12 +5,13 @@
 //
 // Three launches on the caller's stream:
 //   decode_prep_kernel    (B1) one CTA per sequence: index-query prep at
-//       t = L-1 (fp32, f64 angles) into the workspace by 8 warps, and
-//       concurrently, by di/32 more warps, the state update:
-//       the new raw key into token t's K-row tail when t leaves its block
-//       incomplete, else the block t completes is pooled in f64 (from the
-//       K-row tails of its first r-1 tokens and the new key) and its key is
-//       stored in the V-row tail of the block's first token.
+//       t = L-1 (fp32, angles reduced in integer turns) into the workspace by
+//       8 warps, and concurrently, by di/32 more warps, the state update: the new
+//       raw key into token t's K-row tail when t leaves its block incomplete,
+//       else the block t completes is pooled (from the K-row tails of its
+//       first r-1 tokens and the new key; exact mean, double-float norm and
+//       rotation, qsa_blockkey.cuh) and its key is stored in the V-row tail of
+//       the block's first token.
 //   decode_score_kernel   (B2) persistent, one CTA per SM, warp-specialised:
 //       a producer warp streams the key tails of every page that holds
 //       complete blocks (3-D TMA copies, box {64, 128/r, 1} with the 128-byte
@@ -33,6 +34,7 @@
 //       the histogram and its ticket.
 // Waits on TMA barriers are bounded; on expiry the kernel records
 // kErrWaitTimeout in the workspace status word and stops.
+#include "qsa_blockkey.cuh"
 #include "qsa_device.cuh"
 #include "qsa_internal.h"
 
@@ -90,10 +92,6 @@ __device__ __forceinline__ size_t pool_row(int page, int tok_in_page, int Hkv, i
   return (static_cast<size_t>(page) * kTokensPerPage + tok_in_page) * Hkv * poolHeadDim;  // head 0
 }
 
-__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_addr(bar)) : "memory");
 }
@@ -118,11 +116,15 @@ template <int DI>
 __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const PrepArgs a) {
   constexpr int PER = DI / 32;
   __shared__ float y_s[8][DI];
-  __shared__ double m_s[DI];
-  __shared__ double y2_s[DI];
-  __shared__ double part_s[8];
+  __shared__ f2x key_s[DI];
+  __shared__ f2x part_s[DI / 32];
+  __shared__ RopeSmem rs;
+  __shared__ unsigned long long turn_s[64];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x;
+  stage_rope(a.rf, rs);
+  if (tid < 64) turn_s[tid] = a.rf.turn[tid];
+  __syncthreads();
   const int L = max(0, min(a.ctx[b], a.maxPagesPerSeq * kTokensPerPage));
   if (L == 0) return;
   const int t = L - 1;
@@ -167,12 +169,12 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const PrepArg
         float v = y[p];
         if (i < half) {
           float cs, sn;
-          rope_cos_sin_f32(static_cast<double>(t), a.rf.inv_freq[i], cs, sn);
+          rope_cos_sin_turns(static_cast<unsigned>(t), turn_s[i], cs, sn);
           v = y[p] * cs - y_s[h][i + half] * sn;
         } else if (i < a.rot) {
           const int k = i - half;
           float cs, sn;
-          rope_cos_sin_f32(static_cast<double>(t), a.rf.inv_freq[k], cs, sn);
+          rope_cos_sin_turns(static_cast<unsigned>(t), turn_s[k], cs, sn);
           v = y[p] * cs + y_s[h][k] * sn;
         }
         qo[qpos(i)] = v;
@@ -183,15 +185,14 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const PrepArg
     }
     return;
   }
-  const int u = tid - 256;  // dim handled by this thread of the state-update warps
-  const int uw = u >> 5;
+  // warps 8..: the state update
+  const int u = tid - 256;  // dim of the raw key this thread copies
   if (!completes) {
-    if (u < DI) {
-      const int kp = __ldg(ptK + (t >> 7));
-      if (static_cast<unsigned>(kp) < static_cast<unsigned>(a.numFlatPages))
-        a.pool[pool_row(kp, t & 127, a.Hkv, a.poolHeadDim) + a.D + u] = a.idxK[static_cast<size_t>(b) * DI + u];
-      else if (u == 0)
-        atomicOr(a.status, kErrBadPage);
+    const int kp = __ldg(ptK + (t >> 7));
+    if (static_cast<unsigned>(kp) < static_cast<unsigned>(a.numFlatPages)) {
+      a.pool[pool_row(kp, t & 127, a.Hkv, a.poolHeadDim) + a.D + u] = a.idxK[static_cast<size_t>(b) * DI + u];
+    } else if (u == 0) {
+      atomicOr(a.status, kErrBadPage);
     }
     return;
   }
@@ -203,49 +204,12 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const PrepArg
     if (u == 0) atomicOr(a.status, kErrBadPage);
     return;
   }
-  double sq = 0.0;
-  {
-    double acc = 0.0;
-    for (int j = 0; j < a.ratio; ++j) {
-      const int tok = first + j;
-      const __half hv = tok == t ? a.idxK[static_cast<size_t>(b) * DI + u]
-                                 : a.pool[pool_row(kp, tok & 127, a.Hkv, a.poolHeadDim) + a.D + u];
-      acc = __dadd_rn(acc, static_cast<double>(__half2float(hv)));
-    }
-    const double m = __ddiv_rn(acc, static_cast<double>(a.ratio));
-    m_s[u] = m;
-    sq = __dmul_rn(m, m);
-  }
-  {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sq = __dadd_rn(sq, __shfl_xor_sync(kFull, sq, o));
-    if (lane == 0) part_s[uw] = sq;
-  }
-  named_barrier_sync(1, DI);
-  {
-    double ss = 0.0;
-    for (int w = 0; w < DI / 32; ++w) ss = __dadd_rn(ss, part_s[w]);
-    const double inv = __ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(__ddiv_rn(ss, static_cast<double>(DI)),
-                                                           static_cast<double>(a.eps))));
-    y2_s[u] = __dmul_rn(__dmul_rn(m_s[u], inv), __dadd_rn(1.0, static_cast<double>(a.wk[u])));
-  }
-  named_barrier_sync(1, DI);
-  {
-    const int i = u, half = a.rot >> 1;
-    const double pos = static_cast<double>(first);
-    double r = y2_s[i];
-    if (i < half) {
-      double s, c;
-      rope_cos_sin_f64(pos, a.rf.inv_freq[i], c, s);
-      r = __dsub_rn(__dmul_rn(y2_s[i], c), __dmul_rn(y2_s[i + half], s));
-    } else if (i < a.rot) {
-      const int k = i - half;
-      double s, c;
-      rope_cos_sin_f64(pos, a.rf.inv_freq[k], c, s);
-      r = __dadd_rn(__dmul_rn(y2_s[i], c), __dmul_rn(y2_s[k], s));
-    }
-    a.pool[pool_row(vp, first & 127, a.Hkv, a.poolHeadDim) + a.D + i] = __double2half(r);
-  }
+  const __half* newk = a.idxK + static_cast<size_t>(b) * DI;
+  const __half* ktail = a.pool + pool_row(kp, first & 127, a.Hkv, a.poolHeadDim) + a.D;
+  const size_t tok_stride = static_cast<size_t>(a.Hkv) * a.poolHeadDim;
+  block_key<DI, DI / 32>([&](int j, int i) { return first + j == t ? newk[i] : ktail[j * tok_stride + i]; }, a.ratio,
+                         a.wk, a.eps, a.rot, first, rs, key_s, part_s, warp - 8, 1,
+                         a.pool + pool_row(vp, first & 127, a.Hkv, a.poolHeadDim) + a.D);
 }
 
 // ------------------------------------------------------------------ B2

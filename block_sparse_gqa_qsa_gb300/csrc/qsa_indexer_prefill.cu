@@ -4,12 +4,14 @@
 //
 // Two kernels:
 //   block_pool_kernel      one warp per complete block: mean of r raw keys ->
-//                          RMSNorm*(1+w) -> RoPE at the block start, in f64,
-//                          stored fp16 (RNE).  f64 makes the fp16 rounding of
-//                          every key the same decision an exact evaluation
+//                          RMSNorm*(1+w) -> RoPE at the block start, stored
+//                          fp16 (RNE) from an exact mean and double-float
+//                          arithmetic (qsa_blockkey.cuh), so the fp16 rounding
+//                          of every key is the decision an f64 evaluation
 //                          takes; the pass is tiny (S/r * di values).
 //   prefill_select_kernel  one CTA per 8 consecutive query rows of one
-//                          sequence: index-query prep (fp32, f64 angles), block
+//                          sequence: index-query prep (fp32, angles reduced
+//                          in integer turns), block
 //                          scores on the CUDA cores (fp32 FMA, a register-tiled
 //                          contraction of 8 rows x 8 heads against 256-block
 //                          tiles staged in shared memory), the relu/head sum,
@@ -18,6 +20,7 @@
 //                          reductions, exact ties to the lower block id) and
 //                          the expansion into the row's ascending index list.
 //                          A row group's scores never leave shared memory.
+#include "qsa_blockkey.cuh"
 #include "qsa_device.cuh"
 #include "qsa_internal.h"
 
@@ -32,61 +35,24 @@ struct PoolArgs {
   const int32_t* ctx;
   __half* kbar;
   int S, nbmax, ratio, rot;
-  double eps;
+  float eps;
   RopeFreqs rf;
 };
 
 template <int DI>
 __global__ void __launch_bounds__(256) block_pool_kernel(const PoolArgs a) {
-  constexpr int PER = DI / 32;
-  __shared__ double m_s[8][DI];
-  __shared__ double y_s[8][DI];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ f2x y_s[8][DI];
+  __shared__ RopeSmem rs;
+  const int warp = threadIdx.x >> 5;
   const int b = blockIdx.y;
   const int g = blockIdx.x * 8 + warp;
+  stage_rope(a.rf, rs);
+  __syncthreads();
   const int L = max(0, min(a.ctx[b], a.S));  // lengths outside [0, S] are clamped, never trusted
   if (g >= L / a.ratio) return;              // complete blocks only; warp-uniform
   const __half* raw = a.idxK + (static_cast<size_t>(b) * a.S + static_cast<size_t>(g) * a.ratio) * DI;
-#pragma unroll
-  for (int p = 0; p < PER; ++p) {
-    const int i = lane + 32 * p;
-    double acc = 0.0;
-    for (int j = 0; j < a.ratio; ++j) acc = __dadd_rn(acc, static_cast<double>(__half2float(raw[j * DI + i])));
-    m_s[warp][i] = __ddiv_rn(acc, static_cast<double>(a.ratio));
-  }
-  __syncwarp();
-  double ss = 0.0;
-#pragma unroll
-  for (int p = 0; p < PER; ++p) ss = __dadd_rn(ss, __dmul_rn(m_s[warp][lane + 32 * p], m_s[warp][lane + 32 * p]));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss = __dadd_rn(ss, __shfl_xor_sync(kFull, ss, o));
-  const double inv = __ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(__ddiv_rn(ss, static_cast<double>(DI)), a.eps)));
-#pragma unroll
-  for (int p = 0; p < PER; ++p) {
-    const int i = lane + 32 * p;
-    y_s[warp][i] = __dmul_rn(__dmul_rn(m_s[warp][i], inv), __dadd_rn(1.0, static_cast<double>(a.wk[i])));
-  }
-  __syncwarp();
-  const int half = a.rot >> 1;
-  const double pos = static_cast<double>(g) * a.ratio;
-  __half* out = a.kbar + (static_cast<size_t>(b) * a.nbmax + g) * DI;
-#pragma unroll
-  for (int p = 0; p < PER; ++p) {
-    const int i = lane + 32 * p;
-    const double y = y_s[warp][i];
-    double r = y;
-    if (i < half) {
-      double s, c;
-      rope_cos_sin_f64(pos, a.rf.inv_freq[i], c, s);
-      r = __dsub_rn(__dmul_rn(y, c), __dmul_rn(y_s[warp][i + half], s));
-    } else if (i < a.rot) {
-      const int k = i - half;
-      double s, c;
-      rope_cos_sin_f64(pos, a.rf.inv_freq[k], c, s);
-      r = __dadd_rn(__dmul_rn(y, c), __dmul_rn(y_s[warp][k], s));
-    }
-    out[i] = __double2half(r);
-  }
+  block_key<DI, 1>([&](int j, int i) { return raw[j * DI + i]; }, a.ratio, a.wk, a.eps, a.rot, g * a.ratio, rs, y_s[warp],
+                   nullptr, 0, 0, a.kbar + (static_cast<size_t>(b) * a.nbmax + g) * DI);
 }
 
 struct SelArgs {
@@ -145,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_select_kernel(const SelAr
     for (int e = tid; e < kRows * half; e += kThreads) {
       const int r = e / half, i = e - r * half;
       float c = 1.f, s = 0.f;
-      if (r < nlive) rope_cos_sin_f32(static_cast<double>(t0 + r), a.rf.inv_freq[i], c, s);
+      if (r < nlive) rope_cos_sin_turns(static_cast<unsigned>(t0 + r), a.rf.turn[i], c, s);
       cs_s[r * 128 + 2 * i] = c;
       cs_s[r * 128 + 2 * i + 1] = s;
     }
@@ -429,7 +395,7 @@ cudaError_t launch_indexer_prefill(const QsaIndexerPrefillParams& p, const RopeF
     pa.nbmax = nbmax;
     pa.ratio = p.compressRatio;
     pa.rot = p.rotDim;
-    pa.eps = static_cast<double>(p.rmsNormEps);
+    pa.eps = p.rmsNormEps;
     pa.rf = rf;
     dim3 grid((nbmax + 7) / 8, p.batchSize);
     if (p.headDim == 64)

@@ -13,9 +13,18 @@ namespace qsa {
 
 constexpr int kTokensPerPageHost = 128;  // pool page size of the decode contract
 
-// theta^(-2i/rot) for i < rot/2, formed in f64 on the host once per call.
+// theta^(-2i/rot) for i < rot/2, formed in f64 on the host once per call, and
+// the same frequencies as 64-bit fixed-point fractions of a turn:
+// turn[i] = frac(inv_freq[i] / (2 pi)) * 2^64, so that pos * turn[i] mod 2^64
+// is the angle pos * inv_freq[i] as an exact fraction of a full turn.
+// qcos_hi[j] + qcos_lo[j] is cos(pi j / 64) for j = 0..32 (a quarter turn in
+// steps of 1/128 of a turn) as a pair of fp32 numbers, formed in f64 on the host;
+// the block-key rotation evaluates its angles from it.
 struct RopeFreqs {
   double inv_freq[64];
+  unsigned long long turn[64];
+  float qcos_hi[33];
+  float qcos_lo[33];
 };
 
 // Prefill indexer -----------------------------------------------------------
@@ -46,6 +55,7 @@ int gather_max_row_chunks();  // 16-byte chunks of one K (or V) token row a warp
 
 // SMs of the current device (cached per device).
 int sm_count();
+
 
 // Stores msg as the calling thread's qsa_last_error_message() and returns s.
 qsa_status_t record_error(qsa_status_t s, const char* msg);

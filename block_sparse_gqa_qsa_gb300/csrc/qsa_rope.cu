@@ -101,15 +101,6 @@ __device__ __forceinline__ void load_w(const float* p, int G, uint64_t (&w)[4]) 
   w[3] = b.y;
 }
 
-// cos / sin of the angle pos * inv_freq, with inv_freq given as turn = frac(inv_freq / (2 pi)) * 2^64:
-// pos * turn mod 2^64 is the angle's fraction of a full turn, exact in integer arithmetic, and its top
-// 32 bits, read as signed, place it in [-pi, pi).  The only roundings are those of the fp32 argument.
-__device__ __forceinline__ void rope_cos_sin_turns(unsigned pos, unsigned long long turn, float& c, float& s) {
-  const unsigned long long t = turn * pos;
-  const float r = static_cast<float>(static_cast<int>(static_cast<unsigned>(t >> 32))) * 1.4629180792671596e-09f;
-  sincosf(r, &s, &c);
-}
-
 // Position of a CTA's n-th token; advanced by the grid stride without a division.
 struct TokenCursor {
   long long tok;
@@ -275,11 +266,7 @@ cudaError_t launch_rope_qkv(const QsaRopeQkvParams& p, const RopeFreqs& rf) {
   a.numFlatPages = p.numFlatPages;
   a.maxPagesPerSeq = p.maxPagesPerSeq;
   a.eps = p.rmsNormEps;
-  for (int i = 0; i < 64; ++i) {  // frac(inv_freq / (2 pi)) * 2^64, from the host's f64 inv_freq
-    double x = rf.inv_freq[i] / 6.283185307179586;
-    x -= std::floor(x);
-    a.turn[i] = static_cast<unsigned long long>(std::ldexp(x, 64));
-  }
+  for (int i = 0; i < 64; ++i) a.turn[i] = rf.turn[i];
   const int T = p.batchSize * p.seqLen;  // validated <= INT_MAX
   const int nchunk = (p.numQHeads + 2 * p.numKVHeads) * (p.headDim / 8);
   const size_t smem = static_cast<size_t>(kRopeStages) * nchunk * 16;
