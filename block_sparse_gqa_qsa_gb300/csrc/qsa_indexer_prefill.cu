@@ -2,24 +2,28 @@
 // batch ("Qsa Attention Plugin", fused step 2; "spark_model/layers/ops/qsa.rs",
 // qsa_block_pool / qsa_qprep_rows / qsa_score_rows).
 //
-// Two kernels:
+// Three kernels:
 //   block_pool_kernel      one warp per complete block: mean of r raw keys ->
 //                          RMSNorm*(1+w) -> RoPE at the block start, stored
 //                          fp16 (RNE) from an exact mean and double-float
 //                          arithmetic (qsa_blockkey.cuh), so the fp16 rounding
 //                          of every key is the decision an f64 evaluation
 //                          takes; the pass is tiny (S/r * di values).
-//   prefill_select_kernel  one CTA per 8 consecutive query rows of one
-//                          sequence: index-query prep (fp32, angles reduced
-//                          in integer turns), block
-//                          scores on the CUDA cores (fp32 FMA, a register-tiled
-//                          contraction of 8 rows x 8 heads against 256-block
-//                          tiles staged in shared memory), the relu/head sum,
-//                          then one warp per row: a deterministic top-`budget`
-//                          select (bisection on the score bits with warp
-//                          reductions, exact ties to the lower block id) and
-//                          the expansion into the row's ascending index list.
-//                          A row group's scores never leave shared memory.
+//   prefill_score_kernel   one CTA per 8 consecutive query rows of one
+//                          sequence whose rows need a selection (n_c > budget):
+//                          index-query prep (fp32, angles reduced in integer
+//                          turns), block scores on the CUDA cores (fp32 FMA, a
+//                          register-tiled contraction of 8 rows x 8 heads
+//                          against 256-block tiles staged in shared memory),
+//                          the relu/head sum, written to the workspace (each
+//                          row's n_c scores, rows packed back to back).  Two
+//                          CTAs share an SM.
+//   prefill_topk_kernel    one warp per row: a deterministic top-`budget`
+//                          select over the row's scores (bisection on the
+//                          score bits with warp reductions, exact ties to the
+//                          lower block id) and the expansion into the row's
+//                          ascending index list; rows with n_c <= budget list
+//                          0..t and rows t >= L are all -1.
 #include "qsa_blockkey.cuh"
 #include "qsa_device.cuh"
 #include "qsa_internal.h"
@@ -60,8 +64,10 @@ struct SelArgs {
   const float* wq;
   const int32_t* ctx;
   const __half* kbar;
+  float* scores;  // [B][tri_offset(S)]: row t's n_c(t) scores at tri_offset(t)
   int32_t* indices;
   int S, Hi, nbmax, ratio, rot, budget, topK;
+  long long triPerSeq;
   float eps;
   RopeFreqs rf;
 };
@@ -70,23 +76,39 @@ constexpr int kRows = kPrefillRowsPerCta;  // rows per CTA (one warp each)
 constexpr int kThreads = 256;
 constexpr int kTile = 256;                  // blocks per score tile (8 per lane)
 constexpr int kKC = 16;                     // key dims staged per step
-constexpr int kKS = kKC + 4;                // padded row stride (conflict-free float4 reads)
+constexpr int kKS = kKC + 2;                // padded row stride: float2 reads and writes are conflict-free
 constexpr int kHI = 8;                      // heads per thread tile (Hi <= 8, extra heads are zero)
 
-template <int DI, int VPT>
-constexpr size_t select_smem_bytes() {
-  return sizeof(float) * (static_cast<size_t>(DI) * kRows * kHI + 2 * kTile * kKS + kRows * kThreads * VPT +
-                          kRows * DI + kRows * 128);
+// Two fp16 values packed in 32 bits, widened to fp32.
+__device__ __forceinline__ float2 bits_to_float2(uint32_t u) {
+  __half2_raw r;
+  r.x = static_cast<unsigned short>(u & 0xffffu);
+  r.y = static_cast<unsigned short>(u >> 16);
+  return __half22float2(__half2(r));
 }
 
-template <int DI, int VPT>
-__global__ void __launch_bounds__(kThreads, 1) prefill_select_kernel(const SelArgs a) {
-  constexpr int NBMAX = kThreads * VPT;
+// Start of row t's scores within its sequence: sum over u = 1..t of floor(u / r),
+// i.e. the complete-block counts n_c of rows 0..t-1.
+__host__ __device__ __forceinline__ long long tri_offset(long long t, int r) {
+  const long long k = t / r;
+  return r * k * (k - 1) / 2 + k * (t - k * r + 1);
+}
+
+template <int DI>
+constexpr size_t score_smem_bytes() {
+  return sizeof(float) * (static_cast<size_t>(DI) * kRows * kHI + 2 * kTile * kKS + kRows * DI + kRows * 128);
+}
+
+// Block scores of 8 consecutive query rows of one sequence (rows whose n_c
+// exceeds the budget; the others need no scores), written to the workspace.
+// Two CTAs share an SM (80 KB of shared memory each at di = 128), so the
+// staging barriers and shared-memory latencies of one are covered by the other.
+template <int DI>
+__global__ void __launch_bounds__(kThreads, 2) prefill_score_kernel(const SelArgs a) {
   extern __shared__ __align__(16) float smem[];
   float* q_s = smem;                          // [DI][kRows][kHI] prepared queries
   float* kb_s = q_s + DI * kRows * kHI;       // [2][kTile][kKS]  block-key tile (fp32)
-  float* sc_s = kb_s + 2 * kTile * kKS;       // [kRows][NBMAX]   block scores
-  float* ys_s = sc_s + kRows * NBMAX;         // [kRows][DI]      per-warp RoPE scratch
+  float* ys_s = kb_s + 2 * kTile * kKS;       // [kRows][DI]      per-warp RoPE scratch
   float* cs_s = ys_s + kRows * DI;            // [kRows][64][2]   cos/sin per row
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -94,194 +116,222 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_select_kernel(const SelAr
   const int ngroups = (a.S + kRows - 1) / kRows;
   const int t0 = (ngroups - 1 - static_cast<int>(blockIdx.x)) * kRows;  // longest rows first
   const int L = max(0, min(a.ctx[b], a.S));
-  int32_t* ind_b = a.indices + static_cast<size_t>(b) * a.S * a.topK;
   const int t_end = min(t0 + kRows, L);  // live rows [t0, t_end)
-  {
-    const int first_pad = max(t0, t_end);
-    const int npad = min(t0 + kRows, a.S) - first_pad;
-    for (int i = tid; i < npad * a.topK; i += kThreads) ind_b[static_cast<size_t>(first_pad) * a.topK + i] = -1;
-  }
   if (t0 >= L) return;
   const int nlive = t_end - t0;
   const int n_hi = t_end / a.ratio;  // complete blocks seen by the group's last live row
+  if (n_hi <= a.budget) return;
 
-  if (n_hi > a.budget) {
-    // ---------------------------------------------------------- query prep
-    const int half = a.rot >> 1;
-    for (int e = tid; e < kRows * half; e += kThreads) {
-      const int r = e / half, i = e - r * half;
-      float c = 1.f, s = 0.f;
-      if (r < nlive) rope_cos_sin_turns(static_cast<unsigned>(t0 + r), a.rf.turn[i], c, s);
-      cs_s[r * 128 + 2 * i] = c;
-      cs_s[r * 128 + 2 * i + 1] = s;
-    }
-    __syncthreads();
-    {
-      constexpr int PER = DI / 32;
-      const int r = warp;
-      for (int h = 0; h < kHI; ++h) {
-        if (r < nlive && h < a.Hi) {
-          const __half* x = a.idxQ + ((static_cast<size_t>(b) * a.S + t0 + r) * a.Hi + h) * DI;
-          float y[PER];
-          float ss = 0.f;
+  // ------------------------------------------------------------ query prep
+  const int half = a.rot >> 1;
+  for (int e = tid; e < kRows * half; e += kThreads) {
+    const int r = e / half, i = e - r * half;
+    float c = 1.f, s = 0.f;
+    if (r < nlive) rope_cos_sin_turns(static_cast<unsigned>(t0 + r), a.rf.turn[i], c, s);
+    cs_s[r * 128 + 2 * i] = c;
+    cs_s[r * 128 + 2 * i + 1] = s;
+  }
+  __syncthreads();
+  {
+    constexpr int PER = DI / 32;
+    const int r = warp;
+    for (int h = 0; h < kHI; ++h) {
+      if (r < nlive && h < a.Hi) {
+        const __half* x = a.idxQ + ((static_cast<size_t>(b) * a.S + t0 + r) * a.Hi + h) * DI;
+        float y[PER];
+        float ss = 0.f;
 #pragma unroll
-          for (int p = 0; p < PER; ++p) {
-            y[p] = __half2float(x[lane + 32 * p]);
-            ss = fmaf(y[p], y[p], ss);
-          }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
-          const float inv = 1.0f / sqrtf(ss / DI + a.eps);
-#pragma unroll
-          for (int p = 0; p < PER; ++p) {
-            const int i = lane + 32 * p;
-            y[p] = y[p] * inv * (1.0f + a.wq[i]);
-            ys_s[r * DI + i] = y[p];
-          }
-          __syncwarp();
-#pragma unroll
-          for (int p = 0; p < PER; ++p) {
-            const int i = lane + 32 * p;
-            float v = y[p];
-            if (i < half) {
-              v = y[p] * cs_s[r * 128 + 2 * i] - ys_s[r * DI + i + half] * cs_s[r * 128 + 2 * i + 1];
-            } else if (i < a.rot) {
-              const int k = i - half;
-              v = y[p] * cs_s[r * 128 + 2 * k] + ys_s[r * DI + k] * cs_s[r * 128 + 2 * k + 1];
-            }
-            q_s[(i * kRows + r) * kHI + h] = v;
-          }
-          __syncwarp();
-        } else {
-#pragma unroll
-          for (int p = 0; p < PER; ++p) q_s[((lane + 32 * p) * kRows + r) * kHI + h] = 0.f;
+        for (int p = 0; p < PER; ++p) {
+          y[p] = __half2float(x[lane + 32 * p]);
+          ss = fmaf(y[p], y[p], ss);
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
+        const float inv = 1.0f / sqrtf(ss / DI + a.eps);
+#pragma unroll
+        for (int p = 0; p < PER; ++p) {
+          const int i = lane + 32 * p;
+          y[p] = y[p] * inv * (1.0f + a.wq[i]);
+          ys_s[r * DI + i] = y[p];
+        }
+        __syncwarp();
+#pragma unroll
+        for (int p = 0; p < PER; ++p) {
+          const int i = lane + 32 * p;
+          float v = y[p];
+          if (i < half) {
+            v = y[p] * cs_s[r * 128 + 2 * i] - ys_s[r * DI + i + half] * cs_s[r * 128 + 2 * i + 1];
+          } else if (i < a.rot) {
+            const int k = i - half;
+            v = y[p] * cs_s[r * 128 + 2 * k] + ys_s[r * DI + k] * cs_s[r * 128 + 2 * k + 1];
+          }
+          q_s[(i * kRows + r) * kHI + h] = v;
+        }
+        __syncwarp();
+      } else {
+#pragma unroll
+        for (int p = 0; p < PER; ++p) q_s[((lane + 32 * p) * kRows + r) * kHI + h] = 0.f;
       }
     }
-    __syncthreads();
+  }
+  __syncthreads();
 
-    // ------------------------------------------------------- block scores
-    // Lane owns blocks lane + 32 m (m < 8) of the tile, for its warp's row
-    // and all kHI heads: 64 accumulators, each a plain ascending-k FMA chain,
-    // so a block's score does not depend on where the block sits in a tile.
-    const __half* kb_g = a.kbar + static_cast<size_t>(b) * a.nbmax * DI;
-    const int ntiles = (n_hi + kTile - 1) / kTile;
-    for (int tile = 0; tile < ntiles; ++tile) {
-      const int gbase = tile * kTile;
-      const int gl = gbase + tid;  // block staged by this thread
-      const bool gok = gl < n_hi;
-      const uint4* src = reinterpret_cast<const uint4*>(kb_g + static_cast<size_t>(gok ? gl : 0) * DI);
-      const uint4 zero = make_uint4(0, 0, 0, 0);
-      uint4 pre0 = gok ? __ldg(src) : zero;
-      uint4 pre1 = gok ? __ldg(src + 1) : zero;
-      float acc[8][kHI];
+  // ---------------------------------------------------------- block scores
+  // Lane owns blocks lane + 32 m (m < 8) of the tile, for its warp's row
+  // and all kHI heads: 64 accumulators, each a plain ascending-k FMA chain,
+  // so a block's score does not depend on where the block sits in a tile.
+  const int t = t0 + warp;
+  const int n_c = (t + 1) / a.ratio;
+  const bool store = warp < nlive && n_c > a.budget;  // this row needs its scores
+  float* srow = a.scores + static_cast<size_t>(b) * a.triPerSeq + tri_offset(t, a.ratio);
+  const __half* kb_g = a.kbar + static_cast<size_t>(b) * a.nbmax * DI;
+  const int ntiles = (n_hi + kTile - 1) / kTile;
+  for (int tile = 0; tile < ntiles; ++tile) {
+    const int gbase = tile * kTile;
+    const int gl = gbase + tid;  // block staged by this thread
+    const bool gok = gl < n_hi;
+    const uint4* src = reinterpret_cast<const uint4*>(kb_g + static_cast<size_t>(gok ? gl : 0) * DI);
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    uint4 pre0 = gok ? __ldg(src) : zero;
+    uint4 pre1 = gok ? __ldg(src + 1) : zero;
+    float acc[8][kHI];
 #pragma unroll
-      for (int m = 0; m < 8; ++m)
+    for (int m = 0; m < 8; ++m)
 #pragma unroll
-        for (int h = 0; h < kHI; ++h) acc[m][h] = 0.f;
+      for (int h = 0; h < kHI; ++h) acc[m][h] = 0.f;
 
 #pragma unroll 1
-      for (int kc = 0; kc < DI / kKC; ++kc) {
-        float* dst = kb_s + (kc & 1) * kTile * kKS + tid * kKS;
-        {
-          const __half2* h0 = reinterpret_cast<const __half2*>(&pre0);
-          const __half2* h1 = reinterpret_cast<const __half2*>(&pre1);
-          float4 f[4];
-          float2 t;
-          t = __half22float2(h0[0]); f[0].x = t.x; f[0].y = t.y;
-          t = __half22float2(h0[1]); f[0].z = t.x; f[0].w = t.y;
-          t = __half22float2(h0[2]); f[1].x = t.x; f[1].y = t.y;
-          t = __half22float2(h0[3]); f[1].z = t.x; f[1].w = t.y;
-          t = __half22float2(h1[0]); f[2].x = t.x; f[2].y = t.y;
-          t = __half22float2(h1[1]); f[2].z = t.x; f[2].w = t.y;
-          t = __half22float2(h1[2]); f[3].x = t.x; f[3].y = t.y;
-          t = __half22float2(h1[3]); f[3].z = t.x; f[3].w = t.y;
+    for (int kc = 0; kc < DI / kKC; ++kc) {
+      float2* dst = reinterpret_cast<float2*>(kb_s + (kc & 1) * kTile * kKS + tid * kKS);
+      dst[0] = bits_to_float2(pre0.x);
+      dst[1] = bits_to_float2(pre0.y);
+      dst[2] = bits_to_float2(pre0.z);
+      dst[3] = bits_to_float2(pre0.w);
+      dst[4] = bits_to_float2(pre1.x);
+      dst[5] = bits_to_float2(pre1.y);
+      dst[6] = bits_to_float2(pre1.z);
+      dst[7] = bits_to_float2(pre1.w);
+      __syncthreads();
+      if (kc + 1 < DI / kKC) {
+        pre0 = gok ? __ldg(src + 2 * (kc + 1)) : zero;
+        pre1 = gok ? __ldg(src + 2 * (kc + 1) + 1) : zero;
+      }
+      const float* kt = kb_s + (kc & 1) * kTile * kKS;
+      const float* qk = q_s + static_cast<size_t>(kc * kKC) * kRows * kHI + warp * kHI;
+#pragma unroll 4
+      for (int kp = 0; kp < kKC / 2; ++kp) {  // two dims per step: 16 key values, 16 query values, 128 FMAs
+        float2 kv[8];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) reinterpret_cast<float4*>(dst)[i] = f[i];
-        }
-        __syncthreads();
-        if (kc + 1 < DI / kKC) {
-          pre0 = gok ? __ldg(src + 2 * (kc + 1)) : zero;
-          pre1 = gok ? __ldg(src + 2 * (kc + 1) + 1) : zero;
-        }
-        const float* kt = kb_s + (kc & 1) * kTile * kKS;
-        const float* qk = q_s + static_cast<size_t>(kc * kKC) * kRows * kHI + warp * kHI;
+        for (int m = 0; m < 8; ++m) kv[m] = *reinterpret_cast<const float2*>(kt + (lane + 32 * m) * kKS + kp * 2);
 #pragma unroll
-        for (int kq = 0; kq < kKC / 4; ++kq) {
-          float4 kv[8];
+        for (int kk = 0; kk < 2; ++kk) {
+          const float* qp = qk + (kp * 2 + kk) * kRows * kHI;
+          const float4 qa = *reinterpret_cast<const float4*>(qp);
+          const float4 qb = *reinterpret_cast<const float4*>(qp + 4);
 #pragma unroll
-          for (int m = 0; m < 8; ++m) kv[m] = *reinterpret_cast<const float4*>(kt + (lane + 32 * m) * kKS + kq * 4);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const float* qp = qk + (kq * 4 + kk) * kRows * kHI;
-            const float4 qa = *reinterpret_cast<const float4*>(qp);
-            const float4 qb = *reinterpret_cast<const float4*>(qp + 4);
-            const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-              const float kval = kk == 0 ? kv[m].x : kk == 1 ? kv[m].y : kk == 2 ? kv[m].z : kv[m].w;
-#pragma unroll
-              for (int h = 0; h < kHI; ++h) acc[m][h] = fmaf(qv[h], kval, acc[m][h]);
-            }
+          for (int m = 0; m < 8; ++m) {
+            const float kval = kk == 0 ? kv[m].x : kv[m].y;
+            acc[m][0] = fmaf(qa.x, kval, acc[m][0]);
+            acc[m][1] = fmaf(qa.y, kval, acc[m][1]);
+            acc[m][2] = fmaf(qa.z, kval, acc[m][2]);
+            acc[m][3] = fmaf(qa.w, kval, acc[m][3]);
+            acc[m][4] = fmaf(qb.x, kval, acc[m][4]);
+            acc[m][5] = fmaf(qb.y, kval, acc[m][5]);
+            acc[m][6] = fmaf(qb.z, kval, acc[m][6]);
+            acc[m][7] = fmaf(qb.w, kval, acc[m][7]);
           }
         }
       }
+    }
+    if (store) {
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
         const int g = gbase + lane + 32 * m;
-        if (g < n_hi) {
-          float s = 0.f;
+        if (g < n_c) {
+          float sc = 0.f;
 #pragma unroll
-          for (int h = 0; h < kHI; ++h) s += acc[m][h] > 0.f ? acc[m][h] : 0.f;
-          sc_s[warp * NBMAX + g] = s;
+          for (int h = 0; h < kHI; ++h) sc += acc[m][h] > 0.f ? acc[m][h] : 0.f;
+          srow[g] = sc;
         }
       }
     }
-    __syncthreads();
   }
+}
 
-  // ------------------------------------ select + expand, one warp per row
-  // Lane l holds the scores of blocks l + 32 m.  Keys are the score bits + 1
-  // (order-preserving for scores >= 0; 0 marks blocks past the row's n_c).
-  // Bisection on the key finds T with count(key >= T) >= budget >
-  // count(key > T); the blocks above T are kept, and of those equal to T the
-  // lowest ids, so the kept set is the top `budget` by (score desc, id asc).
-  // Walking m upwards visits ids in ascending order, so ballots compact the
-  // kept blocks straight into the ascending list.
-  if (warp < nlive) {
-    constexpr int KPL = NBMAX / 32;
-    const int t = t0 + warp;
-    const int n_c = (t + 1) / a.ratio;
-    int32_t* out = ind_b + static_cast<size_t>(t) * a.topK;
-    if (n_c <= a.budget) {  // every block kept: the row lists 0..t
-      for (int i = lane; i < a.topK; i += 32) out[i] = i <= t ? i : -1;
+// ------------------------------------ select + expand, one warp per row
+// Lane l holds the scores of blocks l + 32 m.  Keys are the score bits + 1
+// (order-preserving for scores >= 0; 0 marks blocks past the row's n_c).
+// Bisection on the key finds T with count(key >= T) >= budget >
+// count(key > T); the blocks above T are kept, and of those equal to T the
+// lowest ids, so the kept set is the top `budget` by (score desc, id asc).
+// Walking m upwards visits ids in ascending order, so ballots compact the
+// kept blocks straight into the ascending list.  Rows t >= L are all -1 and
+// rows with n_c <= budget list 0..t.
+template <int VPT>
+__global__ void __launch_bounds__(kThreads) prefill_topk_kernel(const SelArgs a) {
+  constexpr int KPL = kThreads * VPT / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.y;
+  const int t = blockIdx.x * kRows + warp;
+  if (t >= a.S) return;
+  const int L = max(0, min(a.ctx[b], a.S));
+  int32_t* out = a.indices + (static_cast<size_t>(b) * a.S + t) * a.topK;
+  if (t >= L) {
+    for (int i = lane; i < a.topK; i += 32) out[i] = -1;
+    return;
+  }
+  const int n_c = (t + 1) / a.ratio;
+  if (n_c <= a.budget) {  // every block kept: the row lists 0..t
+    for (int i = lane; i < a.topK; i += 32) out[i] = i <= t ? i : -1;
+    return;
+  }
+  const float* srow = a.scores + static_cast<size_t>(b) * a.triPerSeq + tri_offset(t, a.ratio);
+  // Keys live in registers, KPL per lane; only the first ceil(n_c / 32) of them
+  // can be non-zero, so every pass skips the groups of 8 past that (a
+  // warp-uniform branch, no instructions issued for them).
+  constexpr int KG = 8;
+  const int mlim = (n_c + 31) / 32;
+  const int nslot = KG * ((mlim + KG - 1) / KG);  // keys per lane that the passes visit
+  uint32_t key[KPL];
+#pragma unroll
+  for (int c = 0; c < KPL / KG; ++c) {
+#pragma unroll
+    for (int k = 0; k < KG; ++k) {
+      const int g = lane + 32 * (c * KG + k);
+      key[c * KG + k] = c * KG < mlim && g < n_c ? __float_as_uint(__ldcg(srow + g)) + 1u : 0u;
+    }
+  }
+  uint32_t lo = 1u, hi = 0x80000001u;  // count(>= lo) >= budget > count(>= hi)
+  int c_hi = 0;
+  while (hi - lo > 1u) {
+    const uint32_t mid = lo + ((hi - lo) >> 1);
+    // keys lie in [0, 2^31) and mid in [1, 2^31], so key - mid as a signed
+    // 32-bit value is negative exactly when key < mid
+    int below_mid = 0;
+#pragma unroll
+    for (int c = 0; c < KPL / KG; ++c) {
+      if (c * KG < mlim) {
+#pragma unroll
+        for (int k = 0; k < KG; ++k) below_mid += static_cast<int>(key[c * KG + k] - mid) >> 31;
+      }
+    }
+    const int c = static_cast<int>(__reduce_add_sync(kFull, static_cast<unsigned>(nslot + below_mid)));
+    if (c >= a.budget) {
+      lo = mid;
     } else {
-      uint32_t key[KPL];
+      hi = mid;
+      c_hi = c;
+    }
+  }
+  int quota = a.budget - c_hi;  // blocks with key == lo to keep, lowest ids first
+  int pos = 0;
+  const unsigned below = (1u << lane) - 1u;
 #pragma unroll
-      for (int m = 0; m < KPL; ++m) {
-        const int g = lane + 32 * m;
-        key[m] = g < n_c ? __float_as_uint(sc_s[warp * NBMAX + g]) + 1u : 0u;
-      }
-      uint32_t lo = 1u, hi = 0x80000001u;  // count(>= lo) >= budget > count(>= hi)
-      int c_hi = 0;
-      while (hi - lo > 1u) {
-        const uint32_t mid = lo + ((hi - lo) >> 1);
-        int c = 0;
+  for (int c = 0; c < KPL / KG; ++c) {
+    if (c * KG < mlim) {
 #pragma unroll
-        for (int m = 0; m < KPL; ++m) c += key[m] >= mid ? 1 : 0;
-        c = static_cast<int>(__reduce_add_sync(kFull, static_cast<unsigned>(c)));
-        if (c >= a.budget) {
-          lo = mid;
-        } else {
-          hi = mid;
-          c_hi = c;
-        }
-      }
-      int quota = a.budget - c_hi;  // blocks with key == lo to keep, lowest ids first
-      int pos = 0;
-      const unsigned below = (1u << lane) - 1u;
-#pragma unroll
-      for (int m = 0; m < KPL; ++m) {
+      for (int k = 0; k < KG; ++k) {
+        const int m = c * KG + k;
         const bool eq = key[m] == lo;
         const unsigned eqm = __ballot_sync(kFull, eq);
         const bool take = key[m] > lo || (eq && __popc(eqm & below) < quota);
@@ -293,33 +343,39 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_select_kernel(const SelAr
         }
         pos += __popc(tm);
       }
-      const int head = pos * a.ratio;
-      for (int i = head + lane; i < a.topK; i += 32) {
-        const int j = n_c * a.ratio + (i - head);
-        out[i] = j <= t ? j : -1;
-      }
     }
+  }
+  const int head = pos * a.ratio;
+  for (int i = head + lane; i < a.topK; i += 32) {
+    const int j = n_c * a.ratio + (i - head);
+    out[i] = j <= t ? j : -1;
   }
 }
 
-template <int DI, int VPT>
-cudaError_t launch_select(const SelArgs& a, int B, cudaStream_t st) {
-  constexpr size_t smem = select_smem_bytes<DI, VPT>();
+template <int DI>
+cudaError_t launch_score(const SelArgs& a, int B, cudaStream_t st) {
+  constexpr size_t smem = score_smem_bytes<DI>();
   static const cudaError_t attr = cudaFuncSetAttribute(
-      prefill_select_kernel<DI, VPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      prefill_score_kernel<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (attr != cudaSuccess) return attr;
   dim3 grid((a.S + kRows - 1) / kRows, B);
-  prefill_select_kernel<DI, VPT><<<grid, kThreads, smem, st>>>(a);
+  prefill_score_kernel<DI><<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
-template <int DI>
-cudaError_t launch_select_di(const SelArgs& a, int B, cudaStream_t st) {
+template <int VPT>
+cudaError_t launch_topk(const SelArgs& a, int B, cudaStream_t st) {
+  dim3 grid((a.S + kRows - 1) / kRows, B);
+  prefill_topk_kernel<VPT><<<grid, kThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_any(const SelArgs& a, int B, cudaStream_t st) {
   const int nb = a.nbmax;
-  if (nb <= 2 * kThreads) return launch_select<DI, 2>(a, B, st);
-  if (nb <= 4 * kThreads) return launch_select<DI, 4>(a, B, st);
-  if (nb <= 8 * kThreads) return launch_select<DI, 8>(a, B, st);
-  return launch_select<DI, 16>(a, B, st);
+  if (nb <= 2 * kThreads) return launch_topk<2>(a, B, st);
+  if (nb <= 4 * kThreads) return launch_topk<4>(a, B, st);
+  if (nb <= 8 * kThreads) return launch_topk<8>(a, B, st);
+  return launch_topk<16>(a, B, st);
 }
 
 }  // namespace
@@ -377,8 +433,14 @@ __global__ void __launch_bounds__(256) handoff_kernel(const HandoffArgs a) {
   }
 }
 
+// Workspace: status word, block keys fp16 [B][S/r][di], then the block scores
+// fp32 of every row, per sequence in row order (tri_offset(S) floats each).
+size_t kbar_region_bytes(int B, int S, int di, int ratio) {
+  return (static_cast<size_t>(B) * (S / ratio) * di * sizeof(__half) + 255) / 256 * 256;
+}
 size_t indexer_prefill_workspace_bytes(int B, int S, int di, int ratio) {
-  return kStatusBytes + static_cast<size_t>(B) * (S / ratio) * di * sizeof(__half);
+  return kStatusBytes + kbar_region_bytes(B, S, di, ratio) +
+         static_cast<size_t>(B) * static_cast<size_t>(tri_offset(S, ratio)) * sizeof(float);
 }
 
 cudaError_t launch_indexer_prefill(const QsaIndexerPrefillParams& p, const RopeFreqs& rf) {
@@ -410,6 +472,9 @@ cudaError_t launch_indexer_prefill(const QsaIndexerPrefillParams& p, const RopeF
   sa.wq = p.qNormW;
   sa.ctx = p.contextLengths;
   sa.kbar = kbar;
+  sa.scores = reinterpret_cast<float*>(static_cast<char*>(p.workspace) + kStatusBytes +
+                                       kbar_region_bytes(p.batchSize, p.seqLen, p.headDim, p.compressRatio));
+  sa.triPerSeq = tri_offset(p.seqLen, p.compressRatio);
   sa.indices = p.indices;
   sa.S = p.seqLen;
   sa.Hi = p.numHeads;
@@ -420,7 +485,9 @@ cudaError_t launch_indexer_prefill(const QsaIndexerPrefillParams& p, const RopeF
   sa.topK = p.topK;
   sa.eps = p.rmsNormEps;
   sa.rf = rf;
-  return p.headDim == 64 ? launch_select_di<64>(sa, p.batchSize, st) : launch_select_di<128>(sa, p.batchSize, st);
+  const cudaError_t e = p.headDim == 64 ? launch_score<64>(sa, p.batchSize, st) : launch_score<128>(sa, p.batchSize, st);
+  if (e != cudaSuccess) return e;
+  return launch_topk_any(sa, p.batchSize, st);
 }
 
 cudaError_t launch_indexer_handoff(const QsaIndexerHandoffParams& p) {

@@ -79,7 +79,10 @@ typedef struct {
   const float* kNormW;           /* fp32 [headDim]                                          */
   const int32_t* contextLengths; /* int32 [B], 0 <= L <= S                                  */
   int32_t* indices;              /* out int32 [B, S, topK]                                  */
-  void* workspace;               /* >= qsa_indexer_prefill_workspace_size(), 256-B aligned */
+  void* workspace;               /* >= qsa_indexer_prefill_workspace_size(), 256-B aligned:
+                                    status word, block keys, and the fp32 block scores of
+                                    every row (sum over t < S of floor((t+1)/r) per
+                                    sequence, ~S^2/(2r): 34 MB at S = 8192, r = 4)        */
   size_t workspaceBytes;
   int32_t batchSize;             /* B                                                       */
   int32_t seqLen;                /* S (padded length)                                       */

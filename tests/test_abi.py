@@ -74,7 +74,8 @@ def test_constants_and_sizes(binding):
     B, Hkv, D = 3, 4, 128
     po, ps, pc = binding.sparse_decode_workspace_elems(B, Hkv, D)
     assert (po, ps, pc) == (B * Hkv * 8 * 16 * D, B * Hkv * 8 * 2 * 16, B * Hkv)
-    assert binding.indexer_prefill_workspace_size(2, 1000, 128, 4) == 256 + 2 * 250 * 128 * 2
+    tri = sum((t + 1) // 4 for t in range(1000))  # the complete-block counts n_c(t) of every row
+    assert binding.indexer_prefill_workspace_size(2, 1000, 128, 4) == 256 + 2 * 250 * 128 * 2 + 2 * tri * 4
     assert binding.indexer_prefill_workspace_size(0, 1000, 128, 4) == 0
     # scores, tie keys and tie ids: 12 bytes per possible block of every sequence, at least
     assert binding.indexer_decode_workspace_size(8, 4096, 4, 512) >= 8 * 4096 * 32 * 12
