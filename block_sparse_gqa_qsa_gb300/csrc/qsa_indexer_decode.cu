@@ -24,7 +24,10 @@
 //       sum.  They write the scores and add them to a 4096-bin histogram of
 //       the score bits per sequence.  Pages are split evenly over the CTAs.
 //   decode_select_kernel  (B3) per sequence: the histogram gives the bin T that
-//       holds the budget-th largest score; one CTA per 2048-block slice writes
+//       holds the budget-th largest score.  A sequence of at most 8 slices of
+//       2048 blocks is handled by one CTA, which loads all its scores at once
+//       and compacts the candidates (blocks in bins >= T) in ascending id order
+//       straight into shared memory.  Longer ones: one CTA per slice writes
 //       the slice's candidates (blocks in bins >= T) in ascending id order
 //       into the slice's own region (no global atomics); the last CTA to
 //       finish finds the exact cut inside bin T with two radix digits of the
@@ -47,6 +50,7 @@ constexpr int kBinShift = 19;
 constexpr int kSliceBlocks = 2048;   // blocks one select CTA filters (8 per thread, one round of loads)
 constexpr int kMaxSlices = 1024;     // slices per sequence (blocks <= 2M): their bases live in shared memory
 constexpr int kStageCand = 4096;     // candidates the final CTA stages in shared memory (more: read from L2)
+constexpr int kSingleRounds = 8;     // sequences of up to 8 slices are selected by one CTA, in rounds
 constexpr int kConsumerWarps = 11;  // + 1 producer warp: 12 warps (3 per SM sub-partition), up to 168 registers
 constexpr int kScoreThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 22;
@@ -540,10 +544,14 @@ __device__ __forceinline__ void digit_from_top(const int* rh, int need, int* sca
   __syncthreads();
 }
 
+// kRounds: the most slices one CTA filters on its own (kSingleRounds when every
+// sequence of the launch has at most that many, so the grid has one CTA per
+// sequence; else 1, and longer sequences go through the slice CTAs).
+template <int kRounds>
 __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const SelectArgs a) {
   __shared__ int scan[kSelThreads / 32];
   __shared__ int info[8];
-  __shared__ int wcnt[kSelThreads / 32];
+  __shared__ int wcnt[kRounds * (kSelThreads / 32)];
   __shared__ int sbase[kMaxSlices + 1];
   __shared__ int rh[1024];
   __shared__ uint32_t ck_s[kStageCand];
@@ -567,61 +575,97 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
     }
     return;
   }
-  const int nsplit = (n_c + kSliceBlocks - 1) / kSliceBlocks;
+  const int nslice = (n_c + kSliceBlocks - 1) / kSliceBlocks;
+  // Up to kSingleRounds slices: CTA 0 filters them all (its loads for every
+  // round in flight at once) and keeps the candidates in shared memory, so
+  // they make no round trip through global memory and no CTA waits on another.
+  const bool single = nslice <= kRounds;
+  const int nsplit = single ? 1 : nslice;
   if (s >= nsplit) return;
+  const int nrounds = single ? nslice : 1;
+
+  // ---- candidates (bin >= T), compacted in ascending id order.  Round r
+  // covers blocks g0 + 2048 r + [0, 2048); in it warp w covers 256 w +
+  // [0, 256), visited as lane + 32 m.  The score loads are issued before the
+  // histogram is read, so the two latencies overlap.
+  const float* srow = a.scores + static_cast<size_t>(b) * a.nbmax;
+  const int g0 = s * kSliceBlocks;
+  constexpr int M = kSliceBlocks / kSelThreads;
+  uint32_t keys[kRounds][M];
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r)
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      const int g = g0 + r * kSliceBlocks + warp * 32 * M + m * 32 + lane;
+      keys[r][m] = r < nrounds && g < n_c ? __float_as_uint(__ldcg(srow + g)) : 0u;
+    }
 
   int T, c_above;
   threshold_bin(hrow, a.budget, scan, info, T, c_above);
 
-  // ---- candidates of this slice (bin >= T), compacted in ascending id order:
-  // warp w covers blocks g0 + 256 w + [0, 256), visited as lane + 32 m
-  const float* srow = a.scores + static_cast<size_t>(b) * a.nbmax;
-  const int g0 = s * kSliceBlocks, g1 = min(g0 + kSliceBlocks, n_c);
-  constexpr int M = kSliceBlocks / kSelThreads;
-  uint32_t keys[M];
-  unsigned cm[M];
-  int wc = 0;
+  // every round's ballots first, then one barrier for all the warp counts
+  unsigned cm[kRounds][M];
 #pragma unroll
-  for (int m = 0; m < M; ++m) {
-    const int g = g0 + warp * 32 * M + m * 32 + lane;
-    keys[m] = g < g1 ? __float_as_uint(__ldcg(srow + g)) : 0u;
-  }
+  for (int r = 0; r < kRounds; ++r) {
+    int wc = 0;
 #pragma unroll
-  for (int m = 0; m < M; ++m) {
-    const int g = g0 + warp * 32 * M + m * 32 + lane;
-    cm[m] = __ballot_sync(kFull, g < g1 && static_cast<int>(keys[m] >> kBinShift) >= T);
-    wc += __popc(cm[m]);
+    for (int m = 0; m < M; ++m) {
+      const int g = g0 + r * kSliceBlocks + warp * 32 * M + m * 32 + lane;
+      cm[r][m] = __ballot_sync(kFull, r < nrounds && g < n_c && static_cast<int>(keys[r][m] >> kBinShift) >= T);
+      wc += __popc(cm[r][m]);
+    }
+    if (lane == 0) wcnt[r * (kSelThreads / 32) + warp] = wc;
   }
-  if (lane == 0) wcnt[warp] = wc;
   __syncthreads();
-  int off = 0, tot = 0;
-#pragma unroll
-  for (int w = 0; w < kSelThreads / 32; ++w) {
-    off += w < warp ? wcnt[w] : 0;
-    tot += wcnt[w];
-  }
   uint32_t* ckey = a.candKey + static_cast<size_t>(b) * a.nbmax;
   int32_t* cid = a.candId + static_cast<size_t>(b) * a.nbmax;
   const unsigned below = (1u << lane) - 1u;
+  int run = 0;  // candidates of the earlier rounds
 #pragma unroll
-  for (int m = 0; m < M; ++m) {
-    if ((cm[m] >> lane) & 1u) {
-      const int at = g0 + off + __popc(cm[m] & below);
-      ckey[at] = keys[m];
-      cid[at] = g0 + warp * 32 * M + m * 32 + lane;
+  for (int r = 0; r < kRounds; ++r) {
+    int off = run, tot = 0;
+#pragma unroll
+    for (int w = 0; w < kSelThreads / 32; ++w) {
+      const int c = wcnt[r * (kSelThreads / 32) + w];
+      off += w < warp ? c : 0;
+      tot += c;
     }
-    off += __popc(cm[m]);
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      if ((cm[r][m] >> lane) & 1u) {
+        const int e = off + __popc(cm[r][m] & below);  // position among this CTA's candidates
+        const uint32_t k = keys[r][m];
+        const int g = g0 + r * kSliceBlocks + warp * 32 * M + m * 32 + lane;
+        ckey[g0 + e] = k;
+        cid[g0 + e] = g;
+        if (single && e < kStageCand) {
+          ck_s[e] = k;
+          ci_s[e] = g;
+        }
+      }
+      off += __popc(cm[r][m]);
+    }
+    run += tot;
   }
-  if (tid == 0) a.sliceCnt[static_cast<size_t>(b) * a.nsplitmax + s] = tot;
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) info[6] = atomicAdd(a.ticket + b, 1) == nsplit - 1;
-  __syncthreads();
-  if (!info[6]) return;
-  __threadfence();
+  if (single) {
+    // candidates past kStageCand are read back from global memory (.cg, at
+    // L2) by other threads of this CTA: make the stores visible there first
+    if (run > kStageCand) __threadfence();
+    if (tid == 0) {
+      sbase[0] = 0;
+      sbase[kMaxSlices] = run;
+    }
+    __syncthreads();
+  } else {
+    if (tid == 0) a.sliceCnt[static_cast<size_t>(b) * a.nsplitmax + s] = run;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) info[6] = atomicAdd(a.ticket + b, 1) == nsplit - 1;
+    __syncthreads();
+    if (!info[6]) return;
+    __threadfence();
 
-  // ---- last CTA of the sequence: the candidates of all slices, in id order
-  {
+    // ---- last CTA of the sequence: the candidates of all slices, in id order
     constexpr int PER = kMaxSlices / kSelThreads;
     int v[PER], own = 0;
 #pragma unroll
@@ -631,11 +675,11 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
       own += v[k];
     }
     int total;
-    int run = cta_exclusive_scan<kSelThreads>(own, scan, total);
+    int rs = cta_exclusive_scan<kSelThreads>(own, scan, total);
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
-      sbase[tid * PER + k] = run;
-      run += v[k];
+      sbase[tid * PER + k] = rs;
+      rs += v[k];
     }
     if (tid == 0) sbase[kMaxSlices] = total;
     __syncthreads();
@@ -653,11 +697,25 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
     return lo * kSliceBlocks + (e - sbase[lo]);
   };
   const bool staged = ncand <= kStageCand;
-  if (staged) {
-    for (int e = tid; e < ncand; e += kSelThreads) {
-      const int at = locate(e);
-      ck_s[e] = __ldcg(ckey + at);
-      ci_s[e] = __ldcg(cid + at);
+  if (staged && !single) {  // four candidates per thread per pass, their loads in flight together
+    for (int e0 = tid; e0 < ncand; e0 += 4 * kSelThreads) {
+      uint32_t kk[4];
+      int ii[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * kSelThreads;
+        const int at = e < ncand ? locate(e) : 0;
+        kk[u] = e < ncand ? __ldcg(ckey + at) : 0u;
+        ii[u] = e < ncand ? __ldcg(cid + at) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * kSelThreads;
+        if (e < ncand) {
+          ck_s[e] = kk[u];
+          ci_s[e] = ii[u];
+        }
+      }
     }
     __syncthreads();
   }
@@ -836,8 +894,10 @@ cudaError_t launch_indexer_decode(const QsaIndexerDecodeParams& p, const RopeFre
   se.nbmax = nbmax;
   se.nsplitmax = (nbmax + kSliceBlocks - 1) / kSliceBlocks;
   if (se.nsplitmax > kMaxSlices) return cudaErrorInvalidValue;
-  dim3 sgrid(se.nsplitmax, B);
-  decode_select_kernel<<<sgrid, kSelThreads, 0, st>>>(se);
+  if (se.nsplitmax <= kSingleRounds)
+    decode_select_kernel<kSingleRounds><<<dim3(1, B), kSelThreads, 0, st>>>(se);
+  else
+    decode_select_kernel<1><<<dim3(se.nsplitmax, B), kSelThreads, 0, st>>>(se);
   return cudaGetLastError();
 }
 
