@@ -142,6 +142,18 @@ def test_indexer_decode_edges():
     ind, _ = _gpu_indexer(d_dev, cfg1)
     ref, _ = _oracle_indexer(d_np, pool_np, cfg1)
     assert np.array_equal(to_np(ind)[:, 0], ref)
+    # ties over more than 8 slices of 2048 blocks (n_c = 17500 and 16501): one CTA per slice, and the
+    # last one reads the 17500 candidates back from the workspace
+    cfg2 = dataclasses.replace(cfg0, B=2, ctx_list=(70000, 66007), max_ctx=70016, seed=24)
+    d = syn.make_decode(cfg2)
+    pool = d["pool"]
+    pool[:, :, 0, cfg2.D:] = pool[0, 0, 0, cfg2.D:]
+    d_np = _np(d)
+    pool_np = d_np["pool"].copy()
+    d_dev = _to_dev(d)
+    ind, _ = _gpu_indexer(d_dev, cfg2)
+    ref, _ = _oracle_indexer(d_np, pool_np, cfg2)
+    assert np.array_equal(to_np(ind)[:, 0], ref)
 
 
 def _state(pool, pt, b, L, cfg):
