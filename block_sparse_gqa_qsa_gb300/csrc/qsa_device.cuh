@@ -1,7 +1,6 @@
 // qsa_device.cuh -- device helpers shared by the QSA kernels (sm_103a):
 // inline-PTX wrappers (cp.async, ldmatrix, mma.sync, movmatrix, mbarrier, TMA),
-// CTA-wide reductions and scans, RoPE angles, and the deterministic top-k
-// selection used by both indexers.
+// CTA-wide scans and the RoPE angle from a fixed-point turn fraction.
 #pragma once
 
 #include <cuda.h>
