@@ -231,18 +231,7 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_
     for (int e = tid; e < a.G * kD / 8; e += kThreads) reinterpret_cast<uint4*>(out)[e] = make_uint4(0, 0, 0, 0);
     return;
   }
-  // Stage the list; entries outside [0, L) are skipped.
-  const int32_t* lst = a.indices + static_cast<size_t>(bt) * a.topK;
-  int last = -1;
-  for (int i = tid; i < a.topKpad; i += kThreads) {
-    const int j = i < a.topK ? __ldg(lst + i) : -1;
-    const bool ok = static_cast<unsigned>(j) < static_cast<unsigned>(L);
-    idx_s[i] = ok ? j : -1;
-    last = ok ? i : last;
-  }
-  last = __reduce_max_sync(kFull, last);
-  if (lane == 0) misc[warp] = last;
-  // Q rows of the group (rows >= G zero).
+  // Q rows of the group (rows >= G zero), copied while the list is staged.
   const __half* qsrc = a.q + (static_cast<size_t>(bt) * a.Hq + static_cast<size_t>(kvh) * a.G) * kD;
   for (int e = tid; e < NT * 8 * 16; e += kThreads) {
     const int r = e >> 4, c = e & 15;
@@ -250,25 +239,53 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_
     cp_async16(q_tile + swz(r, c), qsrc + (ok ? r : 0) * kD + c * 8, ok);
   }
   cp_async_commit();
+  // Stage the list, four loads per thread in flight; entries outside [0, L) are skipped.
+  const int32_t* lst = a.indices + static_cast<size_t>(bt) * a.topK;
+  int last = -1;
+  for (int i0 = tid; i0 < a.topKpad; i0 += 4 * kThreads) {
+    int jv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * kThreads;
+      jv[u] = i < a.topK ? __ldg(lst + i) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * kThreads;
+      if (i < a.topKpad) {
+        const bool ok = static_cast<unsigned>(jv[u]) < static_cast<unsigned>(L);
+        idx_s[i] = ok ? jv[u] : -1;
+        last = ok ? i : last;
+      }
+    }
+  }
+  last = __reduce_max_sync(kFull, last);
+  if (lane == 0) misc[warp] = last;
   __syncthreads();
   const int nslots = max(max(misc[0], misc[1]), max(misc[2], misc[3])) + 1;
   const int ntiles = (nslots + kKeys - 1) / kKeys;
 
-  const size_t kv_b = static_cast<size_t>(b) * a.S;
   // 16 consecutive lanes copy one 256-byte row, so every warp instruction reads
-  // whole 128-byte lines (two rows of K, then the same two rows of V).
+  // whole 128-byte lines (two rows of K, then the same two rows of V).  A
+  // thread's chunk, its sequence, head and swizzled slot are fixed, so a key
+  // costs one offset multiply-add from the per-thread bases.
+  const int ch = tid & 15;
+  const size_t head_off = (static_cast<size_t>(b) * a.S * a.Hkv + kvh) * kD + ch * 8;
+  const __half* kbase = a.k + head_off;
+  const __half* vbase = a.v + head_off;
+  const int tok_stride = a.Hkv * kD;                   // elements between consecutive tokens
+  const uint32_t slot0 = swz(tid >> 4, ch);           // key r*8 + tid/16 sits at slot0 + r * 2048
   auto issue = [&](int tile, int stage) {
-    const uint32_t kdst = ring + stage * 2 * kTileBytes;
+    const uint32_t kdst = ring + stage * 2 * kTileBytes + slot0;
     const uint32_t vdst = kdst + kTileBytes;
-    const int ch = tid & 15;
+    const int* ids = idx_s + tile * kKeys + (tid >> 4);
 #pragma unroll
     for (int r = 0; r < kKeys / 8; ++r) {
-      const int key = r * 8 + (tid >> 4);
-      const int j = idx_s[tile * kKeys + key];
+      const int j = ids[r * 8];
       const bool ok = j >= 0;
-      const size_t row = ((kv_b + (ok ? j : 0)) * a.Hkv + kvh) * kD;
-      cp_async16(kdst + swz(key, ch), a.k + row + ch * 8, ok);
-      cp_async16(vdst + swz(key, ch), a.v + row + ch * 8, ok);
+      const size_t off = static_cast<size_t>(ok ? j : 0) * tok_stride;
+      cp_async16(kdst + r * 8 * 256, kbase + off, ok);
+      cp_async16(vdst + r * 8 * 256, vbase + off, ok);
     }
   };
   uint32_t qf[NT][8][2];
@@ -368,23 +385,35 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_k
   const int32_t* lst = a.indices + static_cast<size_t>(b) * a.topK;
   const int32_t* ptK = a.pageTable + static_cast<size_t>(b) * 2 * a.maxPagesPerSeq;
   const int32_t* ptV = ptK + a.maxPagesPerSeq;
+  // Resolve the slice's entries to pool offsets, four per thread per pass with
+  // their list loads, then their page-table loads, in flight together.
   int last = -1;
-  for (int i = tid; i < a.slicePad; i += kThreads) {
-    const int slot = s0 + i;
-    const int j = slot < s1 ? __ldg(lst + slot) : -1;
-    bool ok = static_cast<unsigned>(j) < static_cast<unsigned>(L);
-    long long ko = -1, vo = -1;
-    if (ok) {
-      const int kp = __ldg(ptK + (j >> 7)), vp = __ldg(ptV + (j >> 7));
-      ok = static_cast<unsigned>(kp) < static_cast<unsigned>(a.numFlatPages) &&
-           static_cast<unsigned>(vp) < static_cast<unsigned>(a.numFlatPages);
-      const long long within = static_cast<long long>((j & 127) * a.Hkv + kvh) * a.poolHeadDim;
-      ko = static_cast<long long>(kp) * kTokensPerPage * a.Hkv * a.poolHeadDim + within;
-      vo = static_cast<long long>(vp) * kTokensPerPage * a.Hkv * a.poolHeadDim + within;
+  for (int i0 = tid; i0 < a.slicePad; i0 += 4 * kThreads) {
+    int jv[4], kp[4], vp[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int slot = s0 + i0 + u * kThreads;
+      jv[u] = i0 + u * kThreads < a.slicePad && slot < s1 ? __ldg(lst + slot) : -1;
     }
-    kofs[i] = ok ? ko : -1;
-    vofs[i] = ok ? vo : -1;
-    last = ok ? i : last;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool live = static_cast<unsigned>(jv[u]) < static_cast<unsigned>(L);
+      kp[u] = live ? __ldg(ptK + (jv[u] >> 7)) : -1;
+      vp[u] = live ? __ldg(ptV + (jv[u] >> 7)) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * kThreads;
+      if (i >= a.slicePad) continue;
+      const int j = jv[u];
+      const bool ok = static_cast<unsigned>(j) < static_cast<unsigned>(L) &&
+                      static_cast<unsigned>(kp[u]) < static_cast<unsigned>(a.numFlatPages) &&
+                      static_cast<unsigned>(vp[u]) < static_cast<unsigned>(a.numFlatPages);
+      const long long within = static_cast<long long>((j & 127) * a.Hkv + kvh) * a.poolHeadDim;
+      kofs[i] = ok ? static_cast<long long>(kp[u]) * kTokensPerPage * a.Hkv * a.poolHeadDim + within : -1;
+      vofs[i] = ok ? static_cast<long long>(vp[u]) * kTokensPerPage * a.Hkv * a.poolHeadDim + within : -1;
+      last = ok ? i : last;
+    }
   }
   last = __reduce_max_sync(kFull, last);
   if (lane == 0) misc[warp] = last;
