@@ -54,7 +54,7 @@ def f32(x):
 # capture summarised in profiles/prefill_kernels__prefill_S8192.md.  Reported only while the
 # kernel's sources hash to the value they had when the counters were taken.
 PROFILED_TRAFFIC = {"bytes": 200_749_824, "sources": ("qsa_attention.cu", "qsa_device.cuh"),
-                    "sha256": "19b05d7947ed667b5f50bf27c5c7322753bb08a5477e7baa4d33602e7778cd2b"}
+                    "sha256": "02d938f12fbb14d346d4dfa755415d0cf8fc019093d5d46ce7e783beca2ed9b9"}
 
 
 def profiled_traffic():

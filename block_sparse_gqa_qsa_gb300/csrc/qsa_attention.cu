@@ -489,22 +489,21 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_k
   const size_t part = (static_cast<size_t>(b) * a.Hkv + kvh) * kMaxSplits + split;
   float* pO = a.partialO + part * kPartialRows * kD;
   float* pS = a.partialStats + part * 2 * kPartialRows;
-  for (int e = tid; e < kPartialRows * (kD / 2); e += kThreads) {
+  // Only the group's G rows are written; the combine reads no others.
+  for (int e = tid; e < a.G * (kD / 2); e += kThreads) {
     const int h = e / (kD / 2), d = 2 * (e % (kD / 2));
-    float f[4] = {0.f, 0.f, 0.f, 0.f}, Lsum = 0.f, M = -INFINITY;
-    if (h < a.G) M = merge_weights(mw, lw, h, f, Lsum);
+    float f[4], Lsum;
+    const float M = merge_weights(mw, lw, h, f, Lsum);
     float o0 = 0.f, o1 = 0.f;
-    if (h < a.G) {
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        o0 += f[w] * ow[(w * 16 + h) * kOStride + d];
-        o1 += f[w] * ow[(w * 16 + h) * kOStride + d + 1];
-      }
+    for (int w = 0; w < 4; ++w) {
+      o0 += f[w] * ow[(w * 16 + h) * kOStride + d];
+      o1 += f[w] * ow[(w * 16 + h) * kOStride + d + 1];
     }
     reinterpret_cast<float2*>(pO + h * kD)[d / 2] = make_float2(o0, o1);
     if (d == 0) {
-      pS[h] = h < a.G ? M : -INFINITY;
-      pS[kPartialRows + h] = h < a.G ? Lsum : 0.f;
+      pS[h] = M;
+      pS[kPartialRows + h] = Lsum;
     }
   }
   // Last split to arrive merges the kMaxSplits partials and re-arms the counter.

@@ -377,12 +377,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
   };
   const int b_first = seq_of(lo);
   const int nslot = min(kQSlots, seq_of(hi - 1) - b_first + 1);
-  for (int e = tid; e < nslot * QS; e += blockDim.x) {  // float4 units: 4*QS floats per sequence
-    const int bi = e / QS, w4 = e % QS;
-    reinterpret_cast<float4*>(qcache)[e] =
-        __ldcg(reinterpret_cast<const float4*>(a.q + static_cast<size_t>(b_first + bi) * kQPerSeq) + w4);
+  if (warp < kConsumerWarps) {  // the consumers fill the query cache; the producer starts streaming meanwhile
+    for (int e = tid; e < nslot * QS; e += kConsumerWarps * 32) {  // float4 units: 4*QS floats per sequence
+      const int bi = e / QS, w4 = e % QS;
+      reinterpret_cast<float4*>(qcache)[e] =
+          __ldcg(reinterpret_cast<const float4*>(a.q + static_cast<size_t>(b_first + bi) * kQPerSeq) + w4);
+    }
+    asm volatile("bar.sync 1, %0;\n" ::"n"(kConsumerWarps * 32) : "memory");
   }
-  __syncthreads();
 
   if (warp == kConsumerWarps) {  // ---- producer: page ids 32 at a time, one TMA per 64-dim half
     int bw = 0;  // sequence of the batch's first page
