@@ -126,10 +126,11 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const PrepArg
   __shared__ unsigned long long turn_s[64];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x;
+  const int ctx_b = a.ctx[b];  // issued first: its latency overlaps the table copy
   stage_rope(a.rf, rs);
   if (tid < 64) turn_s[tid] = a.rf.turn[tid];
   __syncthreads();
-  const int L = max(0, min(a.ctx[b], a.maxPagesPerSeq * kTokensPerPage));
+  const int L = max(0, min(ctx_b, a.maxPagesPerSeq * kTokensPerPage));
   if (L == 0) return;
   const int t = L - 1;
   const int n_c = L / a.ratio;

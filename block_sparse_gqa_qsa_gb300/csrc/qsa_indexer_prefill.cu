@@ -264,6 +264,8 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_score_kernel(const SelArg
 // Bisection on the key finds T with count(key >= T) >= budget >
 // count(key > T); the blocks above T are kept, and of those equal to T the
 // lowest ids, so the kept set is the top `budget` by (score desc, id asc).
+// A probe with exactly `budget` keys at or above it ends the search early:
+// those keys are the set (T = probe - 1 and no key equal to T is kept).
 // Walking m upwards visits ids in ascending order, so ballots compact the
 // kept blocks straight into the ascending list.  Rows t >= L are all -1 and
 // rows with n_c <= budget list 0..t.
@@ -316,14 +318,19 @@ __global__ void __launch_bounds__(kThreads) prefill_topk_kernel(const SelArgs a)
       }
     }
     const int c = static_cast<int>(__reduce_add_sync(kFull, static_cast<unsigned>(nslot + below_mid)));
-    if (c >= a.budget) {
+    if (c == a.budget) {  // exactly the budget at or above mid: keep those, no tie to break
+      lo = mid - 1u;
+      c_hi = a.budget;
+      break;
+    }
+    if (c > a.budget) {
       lo = mid;
     } else {
       hi = mid;
       c_hi = c;
     }
   }
-  int quota = a.budget - c_hi;  // blocks with key == lo to keep, lowest ids first
+  int quota = a.budget - c_hi;  // blocks with key == lo to keep, lowest ids first (none after an exact stop)
   int pos = 0;
   const unsigned below = (1u << lane) - 1u;
 #pragma unroll
