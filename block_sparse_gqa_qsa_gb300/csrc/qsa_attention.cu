@@ -220,11 +220,15 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_
   int* misc = idx_s + a.topKpad;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Within a sequence the CTAs run the rows from the last position down: the
+  // longest lists start first and the sequence ends on short ones.  Sequences
+  // follow one another, so one sequence's K/V is the L2 working set.
   const long long bid = blockIdx.x;
   const int kvh = static_cast<int>(bid % a.Hkv);
-  const long long bt = bid / a.Hkv;
-  const int t = static_cast<int>(bt % a.S);
-  const int b = static_cast<int>(bt / a.S);
+  const long long rowid = bid / a.Hkv;
+  const int b = static_cast<int>(rowid / a.S);
+  const int t = a.S - 1 - static_cast<int>(rowid % a.S);
+  const long long bt = static_cast<long long>(b) * a.S + t;
   const int L = max(0, min(a.ctx[b], a.S));
   __half* out = a.o + (static_cast<size_t>(bt) * a.Hq + static_cast<size_t>(kvh) * a.G) * kD;
   if (t >= L) {  // rows at or past the live length are exact zeros
