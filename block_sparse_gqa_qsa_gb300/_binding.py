@@ -144,6 +144,8 @@ def lib() -> ctypes.CDLL:
             L.qsa_status_string.restype = ctypes.c_char_p
             L.qsa_last_error_message.argtypes = []
             L.qsa_last_error_message.restype = ctypes.c_char_p
+            L.qsa_last_device_error.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(_i32)]
+            L.qsa_last_device_error.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -184,6 +186,18 @@ def sparse_decode_workspace_elems(B: int, Hkv: int, D: int) -> tuple[int, int, i
     L = lib()
     return (L.qsa_sparse_decode_partial_o_elems(B, Hkv, D), L.qsa_sparse_decode_partial_stats_elems(B, Hkv),
             L.qsa_sparse_decode_counter_elems(B, Hkv))
+
+
+def last_device_error(workspace: torch.Tensor, stream=None) -> int:
+    """The status word of an indexer workspace (device-side error bits); waits for `stream`."""
+    out = _i32(0)
+    _check(lib().qsa_last_device_error(_ptr(workspace, name="workspace"), _stream(stream), ctypes.byref(out)))
+    st = stream if stream is not None else torch.cuda.current_stream()
+    if hasattr(st, "synchronize"):
+        st.synchronize()
+    else:
+        torch.cuda.synchronize()
+    return int(out.value)
 
 
 def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:

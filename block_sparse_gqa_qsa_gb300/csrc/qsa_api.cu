@@ -165,6 +165,13 @@ const char* qsa_status_string(qsa_status_t s) {
 
 const char* qsa_last_error_message(void) { return g_last_error.c_str(); }
 
+qsa_status_t qsa_last_device_error(const void* workspace, void* stream, int32_t* out) {
+  if (!workspace || !out) return fail(QSA_ERR_INVALID_ARG, "qsa_last_device_error: workspace or out is NULL");
+  const cudaError_t e = cudaMemcpyAsync(out, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost,
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e, "qsa_last_device_error");
+}
+
 int32_t qsa_indexer_prefill_max_blocks(void) { return qsa::kPrefillMaxBlocks; }
 
 size_t qsa_indexer_prefill_workspace_size(int32_t B, int32_t S, int32_t di, int32_t ratio) {

@@ -396,6 +396,17 @@ QSA_API int32_t qsa_sparse_decode_can_implement(int32_t numQHeads, int32_t numKV
  * seqLen up to 16384 at ratio 4); larger shapes return QSA_ERR_UNSUPPORTED. */
 QSA_API int32_t qsa_indexer_prefill_max_blocks(void);
 
+/* Debug read of the status word at the head of an indexer workspace (the
+ * device-side error bits: bit 0 a TMA wait that ran out, bit 1 a page id
+ * outside the pool; see qsa_indexer_decode).  Enqueues a 4-byte copy of that
+ * word into host memory *out on `stream` (a cudaStream_t) and returns without
+ * waiting: *out is valid once the stream has reached the copy (for pageable
+ * host memory CUDA completes the copy before the call returns).  The bits
+ * accumulate; zero-fill the workspace to clear them.  Errors:
+ * QSA_ERR_INVALID_ARG for a NULL pointer, QSA_ERR_CUDA if the copy cannot be
+ * enqueued.  Nothing else is read or written. */
+QSA_API qsa_status_t qsa_last_device_error(const void* workspace, void* stream, int32_t* out);
+
 /* Human-readable name of a status, and the detail of the last failure on the
  * calling thread (never NULL; empty when there was none). */
 QSA_API const char* qsa_status_string(qsa_status_t status);

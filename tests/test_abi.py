@@ -89,6 +89,9 @@ def test_constants_and_sizes(binding):
     assert L.qsa_gather_scratch_elems(0, 4, 128, 2051) == 0
     assert L.qsa_sparse_decode_can_implement(64, 8, 128, 100) == 0
     assert L.qsa_status_string(2) == b"QSA_ERR_UNSUPPORTED"
+    out = ctypes.c_int32(0)
+    assert L.qsa_last_device_error(None, None, ctypes.byref(out)) == binding.QSA_ERR_INVALID_ARG
+    assert L.qsa_last_device_error(ctypes.c_void_p(1 << 20), None, None) == binding.QSA_ERR_INVALID_ARG
 
 
 def _call(binding, fn, params):

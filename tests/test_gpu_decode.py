@@ -96,6 +96,7 @@ def test_indexer_decode_parity_and_state_update(cfg):
     assert np.array_equal(to_np(d_dev["pool"]).view(np.uint16), pool_np.view(np.uint16))
     assert not np.array_equal(pool_np.view(np.uint16), d_np["pool"].view(np.uint16))
     assert int(to_np(ws[:4]).view(np.int32)[0]) == 0, "workspace status word"
+    assert qb.last_device_error(ws) == 0, "status word through qsa_last_device_error"
     # a second call on the updated state gives the same lists and leaves the pool unchanged
     ind2, _ = _gpu_indexer(d_dev, cfg, ws)
     assert torch.equal(ind2, ind)
@@ -154,6 +155,19 @@ def test_indexer_decode_edges():
     ind, _ = _gpu_indexer(d_dev, cfg2)
     ref, _ = _oracle_indexer(d_np, pool_np, cfg2)
     assert np.array_equal(to_np(ind)[:, 0], ref)
+
+
+def test_indexer_decode_bad_page_sets_status_bit():
+    """A V page id outside the pool: the scorer's range check skips it and sets bit 1 of the status word,
+    read back through qsa_last_device_error; the call itself still returns QSA_OK."""
+    cfg = syn.DECODE_PARITY
+    d = syn.make_decode(cfg)
+    num_pages = d["pool"].shape[0]
+    d["page_table"][5, 1, 0] = num_pages + 7  # sequence 5 (L = 6000): its first page holds block keys
+    d_dev = _to_dev(d)
+    _, ws = _gpu_indexer(d_dev, cfg)
+    assert qb.last_device_error(ws) & 2, "bit 1 (page id outside the pool) must be set"
+    assert not qb.last_device_error(ws) & 1, "no wait may time out"
 
 
 def _state(pool, pt, b, L, cfg):
