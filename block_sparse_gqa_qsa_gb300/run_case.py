@@ -12,7 +12,10 @@ of tens).
     python -m block_sparse_gqa_qsa_gb300.run_case prefill_S8192 --op rope --steps 2
 
 `--op rope` runs qsa_rope_qkv on the workload's packed QKV instead (prefill
-workloads: dense q/k/v outputs).
+workloads: dense q/k/v outputs).  `--op handoff` (prefill workloads) runs the
+indexer once, then qsa_indexer_prefill_handoff into a paged pool per step.
+`--op gather` (decode workloads) runs one decode step for its lists, then
+qsa_gather_selected into contiguous scratch per step.
 """
 from __future__ import annotations
 
@@ -50,6 +53,28 @@ def _rope_steps(cfg, steps):
                     k_out=ko, v_out=vo)
 
 
+def _handoff_steps(cfg, steps):
+    t = {k: v.cuda() for k, v in syn.make_prefill(cfg).items()}
+    ws = qb.alloc_workspace(qb.indexer_prefill_workspace_size(cfg.B, cfg.S, cfg.di, cfg.ratio))
+    ind = torch.empty((cfg.B, cfg.S, cfg.topK), dtype=torch.int32, device="cuda")
+    qb.indexer_prefill(t["idxQ"], t["idxK"], t["wq"], t["wk"], t["ctx"], ind, ws, rot=cfg.rot, ratio=cfg.ratio,
+                       budget=cfg.budget, topK=cfg.topK, theta=cfg.theta, eps=cfg.eps)
+    npg = -(-(cfg.S + 1) // syn.TOKENS_PER_PAGE)  # pages for S tokens and the next one, per sequence
+    pool = torch.zeros((2 * cfg.B * npg, syn.TOKENS_PER_PAGE, cfg.Hkv, cfg.D + cfg.di), dtype=torch.float16,
+                       device="cuda")
+    ids = torch.arange(cfg.B * npg, dtype=torch.int32, device="cuda").view(cfg.B, npg)
+    pt = torch.stack([ids, ids + cfg.B * npg], dim=1).contiguous()
+    for _ in range(steps):
+        qb.indexer_prefill_handoff(t["idxK"], t["ctx"], ws, pool, pt, D=cfg.D, ratio=cfg.ratio)
+
+
+def _gather_steps(cfg, steps):
+    d, ind = _decode_steps(cfg, 1)
+    sc = qb.gather_scratch(cfg.B, cfg.Hkv, cfg.D, cfg.topK, device="cuda")
+    for _ in range(steps):
+        qb.gather_selected(d["pool"], d["page_table"], ind, d["ctx"], *sc, D=cfg.D)
+
+
 def _decode_steps(cfg, steps):
     d = syn.make_decode(cfg, device="cuda")
     d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
@@ -65,6 +90,7 @@ def _decode_steps(cfg, steps):
                           D=cfg.D, rot=cfg.rot, ratio=cfg.ratio, budget=cfg.budget, topK=cfg.topK, theta=cfg.theta,
                           eps=cfg.eps)
         qb.sparse_decode(d["q"], d["pool"], d["page_table"], ind, d["ctx"], out, *parts, D=cfg.D, scale=scale)
+    return d, ind
 
 
 def main(argv=None):
@@ -74,16 +100,22 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2)
     ap.add_argument("--B", type=int, default=None, help="override the batch size")
     ap.add_argument("--ctx", type=int, default=None, help="decode: every sequence gets this total length")
-    ap.add_argument("--op", choices=("path", "rope"), default="path", help="rope: qsa_rope_qkv of a prefill workload")
+    ap.add_argument("--op", choices=("path", "rope", "handoff", "gather"), default="path",
+                    help="rope / handoff: qsa_rope_qkv / qsa_indexer_prefill_handoff of a prefill workload; "
+                         "gather: qsa_gather_selected of a decode workload")
     args = ap.parse_args(argv)
     cfg = names[args.workload]
     if args.B is not None:
         cfg = dataclasses.replace(cfg, B=args.B)
     qb.lib()
-    if args.op == "rope":
+    if args.op in ("rope", "handoff"):
         if isinstance(cfg, syn.DecodeConfig):
-            ap.error("--op rope takes a prefill workload")
-        _rope_steps(cfg, args.steps)
+            ap.error(f"--op {args.op} takes a prefill workload")
+        (_rope_steps if args.op == "rope" else _handoff_steps)(cfg, args.steps)
+    elif args.op == "gather":
+        if not isinstance(cfg, syn.DecodeConfig):
+            ap.error("--op gather takes a decode workload")
+        _gather_steps(cfg, args.steps)
     elif isinstance(cfg, syn.DecodeConfig):
         if args.ctx is not None:
             cfg = dataclasses.replace(cfg, ctx_lo=args.ctx, ctx_hi=args.ctx, max_ctx=max(args.ctx, 1), ctx_list=None)
