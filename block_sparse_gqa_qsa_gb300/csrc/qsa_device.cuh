@@ -1,7 +1,6 @@
 // qsa_device.cuh -- device helpers shared by the QSA kernels (sm_103a):
 // inline-PTX wrappers (cp.async, ldmatrix, mma.sync, movmatrix, mbarrier, TMA),
-// the hi/lo query split and relu head sum of the index scores, CTA-wide scans
-// and the RoPE angle from a fixed-point turn fraction.
+// CTA-wide scans and the RoPE angle from a fixed-point turn fraction.
 #pragma once
 
 #include <cuda.h>
@@ -141,49 +140,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       "[%5];\n" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
       : "memory");
-}
-
-// ------------------------------------------------- index scores on tensor cores
-// The index query is carried into the fp16 tensor-core contraction as a pair
-// hi + lo of fp16 values (hi = RN(x), lo = RN(x - hi)): about 22 significant
-// bits of the fp32 query, against exact fp16 block keys, with the products
-// summed in fp32.  Before the split the query is multiplied by a power of two
-// that puts its largest magnitude in [2^13, 2^14): every element stays inside
-// the fp16 range, and the pair is off by at most 2^-22 of the element or
-// 2^-38 of the largest one (a lo part in the fp16 subnormals); the scores are
-// then scaled by the same power of two, which changes no order.
-__device__ __forceinline__ float index_q_scale(float max_abs) {
-  if (!(max_abs > 0.f)) return 1.f;
-  const int e = static_cast<int>((__float_as_uint(max_abs) >> 23) & 0xffu) - 127;
-  const int k = max(-100, min(100, 13 - e));
-  return __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
-}
-// Splits two fp32 values into fp16x2 hi and lo words (element 0 in the low half).
-__device__ __forceinline__ void split_half2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const __half2 h = __floats2half2_rn(x0, x1);
-  const float2 hf = __half22float2(h);
-  const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
-}
-// Relu and head sum of one m16n8 accumulator tile (16 blocks x 8 heads, the
-// hi and lo products in separate accumulators).  Returns, on lane 4i, the
-// score of block i of the tile and, on lane 4i + 1, that of block i + 8 (the
-// other lanes get copies).  Every block's sum runs through the same additions,
-// wherever it sits in the tile.
-__device__ __forceinline__ float relu_head_sum(const float (&hi)[4], const float (&lo)[4]) {
-  float d[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float v = hi[j] + lo[j];
-    d[j] = v > 0.f ? v : 0.f;
-  }
-  float s0 = d[0] + d[1], s1 = d[2] + d[3];
-  s0 += __shfl_xor_sync(kFull, s0, 1);
-  s1 += __shfl_xor_sync(kFull, s1, 1);
-  s0 += __shfl_xor_sync(kFull, s0, 2);
-  s1 += __shfl_xor_sync(kFull, s1, 2);
-  return (threadIdx.x & 1) ? s1 : s0;
 }
 
 // -------------------------------------------------------- CTA reductions

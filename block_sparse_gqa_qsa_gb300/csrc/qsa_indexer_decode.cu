@@ -5,8 +5,7 @@
 //
 // Three launches on the caller's stream:
 //   decode_prep_kernel    (B1) one CTA per sequence: index-query prep at
-//       t = L-1 (fp32, angles reduced in integer turns; scaled by a power of
-//       two and split into fp16 hi/lo mma fragments) into the workspace by
+//       t = L-1 (fp32, angles reduced in integer turns) into the workspace by
 //       8 warps, and concurrently, by di/32 more warps, the state update: the new
 //       raw key into token t's K-row tail when t leaves its block incomplete,
 //       else the block t completes is pooled (from the K-row tails of its
@@ -17,14 +16,13 @@
 //       a producer warp streams the key tails of every page that holds
 //       complete blocks (3-D TMA copies, box {64, 128/r, 1} with the 128-byte
 //       swizzle over a strided view of the pool, page ids fetched 32 at a time)
-//       into a 22-stage ring; 11 consumer warps score one page each on the
-//       tensor cores: the page's keys are the A operands (ldmatrix from the
-//       swizzled stage, m = block, k = dim), the sequence's query fragments
-//       (hi and lo, kept in registers) the B operands (n = head), mma.sync
-//       m16n8k16 with fp32 accumulators, then relu per head and the head sum
-//       on the accumulators.  They write the scores and add them to a
-//       4096-bin histogram of the score bits per sequence.  Pages are split
-//       evenly over the CTAs.
+//       into a 22-stage ring; 11 consumer warps score one page each: four
+//       lanes per key (a quarter of the dims each), four keys per lane, the
+//       queries read by broadcast from the CTA's shared-memory copy (written
+//       by B1 in that layout), dims paired in fp32x2 FMAs; two transposing
+//       shuffle exchanges join the quarters, then relu per head and the head
+//       sum.  They write the scores and add them to a 4096-bin histogram of
+//       the score bits per sequence.  Pages are split evenly over the CTAs.
 //   decode_select_kernel  (B3) per sequence: the histogram gives the bin T that
 //       holds the budget-th largest score.  A sequence of at most 8 slices of
 //       2048 blocks is handled by one CTA, which loads all its scores at once
@@ -57,11 +55,11 @@ constexpr int kConsumerWarps = 11;  // + 1 producer warp: 12 warps (3 per SM sub
 constexpr int kScoreThreads = (kConsumerWarps + 1) * 32;
 constexpr int kStages = 22;
 constexpr int kQSlots = 8;            // sequences whose queries a scorer CTA keeps in shared memory
-// Queries as the scorer reads them: per sequence and lane l of a warp, for each
-// k-step of 16 dims, the mma.sync B fragments of the scaled query split into
-// fp16 hi and lo (hi b0, hi b1, lo b0, lo b1: head l/4, dims 2(l%4) + {0, 1}
-// and + {8, 9} of the k-step); 8 k-steps of 4 words per lane.
-constexpr int kQPerSeq = 32 * 8 * 4;  // 32-bit words per sequence in the workspace
+// Queries as the scorer reads them: per sequence 4 quarters of the dims, each
+// [chunk][head slot][8 dims] plus 4 floats of padding (the quarters then start
+// in different banks); in quarter t, slot p holds head p ^ (4*(t>>1) + 2*(t&1)).
+constexpr int kQS128 = (128 / 32) * 64 + 4;
+constexpr int kQPerSeq = 4 * kQS128;  // floats per sequence in the workspace (the 128-dim layout)
 constexpr int kSelThreads = 256;
 constexpr int kPrepThreads = 256 + 128;  // 8 query-prep warps + up to 4 state-update warps
 constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;  // 0.2 s
@@ -77,7 +75,7 @@ WsLayout ws_layout(int B, int nbmax) {
   WsLayout l;
   size_t off = kStatusBytes;
   l.q = off;
-  off += up256(static_cast<size_t>(B) * kQPerSeq * 4);  // prepared queries, fragment layout [B][kQPerSeq]
+  off += up256(static_cast<size_t>(B) * kQPerSeq * 4);  // prepared queries fp32, scorer layout [B][kQPerSeq]
   l.scores = off;
   off += up256(static_cast<size_t>(B) * nbmax * 4);     // block scores fp32 [B][nbmax]
   l.hist = off;
@@ -111,7 +109,7 @@ struct PrepArgs {
   __half* pool;
   const int32_t* pageTable;
   const int32_t* ctx;
-  uint32_t* q;
+  float* q;
   int32_t* status;
   int Hi, Hkv, D, poolHeadDim, numFlatPages, maxPagesPerSeq, rot, ratio;
   float eps;
@@ -122,8 +120,6 @@ template <int DI>
 __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const PrepArgs a) {
   constexpr int PER = DI / 32;
   __shared__ float y_s[8][DI];
-  __shared__ float qv_s[8][DI + 8];  // rotated queries
-  __shared__ float hmax_s[8];
   __shared__ f2x key_s[DI];
   __shared__ f2x part_s[DI / 32];
   __shared__ RopeSmem rs;
@@ -146,6 +142,12 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const PrepArg
   // warps 8..: the state update, concurrently (named barrier 1 among them)
   if (warp < 8) {
     const int h = warp;
+    float* qo = a.q + static_cast<size_t>(b) * kQPerSeq;
+    constexpr int QS = (DI / 32) * 64 + 4;
+    auto qpos = [&](int i) {  // scorer layout position of (head h, dim i)
+      const int qt = i / (DI / 4), c = (i % (DI / 4)) / 8;
+      return qt * QS + c * 64 + (h ^ (4 * (qt >> 1) + 2 * (qt & 1))) * 8 + (i % 8);
+    };
     if (h < a.Hi) {
       const __half* x = a.idxQ + (static_cast<size_t>(b) * a.Hi + h) * DI;
       float y[PER];
@@ -166,7 +168,6 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const PrepArg
       }
       __syncwarp();
       const int half = a.rot >> 1;
-      float mx = 0.f;
 #pragma unroll
       for (int p = 0; p < PER; ++p) {
         const int i = lane + 32 * p;
@@ -181,30 +182,11 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const PrepArg
           rope_cos_sin_turns(static_cast<unsigned>(t), turn_s[k], cs, sn);
           v = y[p] * cs + y_s[h][k] * sn;
         }
-        qv_s[h][i] = v;
-        mx = fmaxf(mx, fabsf(v));
+        qo[qpos(i)] = v;
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-      if (lane == 0) hmax_s[h] = mx;
     } else {
 #pragma unroll
-      for (int p = 0; p < PER; ++p) qv_s[h][lane + 32 * p] = 0.f;
-      if (lane == 0) hmax_s[h] = 0.f;
-    }
-    asm volatile("bar.sync 2, 256;\n" ::: "memory");
-    // warp ks writes k-step ks of every lane's fragments (the scorer's layout)
-    float m = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) m = fmaxf(m, hmax_s[j]);
-    const float scale = index_q_scale(m);
-    const int ks = warp;
-    if (ks < DI / 16) {
-      const float* qn = &qv_s[lane >> 2][ks * 16 + (lane & 3) * 2];
-      uint4 w;
-      split_half2(qn[0] * scale, qn[1] * scale, w.x, w.z);
-      split_half2(qn[8] * scale, qn[9] * scale, w.y, w.w);
-      reinterpret_cast<uint4*>(a.q + static_cast<size_t>(b) * kQPerSeq)[lane * 8 + ks] = w;
+      for (int p = 0; p < PER; ++p) qo[qpos(lane + 32 * p)] = 0.f;
     }
     return;
   }
@@ -239,7 +221,7 @@ __global__ void __launch_bounds__(kPrepThreads) decode_prep_kernel(const PrepArg
 struct ScoreArgs {
   const int32_t* ctx;
   const int32_t* pageTable;
-  const uint32_t* q;
+  const float* q;
   float* scores;
   int32_t* hist;
   int32_t* status;
@@ -249,7 +231,7 @@ struct ScoreArgs {
 __host__ __device__ __forceinline__ int score_smem_bytes(int di, int ratio, int B) {
   const int stage = (kTokensPerPage / ratio) * di * 2;
   return kStages * stage + 2 * kStages * 8 + ((B + 1 + 3) / 4) * 16 + kConsumerWarps * 128 * 4 +
-         kQSlots * kQPerSeq * 4;
+         kQSlots * 4 * ((di / 32) * 64 + 4) * 4;
 }
 
 // One lane per key row: byte offset of 16-byte chunk c (dims 8c..8c+7 of a
@@ -271,44 +253,67 @@ __device__ __forceinline__ void page_epilogue(const ScoreArgs& a, int b, int p, 
   }
 }
 
-// Scores one page (bpp <= 32 block keys in a swizzled stage) for one warp on
-// the tensor cores: per 16-block m-tile and 16-dim k-step one ldmatrix.x4 of
-// the keys and two mma.sync (query hi and lo, from `qf`), then relu and the
-// head sum on the accumulators.  Writes the page's scores to myscr[0, bpp).
-// Rows of an m-tile past a short page repeat earlier rows (never written).
-template <int DI>
-__device__ __forceinline__ void score_page(const uint8_t* tile, int bpp, const uint32_t (&qf)[DI / 16][4],
-                                           float* myscr) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t tb = smem_addr(tile);
-  const bool two = bpp > 16;  // a second m-tile (warp-uniform)
-  float acc[2][2][4];         // [m-tile][hi, lo][fragment]
+// Scores one page (bpp <= 32 block keys in a swizzled stage) for one warp.
+// Lane (kk, hh) = (lane & 7, lane >> 3) holds keys kk + 8j (j < 4) and their
+// dims [hh*DI/4, (hh+1)*DI/4); its quarter of the queries (qh, scorer layout)
+// is read by broadcast, dims are paired in fp32x2 FMAs, and two transposing
+// exchanges (lane ^ 16, then ^ 8) leave each lane the full dot products of its
+// head slots 0 and 1 -- every step one shuffle and one add.  Writes the page's
+// scores to myscr[0, 32).  kSmemQ: qh points to shared memory (else global).
+template <int DI, bool kSmemQ>
+__device__ __forceinline__ void score_page(const uint8_t* tile, int bpp, const float* qh, float* myscr) {
+  constexpr int NCH = DI / 32;
+  const int lane = threadIdx.x & 31, kk = lane & 7, hh = lane >> 3;
+  uint64_t acc[4][8];
 #pragma unroll
-  for (int u = 0; u < 2; ++u)
+  for (int j = 0; j < 4; ++j)
 #pragma unroll
-    for (int hl = 0; hl < 2; ++hl)
+    for (int h = 0; h < 8; ++h) acc[j][h] = 0ull;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[u][hl][j] = 0.f;
+  for (int c = 0; c < NCH; ++c) {
+    const int cg = hh * NCH + c;  // this lane's chunk: half cg >> 3 of the row, 16-byte slot cg & 7
+    uint64_t kp[4][4];
 #pragma unroll
-  for (int ks = 0; ks < DI / 16; ++ks) {
-    const int c = (ks & 3) * 2 + (lane >> 4);  // 16-byte chunk within the 64-dim half ks / 4
+    for (int j = 0; j < 4; ++j) {
+      const int r = (kk + 8 * j) & (bpp - 1);  // rows past a short page repeat (discarded)
+      const uint4 raw = *reinterpret_cast<const uint4*>(tile + (cg >> 3) * bpp * 128 + swz128(r, cg & 7));
+      const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      if (u == 0 || two) {
-        const int r = (u * 16 + (lane & 15)) & (bpp - 1);
-        uint32_t af[4];
-        ldsm_x4(tb + (ks >> 2) * bpp * 128 + swz128(r, c), af[0], af[1], af[2], af[3]);
-        mma16816(acc[u][0], af, qf[ks][0], qf[ks][1]);
-        mma16816(acc[u][1], af, qf[ks][2], qf[ks][3]);
+      for (int jj = 0; jj < 4; ++jj) {
+        const float2 f = __half22float2(h2[jj]);
+        kp[j][jj] = pack_f2(f.x, f.y);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      const float4* q4 = reinterpret_cast<const float4*>(qh + c * 64 + h * 8);
+      const float4 qa = kSmemQ ? q4[0] : __ldg(q4);
+      const float4 qb = kSmemQ ? q4[1] : __ldg(q4 + 1);
+      const uint64_t q0 = pack_f2(qa.x, qa.y), q1 = pack_f2(qa.z, qa.w);
+      const uint64_t q2 = pack_f2(qb.x, qb.y), q3 = pack_f2(qb.z, qb.w);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        acc[j][h] = ffma2(q0, kp[j][0], acc[j][h]);
+        acc[j][h] = ffma2(q1, kp[j][1], acc[j][h]);
+        acc[j][h] = ffma2(q2, kp[j][2], acc[j][h]);
+        acc[j][h] = ffma2(q3, kp[j][3], acc[j][h]);
       }
     }
   }
+  __syncwarp();  // every lane's reads of the stage are done
 #pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    if (u == 0 || two) {
-      const float sc = relu_head_sum(acc[u][0], acc[u][1]);
-      if ((lane & 2) == 0) myscr[u * 16 + (lane >> 2) + (lane & 1) * 8] = sc;
-    }
+  for (int j = 0; j < 4; ++j) {
+    float d[8];
+#pragma unroll
+    for (int h = 0; h < 8; ++h) d[h] = lo_f2(acc[j][h]) + hi_f2(acc[j][h]);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) d[h] += __shfl_xor_sync(kFull, d[h + 4], 16);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) d[h] += __shfl_xor_sync(kFull, d[h + 2], 8);
+    float t = (d[0] > 0.f ? d[0] : 0.f) + (d[1] > 0.f ? d[1] : 0.f);
+    t += __shfl_xor_sync(kFull, t, 8);
+    t += __shfl_xor_sync(kFull, t, 16);
+    if (hh == 0) myscr[kk + 8 * j] = t;
   }
 }
 
@@ -357,8 +362,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
   const long long lo = W * blockIdx.x / gridDim.x, hi = W * (blockIdx.x + 1) / gridDim.x;
   if (lo >= hi) return;
   // queries of the first kQSlots sequences this CTA's pages belong to
+  constexpr int QS = (DI / 32) * 64 + 4;
   float* myscr0 = reinterpret_cast<float*>(pref + (a.B + 1 + 3) / 4 * 4);
-  uint32_t* qcache = reinterpret_cast<uint32_t*>(myscr0 + kConsumerWarps * 128);
+  float* qcache = myscr0 + kConsumerWarps * 128;
   auto seq_of = [&](long long page) {  // largest b with pref[b] <= page
     int l = 0, h = a.B;
     while (h - l > 1) {
@@ -373,9 +379,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
   const int b_first = seq_of(lo);
   const int nslot = min(kQSlots, seq_of(hi - 1) - b_first + 1);
   if (warp < kConsumerWarps) {  // the consumers fill the query cache; the producer starts streaming meanwhile
-    for (int e = tid; e < nslot * kQPerSeq / 4; e += kConsumerWarps * 32)  // 16-byte units, slots back to back
-      reinterpret_cast<uint4*>(qcache)[e] =
-          __ldcg(reinterpret_cast<const uint4*>(a.q + static_cast<size_t>(b_first) * kQPerSeq) + e);
+    for (int e = tid; e < nslot * QS; e += kConsumerWarps * 32) {  // float4 units: 4*QS floats per sequence
+      const int bi = e / QS, w4 = e % QS;
+      reinterpret_cast<float4*>(qcache)[e] =
+          __ldcg(reinterpret_cast<const float4*>(a.q + static_cast<size_t>(b_first + bi) * kQPerSeq) + w4);
+    }
     asm volatile("bar.sync 1, %0;\n" ::"n"(kConsumerWarps * 32) : "memory");
   }
 
@@ -422,7 +430,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
 
   // ---- consumers: warp w scores pages lo + w, lo + w + kConsumerWarps, ...
   float* myscr = myscr0 + warp * 128;
-  uint32_t qf[DI / 16][4];  // the current sequence's query fragments
+  const int hh = lane >> 3;
   int cached_b = -1, n_c = 0;
   int b = 0;
   for (long long i = lo + warp; i < hi; i += kConsumerWarps) {
@@ -432,17 +440,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
     if (b != cached_b) {
       n_c = max(0, min(a.ctx[b], MAXL)) / a.ratio;
       cached_b = b;
-      const uint4* qsrc = reinterpret_cast<const uint4*>(
-          (b - b_first < kQSlots ? qcache + (b - b_first) * kQPerSeq : a.q + static_cast<size_t>(b) * kQPerSeq) +
-          lane * 32);
-#pragma unroll
-      for (int ks = 0; ks < DI / 16; ++ks) {
-        const uint4 w = qsrc[ks];
-        qf[ks][0] = w.x;
-        qf[ks][1] = w.y;
-        qf[ks][2] = w.z;
-        qf[ks][3] = w.w;
-      }
     }
     // Warps take pages round-robin, so this warp can reach page jx while the
     // stage's previous page (jx - kStages, another warp's) is still landing;
@@ -454,8 +451,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
       if (lane == 0) atomicOr(a.status, kErrWaitTimeout);
       break;
     }
-    score_page<DI>(ring + s * stage_bytes, bpp, qf, myscr);
-    __syncwarp();  // every lane's reads of the stage are done
+    const uint8_t* tile = ring + s * stage_bytes;
+    if (b - b_first < kQSlots)
+      score_page<DI, true>(tile, bpp, qcache + (b - b_first) * 4 * QS + hh * QS, myscr);
+    else
+      score_page<DI, false>(tile, bpp, a.q + static_cast<size_t>(b) * kQPerSeq + hh * QS, myscr);
     if (lane == 0) mbar_arrive(&empty[s]);
     __syncwarp();
     page_epilogue(a, b, p, n_c, bpp, myscr[lane < bpp ? lane : 0]);
@@ -819,7 +819,7 @@ cudaError_t launch_indexer_decode(const QsaIndexerDecodeParams& p, const RopeFre
   const WsLayout l = ws_layout(B, nbmax);
   uint8_t* ws = static_cast<uint8_t*>(p.workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws);
-  uint32_t* q = reinterpret_cast<uint32_t*>(ws + l.q);
+  float* q = reinterpret_cast<float*>(ws + l.q);
   float* scores = reinterpret_cast<float*>(ws + l.scores);
   int32_t* hist = reinterpret_cast<int32_t*>(ws + l.hist);
   cudaStream_t st = static_cast<cudaStream_t>(p.stream);

@@ -72,11 +72,20 @@ struct SelArgs {
   RopeFreqs rf;
 };
 
-constexpr int kRows = kPrefillRowsPerCta;  // rows per top-k CTA (one warp each)
+constexpr int kRows = kPrefillRowsPerCta;  // rows per CTA (one warp each)
 constexpr int kThreads = 256;
-constexpr int kSRows = 16;                 // rows per score CTA (two per warp)
-constexpr int kKT = 64;                    // block keys per staged tile
-constexpr int kKStages = 3;                // tiles in flight
+constexpr int kTile = 256;                  // blocks per score tile (8 per lane)
+constexpr int kKC = 16;                     // key dims staged per step
+constexpr int kKS = kKC + 2;                // padded row stride: float2 reads and writes are conflict-free
+constexpr int kHI = 8;                      // heads per thread tile (Hi <= 8, extra heads are zero)
+
+// Two fp16 values packed in 32 bits, widened to fp32.
+__device__ __forceinline__ float2 bits_to_float2(uint32_t u) {
+  __half2_raw r;
+  r.x = static_cast<unsigned short>(u & 0xffffu);
+  r.y = static_cast<unsigned short>(u >> 16);
+  return __half22float2(__half2(r));
+}
 
 // Start of row t's scores within its sequence: sum over u = 1..t of floor(u / r),
 // i.e. the complete-block counts n_c of rows 0..t-1.
@@ -86,90 +95,49 @@ __host__ __device__ __forceinline__ long long tri_offset(long long t, int r) {
 }
 
 template <int DI>
-__host__ __device__ constexpr int qw_stride() {
-  return DI + 8;
-}
-template <int DI>
 constexpr size_t score_smem_bytes() {
-  return static_cast<size_t>(kKStages) * kKT * DI * 2 + sizeof(float) * 8 * 8 * qw_stride<DI>();
+  return sizeof(float) * (static_cast<size_t>(DI) * kRows * kHI + 2 * kTile * kKS + kRows * DI + kRows * 128);
 }
 
-// Block scores of 16 consecutive query rows of one sequence (rows whose n_c
+// Block scores of 8 consecutive query rows of one sequence (rows whose n_c
 // exceeds the budget; the others need no scores), written to the workspace.
-// Warp w owns rows 2w and 2w+1: it prepares their index queries (RMSNorm*(1+w),
-// RoPE in fp32 with angles reduced in integer turns), scales and splits them
-// into hi/lo fp16 mma fragments held in registers (B operands: n = head,
-// k = dim), and contracts them on the tensor cores (mma.sync m16n8k16, fp32
-// accumulators) against 64-block tiles of fp16 block keys (A operands: m =
-// block, k = dim) that the CTA streams through a 3-stage cp.async ring with a
-// 16-byte XOR swizzle, read by ldmatrix without bank conflicts.  Relu and the
-// head sum run on the accumulators.  Two CTAs share an SM.
+// Two CTAs share an SM (80 KB of shared memory each at di = 128), so the
+// staging barriers and shared-memory latencies of one are covered by the other.
 template <int DI>
 __global__ void __launch_bounds__(kThreads, 2) prefill_score_kernel(const SelArgs a) {
-  constexpr int PER = DI / 32;
-  constexpr int KS = DI / 16;          // k-steps of 16 dims
-  constexpr int ROWB = DI * 2;         // bytes of one block key
-  constexpr int TILEB = kKT * ROWB;    // bytes of one tile
-  constexpr int CPR = DI / 8;          // 16-byte chunks of one block key
-  constexpr int QWS = qw_stride<DI>();
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* tiles = smem;                                               // [kKStages][kKT][DI] fp16, swizzled
-  float* qw = reinterpret_cast<float*>(smem + kKStages * TILEB);       // [8 warps][8 heads][QWS]
-  __shared__ unsigned long long turn_s[64];
+  extern __shared__ __align__(16) float smem[];
+  float* q_s = smem;                          // [DI][kRows][kHI] prepared queries
+  float* kb_s = q_s + DI * kRows * kHI;       // [2][kTile][kKS]  block-key tile (fp32)
+  float* ys_s = kb_s + 2 * kTile * kKS;       // [kRows][DI]      per-warp RoPE scratch
+  float* cs_s = ys_s + kRows * DI;            // [kRows][64][2]   cos/sin per row
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.y;
-  const int ngroups = (a.S + kSRows - 1) / kSRows;
-  const int t0 = (ngroups - 1 - static_cast<int>(blockIdx.x)) * kSRows;  // longest rows first
+  const int ngroups = (a.S + kRows - 1) / kRows;
+  const int t0 = (ngroups - 1 - static_cast<int>(blockIdx.x)) * kRows;  // longest rows first
   const int L = max(0, min(a.ctx[b], a.S));
-  const int t_end = min(t0 + kSRows, L);  // live rows [t0, t_end)
+  const int t_end = min(t0 + kRows, L);  // live rows [t0, t_end)
   if (t0 >= L) return;
+  const int nlive = t_end - t0;
   const int n_hi = t_end / a.ratio;  // complete blocks seen by the group's last live row
   if (n_hi <= a.budget) return;
 
-  // the first tiles start landing while the queries are prepared
-  const __half* kb_g = a.kbar + static_cast<size_t>(b) * a.nbmax * DI;
-  const int ntiles = (n_hi + kKT - 1) / kKT;
-  auto issue = [&](int tile) {
-    uint8_t* dst = tiles + (tile % kKStages) * TILEB;
-    const int gbase = tile * kKT;
-#pragma unroll
-    for (int k = 0; k < kKT * CPR / kThreads; ++k) {
-      const int e = tid + k * kThreads;
-      const int row = e / CPR, c = e % CPR;
-      const bool ok = gbase + row < n_hi;
-      cp_async16(smem_addr(dst + row * ROWB + ((c ^ (row & 7)) << 4)),
-                 kb_g + static_cast<size_t>(ok ? gbase + row : 0) * DI + c * 8, ok);
-    }
-  };
-  issue(0);
-  cp_async_commit();
-  if (ntiles > 1) issue(1);
-  cp_async_commit();
-  if (tid < 64) turn_s[tid] = a.rf.turn[tid];
-  __syncthreads();
-
   // ------------------------------------------------------------ query prep
-  uint32_t qf[2][KS][4];  // per row and k-step: hi b0, hi b1, lo b0, lo b1
-  float* qwarp = qw + warp * 8 * QWS;
   const int half = a.rot >> 1;
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    const int t = t0 + 2 * warp + rr;
-    const bool live = t < t_end;
-    float cs[PER], sn[PER];
-#pragma unroll
-    for (int p = 0; p < PER; ++p) {
-      const int i = lane + 32 * p;
-      cs[p] = 1.f;
-      sn[p] = 0.f;
-      if (live && i < a.rot) rope_cos_sin_turns(static_cast<unsigned>(t), turn_s[i < half ? i : i - half], cs[p], sn[p]);
-    }
-    float mx = 0.f;
-    for (int h = 0; h < 8; ++h) {
-      float* qh = qwarp + h * QWS;
-      if (live && h < a.Hi) {
-        const __half* x = a.idxQ + ((static_cast<size_t>(b) * a.S + t) * a.Hi + h) * DI;
+  for (int e = tid; e < kRows * half; e += kThreads) {
+    const int r = e / half, i = e - r * half;
+    float c = 1.f, s = 0.f;
+    if (r < nlive) rope_cos_sin_turns(static_cast<unsigned>(t0 + r), a.rf.turn[i], c, s);
+    cs_s[r * 128 + 2 * i] = c;
+    cs_s[r * 128 + 2 * i + 1] = s;
+  }
+  __syncthreads();
+  {
+    constexpr int PER = DI / 32;
+    const int r = warp;
+    for (int h = 0; h < kHI; ++h) {
+      if (r < nlive && h < a.Hi) {
+        const __half* x = a.idxQ + ((static_cast<size_t>(b) * a.S + t0 + r) * a.Hi + h) * DI;
         float y[PER];
         float ss = 0.f;
 #pragma unroll
@@ -184,99 +152,110 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_score_kernel(const SelArg
         for (int p = 0; p < PER; ++p) {
           const int i = lane + 32 * p;
           y[p] = y[p] * inv * (1.0f + a.wq[i]);
-          qh[i] = y[p];
+          ys_s[r * DI + i] = y[p];
         }
         __syncwarp();
-        float v[PER];
 #pragma unroll
         for (int p = 0; p < PER; ++p) {
           const int i = lane + 32 * p;
-          v[p] = y[p];
-          if (i < half)
-            v[p] = y[p] * cs[p] - qh[i + half] * sn[p];
-          else if (i < a.rot)
-            v[p] = y[p] * cs[p] + qh[i - half] * sn[p];
-          mx = fmaxf(mx, fabsf(v[p]));
+          float v = y[p];
+          if (i < half) {
+            v = y[p] * cs_s[r * 128 + 2 * i] - ys_s[r * DI + i + half] * cs_s[r * 128 + 2 * i + 1];
+          } else if (i < a.rot) {
+            const int k = i - half;
+            v = y[p] * cs_s[r * 128 + 2 * k] + ys_s[r * DI + k] * cs_s[r * 128 + 2 * k + 1];
+          }
+          q_s[(i * kRows + r) * kHI + h] = v;
         }
         __syncwarp();
-#pragma unroll
-        for (int p = 0; p < PER; ++p) qh[lane + 32 * p] = v[p];
       } else {
 #pragma unroll
-        for (int p = 0; p < PER; ++p) qh[lane + 32 * p] = 0.f;
+        for (int p = 0; p < PER; ++p) q_s[((lane + 32 * p) * kRows + r) * kHI + h] = 0.f;
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-    __syncwarp();
-    const float scale = index_q_scale(mx);
-    const float* qn = qwarp + (lane >> 2) * QWS + (lane & 3) * 2;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      const float2 x0 = *reinterpret_cast<const float2*>(qn + ks * 16);
-      const float2 x1 = *reinterpret_cast<const float2*>(qn + ks * 16 + 8);
-      split_half2(x0.x * scale, x0.y * scale, qf[rr][ks][0], qf[rr][ks][2]);
-      split_half2(x1.x * scale, x1.y * scale, qf[rr][ks][1], qf[rr][ks][3]);
-    }
-    __syncwarp();
   }
+  __syncthreads();
 
   // ---------------------------------------------------------- block scores
-  int n_c[2];
-  bool store[2];
-  float* srow[2];
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    const int t = t0 + 2 * warp + rr;
-    n_c[rr] = (t + 1) / a.ratio;
-    store[rr] = t < t_end && n_c[rr] > a.budget;  // this row needs its scores
-    srow[rr] = a.scores + static_cast<size_t>(b) * a.triPerSeq + tri_offset(t, a.ratio);
-  }
-  const int arow = lane & 15, achunk = lane >> 4;  // this lane's ldmatrix row and chunk within a 16x16 A tile
+  // Lane owns blocks lane + 32 m (m < 8) of the tile, for its warp's row
+  // and all kHI heads: 64 accumulators, each a plain ascending-k FMA chain,
+  // so a block's score does not depend on where the block sits in a tile.
+  const int t = t0 + warp;
+  const int n_c = (t + 1) / a.ratio;
+  const bool store = warp < nlive && n_c > a.budget;  // this row needs its scores
+  float* srow = a.scores + static_cast<size_t>(b) * a.triPerSeq + tri_offset(t, a.ratio);
+  const __half* kb_g = a.kbar + static_cast<size_t>(b) * a.nbmax * DI;
+  const int ntiles = (n_hi + kTile - 1) / kTile;
   for (int tile = 0; tile < ntiles; ++tile) {
-    cp_async_wait<1>();
-    __syncthreads();  // tile `tile` visible to all; every warp is done with tile - 1
-    if (tile + 2 < ntiles) issue(tile + 2);
-    cp_async_commit();
-    const uint32_t tb = smem_addr(tiles + (tile % kKStages) * TILEB);
-    const int gbase = tile * kKT;
+    const int gbase = tile * kTile;
+    const int gl = gbase + tid;  // block staged by this thread
+    const bool gok = gl < n_hi;
+    const uint4* src = reinterpret_cast<const uint4*>(kb_g + static_cast<size_t>(gok ? gl : 0) * DI);
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    uint4 pre0 = gok ? __ldg(src) : zero;
+    uint4 pre1 = gok ? __ldg(src + 1) : zero;
+    float acc[8][kHI];
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+#pragma unroll
+      for (int h = 0; h < kHI; ++h) acc[m][h] = 0.f;
+
 #pragma unroll 1
-    for (int mt = 0; mt < kKT / 16; mt += 2) {
-      float acc[2][2][2][4];  // [m-tile][row][hi, lo][fragment]
+    for (int kc = 0; kc < DI / kKC; ++kc) {
+      float2* dst = reinterpret_cast<float2*>(kb_s + (kc & 1) * kTile * kKS + tid * kKS);
+      dst[0] = bits_to_float2(pre0.x);
+      dst[1] = bits_to_float2(pre0.y);
+      dst[2] = bits_to_float2(pre0.z);
+      dst[3] = bits_to_float2(pre0.w);
+      dst[4] = bits_to_float2(pre1.x);
+      dst[5] = bits_to_float2(pre1.y);
+      dst[6] = bits_to_float2(pre1.z);
+      dst[7] = bits_to_float2(pre1.w);
+      __syncthreads();
+      if (kc + 1 < DI / kKC) {
+        pre0 = gok ? __ldg(src + 2 * (kc + 1)) : zero;
+        pre1 = gok ? __ldg(src + 2 * (kc + 1) + 1) : zero;
+      }
+      const float* kt = kb_s + (kc & 1) * kTile * kKS;
+      const float* qk = q_s + static_cast<size_t>(kc * kKC) * kRows * kHI + warp * kHI;
+#pragma unroll 4
+      for (int kp = 0; kp < kKC / 2; ++kp) {  // two dims per step: 16 key values, 16 query values, 128 FMAs
+        float2 kv[8];
 #pragma unroll
-      for (int u = 0; u < 2; ++u)
+        for (int m = 0; m < 8; ++m) kv[m] = *reinterpret_cast<const float2*>(kt + (lane + 32 * m) * kKS + kp * 2);
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr)
+        for (int kk = 0; kk < 2; ++kk) {
+          const float* qp = qk + (kp * 2 + kk) * kRows * kHI;
+          const float4 qa = *reinterpret_cast<const float4*>(qp);
+          const float4 qb = *reinterpret_cast<const float4*>(qp + 4);
 #pragma unroll
-          for (int hl = 0; hl < 2; ++hl)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[u][rr][hl][j] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int row = (mt + u) * 16 + arow;
-          uint32_t af[4];
-          ldsm_x4(tb + row * ROWB + (((ks * 2 + achunk) ^ (row & 7)) << 4), af[0], af[1], af[2], af[3]);
-#pragma unroll
-          for (int rr = 0; rr < 2; ++rr) {
-            mma16816(acc[u][rr][0], af, qf[rr][ks][0], qf[rr][ks][1]);
-            mma16816(acc[u][rr][1], af, qf[rr][ks][2], qf[rr][ks][3]);
+          for (int m = 0; m < 8; ++m) {
+            const float kval = kk == 0 ? kv[m].x : kv[m].y;
+            acc[m][0] = fmaf(qa.x, kval, acc[m][0]);
+            acc[m][1] = fmaf(qa.y, kval, acc[m][1]);
+            acc[m][2] = fmaf(qa.z, kval, acc[m][2]);
+            acc[m][3] = fmaf(qa.w, kval, acc[m][3]);
+            acc[m][4] = fmaf(qb.x, kval, acc[m][4]);
+            acc[m][5] = fmaf(qb.y, kval, acc[m][5]);
+            acc[m][6] = fmaf(qb.z, kval, acc[m][6]);
+            acc[m][7] = fmaf(qb.w, kval, acc[m][7]);
           }
         }
       }
+    }
+    if (store) {
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int g = gbase + (mt + u) * 16 + (lane >> 2) + (lane & 1) * 8;
+      for (int m = 0; m < 8; ++m) {
+        const int g = gbase + lane + 32 * m;
+        if (g < n_c) {
+          float sc = 0.f;
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          const float sc = relu_head_sum(acc[u][rr][0], acc[u][rr][1]);
-          if (store[rr] && (lane & 2) == 0 && g < n_c[rr]) srow[rr][g] = sc;
+          for (int h = 0; h < kHI; ++h) sc += acc[m][h] > 0.f ? acc[m][h] : 0.f;
+          srow[g] = sc;
         }
       }
     }
   }
-  cp_async_wait<0>();
 }
 
 // ------------------------------------ select + expand, one warp per row
@@ -386,7 +365,7 @@ cudaError_t launch_score(const SelArgs& a, int B, cudaStream_t st) {
   static const cudaError_t attr = cudaFuncSetAttribute(
       prefill_score_kernel<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (attr != cudaSuccess) return attr;
-  dim3 grid((a.S + kSRows - 1) / kSRows, B);
+  dim3 grid((a.S + kRows - 1) / kRows, B);
   prefill_score_kernel<DI><<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
