@@ -19,9 +19,9 @@
 //                          row's n_c scores, rows packed back to back).  Two
 //                          CTAs share an SM.
 //   prefill_topk_kernel    one warp per row: a deterministic top-`budget`
-//                          select over the row's scores (bisection on the
-//                          score bits with warp reductions, exact ties to the
-//                          lower block id) and the expansion into the row's
+//                          select over the row's scores (a radix select on
+//                          the score bits in per-warp histograms, exact ties
+//                          to the lower block id) and the expansion into the row's
 //                          ascending index list; rows with n_c <= budget list
 //                          0..t and rows t >= L are all -1.
 #include "qsa_blockkey.cuh"
@@ -261,17 +261,19 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_score_kernel(const SelArg
 // ------------------------------------ select + expand, one warp per row
 // Lane l holds the scores of blocks l + 32 m.  Keys are the score bits + 1
 // (order-preserving for scores >= 0; 0 marks blocks past the row's n_c).
-// Bisection on the key finds T with count(key >= T) >= budget >
-// count(key > T); the blocks above T are kept, and of those equal to T the
-// lowest ids, so the kept set is the top `budget` by (score desc, id asc).
-// A probe with exactly `budget` keys at or above it ends the search early:
-// those keys are the set (T = probe - 1 and no key equal to T is kept).
-// Walking m upwards visits ids in ascending order, so ballots compact the
-// kept blocks straight into the ascending list.  Rows t >= L are all -1 and
-// rows with n_c <= budget list 0..t.
+// A radix select finds the cut T with count(key > T) < budget <=
+// count(key >= T): 8-bit digits of (key - lo) over the range still in play,
+// counted in a per-warp shared-memory histogram, narrow the range to the bin
+// holding the cut (at most four passes), and once that bin holds at most 32
+// keys their exact order is taken by pairwise counts.  The blocks above T are
+// kept, and of those equal to T the lowest ids, so the kept set is the top
+// `budget` by (score desc, id asc).  Walking m upwards visits ids in ascending
+// order, so ballots compact the kept blocks straight into the ascending list.
+// Rows t >= L are all -1 and rows with n_c <= budget list 0..t.
 template <int VPT>
 __global__ void __launch_bounds__(kThreads) prefill_topk_kernel(const SelArgs a) {
   constexpr int KPL = kThreads * VPT / 32;
+  __shared__ __align__(16) uint32_t hist_s[kThreads / 32][256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.y;
   const int t = blockIdx.x * kRows + warp;
@@ -293,7 +295,6 @@ __global__ void __launch_bounds__(kThreads) prefill_topk_kernel(const SelArgs a)
   // warp-uniform branch, no instructions issued for them).
   constexpr int KG = 8;
   const int mlim = (n_c + 31) / 32;
-  const int nslot = KG * ((mlim + KG - 1) / KG);  // keys per lane that the passes visit
   uint32_t key[KPL];
 #pragma unroll
   for (int c = 0; c < KPL / KG; ++c) {
@@ -303,34 +304,123 @@ __global__ void __launch_bounds__(kThreads) prefill_topk_kernel(const SelArgs a)
       key[c * KG + k] = c * KG < mlim && g < n_c ? __float_as_uint(__ldcg(srow + g)) + 1u : 0u;
     }
   }
-  uint32_t lo = 1u, hi = 0x80000001u;  // count(>= lo) >= budget > count(>= hi)
-  int c_hi = 0;
-  while (hi - lo > 1u) {
-    const uint32_t mid = lo + ((hi - lo) >> 1);
-    // keys lie in [0, 2^31) and mid in [1, 2^31], so key - mid as a signed
-    // 32-bit value is negative exactly when key < mid
-    int below_mid = 0;
+  // The cut key Tk (the budget-th largest key) and the number of keys equal
+  // to it that are kept (lowest ids first).  Score-0 blocks (key 1) sit below
+  // every positive one; among the positive keys a radix select refines a
+  // 256-bin histogram of (key - lo) >> sh in this warp's shared memory until
+  // the bin holding the cut has at most 32 keys (or is one key value), whose
+  // exact order is then taken by counting.
+  uint32_t* hist = hist_s[warp];
+  uint32_t kmx = 0u, kmn = 0xffffffffu;
+  int npos = 0;
 #pragma unroll
-    for (int c = 0; c < KPL / KG; ++c) {
-      if (c * KG < mlim) {
+  for (int c = 0; c < KPL / KG; ++c) {
+    if (c * KG < mlim) {
 #pragma unroll
-        for (int k = 0; k < KG; ++k) below_mid += static_cast<int>(key[c * KG + k] - mid) >> 31;
+      for (int k = 0; k < KG; ++k) {
+        const uint32_t kk = key[c * KG + k];
+        if (kk >= 2u) {
+          kmx = max(kmx, kk);
+          kmn = min(kmn, kk);
+          ++npos;
+        }
       }
     }
-    const int c = static_cast<int>(__reduce_add_sync(kFull, static_cast<unsigned>(nslot + below_mid)));
-    if (c == a.budget) {  // exactly the budget at or above mid: keep those, no tie to break
-      lo = mid - 1u;
-      c_hi = a.budget;
-      break;
-    }
-    if (c > a.budget) {
-      lo = mid;
-    } else {
-      hi = mid;
-      c_hi = c;
+  }
+  kmx = __reduce_max_sync(kFull, kmx);
+  kmn = __reduce_min_sync(kFull, kmn);
+  npos = static_cast<int>(__reduce_add_sync(kFull, static_cast<unsigned>(npos)));
+  uint32_t lo;
+  int quota;
+  if (npos < a.budget) {  // every positive block is kept, then score-0 blocks by lowest id
+    lo = 1u;
+    quota = a.budget - npos;
+  } else {
+    uint32_t blo = kmn, span = kmx - kmn;  // keys of the current bin: [blo, blo + span]
+    int need = a.budget;                   // keys of the current bin to keep
+    for (;;) {
+      const int sh = max(0, 24 - static_cast<int>(__clz(span)));  // span >> sh < 256
+#pragma unroll
+      for (int j = 0; j < 8; ++j) hist[lane * 8 + j] = 0u;
+      __syncwarp();
+#pragma unroll
+      for (int c = 0; c < KPL / KG; ++c) {
+        if (c * KG < mlim) {
+#pragma unroll
+          for (int k = 0; k < KG; ++k) {
+            const uint32_t d = key[c * KG + k] - blo;  // keys below blo wrap past span
+            if (d <= span) atomicAdd(hist + (d >> sh), 1u);
+          }
+        }
+      }
+      __syncwarp();
+      // lane l owns bins 8l .. 8l+7; `run` counts the keys in higher bins
+      const uint4 h0 = *reinterpret_cast<const uint4*>(hist + lane * 8);
+      const uint4 h1 = *reinterpret_cast<const uint4*>(hist + lane * 8 + 4);
+      const int hb[8] = {static_cast<int>(h0.x), static_cast<int>(h0.y), static_cast<int>(h0.z), static_cast<int>(h0.w),
+                         static_cast<int>(h1.x), static_cast<int>(h1.y), static_cast<int>(h1.z), static_cast<int>(h1.w)};
+      int own = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) own += hb[j];
+      int suffix = own;  // keys in the bins of lanes >= this one
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_down_sync(kFull, suffix, o);
+        if (lane + o < 32) suffix += y;
+      }
+      int run = suffix - own, T = -1, above = 0, nT = 0;
+#pragma unroll
+      for (int j = 7; j >= 0; --j) {
+        if (run < need && run + hb[j] >= need) {
+          T = lane * 8 + j;
+          above = run;
+          nT = hb[j];
+        }
+        run += hb[j];
+      }
+      const int src = __ffs(__ballot_sync(kFull, T >= 0)) - 1;  // exactly one lane holds the bin
+      T = __shfl_sync(kFull, T, src);
+      need -= __shfl_sync(kFull, above, src);
+      nT = __shfl_sync(kFull, nT, src);
+      blo += static_cast<uint32_t>(T) << sh;
+      span = sh == 0 ? 0u : min(span - (static_cast<uint32_t>(T) << sh), (1u << sh) - 1u);
+      __syncwarp();  // every lane has read the histogram
+      if (span == 0u) {  // one key value: its `need` lowest ids
+        lo = blo;
+        quota = need;
+        break;
+      }
+      if (nT <= 32) {
+        // the bin's keys, one per lane, then each one's count of larger and equal keys
+        uint32_t* cand = hist;
+        int at = 0;
+#pragma unroll
+        for (int c = 0; c < KPL / KG; ++c) {
+          if (c * KG < mlim) {
+#pragma unroll
+            for (int k = 0; k < KG; ++k) {
+              const bool in = key[c * KG + k] - blo <= span;
+              const unsigned m = __ballot_sync(kFull, in);
+              if (in) cand[at + __popc(m & ((1u << lane) - 1u))] = key[c * KG + k];
+              at += __popc(m);
+            }
+          }
+        }
+        __syncwarp();
+        const uint32_t mine = lane < nT ? cand[lane] : 0u;
+        int gt = 0, eq = 0;
+        for (int j = 0; j < nT; ++j) {
+          const uint32_t v = __shfl_sync(kFull, mine, j);
+          gt += v > mine ? 1 : 0;
+          eq += v == mine ? 1 : 0;
+        }
+        const int hit = __ffs(__ballot_sync(kFull, lane < nT && gt < need && need <= gt + eq)) - 1;
+        lo = __shfl_sync(kFull, mine, hit);
+        quota = need - __shfl_sync(kFull, gt, hit);
+        break;
+      }
     }
   }
-  int quota = a.budget - c_hi;  // blocks with key == lo to keep, lowest ids first (none after an exact stop)
   int pos = 0;
   const unsigned below = (1u << lane) - 1u;
 #pragma unroll
