@@ -49,6 +49,18 @@ def workspace_kbar(ws: torch.Tensor, B: int, S: int, di: int, ratio: int) -> np.
     return to_np(raw).view(np.float16).reshape(B, nb, di)
 
 
+def same_fp16_bits(a: np.ndarray, b: np.ndarray) -> bool:
+    """fp16 arrays equal bit for bit, except that an exact zero may carry either sign.
+
+    Both sides round the same exact value once; a component whose exact value
+    is 0 gets its sign from IEEE sign-of-zero rules, which depend on operation
+    order (0*cos - 0*sin is -0 in f64 when cos < 0), so the sign is no claim.
+    """
+    ab, bb = a.view(np.uint16), b.view(np.uint16)
+    zero = ((ab & 0x7FFF) == 0) & ((bb & 0x7FFF) == 0)
+    return bool(np.all((ab == bb) | zero))
+
+
 def oracle_prefill_lists(t_np: dict, cfg, rows=None, want_scores=False, budget=None, topK=None):
     return oracle.indexer_prefill(t_np["idxQ"], t_np["idxK"], t_np["wq"], t_np["wk"], t_np["ctx"], rot=cfg.rot,
                                   ratio=cfg.ratio, budget=budget or cfg.budget, topK=topK or cfg.topK,
