@@ -449,13 +449,17 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_k
   WarpAcc<NT> A;
   acc_init(A);
   if constexpr (STAGES == 1) {  // one tile per CTA, 5 CTAs per SM (as in prefill)
-    cp_async_wait<0>();
+    if (ntiles > 0) issue(0, 0);  // the first tile's copies travel with Q's
+    cp_async_commit();
+    cp_async_wait<1>();  // Q
     __syncthreads();
     load_q_frags<NT>(q_tile, qf);
     for (int i = 0; i < ntiles; ++i) {
-      __syncthreads();
-      issue(i, 0);
-      cp_async_commit();
+      if (i > 0) {
+        __syncthreads();  // every warp is done with tile i-1
+        issue(i, 0);
+        cp_async_commit();
+      }
       cp_async_wait<0>();
       __syncthreads();
       const int slot = i * kKeys + warp * 16 + (lane >> 2);
