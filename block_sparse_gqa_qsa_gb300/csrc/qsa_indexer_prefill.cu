@@ -304,8 +304,8 @@ __global__ void __launch_bounds__(kThreads) prefill_topk_kernel(const SelArgs a)
       key[c * KG + k] = c * KG < mlim && g < n_c ? __float_as_uint(__ldcg(srow + g)) + 1u : 0u;
     }
   }
-  // The cut key Tk (the budget-th largest key) and the number of keys equal
-  // to it that are kept (lowest ids first).  Score-0 blocks (key 1) sit below
+  // The cut key `lo` (the budget-th largest key) and `quota`, the number of
+  // keys equal to it that are kept (lowest ids first).  Score-0 blocks (key 1) sit below
   // every positive one; among the positive keys a radix select refines a
   // 256-bin histogram of (key - lo) >> sh in this warp's shared memory until
   // the bin holding the cut has at most 32 keys (or is one key value), whose
