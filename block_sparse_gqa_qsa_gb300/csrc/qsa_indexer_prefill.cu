@@ -269,10 +269,13 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_score_kernel(const SelArg
 // kept, and of those equal to T the lowest ids, so the kept set is the top
 // `budget` by (score desc, id asc).  Walking m upwards visits ids in ascending
 // order, so ballots compact the kept blocks straight into the ascending list.
-// Rows t >= L are all -1 and rows with n_c <= budget list 0..t.
-template <int VPT>
+// Rows t >= L are all -1 and rows with n_c <= budget list 0..t.  R: the
+// compress ratio fixed at compile time (the r token ids of a kept block are
+// then straight-line stores), or 0 to read it from the arguments.
+template <int VPT, int R>
 __global__ void __launch_bounds__(kThreads) prefill_topk_kernel(const SelArgs a) {
   constexpr int KPL = kThreads * VPT / 32;
+  const int ratio = R > 0 ? R : a.ratio;
   __shared__ __align__(16) uint32_t hist_s[kThreads / 32][256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.y;
@@ -284,12 +287,12 @@ __global__ void __launch_bounds__(kThreads) prefill_topk_kernel(const SelArgs a)
     for (int i = lane; i < a.topK; i += 32) out[i] = -1;
     return;
   }
-  const int n_c = (t + 1) / a.ratio;
+  const int n_c = (t + 1) / ratio;
   if (n_c <= a.budget) {  // every block kept: the row lists 0..t
     for (int i = lane; i < a.topK; i += 32) out[i] = i <= t ? i : -1;
     return;
   }
-  const float* srow = a.scores + static_cast<size_t>(b) * a.triPerSeq + tri_offset(t, a.ratio);
+  const float* srow = a.scores + static_cast<size_t>(b) * a.triPerSeq + tri_offset(t, ratio);
   // Keys live in registers, KPL per lane; only the first ceil(n_c / 32) of them
   // can be non-zero, so every pass skips the groups of 8 past that (a
   // warp-uniform branch, no instructions issued for them).
@@ -435,16 +438,16 @@ __global__ void __launch_bounds__(kThreads) prefill_topk_kernel(const SelArgs a)
         quota = max(0, quota - __popc(eqm));
         const unsigned tm = __ballot_sync(kFull, take);
         if (take) {
-          const int at = (pos + __popc(tm & below)) * a.ratio, g = lane + 32 * m;
-          for (int j = 0; j < a.ratio; ++j) out[at + j] = g * a.ratio + j;
+          const int at = (pos + __popc(tm & below)) * ratio, g = lane + 32 * m;
+          for (int j = 0; j < ratio; ++j) out[at + j] = g * ratio + j;
         }
         pos += __popc(tm);
       }
     }
   }
-  const int head = pos * a.ratio;
+  const int head = pos * ratio;
   for (int i = head + lane; i < a.topK; i += 32) {
-    const int j = n_c * a.ratio + (i - head);
+    const int j = n_c * ratio + (i - head);
     out[i] = j <= t ? j : -1;
   }
 }
@@ -463,7 +466,10 @@ cudaError_t launch_score(const SelArgs& a, int B, cudaStream_t st) {
 template <int VPT>
 cudaError_t launch_topk(const SelArgs& a, int B, cudaStream_t st) {
   dim3 grid((a.S + kRows - 1) / kRows, B);
-  prefill_topk_kernel<VPT><<<grid, kThreads, 0, st>>>(a);
+  if (a.ratio == 4)
+    prefill_topk_kernel<VPT, 4><<<grid, kThreads, 0, st>>>(a);
+  else
+    prefill_topk_kernel<VPT, 0><<<grid, kThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -86,6 +86,9 @@ def test_indexer_prefill_edges():
                             ctx_hi=None, seed=4),
         dataclasses.replace(base, name="rot_full", B=1, S=900, rot=128, budget=50, ctx_lo=None, ctx_hi=None,
                             seed=5),
+        # ratios other than 4 run the top-k instance that reads r from its arguments
+        dataclasses.replace(base, name="ratio3", B=1, S=1400, ratio=3, budget=60, ctx_lo=None, ctx_hi=None, seed=6),
+        dataclasses.replace(base, name="ratio8", B=2, S=2100, ratio=8, budget=40, ctx_lo=900, ctx_hi=2100, seed=8),
     ]
     for cfg in cases:
         t_np, t_dev = _inputs(cfg)
