@@ -74,7 +74,7 @@ class QsaSparsePrefillParams(ctypes.Structure):
     _fields_ = [("qPtr", _vp), ("kPtr", _vp), ("vPtr", _vp), ("oPtr", _vp), ("indices", _vp),
                 ("contextLengths", _vp), ("batchSize", _i32), ("seqLen", _i32), ("numQHeads", _i32),
                 ("numKVHeads", _i32), ("headDim", _i32), ("topK", _i32), ("attentionScale", _f32),
-                ("stream", _vp)]
+                ("stream", _vp), ("status", _vp)]
 
 
 class QsaSparseDecodeParams(ctypes.Structure):
@@ -82,7 +82,7 @@ class QsaSparseDecodeParams(ctypes.Structure):
                 ("contextLengths", _vp), ("oPtr", _vp), ("partialO", _vp), ("partialStats", _vp),
                 ("splitCounters", _vp), ("batchSize", _i32), ("numQHeads", _i32), ("numKVHeads", _i32),
                 ("headDim", _i32), ("poolHeadDim", _i32), ("numFlatPages", _i32), ("maxPagesPerSeq", _i32),
-                ("topK", _i32), ("attentionScale", _f32), ("stream", _vp)]
+                ("topK", _i32), ("attentionScale", _f32), ("stream", _vp), ("status", _vp)]
 
 
 class QsaGatherParams(ctypes.Structure):
@@ -133,7 +133,7 @@ def lib() -> ctypes.CDLL:
             L.qsa_gather_scratch_pages.argtypes = [_i32]
             L.qsa_gather_scratch_pages.restype = _i32
             for n in ("qsa_sparse_decode_max_splits", "qsa_sparse_decode_partial_rows",
-                      "qsa_indexer_prefill_max_blocks"):
+                      "qsa_indexer_prefill_max_blocks", "qsa_indexer_prefill_max_seq_len"):
                 getattr(L, n).argtypes = []
                 getattr(L, n).restype = _i32
             L.qsa_sparse_prefill_can_implement.argtypes = [_i32] * 3
@@ -283,9 +283,10 @@ def rope_qkv(qkv, wq, wk, ctx, q_out, *, Hq, Hkv, rot, theta, eps, k_out=None, v
     _check(lib().qsa_rope_qkv(ctypes.byref(p)))
 
 
-def sparse_prefill(q, k, v, indices, ctx, out, scale, stream=None):
+def sparse_prefill(q, k, v, indices, ctx, out, scale, stream=None, status=None):
     """qsa_sparse_prefill (fp16 tensors) or qsa_sparse_prefill_bf16 (bfloat16 tensors):
-    q/out [B,S,Hq,D], k/v [B,S,Hkv,D], indices int32 [B,S,topK]."""
+    q/out [B,S,Hq,D], k/v [B,S,Hkv,D], indices int32 [B,S,topK]; status: optional int32 device
+    tensor whose first word collects the error bits."""
     et = q.dtype
     if et not in (torch.float16, torch.bfloat16):
         raise ValueError("sparse_prefill: q must be float16 or bfloat16")
@@ -299,13 +300,14 @@ def sparse_prefill(q, k, v, indices, ctx, out, scale, stream=None):
         qPtr=_ptr(q, et, "q"), kPtr=_ptr(k, et, "k"), vPtr=_ptr(v, et, "v"),
         oPtr=_ptr(out, et, "out"), indices=_ptr(indices, torch.int32, "indices"),
         contextLengths=_ptr(ctx, torch.int32, "contextLengths"), batchSize=B, seqLen=S, numQHeads=Hq,
-        numKVHeads=Hkv, headDim=D, topK=topK, attentionScale=scale, stream=_stream(stream))
+        numKVHeads=Hkv, headDim=D, topK=topK, attentionScale=scale, stream=_stream(stream),
+        status=None if status is None else _ptr(status, torch.int32, "status"))
     fn = lib().qsa_sparse_prefill_bf16 if et == torch.bfloat16 else lib().qsa_sparse_prefill
     _check(fn(ctypes.byref(p)))
 
 
 def sparse_decode(q, pool, page_table, indices, ctx, out, partial_o, partial_stats, counters, *, D, scale,
-                  stream=None):
+                  stream=None, status=None):
     """qsa_sparse_decode (fp16) or qsa_sparse_decode_bf16 (bfloat16 q/pool/out): q/out [B,1,Hq,D]; split-K
     over the pool through the page table."""
     et = q.dtype
@@ -325,7 +327,8 @@ def sparse_decode(q, pool, page_table, indices, ctx, out, partial_o, partial_sta
         partialStats=_ptr(partial_stats, torch.float32, "partialStats"),
         splitCounters=_ptr(counters, torch.int32, "splitCounters"), batchSize=B, numQHeads=Hq, numKVHeads=Hkv,
         headDim=D, poolHeadDim=phd, numFlatPages=nflat, maxPagesPerSeq=page_table.shape[-1], topK=topK,
-        attentionScale=scale, stream=_stream(stream))
+        attentionScale=scale, stream=_stream(stream),
+        status=None if status is None else _ptr(status, torch.int32, "status"))
     fn = lib().qsa_sparse_decode_bf16 if et == torch.bfloat16 else lib().qsa_sparse_decode
     _check(fn(ctypes.byref(p)))
 

@@ -59,7 +59,6 @@ qsa::RopeFreqs rope_freqs(float theta, int rot) {
   return r;
 }
 
-constexpr int kMaxListWidth = 10240;     // prefill indexer stages one list in shared memory
 constexpr int kMaxAttnListWidth = 16384;  // attention stages one list (or slice) in shared memory
 
 // Indexer arguments shared by both indexers ("Qsa Attention Plugin" constructor
@@ -172,7 +171,8 @@ qsa_status_t qsa_last_device_error(const void* workspace, void* stream, int32_t*
   return e == cudaSuccess ? ok() : cuda_fail(e, "qsa_last_device_error");
 }
 
-int32_t qsa_indexer_prefill_max_blocks(void) { return qsa::kPrefillMaxBlocks; }
+int32_t qsa_indexer_prefill_max_blocks(void) { return qsa::kPrefillMaxSeqLen; }
+int32_t qsa_indexer_prefill_max_seq_len(void) { return qsa::kPrefillMaxSeqLen; }
 
 size_t qsa_indexer_prefill_workspace_size(int32_t B, int32_t S, int32_t di, int32_t ratio) {
   if (B < 1 || S < 1 || di < 1 || ratio < 1) return 0;
@@ -216,10 +216,10 @@ qsa_status_t qsa_indexer_prefill(const QsaIndexerPrefillParams* p) {
                                        p->ropeTheta, p->rmsNormEps);
   if (s != QSA_OK) return s;
   if (p->batchSize > 65535) return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_prefill: batchSize > 65535");
-  if (p->seqLen / p->compressRatio > qsa::kPrefillMaxBlocks)
-    return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_prefill: seqLen/compressRatio = %d blocks > %d",
-                p->seqLen / p->compressRatio, qsa::kPrefillMaxBlocks);
-  if (p->topK > kMaxListWidth) return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_prefill: topK > %d", kMaxListWidth);
+  if (p->seqLen > qsa::kPrefillMaxSeqLen)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_prefill: seqLen %d > %d", p->seqLen, qsa::kPrefillMaxSeqLen);
+  if (static_cast<long long>(p->batchSize) * p->seqLen > 0x7fffffffLL)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_indexer_prefill: batchSize*seqLen exceeds 2^31 - 1 rows");
   const size_t need = qsa::indexer_prefill_workspace_bytes(p->batchSize, p->seqLen, p->headDim, p->compressRatio);
   if (!p->workspace || p->workspaceBytes < need || !aligned(p->workspace, 256))
     return fail(QSA_ERR_WORKSPACE, "qsa_indexer_prefill: workspace needs %zu bytes, 256-byte aligned", need);

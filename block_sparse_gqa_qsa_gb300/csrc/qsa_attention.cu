@@ -207,6 +207,7 @@ struct PrefillArgs {
   __half* o;
   const int32_t* indices;
   const int32_t* ctx;
+  int32_t* status;  // optional error word
   int S, Hq, Hkv, G, topK, topKpad;
   float sl2;  // attentionScale * log2(e)
 };
@@ -246,6 +247,7 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_
   // Stage the list, four loads per thread in flight; entries outside [0, L) are skipped.
   const int32_t* lst = a.indices + static_cast<size_t>(bt) * a.topK;
   int last = -1;
+  bool bad = false;
   for (int i0 = tid; i0 < a.topKpad; i0 += 4 * kThreads) {
     int jv[4];
 #pragma unroll
@@ -260,9 +262,11 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_
         const bool ok = static_cast<unsigned>(jv[u]) < static_cast<unsigned>(L);
         idx_s[i] = ok ? jv[u] : -1;
         last = ok ? i : last;
+        bad |= !ok && jv[u] != -1;
       }
     }
   }
+  if (__any_sync(kFull, bad) && lane == 0 && a.status) atomicOr(a.status, kErrBadIndex);
   last = __reduce_max_sync(kFull, last);
   if (lane == 0) misc[warp] = last;
   __syncthreads();
@@ -363,6 +367,7 @@ struct DecodeArgs {
   float* partialO;
   float* partialStats;
   int32_t* counters;
+  int32_t* status;  // optional error word
   int Hq, Hkv, G, poolHeadDim, numFlatPages, maxPagesPerSeq, topK;
   int tilesPerSplit, extraTiles;  // split s owns tilesPerSplit (+1 for s < extraTiles) whole 64-key tiles
   int slicePad;                   // slots of the longest slice
@@ -391,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_k
   const int32_t* ptV = ptK + a.maxPagesPerSeq;
   // Resolve the slice's entries to pool offsets, four per thread per pass with
   // their list loads, then their page-table loads, in flight together.
-  int last = -1;
+  int last = -1, bad = 0;
   for (int i0 = tid; i0 < a.slicePad; i0 += 4 * kThreads) {
     int jv[4], kp[4], vp[4];
 #pragma unroll
@@ -417,8 +422,13 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_k
       kofs[i] = ok ? static_cast<long long>(kp[u]) * kTokensPerPage * a.Hkv * a.poolHeadDim + within : -1;
       vofs[i] = ok ? static_cast<long long>(vp[u]) * kTokensPerPage * a.Hkv * a.poolHeadDim + within : -1;
       last = ok ? i : last;
+      const bool live = static_cast<unsigned>(j) < static_cast<unsigned>(L);
+      bad |= !live && j != -1 ? kErrBadIndex : 0;
+      bad |= live && !ok ? kErrBadPage : 0;
     }
   }
+  bad = __reduce_or_sync(kFull, static_cast<unsigned>(bad));
+  if (bad && lane == 0 && a.status) atomicOr(a.status, bad);
   last = __reduce_max_sync(kFull, last);
   if (lane == 0) misc[warp] = last;
   const __half* qsrc = a.q + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(kvh) * a.G) * kD;
@@ -595,6 +605,7 @@ cudaError_t launch_sparse_prefill(const QsaSparsePrefillParams& p, bool bf16) {
   a.o = static_cast<__half*>(p.oPtr);
   a.indices = p.indices;
   a.ctx = p.contextLengths;
+  a.status = p.status;
   a.S = p.seqLen;
   a.Hq = p.numQHeads;
   a.Hkv = p.numKVHeads;
@@ -619,6 +630,7 @@ cudaError_t launch_sparse_decode(const QsaSparseDecodeParams& p, bool bf16) {
   a.partialO = p.partialO;
   a.partialStats = p.partialStats;
   a.counters = p.splitCounters;
+  a.status = p.status;
   a.Hq = p.numQHeads;
   a.Hkv = p.numKVHeads;
   a.G = p.numQHeads / p.numKVHeads;

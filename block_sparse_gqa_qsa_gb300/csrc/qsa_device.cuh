@@ -19,6 +19,7 @@ constexpr unsigned kFull = 0xffffffffu;
 // Error bits recorded in the status word of an indexer workspace.
 constexpr int kErrWaitTimeout = 1;  // a bounded wait on a TMA barrier expired
 constexpr int kErrBadPage = 2;      // a page-table entry fell outside the pool
+constexpr int kErrBadIndex = 4;     // a list entry other than -1 fell outside [0, L)
 
 // ------------------------------------------------------------ PTX wrappers
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {

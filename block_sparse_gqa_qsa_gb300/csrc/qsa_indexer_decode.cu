@@ -390,6 +390,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
   if (warp == kConsumerWarps) {  // ---- producer: page ids 32 at a time, one TMA per 64-dim half
     int bw = 0;  // sequence of the batch's first page
     bool alive = true;
+    long long issued = 0;  // pages whose copies were issued
     for (long long base = lo; base < hi && alive; base += 32) {
       while (base >= pref[bw + 1]) ++bw;
       const long long i = base + lane;
@@ -421,6 +422,18 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
         }
         if (!__shfl_sync(kFull, ok, 0)) {
           alive = false;
+          break;
+        }
+        ++issued;
+      }
+    }
+    // The CTA must not exit while a copy still writes into its ring (consumers
+    // that gave up have left): wait, bounded, for the last page of each stage.
+    if (lane == 0) {
+      for (long long jx = issued - 1; jx >= 0 && jx >= issued - kStages; --jx) {
+        const int s = static_cast<int>(jx % kStages), n = static_cast<int>(jx / kStages);
+        if (!mbar_wait_bounded(&full[s], n & 1, kWaitLimitNs)) {
+          atomicOr(a.status, kErrWaitTimeout);
           break;
         }
       }

@@ -2,28 +2,31 @@
 // batch ("Qsa Attention Plugin", fused step 2; "spark_model/layers/ops/qsa.rs",
 // qsa_block_pool / qsa_qprep_rows / qsa_score_rows).
 //
-// Three kernels:
+// Two kernels:
 //   block_pool_kernel      one warp per complete block: mean of r raw keys ->
 //                          RMSNorm*(1+w) -> RoPE at the block start, stored
 //                          fp16 (RNE) from an exact mean and double-float
 //                          arithmetic (qsa_blockkey.cuh), so the fp16 rounding
 //                          of every key is the decision an f64 evaluation
 //                          takes; the pass is tiny (S/r * di values).
-//   prefill_score_kernel   one CTA per 8 consecutive query rows of one
-//                          sequence whose rows need a selection (n_c > budget):
-//                          index-query prep (fp32, angles reduced in integer
-//                          turns), block scores on the CUDA cores (fp32 FMA, a
-//                          register-tiled contraction of 8 rows x 8 heads
-//                          against 256-block tiles staged in shared memory),
-//                          the relu/head sum, written to the workspace (each
-//                          row's n_c scores, rows packed back to back).  Two
-//                          CTAs share an SM.
-//   prefill_topk_kernel    one warp per row: a deterministic top-`budget`
-//                          select over the row's scores (a radix select on
-//                          the score bits in per-warp histograms, exact ties
-//                          to the lower block id) and the expansion into the row's
-//                          ascending index list; rows with n_c <= budget list
-//                          0..t and rows t >= L are all -1.
+//   prefill_select_kernel  persistent, two CTAs per SM, work items of 8
+//                          consecutive rows of one sequence taken from a
+//                          counter, longest rows first.  A group whose rows
+//                          need a selection (n_c > budget) is scored by the
+//                          whole CTA: index-query prep (fp32, angles reduced
+//                          in integer turns), block scores on the CUDA cores
+//                          (fp32 FMA, a register-tiled contraction of 8 rows x
+//                          8 heads against 256-block tiles staged in shared
+//                          memory), the relu/head sum into the CTA's own score
+//                          slot and a 256-bin histogram of the score bits per
+//                          row.  Then each warp selects its row: the bin of
+//                          the cut from the histogram, radix narrowing of that
+//                          bin (over the slot, then over at most 1024 keys
+//                          staged in shared memory), exact ties to the lower
+//                          block id, and one pass that expands the kept blocks
+//                          into the ascending list.  Rows with n_c <= budget
+//                          list 0..t and rows t >= L are all -1.  Memory is
+//                          linear in S: no row's scores outlive its selection.
 #include "qsa_blockkey.cuh"
 #include "qsa_device.cuh"
 #include "qsa_internal.h"
@@ -38,6 +41,7 @@ struct PoolArgs {
   const float* wk;
   const int32_t* ctx;
   __half* kbar;
+  int32_t* queue;  // work counter of the select kernel that follows: set to zero here
   int S, nbmax, ratio, rot;
   float eps;
   RopeFreqs rf;
@@ -50,6 +54,7 @@ __global__ void __launch_bounds__(256) block_pool_kernel(const PoolArgs a) {
   const int warp = threadIdx.x >> 5;
   const int b = blockIdx.y;
   const int g = blockIdx.x * 8 + warp;
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *a.queue = 0;
   stage_rope(a.rf, rs);
   __syncthreads();
   const int L = max(0, min(a.ctx[b], a.S));  // lengths outside [0, S] are clamped, never trusted
@@ -64,20 +69,23 @@ struct SelArgs {
   const float* wq;
   const int32_t* ctx;
   const __half* kbar;
-  float* scores;  // [B][tri_offset(S)]: row t's n_c(t) scores at tri_offset(t)
+  float* scores;  // [slots][kRows][nbmax]: the block scores of the rows one CTA is selecting
+  int32_t* queue; // work counter, set to zero by the pool kernel of the same call
   int32_t* indices;
-  int S, Hi, nbmax, ratio, rot, budget, topK;
-  long long triPerSeq;
+  int B, S, Hi, nbmax, ratio, rot, budget, topK, ngroups, nitems;
   float eps;
   RopeFreqs rf;
 };
 
-constexpr int kRows = kPrefillRowsPerCta;  // rows per CTA (one warp each)
+constexpr int kRows = kPrefillRowsPerCta;  // rows per work item (one warp each)
 constexpr int kThreads = 256;
 constexpr int kTile = 256;                  // blocks per score tile (8 per lane)
 constexpr int kKC = 16;                     // key dims staged per step
 constexpr int kKS = kKC + 2;                // padded row stride: float2 reads and writes are conflict-free
 constexpr int kHI = 8;                      // heads per thread tile (Hi <= 8, extra heads are zero)
+constexpr int kBins = 256;                  // per-row histogram of the score bits, filled while scoring
+constexpr int kBinBase = 123 * 16;          // (bits >> 19) of 2^-4: bin 0 holds smaller scores, bin 255 2^12 and up
+constexpr int kCandCap = 1024;              // keys of the cut's range one warp stages in shared memory
 
 // Two fp16 values packed in 32 bits, widened to fp32.
 __device__ __forceinline__ float2 bits_to_float2(uint32_t u) {
@@ -87,40 +95,32 @@ __device__ __forceinline__ float2 bits_to_float2(uint32_t u) {
   return __half22float2(__half2(r));
 }
 
-// Start of row t's scores within its sequence: sum over u = 1..t of floor(u / r),
-// i.e. the complete-block counts n_c of rows 0..t-1.
-__host__ __device__ __forceinline__ long long tri_offset(long long t, int r) {
-  const long long k = t / r;
-  return r * k * (k - 1) / 2 + k * (t - k * r + 1);
+// Scores are sums of relu terms, so they are +0 or positive and their bits
+// order like the values.  Bin b covers one sixteenth of an octave: the
+// exponent and top four mantissa bits, over 16 octaves from 2^-4.
+__device__ __forceinline__ int score_bin(uint32_t key) {
+  return min(max(static_cast<int>(key >> 19) - kBinBase, 0), kBins - 1);
 }
 
 template <int DI>
-constexpr size_t score_smem_bytes() {
-  return sizeof(float) * (static_cast<size_t>(DI) * kRows * kHI + 2 * kTile * kKS + kRows * DI + kRows * 128);
+constexpr size_t select_smem_bytes() {
+  return sizeof(float) * (static_cast<size_t>(DI) * kRows * kHI + 2 * kTile * kKS + kRows * DI + kRows * 128 +
+                          kRows * kBins);
 }
+static_assert(kRows * kCandCap <= 2 * kTile * kKS, "candidate keys reuse the key tiles");
 
-// Block scores of 8 consecutive query rows of one sequence (rows whose n_c
-// exceeds the budget; the others need no scores), written to the workspace.
-// Two CTAs share an SM (80 KB of shared memory each at di = 128), so the
-// staging barriers and shared-memory latencies of one are covered by the other.
+// Index-query prep and block scores of the live rows [t0, t0 + nlive) of
+// sequence b against blocks [0, n_hi): each warp owns one row; the rows that
+// select (srow != nullptr) write their n_c scores to srow and count them in
+// their warp's histogram.  Every thread of the CTA takes part.
 template <int DI>
-__global__ void __launch_bounds__(kThreads, 2) prefill_score_kernel(const SelArgs a) {
-  extern __shared__ __align__(16) float smem[];
+__device__ __noinline__ void score_rows(const SelArgs& a, float* smem, int b, int t0, int nlive, int n_hi,
+                                           float* srow, int n_c, uint32_t* hist) {
   float* q_s = smem;                          // [DI][kRows][kHI] prepared queries
   float* kb_s = q_s + DI * kRows * kHI;       // [2][kTile][kKS]  block-key tile (fp32)
   float* ys_s = kb_s + 2 * kTile * kKS;       // [kRows][DI]      per-warp RoPE scratch
   float* cs_s = ys_s + kRows * DI;            // [kRows][64][2]   cos/sin per row
-
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.y;
-  const int ngroups = (a.S + kRows - 1) / kRows;
-  const int t0 = (ngroups - 1 - static_cast<int>(blockIdx.x)) * kRows;  // longest rows first
-  const int L = max(0, min(a.ctx[b], a.S));
-  const int t_end = min(t0 + kRows, L);  // live rows [t0, t_end)
-  if (t0 >= L) return;
-  const int nlive = t_end - t0;
-  const int n_hi = t_end / a.ratio;  // complete blocks seen by the group's last live row
-  if (n_hi <= a.budget) return;
 
   // ------------------------------------------------------------ query prep
   const int half = a.rot >> 1;
@@ -180,10 +180,6 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_score_kernel(const SelArg
   // Lane owns blocks lane + 32 m (m < 8) of the tile, for its warp's row
   // and all kHI heads: 64 accumulators, each a plain ascending-k FMA chain,
   // so a block's score does not depend on where the block sits in a tile.
-  const int t = t0 + warp;
-  const int n_c = (t + 1) / a.ratio;
-  const bool store = warp < nlive && n_c > a.budget;  // this row needs its scores
-  float* srow = a.scores + static_cast<size_t>(b) * a.triPerSeq + tri_offset(t, a.ratio);
   const __half* kb_g = a.kbar + static_cast<size_t>(b) * a.nbmax * DI;
   const int ntiles = (n_hi + kTile - 1) / kTile;
   for (int tile = 0; tile < ntiles; ++tile) {
@@ -243,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_score_kernel(const SelArg
         }
       }
     }
-    if (store) {
+    if (srow) {
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
         const int g = gbase + lane + 32 * m;
@@ -251,38 +247,195 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_score_kernel(const SelArg
           float sc = 0.f;
 #pragma unroll
           for (int h = 0; h < kHI; ++h) sc += acc[m][h] > 0.f ? acc[m][h] : 0.f;
-          srow[g] = sc;
+          srow[g] = sc;  // read back later by this same lane only
+          atomicAdd(hist + score_bin(__float_as_uint(sc)), 1u);
         }
       }
     }
   }
 }
 
-// ------------------------------------ select + expand, one warp per row
-// Lane l holds the scores of blocks l + 32 m.  Keys are the score bits + 1
-// (order-preserving for scores >= 0; 0 marks blocks past the row's n_c).
-// A radix select finds the cut T with count(key > T) < budget <=
-// count(key >= T): 8-bit digits of (key - lo) over the range still in play,
-// counted in a per-warp shared-memory histogram, narrow the range to the bin
-// holding the cut (at most four passes), and once that bin holds at most 32
-// keys their exact order is taken by pairwise counts.  The blocks above T are
-// kept, and of those equal to T the lowest ids, so the kept set is the top
-// `budget` by (score desc, id asc).  Walking m upwards visits ids in ascending
-// order, so ballots compact the kept blocks straight into the ascending list.
-// Rows t >= L are all -1 and rows with n_c <= budget list 0..t.  R: the
-// compress ratio fixed at compile time (the r token ids of a kept block are
-// then straight-line stores), or 0 to read it from the arguments.
-template <int VPT, int R>
-__global__ void __launch_bounds__(kThreads) prefill_topk_kernel(const SelArgs a) {
-  constexpr int KPL = kThreads * VPT / 32;
+// The bin holding the need-th largest key of a warp's 256-bin histogram
+// (lane l owns bins 8l .. 8l+7): T, the count of keys in higher bins, and the
+// count in bin T.  Every lane gets all three; need must not exceed the total.
+__device__ __forceinline__ void find_bin(const uint32_t* hist, int need, int& T, int& above, int& nT) {
+  const int lane = threadIdx.x & 31;
+  const uint4 h0 = *reinterpret_cast<const uint4*>(hist + lane * 8);
+  const uint4 h1 = *reinterpret_cast<const uint4*>(hist + lane * 8 + 4);
+  const int hb[8] = {static_cast<int>(h0.x), static_cast<int>(h0.y), static_cast<int>(h0.z), static_cast<int>(h0.w),
+                     static_cast<int>(h1.x), static_cast<int>(h1.y), static_cast<int>(h1.z), static_cast<int>(h1.w)};
+  int own = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) own += hb[j];
+  int suffix = own;  // keys in the bins of lanes >= this one
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_down_sync(kFull, suffix, o);
+    if (lane + o < 32) suffix += y;
+  }
+  int run = suffix - own, t = -1, ab = 0, n = 0;
+#pragma unroll
+  for (int j = 7; j >= 0; --j) {
+    if (run < need && run + hb[j] >= need) {
+      t = lane * 8 + j;
+      ab = run;
+      n = hb[j];
+    }
+    run += hb[j];
+  }
+  const int src = __ffs(__ballot_sync(kFull, t >= 0)) - 1;  // exactly one lane holds the bin
+  T = __shfl_sync(kFull, t, src);
+  above = __shfl_sync(kFull, ab, src);
+  nT = __shfl_sync(kFull, n, src);
+}
+
+// Keys of one row for the radix narrowing: the row's n_c scores in global
+// memory (each lane reads back only the blocks it wrote, g = lane mod 32), or
+// the warp's staged candidates in shared memory.
+struct GlobalKeys {
+  const float* srow;
+  int n;
+  template <class F>
+  __device__ __forceinline__ void each(F&& f) const {
+    const int lane = threadIdx.x & 31;
+    constexpr int U = 8;
+    for (int g0 = 0; g0 < n; g0 += 32 * U) {
+      uint32_t k[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int g = g0 + 32 * u + lane;
+        k[u] = g < n ? __float_as_uint(srow[g]) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (g0 + 32 * u + lane < n) f(k[u]);
+    }
+  }
+};
+struct SharedKeys {
+  const uint32_t* keys;
+  int n;
+  template <class F>
+  __device__ __forceinline__ void each(F&& f) const {
+    for (int i = threadIdx.x & 31; i < n; i += 32) f(keys[i]);
+  }
+};
+
+// Narrows the key range [blo, blo + span], which holds nT keys of which the
+// `need` largest are kept, through 256-bin histograms of (key - blo) >> sh in
+// the warp's shared memory, until it holds at most `limit` keys or one value.
+template <class Keys>
+__device__ __forceinline__ void narrow(const Keys& keys, uint32_t* hist, uint32_t& blo, uint32_t& span, int& need,
+                                       int& nT, int limit) {
+  const int lane = threadIdx.x & 31;
+  while (nT > limit && span != 0u) {
+    const int sh = max(0, 24 - static_cast<int>(__clz(span)));  // span >> sh < 256
+#pragma unroll
+    for (int j = 0; j < 8; ++j) hist[lane * 8 + j] = 0u;
+    __syncwarp();
+    const uint32_t lo = blo, sp = span;
+    keys.each([&](uint32_t k) {
+      const uint32_t d = k - lo;  // keys below lo wrap past span
+      if (d <= sp) atomicAdd(hist + (d >> sh), 1u);
+    });
+    __syncwarp();
+    int T, above, n;
+    find_bin(hist, need, T, above, n);
+    need -= above;
+    nT = n;
+    blo += static_cast<uint32_t>(T) << sh;
+    span = sh == 0 ? 0u : min(span - (static_cast<uint32_t>(T) << sh), (1u << sh) - 1u);
+    __syncwarp();  // every lane has read the histogram
+  }
+}
+
+// Row t of sequence b, whose n_c > budget scores sit in srow and are counted
+// in hist: the cut key and how many keys equal to it are kept (lowest ids
+// first), so that the kept set is the top `budget` by (score desc, id asc).
+__device__ __forceinline__ void row_cut(const float* srow, int n_c, int budget, uint32_t* hist, uint32_t* cand,
+                                        uint32_t& cut, int& quota) {
+  const int lane = threadIdx.x & 31;
+  const unsigned below = (1u << lane) - 1u;
+  int T, above, nT;
+  find_bin(hist, budget, T, above, nT);
+  int need = budget - above;
+  // bin T as a key range; the end bins are open
+  uint32_t blo = T == 0 ? 0u : static_cast<uint32_t>(T + kBinBase) << 19;
+  uint32_t span = T == kBins - 1 ? 0xffffffffu - blo : (static_cast<uint32_t>(T + kBinBase + 1) << 19) - 1u - blo;
+  __syncwarp();  // the histogram is read; narrowing reuses it
+  const GlobalKeys gk{srow, n_c};
+  narrow(gk, hist, blo, span, need, nT, kCandCap);
+  if (span == 0u) {
+    cut = blo;
+    quota = need;
+    return;
+  }
+  // stage the range's nT <= kCandCap keys, then narrow in shared memory
+  {
+    int at = 0;
+    constexpr int U = 8;
+    for (int g0 = 0; g0 < n_c; g0 += 32 * U) {
+      uint32_t k[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int g = g0 + 32 * u + lane;
+        k[u] = g < n_c ? __float_as_uint(srow[g]) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const bool in = g0 + 32 * u + lane < n_c && k[u] - blo <= span;
+        const unsigned m = __ballot_sync(kFull, in);
+        const int e = at + __popc(m & below);
+        if (in && e < kCandCap) cand[e] = k[u];
+        at += __popc(m);
+      }
+    }
+    __syncwarp();
+  }
+  const SharedKeys sk{cand, min(nT, kCandCap)};
+  narrow(sk, hist, blo, span, need, nT, 32);
+  if (span == 0u) {
+    cut = blo;
+    quota = need;
+    return;
+  }
+  // at most 32 keys left in range: one per lane, then each one's count of larger and equal keys
+  uint32_t* last = hist;
+  {
+    int at = 0;
+    for (int i0 = 0; i0 < sk.n; i0 += 32) {
+      const int i = i0 + lane;
+      const uint32_t k = i < sk.n ? cand[i] : 0u;
+      const bool in = i < sk.n && k - blo <= span;
+      const unsigned m = __ballot_sync(kFull, in);
+      const int e = at + __popc(m & below);
+      if (in && e < 32) last[e] = k;
+      at += __popc(m);
+    }
+  }
+  __syncwarp();
+  nT = min(nT, 32);
+  const uint32_t mine = lane < nT ? last[lane] : 0u;
+  int gt = 0, eq = 0;
+  for (int j = 0; j < nT; ++j) {
+    const uint32_t v = __shfl_sync(kFull, mine, j);
+    gt += v > mine ? 1 : 0;
+    eq += v == mine ? 1 : 0;
+  }
+  const int hit = __ffs(__ballot_sync(kFull, lane < nT && gt < need && need <= gt + eq)) - 1;
+  cut = __shfl_sync(kFull, mine, hit);
+  quota = need - __shfl_sync(kFull, gt, hit);
+  __syncwarp();
+}
+
+// Writes row t's list: all -1 for t >= L; 0..t when every complete block is
+// kept; else the kept blocks in ascending order (from srow, cut, quota), each
+// expanded to its r token ids, then the causal tail r*n_c .. t, then -1.
+template <int R>
+__device__ __forceinline__ void write_row(const SelArgs& a, int32_t* out, int t, int L, const float* srow, uint32_t cut,
+                                          int quota) {
   const int ratio = R > 0 ? R : a.ratio;
-  __shared__ __align__(16) uint32_t hist_s[kThreads / 32][256];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.y;
-  const int t = blockIdx.x * kRows + warp;
-  if (t >= a.S) return;
-  const int L = max(0, min(a.ctx[b], a.S));
-  int32_t* out = a.indices + (static_cast<size_t>(b) * a.S + t) * a.topK;
+  const int lane = threadIdx.x & 31;
   if (t >= L) {
     for (int i = lane; i < a.topK; i += 32) out[i] = -1;
     return;
@@ -292,193 +445,118 @@ __global__ void __launch_bounds__(kThreads) prefill_topk_kernel(const SelArgs a)
     for (int i = lane; i < a.topK; i += 32) out[i] = i <= t ? i : -1;
     return;
   }
-  const float* srow = a.scores + static_cast<size_t>(b) * a.triPerSeq + tri_offset(t, ratio);
-  // Keys live in registers, KPL per lane; only the first ceil(n_c / 32) of them
-  // can be non-zero, so every pass skips the groups of 8 past that (a
-  // warp-uniform branch, no instructions issued for them).
-  constexpr int KG = 8;
-  const int mlim = (n_c + 31) / 32;
-  uint32_t key[KPL];
-#pragma unroll
-  for (int c = 0; c < KPL / KG; ++c) {
-#pragma unroll
-    for (int k = 0; k < KG; ++k) {
-      const int g = lane + 32 * (c * KG + k);
-      key[c * KG + k] = c * KG < mlim && g < n_c ? __float_as_uint(__ldcg(srow + g)) + 1u : 0u;
-    }
-  }
-  // The cut key `lo` (the budget-th largest key) and `quota`, the number of
-  // keys equal to it that are kept (lowest ids first).  Score-0 blocks (key 1) sit below
-  // every positive one; among the positive keys a radix select refines a
-  // 256-bin histogram of (key - lo) >> sh in this warp's shared memory until
-  // the bin holding the cut has at most 32 keys (or is one key value), whose
-  // exact order is then taken by counting.
-  uint32_t* hist = hist_s[warp];
-  uint32_t kmx = 0u, kmn = 0xffffffffu;
-  int npos = 0;
-#pragma unroll
-  for (int c = 0; c < KPL / KG; ++c) {
-    if (c * KG < mlim) {
-#pragma unroll
-      for (int k = 0; k < KG; ++k) {
-        const uint32_t kk = key[c * KG + k];
-        if (kk >= 2u) {
-          kmx = max(kmx, kk);
-          kmn = min(kmn, kk);
-          ++npos;
-        }
-      }
-    }
-  }
-  kmx = __reduce_max_sync(kFull, kmx);
-  kmn = __reduce_min_sync(kFull, kmn);
-  npos = static_cast<int>(__reduce_add_sync(kFull, static_cast<unsigned>(npos)));
-  uint32_t lo;
-  int quota;
-  if (npos < a.budget) {  // every positive block is kept, then score-0 blocks by lowest id
-    lo = 1u;
-    quota = a.budget - npos;
-  } else {
-    uint32_t blo = kmn, span = kmx - kmn;  // keys of the current bin: [blo, blo + span]
-    int need = a.budget;                   // keys of the current bin to keep
-    for (;;) {
-      const int sh = max(0, 24 - static_cast<int>(__clz(span)));  // span >> sh < 256
-#pragma unroll
-      for (int j = 0; j < 8; ++j) hist[lane * 8 + j] = 0u;
-      __syncwarp();
-#pragma unroll
-      for (int c = 0; c < KPL / KG; ++c) {
-        if (c * KG < mlim) {
-#pragma unroll
-          for (int k = 0; k < KG; ++k) {
-            const uint32_t d = key[c * KG + k] - blo;  // keys below blo wrap past span
-            if (d <= span) atomicAdd(hist + (d >> sh), 1u);
-          }
-        }
-      }
-      __syncwarp();
-      // lane l owns bins 8l .. 8l+7; `run` counts the keys in higher bins
-      const uint4 h0 = *reinterpret_cast<const uint4*>(hist + lane * 8);
-      const uint4 h1 = *reinterpret_cast<const uint4*>(hist + lane * 8 + 4);
-      const int hb[8] = {static_cast<int>(h0.x), static_cast<int>(h0.y), static_cast<int>(h0.z), static_cast<int>(h0.w),
-                         static_cast<int>(h1.x), static_cast<int>(h1.y), static_cast<int>(h1.z), static_cast<int>(h1.w)};
-      int own = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) own += hb[j];
-      int suffix = own;  // keys in the bins of lanes >= this one
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_down_sync(kFull, suffix, o);
-        if (lane + o < 32) suffix += y;
-      }
-      int run = suffix - own, T = -1, above = 0, nT = 0;
-#pragma unroll
-      for (int j = 7; j >= 0; --j) {
-        if (run < need && run + hb[j] >= need) {
-          T = lane * 8 + j;
-          above = run;
-          nT = hb[j];
-        }
-        run += hb[j];
-      }
-      const int src = __ffs(__ballot_sync(kFull, T >= 0)) - 1;  // exactly one lane holds the bin
-      T = __shfl_sync(kFull, T, src);
-      need -= __shfl_sync(kFull, above, src);
-      nT = __shfl_sync(kFull, nT, src);
-      blo += static_cast<uint32_t>(T) << sh;
-      span = sh == 0 ? 0u : min(span - (static_cast<uint32_t>(T) << sh), (1u << sh) - 1u);
-      __syncwarp();  // every lane has read the histogram
-      if (span == 0u) {  // one key value: its `need` lowest ids
-        lo = blo;
-        quota = need;
-        break;
-      }
-      if (nT <= 32) {
-        // the bin's keys, one per lane, then each one's count of larger and equal keys
-        uint32_t* cand = hist;
-        int at = 0;
-#pragma unroll
-        for (int c = 0; c < KPL / KG; ++c) {
-          if (c * KG < mlim) {
-#pragma unroll
-            for (int k = 0; k < KG; ++k) {
-              const bool in = key[c * KG + k] - blo <= span;
-              const unsigned m = __ballot_sync(kFull, in);
-              if (in) cand[at + __popc(m & ((1u << lane) - 1u))] = key[c * KG + k];
-              at += __popc(m);
-            }
-          }
-        }
-        __syncwarp();
-        const uint32_t mine = lane < nT ? cand[lane] : 0u;
-        int gt = 0, eq = 0;
-        for (int j = 0; j < nT; ++j) {
-          const uint32_t v = __shfl_sync(kFull, mine, j);
-          gt += v > mine ? 1 : 0;
-          eq += v == mine ? 1 : 0;
-        }
-        const int hit = __ffs(__ballot_sync(kFull, lane < nT && gt < need && need <= gt + eq)) - 1;
-        lo = __shfl_sync(kFull, mine, hit);
-        quota = need - __shfl_sync(kFull, gt, hit);
-        break;
-      }
-    }
-  }
-  int pos = 0;
   const unsigned below = (1u << lane) - 1u;
+  int pos = 0;
+  constexpr int U = 4;
+  for (int g0 = 0; g0 < n_c; g0 += 32 * U) {
+    uint32_t k[U];
 #pragma unroll
-  for (int c = 0; c < KPL / KG; ++c) {
-    if (c * KG < mlim) {
+    for (int u = 0; u < U; ++u) {
+      const int g = g0 + 32 * u + lane;
+      k[u] = g < n_c ? __float_as_uint(srow[g]) : 0u;
+    }
 #pragma unroll
-      for (int k = 0; k < KG; ++k) {
-        const int m = c * KG + k;
-        const bool eq = key[m] == lo;
-        const unsigned eqm = __ballot_sync(kFull, eq);
-        const bool take = key[m] > lo || (eq && __popc(eqm & below) < quota);
-        quota = max(0, quota - __popc(eqm));
-        const unsigned tm = __ballot_sync(kFull, take);
-        if (take) {
-          const int at = (pos + __popc(tm & below)) * ratio, g = lane + 32 * m;
+    for (int u = 0; u < U; ++u) {
+      const int g = g0 + 32 * u + lane;
+      const bool valid = g < n_c;
+      const bool eq = valid && k[u] == cut;
+      const unsigned eqm = __ballot_sync(kFull, eq);
+      const bool take = valid && (k[u] > cut || (eq && __popc(eqm & below) < quota));
+      quota = max(0, quota - __popc(eqm));
+      const unsigned tm = __ballot_sync(kFull, take);
+      if (take && (pos + __popc(tm & below) + 1) * ratio <= a.topK) {  // the row holds budget * r <= topK
+        const int at = (pos + __popc(tm & below)) * ratio;
+        if (R > 0) {
+#pragma unroll
+          for (int j = 0; j < (R > 0 ? R : 1); ++j) out[at + j] = g * ratio + j;
+        } else {
           for (int j = 0; j < ratio; ++j) out[at + j] = g * ratio + j;
         }
-        pos += __popc(tm);
       }
+      pos += __popc(tm);
     }
   }
-  const int head = pos * ratio;
+  const int head = min(pos * ratio, a.topK);
   for (int i = head + lane; i < a.topK; i += 32) {
     const int j = n_c * ratio + (i - head);
     out[i] = j <= t ? j : -1;
   }
 }
 
+// Persistent: CTAs take work items from a counter.  Item i is the group of 8
+// rows t0 .. t0+7 of sequence i mod B, t0 = 8 * (ngroups - 1 - i / B): the
+// groups of every sequence from the last rows down, so the longest rows start
+// first and the run ends on rows that only write lists.  Each warp owns one
+// row of the group.  A group whose last live row sees more than `budget`
+// complete blocks is scored by the whole CTA (query prep, then the register
+// tiled contraction against 256-block tiles of fp32 keys staged in shared
+// memory); each selecting row's scores go to the CTA's own slot of the
+// workspace and into its warp's 256-bin histogram.  Each warp then finds its
+// row's cut (the bin from the histogram, then narrowing passes over the
+// scores, the last ones on at most kCandCap keys staged in shared memory)
+// and writes its list in one more pass.  Two CTAs share an SM, so one's
+// selection and list writes overlap the other's scoring.
+template <int DI, int R>
+__global__ void __launch_bounds__(kThreads, 2) prefill_select_kernel(const SelArgs a) {
+  extern __shared__ __align__(16) float smem[];
+  __shared__ int item_s[2];
+  float* kb_s = smem + DI * kRows * kHI;
+  uint32_t* hist_s = reinterpret_cast<uint32_t*>(kb_s + 2 * kTile * kKS + kRows * DI + kRows * 128);
+  const int ratio = R > 0 ? R : a.ratio;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint32_t* hist = hist_s + warp * kBins;
+  uint32_t* cand = reinterpret_cast<uint32_t*>(kb_s) + warp * kCandCap;  // valid once scoring is done
+  float* srow = a.scores + (static_cast<size_t>(blockIdx.x) * kRows + warp) * a.nbmax;
+  if (tid == 0) item_s[0] = atomicAdd(a.queue, 1);
+  __syncthreads();
+  for (int it = 0;; ++it) {
+    const int item = item_s[it & 1];
+    if (item >= a.nitems) break;
+    int nxt = 0;
+    if (tid == 0) nxt = atomicAdd(a.queue, 1);  // the next item, waited for only at the end
+    const int pos = item / a.B, b = item - pos * a.B;
+    const int t0 = (a.ngroups - 1 - pos) * kRows;
+    const int L = max(0, min(__ldg(a.ctx + b), a.S));
+    const int nlive = max(0, min(t0 + kRows, L) - t0);
+    const int n_hi = (t0 + nlive) / ratio;  // complete blocks seen by the group's last live row
+    const int t = t0 + warp;
+    const int n_c = (t + 1) / ratio;
+    const bool selects = warp < nlive && n_c > a.budget;
+    uint32_t cut = 0u;
+    int quota = 0;
+    if (nlive > 0 && n_hi > a.budget) {  // uniform over the CTA
+#pragma unroll
+      for (int j = 0; j < kBins / 32; ++j) hist[lane * (kBins / 32) + j] = 0u;
+      score_rows<DI>(a, smem, b, t0, nlive, n_hi, selects ? srow : nullptr, n_c, hist);
+      __syncthreads();  // the key tiles are free: they hold the candidate keys from here on
+      if (selects) row_cut(srow, n_c, a.budget, hist, cand, cut, quota);
+    }
+    if (t < a.S) write_row<R>(a, a.indices + (static_cast<size_t>(b) * a.S + t) * a.topK, t, L, srow, cut, quota);
+    if (tid == 0) item_s[(it + 1) & 1] = nxt;
+    __syncthreads();
+  }
+}
+
 template <int DI>
-cudaError_t launch_score(const SelArgs& a, int B, cudaStream_t st) {
-  constexpr size_t smem = score_smem_bytes<DI>();
-  static const cudaError_t attr = cudaFuncSetAttribute(
-      prefill_score_kernel<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (attr != cudaSuccess) return attr;
-  dim3 grid((a.S + kRows - 1) / kRows, B);
-  prefill_score_kernel<DI><<<grid, kThreads, smem, st>>>(a);
-  return cudaGetLastError();
-}
-
-template <int VPT>
-cudaError_t launch_topk(const SelArgs& a, int B, cudaStream_t st) {
-  dim3 grid((a.S + kRows - 1) / kRows, B);
+cudaError_t launch_select(const SelArgs& a, cudaStream_t st) {
+  constexpr size_t smem = select_smem_bytes<DI>();
+  cudaError_t e = cudaSuccess;
+  if (a.ratio == 4) {
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        prefill_select_kernel<DI, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    e = attr;
+  } else {
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        prefill_select_kernel<DI, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    e = attr;
+  }
+  if (e != cudaSuccess) return e;
+  const int grid = min(min(kPrefillScoreSlots, 2 * sm_count()), a.nitems);
   if (a.ratio == 4)
-    prefill_topk_kernel<VPT, 4><<<grid, kThreads, 0, st>>>(a);
+    prefill_select_kernel<DI, 4><<<grid, kThreads, smem, st>>>(a);
   else
-    prefill_topk_kernel<VPT, 0><<<grid, kThreads, 0, st>>>(a);
+    prefill_select_kernel<DI, 0><<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();
-}
-
-cudaError_t launch_topk_any(const SelArgs& a, int B, cudaStream_t st) {
-  const int nb = a.nbmax;
-  if (nb <= 2 * kThreads) return launch_topk<2>(a, B, st);
-  if (nb <= 4 * kThreads) return launch_topk<4>(a, B, st);
-  if (nb <= 8 * kThreads) return launch_topk<8>(a, B, st);
-  return launch_topk<16>(a, B, st);
 }
 
 }  // namespace
@@ -536,33 +614,39 @@ __global__ void __launch_bounds__(256) handoff_kernel(const HandoffArgs a) {
   }
 }
 
-// Workspace: status word, block keys fp16 [B][S/r][di], then the block scores
-// fp32 of every row, per sequence in row order (tri_offset(S) floats each).
+// Workspace: status word, block keys fp16 [B][S/r][di], the select kernel's
+// work counter, then one score slot per select CTA: fp32 [kRows][S/r], the
+// scores of the rows that CTA is selecting.  Linear in S, independent of B.
 size_t kbar_region_bytes(int B, int S, int di, int ratio) {
   return (static_cast<size_t>(B) * (S / ratio) * di * sizeof(__half) + 255) / 256 * 256;
 }
+constexpr size_t kQueueBytes = 256;
 size_t indexer_prefill_workspace_bytes(int B, int S, int di, int ratio) {
-  return kStatusBytes + kbar_region_bytes(B, S, di, ratio) +
-         static_cast<size_t>(B) * static_cast<size_t>(tri_offset(S, ratio)) * sizeof(float);
+  return kStatusBytes + kbar_region_bytes(B, S, di, ratio) + kQueueBytes +
+         static_cast<size_t>(kPrefillScoreSlots) * kRows * static_cast<size_t>(S / ratio) * sizeof(float);
 }
 
 cudaError_t launch_indexer_prefill(const QsaIndexerPrefillParams& p, const RopeFreqs& rf) {
   cudaStream_t st = static_cast<cudaStream_t>(p.stream);
   const int nbmax = p.seqLen / p.compressRatio;
-  __half* kbar = reinterpret_cast<__half*>(static_cast<char*>(p.workspace) + kStatusBytes);
-  if (nbmax > 0) {
+  char* ws = static_cast<char*>(p.workspace);
+  __half* kbar = reinterpret_cast<__half*>(ws + kStatusBytes);
+  const size_t kb_bytes = kbar_region_bytes(p.batchSize, p.seqLen, p.headDim, p.compressRatio);
+  int32_t* queue = reinterpret_cast<int32_t*>(ws + kStatusBytes + kb_bytes);
+  {  // always launched: it also zeroes the select kernel's work counter
     PoolArgs pa;
     pa.idxK = static_cast<const __half*>(p.idxK);
     pa.wk = p.kNormW;
     pa.ctx = p.contextLengths;
     pa.kbar = kbar;
+    pa.queue = queue;
     pa.S = p.seqLen;
     pa.nbmax = nbmax;
     pa.ratio = p.compressRatio;
     pa.rot = p.rotDim;
     pa.eps = p.rmsNormEps;
     pa.rf = rf;
-    dim3 grid((nbmax + 7) / 8, p.batchSize);
+    dim3 grid(max(1, (nbmax + 7) / 8), p.batchSize);
     if (p.headDim == 64)
       block_pool_kernel<64><<<grid, 256, 0, st>>>(pa);
     else
@@ -575,10 +659,10 @@ cudaError_t launch_indexer_prefill(const QsaIndexerPrefillParams& p, const RopeF
   sa.wq = p.qNormW;
   sa.ctx = p.contextLengths;
   sa.kbar = kbar;
-  sa.scores = reinterpret_cast<float*>(static_cast<char*>(p.workspace) + kStatusBytes +
-                                       kbar_region_bytes(p.batchSize, p.seqLen, p.headDim, p.compressRatio));
-  sa.triPerSeq = tri_offset(p.seqLen, p.compressRatio);
+  sa.scores = reinterpret_cast<float*>(ws + kStatusBytes + kb_bytes + kQueueBytes);
+  sa.queue = queue;
   sa.indices = p.indices;
+  sa.B = p.batchSize;
   sa.S = p.seqLen;
   sa.Hi = p.numHeads;
   sa.nbmax = nbmax;
@@ -586,11 +670,11 @@ cudaError_t launch_indexer_prefill(const QsaIndexerPrefillParams& p, const RopeF
   sa.rot = p.rotDim;
   sa.budget = p.budget;
   sa.topK = p.topK;
+  sa.ngroups = (p.seqLen + kRows - 1) / kRows;
+  sa.nitems = sa.ngroups * p.batchSize;
   sa.eps = p.rmsNormEps;
   sa.rf = rf;
-  const cudaError_t e = p.headDim == 64 ? launch_score<64>(sa, p.batchSize, st) : launch_score<128>(sa, p.batchSize, st);
-  if (e != cudaSuccess) return e;
-  return launch_topk_any(sa, p.batchSize, st);
+  return p.headDim == 64 ? launch_select<64>(sa, st) : launch_select<128>(sa, st);
 }
 
 cudaError_t launch_indexer_handoff(const QsaIndexerHandoffParams& p) {

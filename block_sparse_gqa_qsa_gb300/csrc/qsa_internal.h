@@ -29,7 +29,9 @@ struct RopeFreqs {
 
 // Prefill indexer -----------------------------------------------------------
 constexpr int kPrefillRowsPerCta = 8;      // query rows sharing one CTA's block-key tiles
-constexpr int kPrefillMaxBlocks = 4096;    // block scores of a row group kept in shared memory
+constexpr int kPrefillScoreSlots = 320;    // CTAs of the persistent select kernel at most (2 per SM), one
+                                           // workspace score slot of 8 rows x S/r floats each
+constexpr int kPrefillMaxSeqLen = 1 << 24; // rows per sequence: int32 block and token ids with headroom
 size_t indexer_prefill_workspace_bytes(int B, int S, int di, int ratio);
 cudaError_t launch_indexer_prefill(const QsaIndexerPrefillParams& p, const RopeFreqs& rf);
 cudaError_t launch_indexer_handoff(const QsaIndexerHandoffParams& p);

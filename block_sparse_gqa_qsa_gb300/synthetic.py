@@ -98,6 +98,15 @@ DECODE_LONG = DecodeConfig("decode_long_B8_L512k", B=8, Hq=64, Hkv=8, D=128, Hi=
                            budget=512, ctx_lo=524288, ctx_hi=524288, max_ctx=524288, seed=1005)
 BENCH_CONFIGS = (PREFILL_TINY, PREFILL_8K, PREFILL_RAGGED, DECODE_32, DECODE_LONG)
 
+# Prefill past 16K rows: the 28K prefill the qsa.rs page times (doc comment of
+# qsa_score_rows_tc), 64K, and a ragged batch whose rows see up to 5000 blocks.
+PREFILL_28K = PrefillConfig("prefill_S28672", B=1, S=28672, Hq=32, Hkv=4, D=128, Hi=8, di=128, rot=64,
+                            ratio=4, budget=512, seed=28)
+PREFILL_64K = PrefillConfig("prefill_S65536", B=1, S=65536, Hq=32, Hkv=4, D=128, Hi=8, di=128, rot=64,
+                            ratio=4, budget=512, seed=64)
+PREFILL_LONG_RAGGED = PrefillConfig("prefill_ragged_B2_S20000", B=2, S=20000, Hq=32, Hkv=4, D=128, Hi=8,
+                                    di=128, rot=64, ratio=4, budget=512, ctx_lo=12000, ctx_hi=20000, seed=20)
+
 # Smaller shapes for element-by-element parity (several tiles and a ragged tail).
 PREFILL_PARITY = PrefillConfig("prefill_parity", B=2, S=3001, Hq=16, Hkv=2, D=128, Hi=8, di=128, rot=64,
                                ratio=4, budget=128, ctx_lo=1500, ctx_hi=3001, seed=7)

@@ -71,7 +71,10 @@ typedef enum {
  * (stored fp16), queries are RMSNorm*(1+qNormW) -> RoPE at t (fp32), and the
  * score of block g is sum_h relu(q_h . kbar_g) / sqrt(headDim).  When
  * n_c <= budget every block is kept; exact score ties go to the lower block
- * id.  Lists are written in ascending token order; rows t >= L are all -1. */
+ * id.  Lists are written in ascending token order; rows t >= L are all -1.
+ * Limits: seqLen <= qsa_indexer_prefill_max_seq_len() (2^24), batchSize *
+ * seqLen < 2^31, batchSize <= 65535; other shapes return QSA_ERR_UNSUPPORTED.
+ * Calls that share one workspace must not run concurrently (one stream). */
 typedef struct {
   const void* idxQ;              /* fp16 [B, S, numHeads, headDim] raw index queries     */
   const void* idxK;              /* fp16 [B, S, headDim] raw index keys (one shared head)  */
@@ -79,10 +82,12 @@ typedef struct {
   const float* kNormW;           /* fp32 [headDim]                                          */
   const int32_t* contextLengths; /* int32 [B], 0 <= L <= S                                  */
   int32_t* indices;              /* out int32 [B, S, topK]                                  */
-  void* workspace;               /* >= qsa_indexer_prefill_workspace_size(), 256-B aligned:
-                                    status word, block keys, and the fp32 block scores of
-                                    every row (sum over t < S of floor((t+1)/r) per
-                                    sequence, ~S^2/(2r): 34 MB at S = 8192, r = 4)        */
+  void* workspace;               /* >= qsa_indexer_prefill_workspace_size(), 256-B aligned,
+                                    no initial contents required: status word, block keys
+                                    fp16 [B, S/r, headDim], a work counter, and 320 score
+                                    slots of 8 x S/r fp32 (the rows being selected), i.e.
+                                    ~(2*B*headDim/r + 2560/r*4) bytes per row of S: 21 MB
+                                    at B = 1, S = 8192, 336 MB at S = 131072. Linear in S */
   size_t workspaceBytes;
   int32_t batchSize;             /* B                                                       */
   int32_t seqLen;                /* S (padded length)                                       */
@@ -236,7 +241,13 @@ typedef struct {
  * list: no positional mask is applied.  Output rows t >= L are exact zeros;
  * a live row whose list has no valid entry is zero too.  K/V rows are only
  * read where a list names them; an entry outside [0, L) is skipped (a list
- * must only name live tokens). */
+ * must only name live tokens).
+ * status (not on the pages; may be NULL): a device int32 that the kernel ORs
+ * error bits into and never clears -- bit 2 (value 4): an entry other than -1
+ * fell outside [0, L) and was skipped.  Zero it before the calls it should
+ * cover; read it once the stream has reached them (qsa_last_device_error
+ * reads it as well).  A NULL status records nothing; the entries are
+ * skipped all the same. */
 typedef struct {
   const void* qPtr;              /* fp16 [B, S, numQHeads, headDim]  */
   const void* kPtr;              /* fp16 [B, S, numKVHeads, headDim] */
@@ -252,6 +263,7 @@ typedef struct {
   int32_t topK;
   float attentionScale;          /* multiplier of q . k (not assumed 1/sqrt(D)) */
   void* stream;
+  int32_t* status;               /* optional device error word (see above), or NULL */
 } QsaSparsePrefillParams;
 
 /* Split-K sparse GQA decode ("Cute Dsl Qsa Sparse Runner", struct
@@ -261,7 +273,12 @@ typedef struct {
  * is cut into kMaxSplits = 8 contiguous slices; each slice writes an fp32
  * partial (O, m, l) and the last slice to finish merges the eight partials
  * into oPtr and resets its counter to zero.  splitCounters MUST be zero on
- * entry (zero-fill the buffer once; every call leaves it zeroed). */
+ * entry (zero-fill the buffer once; every call leaves it zeroed).
+ * status (not on the pages; may be NULL): a device int32 that the kernels OR
+ * error bits into and never clear -- bit 1 (value 2): a list entry's page id
+ * fell outside [0, numFlatPages); bit 2 (value 4): an entry other than -1
+ * fell outside [0, L).  Such entries are skipped (never read) whether or not
+ * status is given. */
 typedef struct {
   const void* qPtr;              /* fp16 [B, 1, numQHeads, headDim] */
   const void* kvPoolPtr;         /* fp16 [numFlatPages, 128, numKVHeads, poolHeadDim] */
@@ -282,6 +299,7 @@ typedef struct {
   int32_t topK;
   float attentionScale;
   void* stream;
+  int32_t* status;               /* optional device error word (see above), or NULL */
 } QsaSparseDecodeParams;
 
 /* ------------------------------------------------------------ entry points */
@@ -317,9 +335,13 @@ QSA_API qsa_status_t qsa_sparse_decode_bf16(const QsaSparseDecodeParams* params)
  *     when the library's code is loaded onto that GPU).  It holds
  *     batchSize * numKVHeads <= 256 (sequence, KV head) pairs at headDim 128;
  *     larger shapes return QSA_ERR_UNSUPPORTED and launch nothing.
- *   - The first call on each GPU (made with that GPU current) looks up the
- *     scratch's address and clears its counters on `stream`.  Make that first
- *     call before any stream capture.  Later calls only launch the kernels.
+ *   - The first call in each CUDA context (per GPU: its primary context, which
+ *     the runtime uses) looks up the scratch's address and clears its
+ *     counters on `stream`.  Make that first call before any stream capture.
+ *     Later calls in the same context only launch the kernels.  After
+ *     cudaDeviceReset the next call sees a new context, where the library's
+ *     code and scratch are loaded afresh, and does the set-up again (so that
+ *     call too belongs before any capture).
  *   - All calls on one GPU within a process share that scratch.  Two calls
  *     whose kernels may run at the same time (different streams, or
  *     different threads) race and corrupt each other's outputs: issue them on
@@ -391,9 +413,12 @@ QSA_API int32_t qsa_sparse_prefill_can_implement(int32_t numQHeads, int32_t numK
 QSA_API int32_t qsa_sparse_decode_can_implement(int32_t numQHeads, int32_t numKVHeads, int32_t headDim,
                                         int32_t poolHeadDim);
 
-/* The prefill indexer keeps a row group's block scores in shared memory:
- * floor(seqLen / compressRatio) may not exceed this many blocks (4096, i.e.
- * seqLen up to 16384 at ratio 4); larger shapes return QSA_ERR_UNSUPPORTED. */
+/* Longest padded sequence the prefill indexer takes (2^24 rows; longer
+ * seqLen returns QSA_ERR_UNSUPPORTED).  Its memory is linear in seqLen (the
+ * workspace above); the bound keeps token and block ids in int32 with room.
+ * qsa_indexer_prefill_max_blocks() returns the same number: the largest
+ * floor(seqLen / compressRatio) a call can have (ratio 1). */
+QSA_API int32_t qsa_indexer_prefill_max_seq_len(void);
 QSA_API int32_t qsa_indexer_prefill_max_blocks(void);
 
 /* Debug read of the status word at the head of an indexer workspace (the

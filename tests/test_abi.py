@@ -70,12 +70,18 @@ def test_constants_and_sizes(binding):
     L = binding.lib()
     assert L.qsa_sparse_decode_max_splits() == 8
     assert L.qsa_sparse_decode_partial_rows() == 16
-    assert L.qsa_indexer_prefill_max_blocks() == 4096
+    assert L.qsa_indexer_prefill_max_seq_len() == 1 << 24
+    assert L.qsa_indexer_prefill_max_blocks() == 1 << 24
     B, Hkv, D = 3, 4, 128
     po, ps, pc = binding.sparse_decode_workspace_elems(B, Hkv, D)
     assert (po, ps, pc) == (B * Hkv * 8 * 16 * D, B * Hkv * 8 * 2 * 16, B * Hkv)
-    tri = sum((t + 1) // 4 for t in range(1000))  # the complete-block counts n_c(t) of every row
-    assert binding.indexer_prefill_workspace_size(2, 1000, 128, 4) == 256 + 2 * 250 * 128 * 2 + 2 * tri * 4
+    # status, block keys (256-byte rounded), work counter, 320 score slots of 8 rows x S/r floats
+    kb = -(-(2 * 250 * 128 * 2) // 256) * 256
+    assert binding.indexer_prefill_workspace_size(2, 1000, 128, 4) == 256 + kb + 256 + 320 * 8 * 250 * 4
+    # linear in S: doubling S doubles every term that depends on it
+    w1 = binding.indexer_prefill_workspace_size(1, 65536, 128, 4) - 512
+    w2 = binding.indexer_prefill_workspace_size(1, 131072, 128, 4) - 512
+    assert w2 == 2 * w1
     assert binding.indexer_prefill_workspace_size(0, 1000, 128, 4) == 0
     # scores, tie keys and tie ids: 12 bytes per possible block of every sequence, at least
     assert binding.indexer_decode_workspace_size(8, 4096, 4, 512) >= 8 * 4096 * 32 * 12
@@ -127,8 +133,13 @@ def test_validation_rejects_before_launch(binding):
     assert _call(binding, "qsa_indexer_prefill", ip) == binding.QSA_ERR_INVALID_ARG  # topK < 2051
     ip.topK = 2051
     assert _call(binding, "qsa_indexer_prefill", ip) == binding.QSA_ERR_WORKSPACE  # 16 bytes
-    ip.seqLen = 16392
-    assert _call(binding, "qsa_indexer_prefill", ip) == binding.QSA_ERR_UNSUPPORTED  # 4098 blocks
+    ip.seqLen = 131072  # long sequences are taken: only the workspace is short
+    assert _call(binding, "qsa_indexer_prefill", ip) == binding.QSA_ERR_WORKSPACE
+    ip.seqLen = (1 << 24) + 8
+    assert _call(binding, "qsa_indexer_prefill", ip) == binding.QSA_ERR_UNSUPPORTED  # past 2^24 rows
+    ip.seqLen, ip.batchSize = 1 << 20, 4096
+    assert _call(binding, "qsa_indexer_prefill", ip) == binding.QSA_ERR_UNSUPPORTED  # B*S >= 2^31
+    ip.batchSize = 1
     ip.seqLen, ip.headDim = 8192, 96
     assert _call(binding, "qsa_indexer_prefill", ip) == binding.QSA_ERR_UNSUPPORTED
     ip.headDim, ip.rotDim = 128, 63

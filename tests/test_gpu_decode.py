@@ -280,3 +280,53 @@ def test_sparse_decode_page_permutation_and_empty():
     d2 = dict(d_dev, pool=pool2, page_table=mapping[d_dev["page_table"].long()].int())
     out2, _ = _gpu_attention(d2, lists_dev, cfg, 0.08, ws)
     assert torch.equal(out2.view(torch.int16), out.view(torch.int16))
+
+
+def test_sparse_decode_status_word_reports_bad_entries():
+    """A list entry past the sequence's length and a page id outside the pool
+    are skipped without a fault, and the optional status word says so (bit 2,
+    bit 1); the output equals the oracle's on the list with those entries
+    dropped.  Clean inputs leave the word at zero."""
+    cfg = syn.DECODE_PARITY
+    d = syn.make_decode(cfg)
+    d_np = {k: (v.numpy() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    ctx = d_np["ctx"]
+    rng = np.random.default_rng(5)
+    lists = np.full((cfg.B, cfg.topK), -1, np.int32)
+    for b, L in enumerate(ctx):
+        n = min(int(L), 300)
+        lists[b, :n] = np.sort(rng.choice(int(L), size=n, replace=False))
+    d_dev = _to_dev(d)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    po, ps, pc = qb.sparse_decode_workspace_elems(cfg.B, cfg.Hkv, cfg.D)
+
+    def run(lst, pt):
+        ws = (torch.zeros(po, dtype=torch.float32, device=DEV), torch.zeros(ps, dtype=torch.float32, device=DEV),
+              torch.zeros(pc, dtype=torch.int32, device=DEV))
+        out = torch.full((cfg.B, 1, cfg.Hq, cfg.D), float("nan"), dtype=torch.float16, device=DEV)
+        qb.sparse_decode(d_dev["q"], d_dev["pool"], pt, torch.from_numpy(lst[:, None, :].copy()).to(DEV),
+                         d_dev["ctx"], out, *ws, D=cfg.D, scale=f32(cfg.scale), status=status)
+        torch.cuda.synchronize()
+        return to_np(out)[:, 0]
+
+    run(lists, d_dev["page_table"])
+    assert int(status.item()) == 0, "clean inputs set status bits"
+    b_idx, b_page = 3, 5  # L = 2048 and 6000
+    bad = lists.copy()
+    bad[b_idx, 7] = int(ctx[b_idx]) + 11  # past the live length
+    bad[b_idx, 9] = -5                    # negative, not the -1 padding
+    pt_bad = d_np["page_table"].copy()
+    page = int(lists[b_page, 0]) // TPP
+    pt_bad[b_page, 0, page] = int(d["num_pages"]) * 2 + 3  # K page id outside the pool
+    got = run(bad, torch.from_numpy(pt_bad).to(DEV))
+    assert int(status.item()) == 6, f"status {int(status.item())} != bit 1 | bit 2"
+    want_list = lists.copy()
+    want_list[b_idx, 7] = -1
+    want_list[b_idx, 9] = -1
+    on_page = (want_list[b_page] >= 0) & (want_list[b_page] // TPP == page)
+    assert on_page.sum() > 0
+    want_list[b_page, on_page] = -1
+    want = oracle.sparse_decode(d_np["q"][:, 0], d_np["pool"], d_np["page_table"], want_list, ctx, D=cfg.D,
+                                scale=f32(cfg.scale))
+    check_attention(got, want, "decode with bad entries dropped")
+    assert qb.last_device_error(status) == 6  # the documented read of a device error word

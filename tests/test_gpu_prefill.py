@@ -108,9 +108,13 @@ def test_indexer_prefill_wider_topk_pads():
         compare_selection(g[0, t], o[0, t], sc[t], t, cfg.ratio, cfg.budget)
 
 
-def test_indexer_prefill_exact_ties_take_lowest_ids():
-    """Identical block keys (no RoPE) tie exactly on both sides; so do all-zero scores."""
-    cfg = dataclasses.replace(syn.PREFILL_PARITY, B=2, S=1100, rot=0, budget=30, ctx_lo=None, ctx_hi=None)
+@pytest.mark.parametrize("S,budget", [(1100, 30), (6000, 300)])
+def test_indexer_prefill_exact_ties_take_lowest_ids(S, budget):
+    """Identical block keys (no RoPE) tie exactly on both sides; so do all-zero scores.
+
+    At S = 6000 a row's 1500 tied keys exceed what the select stages in shared
+    memory, so the cut is narrowed over the scores in global memory first."""
+    cfg = dataclasses.replace(syn.PREFILL_PARITY, B=2, S=S, rot=0, budget=budget, ctx_lo=None, ctx_hi=None)
     t_np, t_dev = _inputs(cfg)
     x = t_np["idxK"][0, 0].copy()
     t_np["idxK"][:] = x
@@ -166,6 +170,47 @@ def test_indexer_prefill_full_size(cfg):
     _check_indexer(cfg, t_np, t_dev, rows=np.array(rows, np.int64))
 
 
+@pytest.mark.parametrize("cfg", [syn.PREFILL_28K, syn.PREFILL_64K, syn.PREFILL_LONG_RAGGED],
+                         ids=lambda c: c.name)
+def test_indexer_prefill_long(cfg):
+    """Sequences past 16K rows: every list's structure on the device, block keys
+    bit-exact, and sampled rows (random, around the budget and at the ends)
+    against the oracle's selection.  At 64K the longest rows hold more keys in
+    the cut's histogram bin than the select stages in shared memory."""
+    t_np, t_dev = _inputs(cfg)
+    rng = np.random.default_rng(cfg.seed)
+    rows = []
+    for b in range(cfg.B):
+        L = int(t_np["ctx"][b])
+        pick = set(rng.integers(0, L, size=40).tolist()) | {0, 2050, 2051, 16383, 16387, L - 2, L - 1}
+        pick |= set(rng.integers(max(0, L - 2000), L, size=16).tolist())
+        pick |= {L, min(cfg.S - 1, L + 5)} if L < cfg.S else set()
+        rows += [b * cfg.S + r for r in sorted(pick) if 0 <= r < cfg.S]
+    _check_indexer(cfg, t_np, t_dev, rows=np.array(rows, np.int64))
+
+
+def test_indexer_prefill_workspace_reuse_across_shapes():
+    """One workspace serves a long call, then a short one, then the long one
+    again: the work counter is re-armed by every call and no score slot
+    carries state from one call to the next."""
+    long_cfg = dataclasses.replace(syn.PREFILL_LONG_RAGGED, B=1, S=18000, ctx_lo=None, ctx_hi=None, seed=21)
+    short_cfg = syn.PREFILL_PARITY
+    tl_np, tl = _inputs(long_cfg)
+    ts_np, ts = _inputs(short_cfg)
+    ws = qb.alloc_workspace(qb.indexer_prefill_workspace_size(1, long_cfg.S, long_cfg.di, long_cfg.ratio), DEV)
+    outs = []
+    for cfg, t in ((long_cfg, tl), (short_cfg, ts), (long_cfg, tl)):
+        ind = torch.full((cfg.B, cfg.S, cfg.topK), 7, dtype=torch.int32, device=DEV)
+        qb.indexer_prefill(t["idxQ"], t["idxK"], t["wq"], t["wk"], t["ctx"], ind, ws, rot=cfg.rot, ratio=cfg.ratio,
+                           budget=cfg.budget, topK=cfg.topK, theta=cfg.theta, eps=cfg.eps)
+        outs.append(ind)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[2])
+    ref, _ = gpu_indexer_prefill(ts, short_cfg)
+    assert torch.equal(outs[1], ref)
+    check_lists_device(outs[0], tl_np["ctx"], long_cfg.ratio, long_cfg.budget)
+
+
 # ------------------------------------------------------------------ attention
 def _gpu_attention(t_dev, lists_dev, cfg, scale):
     out = torch.full((cfg.B, cfg.S, cfg.Hq, cfg.D), float("nan"), dtype=torch.float16, device=DEV)
@@ -184,6 +229,35 @@ def _check_rows(out, t_np, lists_np, cfg, rows, scale, what):
         if t >= int(t_np["ctx"][b]):
             assert np.all(got[i].view(np.uint16) == 0), f"{what}: padded row {t} not exactly zero"
     return err
+
+
+def test_sparse_prefill_status_word_reports_bad_entries():
+    """Entries past the live length or negative (other than the -1 padding)
+    are skipped without a fault, and the optional status word's bit 2 says so;
+    the output equals the oracle's on the lists with those entries dropped."""
+    cfg = dataclasses.replace(syn.PREFILL_PARITY, B=2, S=900, ctx_lo=500, ctx_hi=900, seed=31)
+    t_np, t_dev = _inputs(cfg)
+    lists = oracle_prefill_lists(t_np, cfg)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = torch.empty((cfg.B, cfg.S, cfg.Hq, cfg.D), dtype=torch.float16, device=DEV)
+    qb.sparse_prefill(t_dev["q"], t_dev["k"], t_dev["v"], torch.from_numpy(lists).to(DEV), t_dev["ctx"], out,
+                      f32(cfg.scale), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, "clean lists set a status bit"
+    bad = lists.copy()
+    L0 = int(t_np["ctx"][0])
+    bad[0, 400, 3] = L0 + 7         # past the live length
+    bad[0, 401, 0] = -9             # negative, not the padding
+    bad[1, 10, 2] = 1 << 30         # far out of range
+    want = lists.copy()
+    want[0, 400, 3] = want[0, 401, 0] = want[1, 10, 2] = -1
+    out = _gpu_attention(t_dev, torch.from_numpy(bad).to(DEV), cfg, f32(cfg.scale))
+    qb.sparse_prefill(t_dev["q"], t_dev["k"], t_dev["v"], torch.from_numpy(bad).to(DEV), t_dev["ctx"], out,
+                      f32(cfg.scale), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 4, f"status {int(status.item())} != bit 2"
+    rows = np.array([400, 401, 402, cfg.S + 10, cfg.S + 11], np.int64)
+    _check_rows(out, t_np, want, cfg, rows, f32(cfg.scale), "bad entries dropped")
 
 
 def test_sparse_prefill_parity_oracle_lists():

@@ -103,3 +103,23 @@ def test_noalloc_matches_workspace_entry_twice(binding, cfg):
         want = oracle.sparse_decode(d_np["q"][:, 0], d_np["pool"], d_np["page_table"], lists[:, 0], d_np["ctx"],
                                     D=cfg.D, scale=f32(cfg.scale))
         check_attention(to_np(out)[:, 0], want, "noalloc decode")
+
+
+@pytest.mark.gpu
+def test_noalloc_small_after_capacity(binding):
+    """The shared scratch after a call at full capacity (256 pairs, 8 splits
+    each): a smaller call with other shapes must find its counters at zero and
+    match the workspace entry."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    runs = []
+    for cfg in (CASES[1], CASES[0]):
+        d = syn.make_decode(cfg)
+        d_dev = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+        lists_dev = torch.from_numpy(_lists(d["ctx"].numpy(), cfg.topK, cfg.seed)).to(DEV)
+        runs.append((cfg, d_dev, lists_dev, _noalloc(d_dev, lists_dev, cfg)))
+    torch.cuda.synchronize()
+    for cfg, d_dev, lists_dev, out in runs:
+        ref = _with_workspace(d_dev, lists_dev, cfg)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"{cfg.name}: differs from the workspace entry"
