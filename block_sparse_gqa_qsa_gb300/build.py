@@ -17,6 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libqsa.so")
+PEAKS_SRC = os.path.join(CSRC, "probes", "qsa_peaks.cu")
+PEAKS_LIB = os.path.join(PKG, "libqsa_peaks.so")  # the benchmark's roofline probes (not part of the C ABI)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
@@ -38,11 +40,31 @@ def _deps():
         [os.path.join(ROOT, "include", "qsa.h")]
 
 
+def _fresh(lib: str, deps) -> bool:
+    return os.path.exists(lib) and os.path.getmtime(lib) >= max(os.path.getmtime(p) for p in deps)
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and os.path.exists(LIB):
-        newest = max(os.path.getmtime(p) for p in _deps())
-        if os.path.getmtime(LIB) >= newest:
-            return LIB
+    """Builds libqsa.so (and libqsa_peaks.so) when a source is newer; returns the libqsa.so path."""
+    peaks = None
+    if force or not _fresh(PEAKS_LIB, [PEAKS_SRC]):
+        tmp_p = PEAKS_LIB + f".tmp{os.getpid()}"
+        cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-shared", PEAKS_SRC, "-o", tmp_p]
+        peaks = (tmp_p, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True))
+    try:
+        return _build_lib(force, verbose, extra_flags)
+    finally:
+        if peaks:
+            out, _ = peaks[1].communicate()
+            if peaks[1].returncode:
+                print(out, file=sys.stderr)
+                raise RuntimeError("nvcc failed for qsa_peaks.cu")
+            os.replace(peaks[0], PEAKS_LIB)
+
+
+def _build_lib(force: bool, verbose: bool, extra_flags) -> str:
+    if not force and _fresh(LIB, _deps()):
+        return LIB
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
     procs = []

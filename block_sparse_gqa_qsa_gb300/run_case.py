@@ -94,7 +94,7 @@ def _decode_steps(cfg, steps):
 
 
 def main(argv=None):
-    names = {c.name: c for c in syn.BENCH_CONFIGS}
+    names = {c.name: c for c in syn.BENCH_CONFIGS + (syn.PREFILL_28K, syn.PREFILL_64K)}
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("workload", choices=sorted(names))
     ap.add_argument("--steps", type=int, default=2)
