@@ -112,6 +112,8 @@ def lib() -> ctypes.CDLL:
                              ("qsa_sparse_decode_noalloc", QsaSparseDecodeParams),
                              ("qsa_indexer_prefill_handoff", QsaIndexerHandoffParams),
                              ("qsa_sparse_prefill_bf16", QsaSparsePrefillParams),
+                             ("qsa_sparse_prefill_tcgen05", QsaSparsePrefillParams),
+                             ("qsa_sparse_prefill_tcgen05_bf16", QsaSparsePrefillParams),
                              ("qsa_sparse_decode_bf16", QsaSparseDecodeParams),
                              ("qsa_rope_qkv", QsaRopeQkvParams),
                              ("qsa_gather_selected", QsaGatherParams)):
@@ -283,10 +285,13 @@ def rope_qkv(qkv, wq, wk, ctx, q_out, *, Hq, Hkv, rot, theta, eps, k_out=None, v
     _check(lib().qsa_rope_qkv(ctypes.byref(p)))
 
 
-def sparse_prefill(q, k, v, indices, ctx, out, scale, stream=None, status=None):
+def sparse_prefill(q, k, v, indices, ctx, out, scale, stream=None, status=None, impl="mma"):
     """qsa_sparse_prefill (fp16 tensors) or qsa_sparse_prefill_bf16 (bfloat16 tensors):
     q/out [B,S,Hq,D], k/v [B,S,Hkv,D], indices int32 [B,S,topK]; status: optional int32 device
-    tensor whose first word collects the error bits."""
+    tensor whose first word collects the error bits.  impl="tcgen05" calls the tensor-core
+    variants qsa_sparse_prefill_tcgen05(_bf16) with the same arguments."""
+    if impl not in ("mma", "tcgen05"):
+        raise ValueError("sparse_prefill: impl must be 'mma' or 'tcgen05'")
     et = q.dtype
     if et not in (torch.float16, torch.bfloat16):
         raise ValueError("sparse_prefill: q must be float16 or bfloat16")
@@ -302,8 +307,8 @@ def sparse_prefill(q, k, v, indices, ctx, out, scale, stream=None, status=None):
         contextLengths=_ptr(ctx, torch.int32, "contextLengths"), batchSize=B, seqLen=S, numQHeads=Hq,
         numKVHeads=Hkv, headDim=D, topK=topK, attentionScale=scale, stream=_stream(stream),
         status=None if status is None else _ptr(status, torch.int32, "status"))
-    fn = lib().qsa_sparse_prefill_bf16 if et == torch.bfloat16 else lib().qsa_sparse_prefill
-    _check(fn(ctypes.byref(p)))
+    name = "qsa_sparse_prefill" + ("_tcgen05" if impl == "tcgen05" else "") + ("_bf16" if et == torch.bfloat16 else "")
+    _check(getattr(lib(), name)(ctypes.byref(p)))
 
 
 def sparse_decode(q, pool, page_table, indices, ctx, out, partial_o, partial_stats, counters, *, D, scale,

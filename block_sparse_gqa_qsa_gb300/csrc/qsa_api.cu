@@ -99,7 +99,7 @@ EncodeTiledFn encode_tiled() {
 namespace {
 
 // The attention entry points share their checks; fn names the caller in messages.
-qsa_status_t sparse_prefill_entry(const QsaSparsePrefillParams* p, const char* fn, bool bf16) {
+qsa_status_t sparse_prefill_entry(const QsaSparsePrefillParams* p, const char* fn, bool bf16, bool tcgen05 = false) {
   if (!p) return fail(QSA_ERR_INVALID_ARG, "%s: params is NULL", fn);
   if (!p->qPtr || !p->kPtr || !p->vPtr || !p->oPtr || !p->indices || !p->contextLengths)
     return fail(QSA_ERR_INVALID_ARG, "%s: a tensor pointer is NULL", fn);
@@ -115,7 +115,7 @@ qsa_status_t sparse_prefill_entry(const QsaSparsePrefillParams* p, const char* f
     return fail(QSA_ERR_UNSUPPORTED, "%s: batchSize*seqLen*numKVHeads exceeds the grid", fn);
   if (!aligned(p->qPtr, 16) || !aligned(p->kPtr, 16) || !aligned(p->vPtr, 16) || !aligned(p->oPtr, 16))
     return fail(QSA_ERR_INVALID_ARG, "%s: Q/K/V/O must be 16-byte aligned", fn);
-  const cudaError_t e = qsa::launch_sparse_prefill(*p, bf16);
+  const cudaError_t e = tcgen05 ? qsa::launch_sparse_prefill_tc(*p, bf16) : qsa::launch_sparse_prefill(*p, bf16);
   return e == cudaSuccess ? ok() : cuda_fail(e, fn);
 }
 
@@ -286,6 +286,12 @@ qsa_status_t qsa_sparse_prefill(const QsaSparsePrefillParams* p) {
 }
 qsa_status_t qsa_sparse_prefill_bf16(const QsaSparsePrefillParams* p) {
   return sparse_prefill_entry(p, "qsa_sparse_prefill_bf16", true);
+}
+qsa_status_t qsa_sparse_prefill_tcgen05(const QsaSparsePrefillParams* p) {
+  return sparse_prefill_entry(p, "qsa_sparse_prefill_tcgen05", false, true);
+}
+qsa_status_t qsa_sparse_prefill_tcgen05_bf16(const QsaSparsePrefillParams* p) {
+  return sparse_prefill_entry(p, "qsa_sparse_prefill_tcgen05_bf16", true, true);
 }
 
 qsa_status_t qsa_rope_qkv(const QsaRopeQkvParams* p) {

@@ -19,6 +19,7 @@
 // (m, l, O) and are merged once at the end.
 #include "qsa_device.cuh"
 #include "qsa_internal.h"
+#include "qsa_tcgen05.cuh"
 
 namespace qsa {
 namespace {
@@ -555,6 +556,276 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_k
   if (tid == 0) a.counters[b * a.Hkv + kvh] = 0;
 }
 
+
+// ------------------------------------------------- prefill on tcgen05 / TMEM
+// The same contract as sparse_prefill_kernel, on the 5th-generation tensor
+// cores.  One CTA of 4 warps (one warpgroup, TMEM lanes 0..127) per (query
+// token, KV head); tiles of 128 keys.  Per tile:
+//   - the K and V rows the list names are gathered (16 lanes per 256-byte row,
+//     cp.async, zero-filled for skipped entries) into two 32 KB tiles in the
+//     SW128 layout, the 128 dims of a row split into two 64-dim halves;
+//   - one thread issues S^T = K Q^T (M = 128 keys, N = 8 heads, 8 MMAs of 16
+//     dims, both operands K-major) into TMEM and commits it to an mbarrier;
+//   - thread k reads key k's 8 scores from TMEM: scale, mask, the tile's max per
+//     head (a warp max on order-preserving integers, then across the 4 warps
+//     through shared memory), online-softmax rescale, P = 2^(x - m) rounded to
+//     fp16 and stored as one 16-byte row [key][8 heads];
+//   - one thread issues O^T = V^T P^T (M = 128 dims, N = 8 heads, 8 MMAs of 16
+//     keys; V read MN-major from the same SW128 tile, P MN-major) into TMEM;
+//   - thread d adds dim d's 8 outputs to its registers (rescaled).
+// The next tile's K rows are requested as soon as this tile's S MMA has read
+// them, so they travel while the softmax and the PV MMA run.  No operand goes
+// through the register file: the tensor cores read K, V, Q and P from shared
+// memory by descriptor.  A head group of 9..16 runs as two groups of 8.
+constexpr int kTcKeys = 128;
+constexpr int kTcHalf = kTcKeys * 128;          // bytes of one 64-dim half of a 128-key tile
+constexpr int kTcTile = 2 * kTcHalf;            // 32 KB
+constexpr uint64_t kTcWaitNs = 200ull * 1000 * 1000;
+
+template <int NT>
+constexpr size_t tc_prefill_smem() {  // + 1 KB to align the base to 1024 bytes
+  return 1024 + 2 * kTcTile + NT * 2048 /*Q*/ + NT * 2048 /*P*/ + 4 * 8 * NT * 4 /*maxima*/ + 4 * 8 * NT * 4 /*sums*/ +
+         64 /*barriers, TMEM slot, counts*/;
+}
+
+// Order-preserving map between fp32 and int32 (and back).
+__device__ __forceinline__ int f2ord(float x) {
+  const int i = __float_as_int(x);
+  return i >= 0 ? i : i ^ 0x7fffffff;
+}
+__device__ __forceinline__ float ord2f(int o) { return __int_as_float(o >= 0 ? o : o ^ 0x7fffffff); }
+
+template <int NT, bool kBf16>
+__global__ void __launch_bounds__(kThreads, 3) sparse_prefill_tc_kernel(const PrefillArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const uint32_t kt = smem_addr(base);               // K tile [2 halves][128 keys][128 B], SW128
+  const uint32_t vt = kt + kTcTile;                  // V tile, same layout
+  const uint32_t qt = vt + kTcTile;                  // Q: NT x [2 halves][8 heads][128 B], SW128
+  const uint32_t pt = qt + NT * 2048;                // P: NT x [128 keys][8 heads] fp16 (16 B rows)
+  int* redmax = reinterpret_cast<int*>(base + 2 * kTcTile + NT * 4096);  // [4 warps][8*NT]
+  float* redsum = reinterpret_cast<float*>(redmax + 4 * 8 * NT);          // [4 warps][8*NT]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(redsum + 4 * 8 * NT);     // S done, O done
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
+  int* misc = reinterpret_cast<int*>(tslot + 1);                          // [4] last valid slot per warp
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long bid = blockIdx.x;
+  const int kvh = static_cast<int>(bid % a.Hkv);
+  const long long rowid = bid / a.Hkv;
+  const int b = static_cast<int>(rowid / a.S);
+  const int t = a.S - 1 - static_cast<int>(rowid % a.S);  // longest lists first within a sequence
+  const long long bt = static_cast<long long>(b) * a.S + t;
+  const int L = max(0, min(a.ctx[b], a.S));
+  __half* out = a.o + (static_cast<size_t>(bt) * a.Hq + static_cast<size_t>(kvh) * a.G) * kD;
+  if (t >= L) {  // rows at or past the live length are exact zeros
+    for (int e = tid; e < a.G * kD / 8; e += kThreads) reinterpret_cast<uint4*>(out)[e] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  // Q rows of the group (heads >= G zero), in the SW128 K-major layout.
+  const __half* qsrc = a.q + (static_cast<size_t>(bt) * a.Hq + static_cast<size_t>(kvh) * a.G) * kD;
+  for (int e = tid; e < NT * 8 * 16; e += kThreads) {
+    const int h = e >> 4, c = e & 15, hr = h & 7;
+    const bool ok = h < a.G;
+    cp_async16(qt + (h >> 3) * 2048 + (c >> 3) * 1024 + hr * 128 + (((c & 7) ^ hr) << 4), qsrc + (ok ? h : 0) * kD + c * 8,
+               ok);
+  }
+  cp_async_commit();
+  // The list's last valid slot fixes the tile count (entries outside [0, L) are skipped).
+  const int32_t* lst = a.indices + static_cast<size_t>(bt) * a.topK;
+  int last = -1;
+  bool bad = false;
+  for (int i = tid; i < a.topK; i += kThreads) {
+    const int j = __ldg(lst + i);
+    const bool ok = static_cast<unsigned>(j) < static_cast<unsigned>(L);
+    last = ok ? i : last;
+    bad |= !ok && j != -1;
+  }
+  if (__any_sync(kFull, bad) && lane == 0 && a.status) atomicOr(a.status, kErrBadIndex);
+  last = __reduce_max_sync(kFull, last);
+  if (lane == 0) misc[warp] = last;
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) tmem_alloc(tslot, 32);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;  // columns [0, 8 NT): S^T; [16, 16 + 8 NT): this tile's O^T
+  const int nslots = max(max(misc[0], misc[1]), max(misc[2], misc[3])) + 1;
+  const int ntiles = (nslots + kTcKeys - 1) / kTcKeys;
+
+  // Gathers: 16 lanes per 256-byte row, rows r*8 + tid/16 (r < 16); the chunk's
+  // swizzled slot depends only on the thread.
+  const int ch = tid & 15, rsub = tid >> 4;
+  const size_t head_off = (static_cast<size_t>(b) * a.S * a.Hkv + kvh) * kD + ch * 8;
+  const __half* kbase = a.k + head_off;
+  const __half* vbase = a.v + head_off;
+  const int tok_stride = a.Hkv * kD;
+  const uint32_t slot0 = (ch >> 3) * kTcHalf + rsub * 128 + (((ch & 7) ^ rsub) << 4);
+  auto issue = [&](int tile, uint32_t dst_tile, const __half* src_base) {
+    const int32_t* ids = lst + tile * kTcKeys + rsub;
+#pragma unroll 4
+    for (int r = 0; r < kTcKeys / 8; ++r) {
+      const int slot = tile * kTcKeys + r * 8 + rsub;
+      const int j = slot < a.topK ? __ldg(ids + r * 8) : -1;
+      const bool ok = static_cast<unsigned>(j) < static_cast<unsigned>(L);
+      cp_async16(dst_tile + slot0 + r * 1024, src_base + static_cast<size_t>(ok ? j : 0) * tok_stride, ok);
+    }
+  };
+  const float sl2 = a.sl2;
+  float o_acc[NT][8], l_part[NT][8], m_run[NT][8];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      o_acc[nt][h] = 0.f;
+      l_part[nt][h] = 0.f;
+      m_run[nt][h] = -INFINITY;
+    }
+  const uint32_t lane_addr = static_cast<uint32_t>(32 * warp) << 16;
+  // A wait that runs out (a tensor-core fault) records a status bit; every
+  // exit from the loop is decided at a barrier, so all threads leave together.
+  bool ok = true, alive = true;
+  if (ntiles > 0) {
+    issue(0, kt, kbase);
+    issue(0, vt, vbase);
+  }
+  cp_async_commit();
+  for (int i = 0; i < ntiles; ++i) {
+    cp_async_wait<0>();
+    fence_proxy_async();  // cp.async writes -> the tensor cores' reads
+    tc_fence_before();
+    if (__syncthreads_or(!ok)) {
+      alive = false;
+      break;
+    }
+    tc_fence_after();
+    if (tid == 0) {
+      constexpr uint32_t idS = mma_idesc_f16(128, 8, kBf16, false, false);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          const uint32_t koff = (s >> 2) * kTcHalf + (s & 3) * 32;
+          umma_f16(tmem + nt * 8, smem_desc(kt + koff, 16, 1024, kSmemSwizzle128B),
+                   smem_desc(qt + nt * 2048 + (s >> 2) * 1024 + (s & 3) * 32, 16, 1024, kSmemSwizzle128B), idS, s > 0);
+        }
+      umma_commit(&bars[0]);
+    }
+    __syncwarp();
+    ok = mbar_wait_bounded(&bars[0], i & 1, kTcWaitNs);
+    if (!ok && a.status) atomicOr(a.status, kErrWaitTimeout);
+    tc_fence_after();
+    // K has been read: the next tile's K rows can travel now.
+    if (i + 1 < ntiles) issue(i + 1, kt, kbase);
+    cp_async_commit();
+    const int key_slot = i * kTcKeys + tid;
+    const int jk = key_slot < a.topK ? __ldg(lst + key_slot) : -1;
+    const bool valid = static_cast<unsigned>(jk) < static_cast<unsigned>(L);
+    float x[NT][8];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float sv[8];
+      tmem_ld8(tmem + lane_addr + nt * 8, sv);
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        x[nt][h] = valid ? sv[h] * sl2 : -INFINITY;
+        const int mx = __reduce_max_sync(kFull, f2ord(x[nt][h]));
+        if (lane == 0) redmax[warp * 8 * NT + nt * 8 + h] = mx;
+      }
+    }
+    tc_fence_before();
+    if (__syncthreads_or(!ok)) {
+      alive = false;
+      break;
+    }
+    float alpha[NT][8];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      uint32_t pk[4];
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        const int c = nt * 8 + h;
+        const float tmax = ord2f(max(max(redmax[c], redmax[8 * NT + c]), max(redmax[16 * NT + c], redmax[24 * NT + c])));
+        const float mn = fmaxf(m_run[nt][h], tmax);
+        const float mu = mn == -INFINITY ? 0.f : mn;
+        alpha[nt][h] = ex2_ftz(m_run[nt][h] - mu);
+        m_run[nt][h] = mn;
+        const float p = ex2_ftz(x[nt][h] - mu);
+        l_part[nt][h] = l_part[nt][h] * alpha[nt][h] + p;
+        x[nt][h] = p;
+      }
+#pragma unroll
+      for (int h = 0; h < 4; ++h) pk[h] = pack_p<kBf16>(x[nt][2 * h], x[nt][2 * h + 1]);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(pt + nt * 2048 + tid * 16), "r"(pk[0]),
+                   "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
+                   : "memory");
+    }
+    fence_proxy_async();  // P stores -> the tensor cores' reads
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+      constexpr uint32_t idO = mma_idesc_f16(128, 8, kBf16, true, true);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          umma_f16(tmem + 16 + nt * 8, smem_desc(vt + s * 2048, kTcHalf, 1024, kSmemSwizzle128B),
+                   smem_desc(pt + nt * 2048 + s * 256, 128, 128, kSmemSwizzleNone), idO, s > 0);
+      umma_commit(&bars[1]);
+    }
+    __syncwarp();
+    ok = mbar_wait_bounded(&bars[1], i & 1, kTcWaitNs);
+    if (!ok && a.status) atomicOr(a.status, kErrWaitTimeout);
+    tc_fence_after();
+    if (i + 1 < ntiles) issue(i + 1, vt, vbase);  // V has been read
+    cp_async_commit();
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float ov[8];
+      tmem_ld8(tmem + lane_addr + 16 + nt * 8, ov);
+#pragma unroll
+      for (int h = 0; h < 8; ++h) o_acc[nt][h] = o_acc[nt][h] * alpha[nt][h] + ov[h];
+    }
+  }
+  cp_async_wait<0>();
+  alive = alive && __syncthreads_and(ok);
+  // l: the sum over the CTA of each thread's share
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      float v = l_part[nt][h];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+      if (lane == 0) redsum[warp * 8 * NT + nt * 8 + h] = v;
+    }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 32);
+  if (!alive) return;
+  // thread d writes dim d of every head of the group
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      const int c = nt * 8 + h;
+      if (c < a.G) {
+        const float Ls = redsum[c] + redsum[8 * NT + c] + redsum[16 * NT + c] + redsum[24 * NT + c];
+        const float v = Ls > 0.f ? o_acc[nt][h] / Ls : 0.f;
+        if constexpr (kBf16)
+          reinterpret_cast<__nv_bfloat16*>(out)[c * kD + tid] = __float2bfloat16_rn(v);
+        else
+          out[c * kD + tid] = __float2half_rn(v);
+      }
+    }
+}
+
 // Ring depth of both kernels: one 64-key tile (42 KB of shared memory, 5 CTAs
 // per SM, each CTA's gather latency covered by the others) for a head group
 // of up to 8; two (3 CTAs per SM, the register budget of the 16-head group)
@@ -595,7 +866,39 @@ cudaError_t decode_nt(const DecodeArgs& a, int B, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <int NT, bool kBf16>
+cudaError_t prefill_tc_nt(const PrefillArgs& a, long long nblocks, cudaStream_t st) {
+  constexpr size_t smem = tc_prefill_smem<NT>();
+  static const cudaError_t attr = cudaFuncSetAttribute(sparse_prefill_tc_kernel<NT, kBf16>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (attr != cudaSuccess) return attr;
+  sparse_prefill_tc_kernel<NT, kBf16><<<static_cast<unsigned>(nblocks), kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_sparse_prefill_tc(const QsaSparsePrefillParams& p, bool bf16) {
+  PrefillArgs a;
+  a.q = static_cast<const __half*>(p.qPtr);
+  a.k = static_cast<const __half*>(p.kPtr);
+  a.v = static_cast<const __half*>(p.vPtr);
+  a.o = static_cast<__half*>(p.oPtr);
+  a.indices = p.indices;
+  a.ctx = p.contextLengths;
+  a.status = p.status;
+  a.S = p.seqLen;
+  a.Hq = p.numQHeads;
+  a.Hkv = p.numKVHeads;
+  a.G = p.numQHeads / p.numKVHeads;
+  a.topK = p.topK;
+  a.topKpad = (p.topK + kTcKeys - 1) / kTcKeys * kTcKeys;
+  a.sl2 = p.attentionScale * kLog2e;
+  const long long nblocks = static_cast<long long>(p.batchSize) * p.seqLen * p.numKVHeads;
+  cudaStream_t st = static_cast<cudaStream_t>(p.stream);
+  if (bf16) return a.G <= 8 ? prefill_tc_nt<1, true>(a, nblocks, st) : prefill_tc_nt<2, true>(a, nblocks, st);
+  return a.G <= 8 ? prefill_tc_nt<1, false>(a, nblocks, st) : prefill_tc_nt<2, false>(a, nblocks, st);
+}
 
 cudaError_t launch_sparse_prefill(const QsaSparsePrefillParams& p, bool bf16) {
   PrefillArgs a;

@@ -45,6 +45,7 @@ cudaError_t launch_indexer_decode(const QsaIndexerDecodeParams& p, const RopeFre
 // Attention -----------------------------------------------------------------
 // bf16: Q/K/V/O (prefill) or q/pool/o (decode) hold bfloat16 instead of fp16.
 cudaError_t launch_sparse_prefill(const QsaSparsePrefillParams& p, bool bf16 = false);
+cudaError_t launch_sparse_prefill_tc(const QsaSparsePrefillParams& p, bool bf16 = false);  // tcgen05 / TMEM
 cudaError_t launch_sparse_decode(const QsaSparseDecodeParams& p, bool bf16 = false);
 
 // Upstream q/k norm + RoPE ------------------------------------------------------

@@ -321,6 +321,20 @@ QSA_API qsa_status_t qsa_rope_qkv(const QsaRopeQkvParams* params);
 QSA_API qsa_status_t qsa_sparse_prefill_bf16(const QsaSparsePrefillParams* params);
 QSA_API qsa_status_t qsa_sparse_decode_bf16(const QsaSparseDecodeParams* params);
 
+/* The sparse prefill attention ("Cute Dsl Qsa Sparse Runner",
+ * QsaSparsePrefillParams: per-row gathers, one CTA per (query token, KV
+ * head)) on the 5th-generation tensor cores: tcgen05.mma with its operands
+ * read from shared memory by descriptor and its accumulators in tensor memory,
+ * over tiles of 128 keys.  Same params, contract, checks and errors as
+ * qsa_sparse_prefill / qsa_sparse_prefill_bf16 (fp16 or bf16 tensors);
+ * arithmetic: q.k products accumulated in fp32, softmax in fp32, P rounded to
+ * the element type for the PV product, fp32 accumulation, output rounded once.
+ * The result differs from qsa_sparse_prefill only by rounding order.
+ * status bit 0 (value 1), added to the bits above: a wait on the tensor cores
+ * ran past 0.2 s and the row was left unwritten. */
+QSA_API qsa_status_t qsa_sparse_prefill_tcgen05(const QsaSparsePrefillParams* params);
+QSA_API qsa_status_t qsa_sparse_prefill_tcgen05_bf16(const QsaSparsePrefillParams* params);
+
 /* Split-K sparse decode with no caller workspace.  The pages have no
  * counterpart to this entry point.  It serves callers that cannot hand device
  * memory to a library call on their decode path: an engine whose memory is

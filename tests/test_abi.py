@@ -108,6 +108,7 @@ def test_validation_rejects_before_launch(binding):
     L = binding.lib()
     for fn in ("qsa_indexer_prefill", "qsa_indexer_decode", "qsa_sparse_prefill", "qsa_sparse_decode",
                "qsa_indexer_prefill_handoff", "qsa_rope_qkv", "qsa_sparse_prefill_bf16", "qsa_sparse_decode_bf16",
+               "qsa_sparse_prefill_tcgen05", "qsa_sparse_prefill_tcgen05_bf16",
                "qsa_gather_selected"):
         assert getattr(L, fn)(None) == binding.QSA_ERR_INVALID_ARG
     fake = 1 << 20  # never dereferenced: every case below fails validation first

@@ -40,14 +40,16 @@ def _tol(v: torch.Tensor) -> float:
     return 2.0 ** -8 * float(v.float().abs().nan_to_num(0.0).max()) + 1e-4
 
 
+@pytest.mark.parametrize("impl", ["mma", "tcgen05"])
 @pytest.mark.parametrize("Hq,Hkv", [(16, 2), (32, 2)])
-def test_sparse_prefill_bf16(Hq, Hkv):
+def test_sparse_prefill_bf16(Hq, Hkv, impl):
     cfg = dataclasses.replace(syn.PREFILL_PARITY, Hq=Hq, Hkv=Hkv, seed=51 + Hq)
     t = syn.make_prefill(cfg)
     q, k, v = (t[n].float().to(torch.bfloat16) for n in ("q", "k", "v"))  # NaN rows past L stay NaN
     lists = syn.random_lists(cfg.B, cfg.S, cfg.topK, t["ctx"], seed=cfg.seed)
     out = torch.full((cfg.B, cfg.S, cfg.Hq, cfg.D), float("nan"), dtype=torch.bfloat16, device=DEV)
-    qb.sparse_prefill(q.to(DEV), k.to(DEV), v.to(DEV), lists.to(DEV), t["ctx"].to(DEV), out, f32(cfg.scale))
+    qb.sparse_prefill(q.to(DEV), k.to(DEV), v.to(DEV), lists.to(DEV), t["ctx"].to(DEV), out, f32(cfg.scale),
+                      impl=impl)
     torch.cuda.synchronize()
     ref = oracle.sparse_prefill(_bits(q), _bits(k), _bits(v), lists.numpy(), t["ctx"].numpy(), f32(cfg.scale),
                                 bf16=True)
@@ -62,7 +64,8 @@ def test_sparse_prefill_bf16(Hq, Hkv):
     # a single entry: P = 1 exactly, so o is the bf16 value row bit for bit
     one = torch.full_like(lists, -1)
     one[:, :, 0] = 5
-    qb.sparse_prefill(q.to(DEV), k.to(DEV), v.to(DEV), one.to(DEV), t["ctx"].to(DEV), out, f32(cfg.scale))
+    qb.sparse_prefill(q.to(DEV), k.to(DEV), v.to(DEV), one.to(DEV), t["ctx"].to(DEV), out, f32(cfg.scale),
+                      impl=impl)
     torch.cuda.synchronize()
     G = cfg.Hq // cfg.Hkv
     for b in range(cfg.B):

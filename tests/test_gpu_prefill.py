@@ -212,9 +212,12 @@ def test_indexer_prefill_workspace_reuse_across_shapes():
 
 
 # ------------------------------------------------------------------ attention
-def _gpu_attention(t_dev, lists_dev, cfg, scale):
+IMPLS = ("mma", "tcgen05")  # mma.sync tiles, and the tcgen05 / TMEM variant of the same contract
+
+
+def _gpu_attention(t_dev, lists_dev, cfg, scale, impl="mma"):
     out = torch.full((cfg.B, cfg.S, cfg.Hq, cfg.D), float("nan"), dtype=torch.float16, device=DEV)
-    qb.sparse_prefill(t_dev["q"], t_dev["k"], t_dev["v"], lists_dev, t_dev["ctx"], out, scale)
+    qb.sparse_prefill(t_dev["q"], t_dev["k"], t_dev["v"], lists_dev, t_dev["ctx"], out, scale, impl=impl)
     torch.cuda.synchronize()
     return out
 
@@ -231,7 +234,8 @@ def _check_rows(out, t_np, lists_np, cfg, rows, scale, what):
     return err
 
 
-def test_sparse_prefill_status_word_reports_bad_entries():
+@pytest.mark.parametrize("impl", IMPLS)
+def test_sparse_prefill_status_word_reports_bad_entries(impl):
     """Entries past the live length or negative (other than the -1 padding)
     are skipped without a fault, and the optional status word's bit 2 says so;
     the output equals the oracle's on the lists with those entries dropped."""
@@ -241,7 +245,7 @@ def test_sparse_prefill_status_word_reports_bad_entries():
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     out = torch.empty((cfg.B, cfg.S, cfg.Hq, cfg.D), dtype=torch.float16, device=DEV)
     qb.sparse_prefill(t_dev["q"], t_dev["k"], t_dev["v"], torch.from_numpy(lists).to(DEV), t_dev["ctx"], out,
-                      f32(cfg.scale), status=status)
+                      f32(cfg.scale), status=status, impl=impl)
     torch.cuda.synchronize()
     assert int(status.item()) == 0, "clean lists set a status bit"
     bad = lists.copy()
@@ -251,41 +255,44 @@ def test_sparse_prefill_status_word_reports_bad_entries():
     bad[1, 10, 2] = 1 << 30         # far out of range
     want = lists.copy()
     want[0, 400, 3] = want[0, 401, 0] = want[1, 10, 2] = -1
-    out = _gpu_attention(t_dev, torch.from_numpy(bad).to(DEV), cfg, f32(cfg.scale))
+    out = _gpu_attention(t_dev, torch.from_numpy(bad).to(DEV), cfg, f32(cfg.scale), impl)
     qb.sparse_prefill(t_dev["q"], t_dev["k"], t_dev["v"], torch.from_numpy(bad).to(DEV), t_dev["ctx"], out,
-                      f32(cfg.scale), status=status)
+                      f32(cfg.scale), status=status, impl=impl)
     torch.cuda.synchronize()
     assert int(status.item()) == 4, f"status {int(status.item())} != bit 2"
     rows = np.array([400, 401, 402, cfg.S + 10, cfg.S + 11], np.int64)
     _check_rows(out, t_np, want, cfg, rows, f32(cfg.scale), "bad entries dropped")
 
 
-def test_sparse_prefill_parity_oracle_lists():
+@pytest.mark.parametrize("impl", IMPLS)
+def test_sparse_prefill_parity_oracle_lists(impl):
     cfg = syn.PREFILL_PARITY
     t_np, t_dev = _inputs(cfg)
     lists = oracle_prefill_lists(t_np, cfg)
-    out = _gpu_attention(t_dev, torch.from_numpy(lists).to(DEV), cfg, f32(cfg.scale))
+    out = _gpu_attention(t_dev, torch.from_numpy(lists).to(DEV), cfg, f32(cfg.scale), impl)
     rows = np.arange(cfg.B * cfg.S, dtype=np.int64)
     _check_rows(out, t_np, lists, cfg, rows, f32(cfg.scale), "parity")
 
 
+@pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2), (16, 2), (32, 2), (24, 2)])
-def test_sparse_prefill_group_sizes_and_list_shapes(Hq, Hkv):
+def test_sparse_prefill_group_sizes_and_list_shapes(Hq, Hkv, impl):
     cfg = dataclasses.replace(syn.PREFILL_PARITY, name=f"g{Hq // Hkv}", B=2, S=700, Hq=Hq, Hkv=Hkv,
                               ctx_lo=300, ctx_hi=700, seed=Hq)
     t_np, t_dev = _inputs(cfg)
     rows = np.arange(cfg.B * cfg.S, dtype=np.int64)
     # random order, causal
     lists = syn.random_lists(cfg.B, cfg.S, 150, t_np["ctx"], seed=1, fill=0.7).numpy()
-    out = _gpu_attention(t_dev, torch.from_numpy(lists).to(DEV), cfg, 0.07)
+    out = _gpu_attention(t_dev, torch.from_numpy(lists).to(DEV), cfg, 0.07, impl)
     _check_rows(out, t_np, lists, cfg, rows, f32(0.07), "random causal")
     # non-causal entries (no positional mask), several tiles wide
     lists = syn.random_lists(cfg.B, cfg.S, 300, t_np["ctx"], seed=2, fill=0.9, causal=False).numpy()
-    out = _gpu_attention(t_dev, torch.from_numpy(lists).to(DEV), cfg, 0.1)
+    out = _gpu_attention(t_dev, torch.from_numpy(lists).to(DEV), cfg, 0.1, impl)
     _check_rows(out, t_np, lists, cfg, rows, f32(0.1), "non-causal")
 
 
-def test_sparse_prefill_special_lists():
+@pytest.mark.parametrize("impl", IMPLS)
+def test_sparse_prefill_special_lists(impl):
     cfg = dataclasses.replace(syn.PREFILL_PARITY, B=1, S=300, ctx_lo=None, ctx_hi=None)
     t_np, t_dev = _inputs(cfg)
     topK = 67
@@ -294,7 +301,7 @@ def test_sparse_prefill_special_lists():
     js = rng.integers(0, cfg.S, size=cfg.S)
     lists[0, :, 0] = js  # one entry: the output is that value row, exactly
     lists[0, 7] = -1     # empty list: zeros
-    out = to_np(_gpu_attention(t_dev, torch.from_numpy(lists).to(DEV), cfg, 0.09))
+    out = to_np(_gpu_attention(t_dev, torch.from_numpy(lists).to(DEV), cfg, 0.09, impl))
     for t in range(cfg.S):
         for h in range(cfg.Hq):
             want = np.zeros(cfg.D, np.float16) if t == 7 else t_np["v"][0, js[t], h // (cfg.Hq // cfg.Hkv)]
@@ -305,25 +312,27 @@ def test_sparse_prefill_special_lists():
     lists = syn.random_lists(1, cfg.S, topK, t_np["ctx"], seed=3, fill=0.5).numpy()
     bad = lists.copy()
     bad[0, :200, -1] = 250  # names a padded (NaN) row
-    out = _gpu_attention(t_dev, torch.from_numpy(bad).to(DEV), cfg2, 0.09)
+    out = _gpu_attention(t_dev, torch.from_numpy(bad).to(DEV), cfg2, 0.09, impl)
     _check_rows(out, t_np, lists, cfg2, np.arange(cfg.S, dtype=np.int64), f32(0.09), "skip >= L")
 
 
-def test_sparse_prefill_full_size_8k():
+@pytest.mark.parametrize("impl", IMPLS)
+def test_sparse_prefill_full_size_8k(impl):
     cfg = syn.PREFILL_8K
     t_np, t_dev = _inputs(cfg)
     lists = oracle_prefill_lists(t_np, cfg)
-    out = _gpu_attention(t_dev, torch.from_numpy(lists).to(DEV), cfg, f32(cfg.scale))
+    out = _gpu_attention(t_dev, torch.from_numpy(lists).to(DEV), cfg, f32(cfg.scale), impl)
     rows = np.unique(np.concatenate([np.arange(0, 8192, 97), [1, 2047, 2048, 2049, 8190, 8191]])).astype(np.int64)
     _check_rows(out, t_np, lists, cfg, rows, f32(cfg.scale), "8k")
     assert not torch.isnan(out).any()
 
 
-def test_sparse_prefill_full_size_ragged():
+@pytest.mark.parametrize("impl", IMPLS)
+def test_sparse_prefill_full_size_ragged(impl):
     cfg = syn.PREFILL_RAGGED
     t_np, t_dev = _inputs(cfg)
     lists_dev = syn.qsa_like_lists(cfg.B, cfg.S, t_np["ctx"], cfg.ratio, cfg.budget, cfg.topK, seed=9, device=DEV)
-    out = _gpu_attention(t_dev, lists_dev, cfg, f32(cfg.scale))
+    out = _gpu_attention(t_dev, lists_dev, cfg, f32(cfg.scale), impl)
     lists = to_np(lists_dev)
     rows = []
     for b in range(cfg.B):
@@ -338,12 +347,13 @@ def test_sparse_prefill_full_size_ragged():
     assert not torch.isnan(out).any()
 
 
-def test_prefill_end_to_end_8k():
+@pytest.mark.parametrize("impl", IMPLS)
+def test_prefill_end_to_end_8k(impl):
     """Raw inputs through both whole paths; sets agree up to ties, outputs agree where sets do."""
     cfg = syn.PREFILL_8K
     t_np, t_dev = _inputs(cfg)
     ind, _ = gpu_indexer_prefill(t_dev, cfg)
-    out = _gpu_attention(t_dev, ind, cfg, f32(cfg.scale))
+    out = _gpu_attention(t_dev, ind, cfg, f32(cfg.scale), impl)
     rows = np.arange(0, cfg.S, 61, dtype=np.int64)
     ora, sc = oracle_prefill_lists(t_np, cfg, rows=rows, want_scores=True)
     gpu = to_np(ind)[0][rows]
