@@ -530,6 +530,30 @@ def run_ours(args, rank, world, dev):
             if i >= 3:
                 ts.append(e0.elapsed_time(e1))
     bf16_ms = statistics.mean(ts)
+
+    # the attention on the tcgen05 tensor cores (qsa_sparse_prefill_tcgen05) on the same lists: an A/B
+    out_tc = torch.empty_like(pf.out)
+    ts = []
+    with clk.window():
+        for i in range(args.steps + 3):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            pf.qb.sparse_prefill(pf.t["q"], pf.t["k"], pf.t["v"], pf.ind, pf.t["ctx"], out_tc, f32(cfg.scale),
+                                 impl="tcgen05")
+            e1.record()
+            e1.synchronize()
+            if i >= 3:
+                ts.append(e0.elapsed_time(e1))
+    pf.attention()
+    torch.cuda.synchronize()
+    tc_ms = statistics.mean(ts)
+    impl_ab = {"workload": cfg.name, "mma_sync_ms": round(att_ms, 4), "tcgen05_ms": round(tc_ms, 4),
+               "tcgen05_l2_frac": round(gbytes / (tc_ms / 1000.0) / 1e9 / l2["gbs"], 4),
+               "max_abs_diff": float((out_tc.float() - pf.out.float()).abs().max()),
+               "note": "the same lists through qsa_sparse_prefill (mma.sync tiles) and qsa_sparse_prefill_tcgen05 "
+                       "(tcgen05.mma, TMEM accumulators); the headline uses the faster"}
+    del out_tc
     bf16 = {"workload": cfg.name, "kernel": "sparse_prefill_kernel (bf16)", "ms": round(bf16_ms, 4),
             "achieved_gbs": round(gbytes / (bf16_ms / 1000.0) / 1e9, 1),
             "l2_frac": round(gbytes / (bf16_ms / 1000.0) / 1e9 / l2["gbs"], 4)}
@@ -633,6 +657,7 @@ def run_ours(args, rank, world, dev):
         "peaks": {"l2_read": l2, "ffma": fma, "hbm_gbs": hbm_peak, "bf16_tflops": mma_peak, "hbm_source": peak_kind},
         "e2e": e2e_value, "h2d": h2d, "d2h": d2h, "clocks": clk.summary(), "side_prefill": side,
         "decode": decode, "handoff": handoff, "bf16_prefill_attention": bf16, "rope_qkv": rope,
+        "attention_impl_ab": impl_ab,
         # per timed prefill step: block_pool, prefill_select, sparse_prefill
         "launches": 3 * args.steps,
     }
@@ -748,6 +773,7 @@ def main():
             "decode": r["decode"],
             "handoff": r["handoff"],
             "bf16_prefill_attention": r["bf16_prefill_attention"],
+            "attention_impl_ab": r["attention_impl_ab"],
             "rope_qkv": r["rope_qkv"],
             "e2e": {"value": r["e2e"], "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                     "note": "each step copies its inputs from pinned host memory and its output back; a second "

@@ -560,32 +560,35 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_k
 // ------------------------------------------------- prefill on tcgen05 / TMEM
 // The same contract as sparse_prefill_kernel, on the 5th-generation tensor
 // cores.  One CTA of 4 warps (one warpgroup, TMEM lanes 0..127) per (query
-// token, KV head); tiles of 128 keys.  Per tile:
+// token, KV head); tiles of 64 keys.  Per tile:
 //   - the K and V rows the list names are gathered (16 lanes per 256-byte row,
-//     cp.async, zero-filled for skipped entries) into two 32 KB tiles in the
+//     cp.async, zero-filled for skipped entries) into two 16 KB tiles in the
 //     SW128 layout, the 128 dims of a row split into two 64-dim halves;
-//   - one thread issues S^T = K Q^T (M = 128 keys, N = 8 heads, 8 MMAs of 16
-//     dims, both operands K-major) into TMEM and commits it to an mbarrier;
-//   - thread k reads key k's 8 scores from TMEM: scale, mask, the tile's max per
-//     head (a warp max on order-preserving integers, then across the 4 warps
-//     through shared memory), online-softmax rescale, P = 2^(x - m) rounded to
-//     fp16 and stored as one 16-byte row [key][8 heads];
-//   - one thread issues O^T = V^T P^T (M = 128 dims, N = 8 heads, 8 MMAs of 16
+//   - one thread issues S^T = K Q^T (M = 64 keys, N = 8 heads, 8 MMAs of 16
+//     dims, both operands K-major) into TMEM and commits it to an mbarrier; an
+//     M = 64 accumulator puts key 16w + l in lane l of warp w's quadrant;
+//   - lanes 0..15 of each warp read their key's 8 scores from TMEM: scale,
+//     mask, the tile's max per head (a warp max on order-preserving integers,
+//     then across the 4 warps through shared memory), online-softmax rescale,
+//     P = 2^(x - m) rounded to the element type and stored as one 16-byte row
+//     [key][8 heads];
+//   - one thread issues O^T = V^T P^T (M = 128 dims, N = 8 heads, 4 MMAs of 16
 //     keys; V read MN-major from the same SW128 tile, P MN-major) into TMEM;
 //   - thread d adds dim d's 8 outputs to its registers (rescaled).
 // The next tile's K rows are requested as soon as this tile's S MMA has read
-// them, so they travel while the softmax and the PV MMA run.  No operand goes
-// through the register file: the tensor cores read K, V, Q and P from shared
-// memory by descriptor.  A head group of 9..16 runs as two groups of 8.
-constexpr int kTcKeys = 128;
-constexpr int kTcHalf = kTcKeys * 128;          // bytes of one 64-dim half of a 128-key tile
-constexpr int kTcTile = 2 * kTcHalf;            // 32 KB
+// them, its V rows once the PV MMA has.  A CTA needs 37 KB of shared memory,
+// so six share an SM.  No operand goes through the register file: the tensor
+// cores read K, V, Q and P from shared memory by descriptor.  A head group of
+// 9..16 runs as two groups of 8.
+constexpr int kTcKeys = 64;
+constexpr int kTcHalf = kTcKeys * 128;          // bytes of one 64-dim half of a tile (8 KB)
+constexpr int kTcTile = 2 * kTcHalf;            // 16 KB
 constexpr uint64_t kTcWaitNs = 200ull * 1000 * 1000;
 
 template <int NT>
 constexpr size_t tc_prefill_smem() {  // + 1 KB to align the base to 1024 bytes
-  return 1024 + 2 * kTcTile + NT * 2048 /*Q*/ + NT * 2048 /*P*/ + 4 * 8 * NT * 4 /*maxima*/ + 4 * 8 * NT * 4 /*sums*/ +
-         64 /*barriers, TMEM slot, counts*/;
+  return 1024 + 2 * kTcTile + NT * 2048 /*Q*/ + NT * kTcKeys * 16 /*P*/ + 4 * 8 * NT * 4 /*maxima*/ +
+         4 * 8 * NT * 4 /*sums*/ + 64 /*barriers, TMEM slot, counts*/;
 }
 
 // Order-preserving map between fp32 and int32 (and back).
@@ -596,19 +599,19 @@ __device__ __forceinline__ int f2ord(float x) {
 __device__ __forceinline__ float ord2f(int o) { return __int_as_float(o >= 0 ? o : o ^ 0x7fffffff); }
 
 template <int NT, bool kBf16>
-__global__ void __launch_bounds__(kThreads, 3) sparse_prefill_tc_kernel(const PrefillArgs a) {
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 6 : 5) sparse_prefill_tc_kernel(const PrefillArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  const uint32_t kt = smem_addr(base);               // K tile [2 halves][128 keys][128 B], SW128
+  const uint32_t kt = smem_addr(base);               // K tile [2 halves][64 keys][128 B], SW128
   const uint32_t vt = kt + kTcTile;                  // V tile, same layout
   const uint32_t qt = vt + kTcTile;                  // Q: NT x [2 halves][8 heads][128 B], SW128
-  const uint32_t pt = qt + NT * 2048;                // P: NT x [128 keys][8 heads] fp16 (16 B rows)
-  int* redmax = reinterpret_cast<int*>(base + 2 * kTcTile + NT * 4096);  // [4 warps][8*NT]
-  float* redsum = reinterpret_cast<float*>(redmax + 4 * 8 * NT);          // [4 warps][8*NT]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(redsum + 4 * 8 * NT);     // S done, O done
+  const uint32_t pt = qt + NT * 2048;                // P: NT x [64 keys][8 heads] (16 B rows)
+  int* redmax = reinterpret_cast<int*>(base + 2 * kTcTile + NT * 2048 + NT * kTcKeys * 16);  // [4][8 NT]
+  float* redsum = reinterpret_cast<float*>(redmax + 4 * 8 * NT);                            // [4][8 NT]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(redsum + 4 * 8 * NT);                       // S done, O done
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
-  int* misc = reinterpret_cast<int*>(tslot + 1);                          // [4] last valid slot per warp
+  int* misc = reinterpret_cast<int*>(tslot + 1);                                            // [4] last valid slot
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const long long bid = blockIdx.x;
@@ -658,23 +661,29 @@ __global__ void __launch_bounds__(kThreads, 3) sparse_prefill_tc_kernel(const Pr
   const int nslots = max(max(misc[0], misc[1]), max(misc[2], misc[3])) + 1;
   const int ntiles = (nslots + kTcKeys - 1) / kTcKeys;
 
-  // Gathers: 16 lanes per 256-byte row, rows r*8 + tid/16 (r < 16); the chunk's
-  // swizzled slot depends only on the thread.
+  // Gathers: 16 lanes per 256-byte row, rows r*8 + tid/16 (r < 8); the chunk's
+  // swizzled slot depends only on the thread.  A tile's row offsets are loaded
+  // once and serve both the K and the V copies.
   const int ch = tid & 15, rsub = tid >> 4;
   const size_t head_off = (static_cast<size_t>(b) * a.S * a.Hkv + kvh) * kD + ch * 8;
   const __half* kbase = a.k + head_off;
   const __half* vbase = a.v + head_off;
   const int tok_stride = a.Hkv * kD;
   const uint32_t slot0 = (ch >> 3) * kTcHalf + rsub * 128 + (((ch & 7) ^ rsub) << 4);
-  auto issue = [&](int tile, uint32_t dst_tile, const __half* src_base) {
-    const int32_t* ids = lst + tile * kTcKeys + rsub;
-#pragma unroll 4
+  int rows[kTcKeys / 8];  // token ids of this thread's rows of the next tile, -1 when skipped
+  auto load_rows = [&](int tile) {
+#pragma unroll
     for (int r = 0; r < kTcKeys / 8; ++r) {
       const int slot = tile * kTcKeys + r * 8 + rsub;
-      const int j = slot < a.topK ? __ldg(ids + r * 8) : -1;
-      const bool ok = static_cast<unsigned>(j) < static_cast<unsigned>(L);
-      cp_async16(dst_tile + slot0 + r * 1024, src_base + static_cast<size_t>(ok ? j : 0) * tok_stride, ok);
+      const int j = slot < a.topK ? __ldg(lst + slot) : -1;
+      rows[r] = static_cast<unsigned>(j) < static_cast<unsigned>(L) ? j : -1;
     }
+  };
+  auto issue = [&](uint32_t dst_tile, const __half* src_base) {
+#pragma unroll
+    for (int r = 0; r < kTcKeys / 8; ++r)
+      cp_async16(dst_tile + slot0 + r * 1024, src_base + static_cast<size_t>(rows[r] >= 0 ? rows[r] : 0) * tok_stride,
+                 rows[r] >= 0);
   };
   const float sl2 = a.sl2;
   float o_acc[NT][8], l_part[NT][8], m_run[NT][8];
@@ -687,12 +696,14 @@ __global__ void __launch_bounds__(kThreads, 3) sparse_prefill_tc_kernel(const Pr
       m_run[nt][h] = -INFINITY;
     }
   const uint32_t lane_addr = static_cast<uint32_t>(32 * warp) << 16;
+  const bool has_key = lane < 16;  // M = 64: lanes 0..15 of each quadrant hold keys 16w .. 16w+15
   // A wait that runs out (a tensor-core fault) records a status bit; every
   // exit from the loop is decided at a barrier, so all threads leave together.
   bool ok = true, alive = true;
   if (ntiles > 0) {
-    issue(0, kt, kbase);
-    issue(0, vt, vbase);
+    load_rows(0);
+    issue(kt, kbase);
+    issue(vt, vbase);
   }
   cp_async_commit();
   for (int i = 0; i < ntiles; ++i) {
@@ -705,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 3) sparse_prefill_tc_kernel(const Pr
     }
     tc_fence_after();
     if (tid == 0) {
-      constexpr uint32_t idS = mma_idesc_f16(128, 8, kBf16, false, false);
+      constexpr uint32_t idS = mma_idesc_f16(64, 8, kBf16, false, false);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -717,15 +728,15 @@ __global__ void __launch_bounds__(kThreads, 3) sparse_prefill_tc_kernel(const Pr
       umma_commit(&bars[0]);
     }
     __syncwarp();
+    const int key_slot = i * kTcKeys + 16 * warp + (lane & 15);
+    const int jk = key_slot < a.topK ? __ldg(lst + key_slot) : -1;
+    const bool valid = has_key && static_cast<unsigned>(jk) < static_cast<unsigned>(L);
+    if (i + 1 < ntiles) load_rows(i + 1);
     ok = mbar_wait_bounded(&bars[0], i & 1, kTcWaitNs);
     if (!ok && a.status) atomicOr(a.status, kErrWaitTimeout);
     tc_fence_after();
-    // K has been read: the next tile's K rows can travel now.
-    if (i + 1 < ntiles) issue(i + 1, kt, kbase);
+    if (i + 1 < ntiles) issue(kt, kbase);  // K has been read: the next tile's K rows travel now
     cp_async_commit();
-    const int key_slot = i * kTcKeys + tid;
-    const int jk = key_slot < a.topK ? __ldg(lst + key_slot) : -1;
-    const bool valid = static_cast<unsigned>(jk) < static_cast<unsigned>(L);
     float x[NT][8];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -761,9 +772,10 @@ __global__ void __launch_bounds__(kThreads, 3) sparse_prefill_tc_kernel(const Pr
       }
 #pragma unroll
       for (int h = 0; h < 4; ++h) pk[h] = pack_p<kBf16>(x[nt][2 * h], x[nt][2 * h + 1]);
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(pt + nt * 2048 + tid * 16), "r"(pk[0]),
-                   "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
-                   : "memory");
+      if (has_key)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(pt + nt * kTcKeys * 16 + (16 * warp + lane) * 16),
+                     "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
+                     : "memory");
     }
     fence_proxy_async();  // P stores -> the tensor cores' reads
     tc_fence_before();
@@ -774,16 +786,16 @@ __global__ void __launch_bounds__(kThreads, 3) sparse_prefill_tc_kernel(const Pr
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int s = 0; s < 8; ++s)
+        for (int s = 0; s < kTcKeys / 16; ++s)
           umma_f16(tmem + 16 + nt * 8, smem_desc(vt + s * 2048, kTcHalf, 1024, kSmemSwizzle128B),
-                   smem_desc(pt + nt * 2048 + s * 256, 128, 128, kSmemSwizzleNone), idO, s > 0);
+                   smem_desc(pt + nt * kTcKeys * 16 + s * 256, 128, 128, kSmemSwizzleNone), idO, s > 0);
       umma_commit(&bars[1]);
     }
     __syncwarp();
     ok = mbar_wait_bounded(&bars[1], i & 1, kTcWaitNs);
     if (!ok && a.status) atomicOr(a.status, kErrWaitTimeout);
     tc_fence_after();
-    if (i + 1 < ntiles) issue(i + 1, vt, vbase);  // V has been read
+    if (i + 1 < ntiles) issue(vt, vbase);  // V has been read
     cp_async_commit();
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -795,14 +807,14 @@ __global__ void __launch_bounds__(kThreads, 3) sparse_prefill_tc_kernel(const Pr
   }
   cp_async_wait<0>();
   alive = alive && __syncthreads_and(ok);
-  // l: the sum over the CTA of each thread's share
+  // l: the sum over the CTA of each key lane's share
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int h = 0; h < 8; ++h) {
-      float v = l_part[nt][h];
+      float v = has_key ? l_part[nt][h] : 0.f;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+      for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
       if (lane == 0) redsum[warp * 8 * NT + nt * 8 + h] = v;
     }
   tc_fence_before();
