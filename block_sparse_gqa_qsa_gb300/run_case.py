@@ -10,6 +10,7 @@ of tens).
     python -m block_sparse_gqa_qsa_gb300.run_case prefill_S8192 --steps 2
     python -m block_sparse_gqa_qsa_gb300.run_case decode_long_B8_L512k --B 1 --steps 2
     python -m block_sparse_gqa_qsa_gb300.run_case prefill_S8192 --op rope --steps 2
+    python -m block_sparse_gqa_qsa_gb300.run_case prefill_S8192 --impl tcgen05 --steps 1
 
 `--op rope` runs qsa_rope_qkv on the workload's packed QKV instead (prefill
 workloads: dense q/k/v outputs).  `--op handoff` (prefill workloads) runs the
@@ -29,7 +30,7 @@ from . import _binding as qb
 from . import synthetic as syn
 
 
-def _prefill_steps(cfg, steps):
+def _prefill_steps(cfg, steps, impl="mma"):
     t = {k: v.cuda() for k, v in syn.make_prefill(cfg).items()}
     ws = qb.alloc_workspace(qb.indexer_prefill_workspace_size(cfg.B, cfg.S, cfg.di, cfg.ratio))
     ind = torch.empty((cfg.B, cfg.S, cfg.topK), dtype=torch.int32, device="cuda")
@@ -38,7 +39,7 @@ def _prefill_steps(cfg, steps):
     for _ in range(steps):
         qb.indexer_prefill(t["idxQ"], t["idxK"], t["wq"], t["wk"], t["ctx"], ind, ws, rot=cfg.rot, ratio=cfg.ratio,
                            budget=cfg.budget, topK=cfg.topK, theta=cfg.theta, eps=cfg.eps)
-        qb.sparse_prefill(t["q"], t["k"], t["v"], ind, t["ctx"], out, scale)
+        qb.sparse_prefill(t["q"], t["k"], t["v"], ind, t["ctx"], out, scale, impl=impl)
 
 
 def _rope_steps(cfg, steps):
@@ -100,6 +101,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2)
     ap.add_argument("--B", type=int, default=None, help="override the batch size")
     ap.add_argument("--ctx", type=int, default=None, help="decode: every sequence gets this total length")
+    ap.add_argument("--impl", choices=("mma", "tcgen05"), default="mma",
+                    help="prefill attention: qsa_sparse_prefill (mma.sync) or qsa_sparse_prefill_tcgen05")
     ap.add_argument("--op", choices=("path", "rope", "handoff", "gather"), default="path",
                     help="rope / handoff: qsa_rope_qkv / qsa_indexer_prefill_handoff of a prefill workload; "
                          "gather: qsa_gather_selected of a decode workload")
@@ -121,7 +124,7 @@ def main(argv=None):
             cfg = dataclasses.replace(cfg, ctx_lo=args.ctx, ctx_hi=args.ctx, max_ctx=max(args.ctx, 1), ctx_list=None)
         _decode_steps(cfg, args.steps)
     else:
-        _prefill_steps(cfg, args.steps)
+        _prefill_steps(cfg, args.steps, args.impl)
     torch.cuda.synchronize()
     print(f"ok: {args.steps} steps of {cfg.name} (B={cfg.B})")
 
