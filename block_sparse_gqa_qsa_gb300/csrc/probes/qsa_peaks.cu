@@ -9,6 +9,10 @@
 //       A warp instruction reads 512 contiguous bytes.  Bytes per launch:
 //       passes * bytes.  The buffer's lines are spread over both L2 halves of
 //       the two-die part, as the attention's K/V rows are.
+//   qsa_peaks_l2_cpasync  the same L2 -> SM bandwidth through cp.async.cg
+//       16-byte copies into shared memory (the attention kernels' path): every
+//       thread keeps 8 copies in flight into a 64 KB ring of its CTA, three
+//       CTAs per SM.  Bytes per launch: passes * bytes.
 //   qsa_peaks_ffma     CUDA-core fp32 FMA rate: 16 independent FMA chains per
 //       thread, `iters` steps each, so issue, not latency, is the limit.
 //       FMAs per launch: grid * 256 * 16 * iters.
@@ -39,6 +43,29 @@ __global__ void __launch_bounds__(512) l2_read_kernel(const uint4* __restrict__ 
   if (x == 0x9e3779b9u) sink[0] = x;  // keeps the loads; practically never stores
 }
 
+__global__ void __launch_bounds__(512) l2_cpasync_kernel(const uint4* __restrict__ buf, size_t mask, size_t total,
+                                                          unsigned* sink) {
+  extern __shared__ __align__(16) uint4 ring[];  // 512 threads x 8 chunks x 16 B = 64 KB
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(ring + threadIdx.x));
+  for (; e + 7 * stride < total; e += 8 * stride) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(base + u * 512 * 16),
+                   "l"(buf + ((e + u * stride) & mask))
+                   : "memory");
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+    asm volatile("cp.async.wait_group 1;\n" ::: "memory");  // one group of 8 copies stays in flight
+  }
+  for (int u = 0; e < total; e += stride, ++u)  // the last partial round: every counted byte is read
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(base + (u & 7) * 512 * 16), "l"(buf + (e & mask))
+                 : "memory");
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+  if (ring[threadIdx.x].x == 0x9e3779b9u && ring[threadIdx.x].y == 0x9e3779b9u) sink[0] = 1u;  // keeps the copies
+}
+
 __global__ void __launch_bounds__(256) ffma_kernel(float* out, int iters, float seed) {
   float a[16];
 #pragma unroll
@@ -66,6 +93,20 @@ __attribute__((visibility("default"))) int qsa_peaks_l2_read(const void* buf, si
   const size_t n16 = bytes / 16;
   l2_read_kernel<<<grid, 512, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<const uint4*>(buf), n16 - 1,
                                                                       n16 * static_cast<size_t>(passes), sink);
+  return static_cast<int>(cudaGetLastError());
+}
+
+// The same read through cp.async.cg into shared memory, `grid` CTAs of 512 threads (64 KB each).
+__attribute__((visibility("default"))) int qsa_peaks_l2_cpasync(const void* buf, size_t bytes, int passes,
+                                                                unsigned* sink, int grid, void* stream) {
+  if (!buf || !sink || bytes < 16 || (bytes & (bytes - 1)) || passes < 1 || grid < 1) return cudaErrorInvalidValue;
+  constexpr int kSmem = 512 * 8 * 16;
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(l2_cpasync_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (attr != cudaSuccess) return static_cast<int>(attr);
+  const size_t n16 = bytes / 16;
+  l2_cpasync_kernel<<<grid, 512, kSmem, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(buf), n16 - 1, n16 * static_cast<size_t>(passes), sink);
   return static_cast<int>(cudaGetLastError());
 }
 

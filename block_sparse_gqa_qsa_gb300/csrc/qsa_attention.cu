@@ -558,27 +558,25 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_k
 
 
 // ------------------------------------------------- prefill on tcgen05 / TMEM
-// The same contract as sparse_prefill_kernel, on the 5th-generation tensor
-// cores.  One CTA of 4 warps (one warpgroup, TMEM lanes 0..127) per (query
-// token, KV head); tiles of 64 keys.  Per tile:
+// The same contract as sparse_prefill_kernel, with S = q.k on the
+// 5th-generation tensor cores.  One CTA of 4 warps (one warpgroup, TMEM lanes
+// 0..127) per (query token, KV head); tiles of 64 keys.  Per tile:
 //   - the K and V rows the list names are gathered (16 lanes per 256-byte row,
 //     cp.async, zero-filled for skipped entries) into two 16 KB tiles in the
 //     SW128 layout, the 128 dims of a row split into two 64-dim halves;
-//   - one thread issues S^T = K Q^T (M = 64 keys, N = 8 heads, 8 MMAs of 16
-//     dims, both operands K-major) into TMEM and commits it to an mbarrier; an
-//     M = 64 accumulator puts key 16w + l in lane l of warp w's quadrant;
-//   - lanes 0..15 of each warp read their key's 8 scores from TMEM: scale,
-//     mask, the tile's max per head (a warp max on order-preserving integers,
-//     then across the 4 warps through shared memory), online-softmax rescale,
-//     P = 2^(x - m) rounded to the element type and stored as one 16-byte row
-//     [key][8 heads];
-//   - one thread issues O^T = V^T P^T (M = 128 dims, N = 8 heads, 4 MMAs of 16
-//     keys; V read MN-major from the same SW128 tile, P MN-major) into TMEM;
-//   - thread d adds dim d's 8 outputs to its registers (rescaled).
-// The next tile's K rows are requested as soon as this tile's S MMA has read
-// them, its V rows once the PV MMA has.  A CTA needs 37 KB of shared memory,
-// so six share an SM.  No operand goes through the register file: the tensor
-// cores read K, V, Q and P from shared memory by descriptor.  A head group of
+//   - one thread issues S^T = K Q^T (M = 64 keys, N = 8 heads, eight MMAs of
+//     16 dims, both operands read from shared memory by descriptor) into TMEM
+//     and commits it to an mbarrier: no thread loads K into registers;
+//   - an M = 64 accumulator puts key 16w + l in lane l of warp w's quadrant,
+//     so warp w reads the scores of exactly its 16 keys (tcgen05.ld) and runs
+//     its own online softmax over them, as the mma.sync kernel's warps do:
+//     a warp max per head (redux on order-preserving integers), rescale, P
+//     rounded to the element type and stored as 16-byte rows [key][8 heads];
+//   - the warp multiplies P into V with mma.sync (O^T += V^T P^T, V^T by
+//     ldmatrix.trans from the SW128 tile, P^T by ldmatrix.trans), keeping
+//     (m, l, O) in registers; the four warps merge once at the end.
+// Per gathered byte shared memory sees the cp.async write and the V read,
+// not the K read.  A CTA needs 37 KB, so six share an SM.  A head group of
 // 9..16 runs as two groups of 8.
 constexpr int kTcKeys = 64;
 constexpr int kTcHalf = kTcKeys * 128;          // bytes of one 64-dim half of a tile (8 KB)
@@ -587,8 +585,7 @@ constexpr uint64_t kTcWaitNs = 200ull * 1000 * 1000;
 
 template <int NT>
 constexpr size_t tc_prefill_smem() {  // + 1 KB to align the base to 1024 bytes
-  return 1024 + 2 * kTcTile + NT * 2048 /*Q*/ + NT * kTcKeys * 16 /*P*/ + 4 * 8 * NT * 4 /*maxima*/ +
-         4 * 8 * NT * 4 /*sums*/ + 64 /*barriers, TMEM slot, counts*/;
+  return 1024 + 2 * kTcTile + NT * 2048 /*Q*/ + 4 * NT * 256 /*P per warp*/ + 64 /*barrier, TMEM slot, counts*/;
 }
 
 // Order-preserving map between fp32 and int32 (and back).
@@ -598,6 +595,11 @@ __device__ __forceinline__ int f2ord(float x) {
 }
 __device__ __forceinline__ float ord2f(int o) { return __int_as_float(o >= 0 ? o : o ^ 0x7fffffff); }
 
+// Byte offset of 16-byte chunk c (dims 8c .. 8c+7) of key row r in a two-half SW128 tile.
+__device__ __forceinline__ uint32_t sw128h(int r, int c) {
+  return (c >> 3) * kTcHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
 template <int NT, bool kBf16>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 6 : 5) sparse_prefill_tc_kernel(const PrefillArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -606,12 +608,10 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 6 : 5) sparse_prefill_tc_k
   const uint32_t kt = smem_addr(base);               // K tile [2 halves][64 keys][128 B], SW128
   const uint32_t vt = kt + kTcTile;                  // V tile, same layout
   const uint32_t qt = vt + kTcTile;                  // Q: NT x [2 halves][8 heads][128 B], SW128
-  const uint32_t pt = qt + NT * 2048;                // P: NT x [64 keys][8 heads] (16 B rows)
-  int* redmax = reinterpret_cast<int*>(base + 2 * kTcTile + NT * 2048 + NT * kTcKeys * 16);  // [4][8 NT]
-  float* redsum = reinterpret_cast<float*>(redmax + 4 * 8 * NT);                            // [4][8 NT]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(redsum + 4 * 8 * NT);                       // S done, O done
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
-  int* misc = reinterpret_cast<int*>(tslot + 1);                                            // [4] last valid slot
+  const uint32_t pt = qt + NT * 2048;                // P: [4 warps][NT][16 keys][8 heads] (16 B rows)
+  uint64_t* bar = reinterpret_cast<uint64_t*>(base + 2 * kTcTile + NT * 2048 + 4 * NT * 256);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+  int* misc = reinterpret_cast<int*>(tslot + 1);     // [4] last valid slot per warp
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const long long bid = blockIdx.x;
@@ -649,64 +649,76 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 6 : 5) sparse_prefill_tc_k
   last = __reduce_max_sync(kFull, last);
   if (lane == 0) misc[warp] = last;
   if (tid == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
+    mbar_init(bar, 1);
     fence_barrier_init();
   }
   if (warp == 0) tmem_alloc(tslot, 32);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tslot;  // columns [0, 8 NT): S^T; [16, 16 + 8 NT): this tile's O^T
+  const uint32_t tmem = *tslot;  // columns [0, 8 NT): this tile's S^T
   const int nslots = max(max(misc[0], misc[1]), max(misc[2], misc[3])) + 1;
   const int ntiles = (nslots + kTcKeys - 1) / kTcKeys;
 
   // Gathers: 16 lanes per 256-byte row, rows r*8 + tid/16 (r < 8); the chunk's
-  // swizzled slot depends only on the thread.  A tile's row offsets are loaded
-  // once and serve both the K and the V copies.
+  // swizzled slot depends only on the thread.  A tile's row ids are loaded
+  // one tile ahead and serve both the K and the V copies.
   const int ch = tid & 15, rsub = tid >> 4;
   const size_t head_off = (static_cast<size_t>(b) * a.S * a.Hkv + kvh) * kD + ch * 8;
   const __half* kbase = a.k + head_off;
   const __half* vbase = a.v + head_off;
   const int tok_stride = a.Hkv * kD;
-  const uint32_t slot0 = (ch >> 3) * kTcHalf + rsub * 128 + (((ch & 7) ^ rsub) << 4);
-  int rows[kTcKeys / 8];  // token ids of this thread's rows of the next tile, -1 when skipped
-  auto load_rows = [&](int tile) {
+  const uint32_t slot0 = sw128h(rsub, ch);
+  int rows[kTcKeys / 8];  // token ids of this thread's rows of a tile, -1 when skipped
+  int key_id;             // lanes 0..15: the id of key 16 w + lane of a tile
+  auto load_ids = [&](int tile) {
 #pragma unroll
     for (int r = 0; r < kTcKeys / 8; ++r) {
       const int slot = tile * kTcKeys + r * 8 + rsub;
       const int j = slot < a.topK ? __ldg(lst + slot) : -1;
       rows[r] = static_cast<unsigned>(j) < static_cast<unsigned>(L) ? j : -1;
     }
+    const int ks = tile * kTcKeys + 16 * warp + (lane & 15);
+    key_id = ks < a.topK ? __ldg(lst + ks) : -1;
   };
-  auto issue = [&](uint32_t dst_tile, const __half* src_base) {
+  auto issue = [&]() {
 #pragma unroll
-    for (int r = 0; r < kTcKeys / 8; ++r)
-      cp_async16(dst_tile + slot0 + r * 1024, src_base + static_cast<size_t>(rows[r] >= 0 ? rows[r] : 0) * tok_stride,
-                 rows[r] >= 0);
+    for (int r = 0; r < kTcKeys / 8; ++r) {
+      const size_t off = static_cast<size_t>(rows[r] >= 0 ? rows[r] : 0) * tok_stride;
+      cp_async16(kt + slot0 + r * 1024, kbase + off, rows[r] >= 0);
+      cp_async16(vt + slot0 + r * 1024, vbase + off, rows[r] >= 0);
+    }
   };
+
   const float sl2 = a.sl2;
-  float o_acc[NT][8], l_part[NT][8], m_run[NT][8];
+  const int g = lane >> 2, q = lane & 3, mi = lane >> 3;
+  float o[8][NT][4];  // O^T fragments: dims 16*mt + (g, g+8), heads 8*nt + (2q, 2q+1)
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[mt][nt][i] = 0.f;
+  float m_run[NT][8], l_part[NT][8];  // per warp (uniform) running max; this lane's key's share of l
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int h = 0; h < 8; ++h) {
-      o_acc[nt][h] = 0.f;
-      l_part[nt][h] = 0.f;
       m_run[nt][h] = -INFINITY;
+      l_part[nt][h] = 0.f;
     }
   const uint32_t lane_addr = static_cast<uint32_t>(32 * warp) << 16;
-  const bool has_key = lane < 16;  // M = 64: lanes 0..15 of each quadrant hold keys 16w .. 16w+15
+  const uint32_t pw = pt + warp * NT * 256;  // this warp's P rows
   // A wait that runs out (a tensor-core fault) records a status bit; every
   // exit from the loop is decided at a barrier, so all threads leave together.
   bool ok = true, alive = true;
   if (ntiles > 0) {
-    load_rows(0);
-    issue(kt, kbase);
-    issue(vt, vbase);
+    load_ids(0);
+    issue();
   }
   cp_async_commit();
   for (int i = 0; i < ntiles; ++i) {
+    const int my_key = key_id;
     cp_async_wait<0>();
     fence_proxy_async();  // cp.async writes -> the tensor cores' reads
     tc_fence_before();
@@ -725,117 +737,115 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 6 : 5) sparse_prefill_tc_k
           umma_f16(tmem + nt * 8, smem_desc(kt + koff, 16, 1024, kSmemSwizzle128B),
                    smem_desc(qt + nt * 2048 + (s >> 2) * 1024 + (s & 3) * 32, 16, 1024, kSmemSwizzle128B), idS, s > 0);
         }
-      umma_commit(&bars[0]);
+      umma_commit(bar);
     }
     __syncwarp();
-    const int key_slot = i * kTcKeys + 16 * warp + (lane & 15);
-    const int jk = key_slot < a.topK ? __ldg(lst + key_slot) : -1;
-    const bool valid = has_key && static_cast<unsigned>(jk) < static_cast<unsigned>(L);
-    if (i + 1 < ntiles) load_rows(i + 1);
-    ok = mbar_wait_bounded(&bars[0], i & 1, kTcWaitNs);
+    if (i + 1 < ntiles) load_ids(i + 1);  // the next tile's ids travel while S is computed
+    ok = mbar_wait_bounded(bar, i & 1, kTcWaitNs);
     if (!ok && a.status) atomicOr(a.status, kErrWaitTimeout);
     tc_fence_after();
-    if (i + 1 < ntiles) issue(kt, kbase);  // K has been read: the next tile's K rows travel now
-    cp_async_commit();
-    float x[NT][8];
+    const bool valid = lane < 16 && static_cast<unsigned>(my_key) < static_cast<unsigned>(L);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float sv[8];
       tmem_ld8(tmem + lane_addr + nt * 8, sv);
-#pragma unroll
-      for (int h = 0; h < 8; ++h) {
-        x[nt][h] = valid ? sv[h] * sl2 : -INFINITY;
-        const int mx = __reduce_max_sync(kFull, f2ord(x[nt][h]));
-        if (lane == 0) redmax[warp * 8 * NT + nt * 8 + h] = mx;
-      }
-    }
-    tc_fence_before();
-    if (__syncthreads_or(!ok)) {
-      alive = false;
-      break;
-    }
-    float alpha[NT][8];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
+      float al[8];
       uint32_t pk[4];
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
-        const int c = nt * 8 + h;
-        const float tmax = ord2f(max(max(redmax[c], redmax[8 * NT + c]), max(redmax[16 * NT + c], redmax[24 * NT + c])));
+        const float x = valid ? sv[h] * sl2 : -INFINITY;
+        const float tmax = ord2f(__reduce_max_sync(kFull, f2ord(x)));
         const float mn = fmaxf(m_run[nt][h], tmax);
         const float mu = mn == -INFINITY ? 0.f : mn;
-        alpha[nt][h] = ex2_ftz(m_run[nt][h] - mu);
+        al[h] = ex2_ftz(m_run[nt][h] - mu);
         m_run[nt][h] = mn;
-        const float p = ex2_ftz(x[nt][h] - mu);
-        l_part[nt][h] = l_part[nt][h] * alpha[nt][h] + p;
-        x[nt][h] = p;
+        const float p = ex2_ftz(x - mu);
+        l_part[nt][h] = l_part[nt][h] * al[h] + p;
+        sv[h] = p;
       }
 #pragma unroll
-      for (int h = 0; h < 4; ++h) pk[h] = pack_p<kBf16>(x[nt][2 * h], x[nt][2 * h + 1]);
-      if (has_key)
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(pt + nt * kTcKeys * 16 + (16 * warp + lane) * 16),
-                     "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
+      for (int h = 0; h < 4; ++h) pk[h] = pack_p<kBf16>(sv[2 * h], sv[2 * h + 1]);
+      if (lane < 16)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(pw + nt * 256 + lane * 16), "r"(pk[0]),
+                     "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
                      : "memory");
-    }
-    fence_proxy_async();  // P stores -> the tensor cores' reads
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {
-      constexpr uint32_t idO = mma_idesc_f16(128, 8, kBf16, true, true);
+      // rescale this thread's O^T fragments (heads 2q, 2q+1 of group nt)
+      const float a0 = q == 0 ? al[0] : q == 1 ? al[2] : q == 2 ? al[4] : al[6];
+      const float a1 = q == 0 ? al[1] : q == 1 ? al[3] : q == 2 ? al[5] : al[7];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int s = 0; s < kTcKeys / 16; ++s)
-          umma_f16(tmem + 16 + nt * 8, smem_desc(vt + s * 2048, kTcHalf, 1024, kSmemSwizzle128B),
-                   smem_desc(pt + nt * kTcKeys * 16 + s * 256, 128, 128, kSmemSwizzleNone), idO, s > 0);
-      umma_commit(&bars[1]);
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][nt][0] *= a0;
+        o[mt][nt][1] *= a1;
+        o[mt][nt][2] *= a0;
+        o[mt][nt][3] *= a1;
+      }
     }
     __syncwarp();
-    ok = mbar_wait_bounded(&bars[1], i & 1, kTcWaitNs);
-    if (!ok && a.status) atomicOr(a.status, kErrWaitTimeout);
-    tc_fence_after();
-    if (i + 1 < ntiles) issue(vt, vbase);  // V has been read
-    cp_async_commit();
+    uint32_t pb[NT][2];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float ov[8];
-      tmem_ld8(tmem + lane_addr + 16 + nt * 8, ov);
+    for (int nt = 0; nt < NT; ++nt) ldsm_x2_t(pw + nt * 256 + (lane & 15) * 16, pb[nt][0], pb[nt][1]);
+    // O^T += V^T P^T over the warp's 16 keys (rows 16 w .. 16 w + 15 of the V tile)
+    const int kr0 = warp * 16;
 #pragma unroll
-      for (int h = 0; h < 8; ++h) o_acc[nt][h] = o_acc[nt][h] * alpha[nt][h] + ov[h];
+    for (int mt = 0; mt < 8; ++mt) {
+      uint32_t av[4];
+      ldsm_x4_t(vt + sw128h(kr0 + (lane & 7) + 8 * (mi >> 1), 2 * mt + (mi & 1)), av[0], av[1], av[2], av[3]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_tile<kBf16>(o[mt][nt], av, pb[nt][0], pb[nt][1]);
     }
+    tc_fence_before();
+    __syncthreads();  // every warp is done with the V tile and its P rows; S has been read
+    if (i + 1 < ntiles) issue();
+    cp_async_commit();
   }
   cp_async_wait<0>();
   alive = alive && __syncthreads_and(ok);
-  // l: the sum over the CTA of each key lane's share
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int h = 0; h < 8; ++h) {
-      float v = has_key ? l_part[nt][h] : 0.f;
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-      if (lane == 0) redsum[warp * 8 * NT + nt * 8 + h] = v;
-    }
-  tc_fence_before();
-  __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 32);
   if (!alive) return;
-  // thread d writes dim d of every head of the group
+  // Each warp's (m, l, O^T) to shared memory (the tiles are free), then the
+  // four warps merge: mw/lw [4][16], ow [4][16][kOStride].
+  float* mw = reinterpret_cast<float*>(base);
+  float* lw = mw + 64;
+  float* ow = lw + 64;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int h = 0; h < 8; ++h) {
-      const int c = nt * 8 + h;
-      if (c < a.G) {
-        const float Ls = redsum[c] + redsum[8 * NT + c] + redsum[16 * NT + c] + redsum[24 * NT + c];
-        const float v = Ls > 0.f ? o_acc[nt][h] / Ls : 0.f;
-        if constexpr (kBf16)
-          reinterpret_cast<__nv_bfloat16*>(out)[c * kD + tid] = __float2bfloat16_rn(v);
-        else
-          out[c * kD + tid] = __float2half_rn(v);
+      float v = lane < 16 ? l_part[nt][h] : 0.f;
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+      if (lane == 0) {
+        mw[warp * 16 + 8 * nt + h] = m_run[nt][h];
+        lw[warp * 16 + 8 * nt + h] = v;
       }
     }
+  {
+    float* ob = ow + warp * 16 * kOStride;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int h = 8 * nt + 2 * q, d = 16 * mt + g;
+        ob[h * kOStride + d] = o[mt][nt][0];
+        ob[(h + 1) * kOStride + d] = o[mt][nt][1];
+        ob[h * kOStride + d + 8] = o[mt][nt][2];
+        ob[(h + 1) * kOStride + d + 8] = o[mt][nt][3];
+      }
+  }
+  __syncthreads();
+  for (int e = tid; e < a.G * (kD / 2); e += kThreads) {
+    const int h = e / (kD / 2), d = 2 * (e % (kD / 2));
+    float f[4], Lsum;
+    merge_weights(mw, lw, h, f, Lsum);
+    float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      o0 += f[w] * ow[(w * 16 + h) * kOStride + d];
+      o1 += f[w] * ow[(w * 16 + h) * kOStride + d + 1];
+    }
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    store_pair<kBf16>(out + h * kD + d, o0 * inv, o1 * inv);
+  }
 }
 
 // Ring depth of both kernels: one 64-key tile (42 KB of shared memory, 5 CTAs
