@@ -201,6 +201,14 @@ __device__ __forceinline__ float merge_weights(const float* mw, const float* lw,
 }
 
 // ------------------------------------------------------------------ prefill
+// The staged list is permuted within each 64-key tile so that the 8 rows one
+// gathering thread copies (keys 8r + c, r < 8, for its row-in-group c) sit in 8
+// consecutive ints: slot 8c + r of the tile holds key 8r + c.
+__device__ __forceinline__ int perm_slot(int i) {
+  const int k = i & (kKeys - 1);
+  return (i & ~(kKeys - 1)) | ((k & 7) << 3) | (k >> 3);
+}
+
 struct PrefillArgs {
   const __half* q;
   const __half* k;
@@ -261,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_
       const int i = i0 + u * kThreads;
       if (i < a.topKpad) {
         const bool ok = static_cast<unsigned>(jv[u]) < static_cast<unsigned>(L);
-        idx_s[i] = ok ? jv[u] : -1;
+        idx_s[perm_slot(i)] = ok ? jv[u] : -1;
         last = ok ? i : last;
         bad |= !ok && jv[u] != -1;
       }
@@ -287,10 +295,12 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_
   auto issue = [&](int tile, int stage) {
     const uint32_t kdst = ring + stage * 2 * kTileBytes + slot0;
     const uint32_t vdst = kdst + kTileBytes;
-    const int* ids = idx_s + tile * kKeys + (tid >> 4);
+    const int4* ids4 = reinterpret_cast<const int4*>(idx_s + tile * kKeys + (tid >> 4) * 8);
+    const int4 i0 = ids4[0], i1 = ids4[1];
+    const int idv[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
 #pragma unroll
     for (int r = 0; r < kKeys / 8; ++r) {
-      const int j = ids[r * 8];
+      const int j = idv[r];
       const bool ok = j >= 0;
       const size_t off = static_cast<size_t>(ok ? j : 0) * tok_stride;
       cp_async16(kdst + r * 8 * 256, kbase + off, ok);
@@ -313,7 +323,8 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_
       cp_async_wait<0>();
       __syncthreads();
       const int slot = i * kKeys + warp * 16 + (lane >> 2);
-      attend16<NT, kBf16>(A, ring, ring + kTileBytes, qf, idx_s[slot] >= 0, idx_s[slot + 8] >= 0, a.sl2);
+      attend16<NT, kBf16>(A, ring, ring + kTileBytes, qf, idx_s[perm_slot(slot)] >= 0,
+                          idx_s[perm_slot(slot + 8)] >= 0, a.sl2);
     }
   } else {
 #pragma unroll
@@ -332,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_
       const int stage = i % STAGES;
       const int slot = i * kKeys + warp * 16 + (lane >> 2);
       attend16<NT, kBf16>(A, ring + stage * 2 * kTileBytes, ring + stage * 2 * kTileBytes + kTileBytes, qf,
-                   idx_s[slot] >= 0, idx_s[slot + 8] >= 0, a.sl2);
+                   idx_s[perm_slot(slot)] >= 0, idx_s[perm_slot(slot + 8)] >= 0, a.sl2);
     }
   }
   cp_async_wait<0>();
