@@ -431,8 +431,8 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_k
                       static_cast<unsigned>(kp[u]) < static_cast<unsigned>(a.numFlatPages) &&
                       static_cast<unsigned>(vp[u]) < static_cast<unsigned>(a.numFlatPages);
       const long long within = static_cast<long long>((j & 127) * a.Hkv + kvh) * a.poolHeadDim;
-      kofs[i] = ok ? static_cast<long long>(kp[u]) * kTokensPerPage * a.Hkv * a.poolHeadDim + within : -1;
-      vofs[i] = ok ? static_cast<long long>(vp[u]) * kTokensPerPage * a.Hkv * a.poolHeadDim + within : -1;
+      kofs[perm_slot(i)] = ok ? static_cast<long long>(kp[u]) * kTokensPerPage * a.Hkv * a.poolHeadDim + within : -1;
+      vofs[perm_slot(i)] = ok ? static_cast<long long>(vp[u]) * kTokensPerPage * a.Hkv * a.poolHeadDim + within : -1;
       last = ok ? i : last;
       const bool live = static_cast<unsigned>(j) < static_cast<unsigned>(L);
       bad |= !live && j != -1 ? kErrBadIndex : 0;
@@ -458,13 +458,21 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_k
     const uint32_t kdst = ring + stage * 2 * kTileBytes;
     const uint32_t vdst = kdst + kTileBytes;
     const int ch = tid & 15;
+    // this thread's 8 rows (keys 8r + tid/16) sit in 8 consecutive slots of the permuted offsets
+    const longlong2* k2 = reinterpret_cast<const longlong2*>(kofs + tile * kKeys + (tid >> 4) * 8);
+    const longlong2* v2 = reinterpret_cast<const longlong2*>(vofs + tile * kKeys + (tid >> 4) * 8);
 #pragma unroll
-    for (int r = 0; r < kKeys / 8; ++r) {
-      const int key = r * 8 + (tid >> 4);
-      const long long ko = kofs[tile * kKeys + key], vo = vofs[tile * kKeys + key];
-      const bool ok = ko >= 0;
-      cp_async16(kdst + swz(key, ch), a.pool + (ok ? ko : 0) + ch * 8, ok);
-      cp_async16(vdst + swz(key, ch), a.pool + (ok ? vo : 0) + ch * 8, ok);
+    for (int hf = 0; hf < 2; ++hf) {  // rows 4 hf .. 4 hf + 3: four offsets of each kind live at a time
+      const longlong2 ka = k2[2 * hf], kb = k2[2 * hf + 1], va = v2[2 * hf], vb = v2[2 * hf + 1];
+      const long long kov[4] = {ka.x, ka.y, kb.x, kb.y}, vov[4] = {va.x, va.y, vb.x, vb.y};
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int key = (4 * hf + rr) * 8 + (tid >> 4);
+        const long long ko = kov[rr], vo = vov[rr];
+        const bool ok = ko >= 0;
+        cp_async16(kdst + swz(key, ch), a.pool + (ok ? ko : 0) + ch * 8, ok);
+        cp_async16(vdst + swz(key, ch), a.pool + (ok ? vo : 0) + ch * 8, ok);
+      }
     }
   };
   uint32_t qf[NT][8][2];
@@ -485,7 +493,8 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_k
       cp_async_wait<0>();
       __syncthreads();
       const int slot = i * kKeys + warp * 16 + (lane >> 2);
-      attend16<NT, kBf16>(A, ring, ring + kTileBytes, qf, kofs[slot] >= 0, kofs[slot + 8] >= 0, a.sl2);
+      attend16<NT, kBf16>(A, ring, ring + kTileBytes, qf, kofs[perm_slot(slot)] >= 0,
+                          kofs[perm_slot(slot + 8)] >= 0, a.sl2);
     }
   } else {
 #pragma unroll
@@ -504,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_k
       const int stage = i % STAGES;
       const int slot = i * kKeys + warp * 16 + (lane >> 2);
       attend16<NT, kBf16>(A, ring + stage * 2 * kTileBytes, ring + stage * 2 * kTileBytes + kTileBytes, qf,
-                   kofs[slot] >= 0, kofs[slot + 8] >= 0, a.sl2);
+                   kofs[perm_slot(slot)] >= 0, kofs[perm_slot(slot + 8)] >= 0, a.sl2);
     }
   }
   cp_async_wait<0>();
