@@ -227,7 +227,8 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_
   const uint32_t ring = smem_addr(smem);                       // [STAGES][K 16 KB | V 16 KB]
   const uint32_t q_tile = ring + STAGES * 2 * kTileBytes;      // [8*NT][256 B]
   int* idx_s = reinterpret_cast<int*>(smem + STAGES * 2 * kTileBytes + NT * 8 * 256);
-  int* misc = idx_s + a.topKpad;
+  uint32_t* vmask = reinterpret_cast<uint32_t*>(idx_s + a.topKpad);  // bit k of word w: slot 32 w + k is valid
+  int* misc = reinterpret_cast<int*>(vmask + a.topKpad / 32);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Within a sequence the CTAs run the rows from the last position down: the
@@ -270,6 +271,8 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_
       if (i < a.topKpad) {
         const bool ok = static_cast<unsigned>(jv[u]) < static_cast<unsigned>(L);
         idx_s[perm_slot(i)] = ok ? jv[u] : -1;
+        const unsigned m = __ballot_sync(kFull, ok);  // the warp holds 32 consecutive slots
+        if (lane == 0) vmask[i >> 5] = m;
         last = ok ? i : last;
         bad |= !ok && jv[u] != -1;
       }
@@ -322,9 +325,11 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_
       cp_async_commit();
       cp_async_wait<0>();
       __syncthreads();
-      const int slot = i * kKeys + warp * 16 + (lane >> 2);
-      attend16<NT, kBf16>(A, ring, ring + kTileBytes, qf, idx_s[perm_slot(slot)] >= 0,
-                          idx_s[perm_slot(slot + 8)] >= 0, a.sl2);
+      const uint2 vm = *reinterpret_cast<const uint2*>(vmask + 2 * i);  // the tile's 64 validity bits
+      const int k0 = warp * 16 + (lane >> 2);
+      const uint32_t w0 = k0 < 32 ? vm.x : vm.y, w1 = k0 + 8 < 32 ? vm.x : vm.y;
+      attend16<NT, kBf16>(A, ring, ring + kTileBytes, qf, (w0 >> (k0 & 31)) & 1u, (w1 >> ((k0 + 8) & 31)) & 1u,
+                          a.sl2);
     }
   } else {
 #pragma unroll
@@ -341,9 +346,11 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_
       if (i + STAGES - 1 < ntiles) issue(i + STAGES - 1, (i + STAGES - 1) % STAGES);
       cp_async_commit();
       const int stage = i % STAGES;
-      const int slot = i * kKeys + warp * 16 + (lane >> 2);
+      const uint2 vm = *reinterpret_cast<const uint2*>(vmask + 2 * i);
+      const int k0 = warp * 16 + (lane >> 2);
+      const uint32_t w0 = k0 < 32 ? vm.x : vm.y, w1 = k0 + 8 < 32 ? vm.x : vm.y;
       attend16<NT, kBf16>(A, ring + stage * 2 * kTileBytes, ring + stage * 2 * kTileBytes + kTileBytes, qf,
-                   idx_s[perm_slot(slot)] >= 0, idx_s[perm_slot(slot + 8)] >= 0, a.sl2);
+                   (w0 >> (k0 & 31)) & 1u, (w1 >> ((k0 + 8) & 31)) & 1u, a.sl2);
     }
   }
   cp_async_wait<0>();
@@ -878,7 +885,7 @@ constexpr int kRingStagesFor = NT == 1 ? 1 : 2;
 template <int NT>
 size_t prefill_smem(int topKpad) {
   return static_cast<size_t>(kRingStagesFor<NT>) * 2 * kTileBytes + NT * 8 * 256 +
-         static_cast<size_t>(topKpad) * 4 + 64;
+         static_cast<size_t>(topKpad) * 4 + topKpad / 8 + 64;
 }
 template <int NT>
 size_t decode_smem(int slicePad) {
