@@ -17,7 +17,8 @@
 //                          in integer turns), block scores on the CUDA cores
 //                          (fp32 FMA, a register-tiled contraction of 8 rows x
 //                          8 heads against 256-block tiles staged in shared
-//                          memory), the relu/head sum into the CTA's own score
+//                          memory, heads paired in fp32x2 FMAs), the
+//                          relu/head sum into the CTA's own score
 //                          slot and a 256-bin histogram of the score bits per
 //                          row.  Then each warp selects its row: the bin of
 //                          the cut from the histogram, radix narrowing of that
@@ -190,11 +191,11 @@ __device__ __noinline__ void score_rows(const SelArgs& a, float* smem, int b, in
     const uint4 zero = make_uint4(0, 0, 0, 0);
     uint4 pre0 = gok ? __ldg(src) : zero;
     uint4 pre1 = gok ? __ldg(src + 1) : zero;
-    float acc[8][kHI];
+    uint64_t acc[8][kHI / 2];  // heads (2j, 2j+1) of block lane + 32 m as one fp32 pair
 #pragma unroll
     for (int m = 0; m < 8; ++m)
 #pragma unroll
-      for (int h = 0; h < kHI; ++h) acc[m][h] = 0.f;
+      for (int j = 0; j < kHI / 2; ++j) acc[m][j] = 0ull;
 
 #pragma unroll 1
     for (int kc = 0; kc < DI / kKC; ++kc) {
@@ -215,26 +216,24 @@ __device__ __noinline__ void score_rows(const SelArgs& a, float* smem, int b, in
       const float* kt = kb_s + (kc & 1) * kTile * kKS;
       const float* qk = q_s + static_cast<size_t>(kc * kKC) * kRows * kHI + warp * kHI;
 #pragma unroll 4
-      for (int kp = 0; kp < kKC / 2; ++kp) {  // two dims per step: 16 key values, 16 query values, 128 FMAs
+      for (int kp = 0; kp < kKC / 2; ++kp) {  // two dims per step: 16 key values, 16 query values, 128 FMAs in 64 pair FMAs
         float2 kv[8];
 #pragma unroll
         for (int m = 0; m < 8; ++m) kv[m] = *reinterpret_cast<const float2*>(kt + (lane + 32 * m) * kKS + kp * 2);
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
-          const float* qp = qk + (kp * 2 + kk) * kRows * kHI;
-          const float4 qa = *reinterpret_cast<const float4*>(qp);
-          const float4 qb = *reinterpret_cast<const float4*>(qp + 4);
+          // the 8 heads' query values as 4 fp32 pairs; each pair FMA is two independent fp32 FMAs,
+          // so every accumulator stays the plain ascending-k chain
+          const ulonglong2* qp = reinterpret_cast<const ulonglong2*>(qk + (kp * 2 + kk) * kRows * kHI);
+          const ulonglong2 qa = qp[0], qb = qp[1];
 #pragma unroll
           for (int m = 0; m < 8; ++m) {
             const float kval = kk == 0 ? kv[m].x : kv[m].y;
-            acc[m][0] = fmaf(qa.x, kval, acc[m][0]);
-            acc[m][1] = fmaf(qa.y, kval, acc[m][1]);
-            acc[m][2] = fmaf(qa.z, kval, acc[m][2]);
-            acc[m][3] = fmaf(qa.w, kval, acc[m][3]);
-            acc[m][4] = fmaf(qb.x, kval, acc[m][4]);
-            acc[m][5] = fmaf(qb.y, kval, acc[m][5]);
-            acc[m][6] = fmaf(qb.z, kval, acc[m][6]);
-            acc[m][7] = fmaf(qb.w, kval, acc[m][7]);
+            const uint64_t k2 = pack_f2(kval, kval);
+            acc[m][0] = ffma2(qa.x, k2, acc[m][0]);
+            acc[m][1] = ffma2(qa.y, k2, acc[m][1]);
+            acc[m][2] = ffma2(qb.x, k2, acc[m][2]);
+            acc[m][3] = ffma2(qb.y, k2, acc[m][3]);
           }
         }
       }
@@ -246,7 +245,11 @@ __device__ __noinline__ void score_rows(const SelArgs& a, float* smem, int b, in
         if (g < n_c) {
           float sc = 0.f;
 #pragma unroll
-          for (int h = 0; h < kHI; ++h) sc += acc[m][h] > 0.f ? acc[m][h] : 0.f;
+          for (int j = 0; j < kHI / 2; ++j) {
+            const float h0 = lo_f2(acc[m][j]), h1 = hi_f2(acc[m][j]);
+            sc += h0 > 0.f ? h0 : 0.f;
+            sc += h1 > 0.f ? h1 : 0.f;
+          }
           srow[g] = sc;  // read back later by this same lane only
           atomicAdd(hist + score_bin(__float_as_uint(sc)), 1u);
         }
