@@ -148,6 +148,8 @@ def lib() -> ctypes.CDLL:
             L.qsa_last_error_message.restype = ctypes.c_char_p
             L.qsa_last_device_error.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(_i32)]
             L.qsa_last_device_error.restype = ctypes.c_int
+            L.qsa_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+            L.qsa_debug_set_wait_limit_ns.restype = None
             _lib = L
     return _lib
 
@@ -188,6 +190,11 @@ def sparse_decode_workspace_elems(B: int, Hkv: int, D: int) -> tuple[int, int, i
     L = lib()
     return (L.qsa_sparse_decode_partial_o_elems(B, Hkv, D), L.qsa_sparse_decode_partial_stats_elems(B, Hkv),
             L.qsa_sparse_decode_counter_elems(B, Hkv))
+
+
+def debug_set_wait_limit_ns(ns: int) -> None:
+    """qsa_debug_set_wait_limit_ns: a test bound on the decode scorer's progress waits (0 restores 0.2 s)."""
+    lib().qsa_debug_set_wait_limit_ns(int(ns))
 
 
 def last_device_error(workspace: torch.Tensor, stream=None) -> int:

@@ -171,6 +171,8 @@ qsa_status_t qsa_last_device_error(const void* workspace, void* stream, int32_t*
   return e == cudaSuccess ? ok() : cuda_fail(e, "qsa_last_device_error");
 }
 
+void qsa_debug_set_wait_limit_ns(uint64_t ns) { qsa::set_decode_wait_limit_ns(ns); }
+
 int32_t qsa_indexer_prefill_max_blocks(void) { return qsa::kPrefillMaxSeqLen; }
 int32_t qsa_indexer_prefill_max_seq_len(void) { return qsa::kPrefillMaxSeqLen; }
 

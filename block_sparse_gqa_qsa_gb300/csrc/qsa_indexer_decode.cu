@@ -37,6 +37,8 @@
 //       the histogram and its ticket.
 // Waits on TMA barriers are bounded; on expiry the kernel records
 // kErrWaitTimeout in the workspace status word and stops.
+#include <atomic>
+
 #include "qsa_blockkey.cuh"
 #include "qsa_device.cuh"
 #include "qsa_internal.h"
@@ -226,6 +228,7 @@ struct ScoreArgs {
   int32_t* hist;
   int32_t* status;
   int B, maxPagesPerSeq, numFlatPages, ratio, nbmax;
+  uint64_t waitNs;  // bound of the waits on the stream's progress (copies in flight keep kWaitLimitNs)
 };
 
 __host__ __device__ __forceinline__ int score_smem_bytes(int di, int ratio, int B) {
@@ -410,7 +413,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
         int ok = 1;
         if (lane == 0) {
           const int jdx = static_cast<int>(base + k - lo), s = jdx % kStages, n = jdx / kStages;
-          if (!mbar_wait_bounded(&empty[s], (n & 1) ^ 1, kWaitLimitNs)) {
+          if (!mbar_wait_bounded(&empty[s], (n & 1) ^ 1, a.waitNs)) {
             atomicOr(a.status, kErrWaitTimeout);
             ok = 0;
           } else {
@@ -459,8 +462,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1) decode_score_kernel(const Sc
     // its full phase would then look complete to a parity wait.  Waiting first
     // for that page to be consumed (empty phase n-1) leaves the full barrier
     // exactly one phase short of page jx's, so the parity wait is exact.
-    if ((n > 0 && !mbar_wait_bounded(&empty[s], (n - 1) & 1, kWaitLimitNs)) ||
-        !mbar_wait_bounded(&full[s], n & 1, kWaitLimitNs)) {
+    if ((n > 0 && !mbar_wait_bounded(&empty[s], (n - 1) & 1, a.waitNs)) ||
+        !mbar_wait_bounded(&full[s], n & 1, a.waitNs)) {
       if (lane == 0) atomicOr(a.status, kErrWaitTimeout);
       break;
     }
@@ -804,7 +807,11 @@ __global__ void __launch_bounds__(kSelThreads) decode_select_kernel(const Select
   if (tid == 0) a.ticket[b] = 0;
 }
 
+std::atomic<uint64_t> g_wait_limit_ns{0};
+
 }  // namespace
+
+void set_decode_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns, std::memory_order_relaxed); }
 
 int sm_count() {
   static int cached[64] = {0};
@@ -876,6 +883,8 @@ cudaError_t launch_indexer_decode(const QsaIndexerDecodeParams& p, const RopeFre
   sa.numFlatPages = p.numFlatPages;
   sa.ratio = p.compressRatio;
   sa.nbmax = nbmax;
+  const uint64_t wl = g_wait_limit_ns.load(std::memory_order_relaxed);
+  sa.waitNs = wl ? wl : kWaitLimitNs;
   const int smem = score_smem_bytes(p.headDim, p.compressRatio, B);
   if (smem > kMaxDynSmem) return cudaErrorInvalidValue;
   const long long maxPages = static_cast<long long>(B) * p.maxPagesPerSeq;

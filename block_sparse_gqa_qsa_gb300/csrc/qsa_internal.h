@@ -41,6 +41,8 @@ constexpr int kDecodeMaxBatch = 1024;   // the streaming scorer keeps a per-sequ
 size_t indexer_decode_workspace_bytes(int B, int maxPagesPerSeq, int ratio, int budget);
 cudaError_t launch_indexer_decode(const QsaIndexerDecodeParams& p, const RopeFreqs& rf,
                                   const CUtensorMap& kbarMap);
+// Bound of the decode scorer's progress waits (0: the default 0.2 s); see qsa_debug_set_wait_limit_ns.
+void set_decode_wait_limit_ns(uint64_t ns);
 
 // Attention -----------------------------------------------------------------
 // bf16: Q/K/V/O (prefill) or q/pool/o (decode) hold bfloat16 instead of fp16.

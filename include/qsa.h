@@ -446,6 +446,16 @@ QSA_API int32_t qsa_indexer_prefill_max_blocks(void);
  * enqueued.  Nothing else is read or written. */
 QSA_API qsa_status_t qsa_last_device_error(const void* workspace, void* stream, int32_t* out);
 
+/* Testing hook for the device-side error path (process-wide, not for
+ * production use): bounds every later qsa_indexer_decode call's waits on the
+ * progress of its own page stream to `ns` nanoseconds instead of 0.2 s, so
+ * that a test can make them run out and read bit 0 of the status word.  0
+ * restores the 0.2 s bound.  The wait for copies already in flight before a
+ * CTA exits keeps its 0.2 s bound whatever is set, so no copy outlives its
+ * CTA.  The lists of a call whose waits ran out are not valid; zero-fill the
+ * workspace before the next call. */
+QSA_API void qsa_debug_set_wait_limit_ns(uint64_t ns);
+
 /* Human-readable name of a status, and the detail of the last failure on the
  * calling thread (never NULL; empty when there was none). */
 QSA_API const char* qsa_status_string(qsa_status_t status);

@@ -170,6 +170,39 @@ def test_indexer_decode_bad_page_sets_status_bit():
     assert not qb.last_device_error(ws) & 1, "no wait may time out"
 
 
+def test_indexer_decode_wait_timeout_sets_status_bit():
+    """The device-side error path of the page stream: with its progress waits bounded to 1 ns they run
+    out, the scorer stops early and records bit 0 of the status word instead of hanging; the call itself
+    returns QSA_OK.  Copies already in flight are still waited for (their own 0.2 s bound), so the
+    context stays usable: with the default bound restored and a zero-filled workspace, the next call
+    matches the oracle with a clean status word."""
+    # 4 sequences of 256K tokens: 8192 pages of block keys, ~54 per scorer CTA, more than its 22-stage
+    # ring, so right after filling the ring the producer waits on a page its consumers cannot have
+    # released yet, and gives up
+    cfg = dataclasses.replace(syn.DECODE_PARITY, B=4, Hkv=1, Hq=8, ctx_list=(262144,) * 4, max_ctx=262144, seed=41)
+    d = syn.make_decode(cfg, device=DEV)
+    d_dev = _to_dev(d)
+    try:
+        qb.debug_set_wait_limit_ns(1)
+        _, ws = _gpu_indexer(d_dev, cfg)
+    finally:
+        qb.debug_set_wait_limit_ns(0)
+    assert qb.last_device_error(ws) & 1, "bit 0 (a wait ran out) must be set"
+    torch.cuda.synchronize()  # the context is still usable
+    cfg2 = syn.DECODE_PARITY
+    d2 = syn.make_decode(cfg2)
+    d2_np = _np(d2)
+    pool_np = d2_np["pool"].copy()
+    d2_dev = _to_dev(d2)
+    ind, ws2 = _gpu_indexer(d2_dev, cfg2)
+    ref, sc = _oracle_indexer(d2_np, pool_np, cfg2)
+    g = to_np(ind)[:, 0]
+    for b in range(cfg2.B):
+        L = int(d2_np["ctx"][b])
+        compare_selection(g[b], ref[b], sc[b], L - 1, cfg2.ratio, cfg2.budget)
+    assert qb.last_device_error(ws2) == 0
+
+
 def _state(pool, pt, b, L, cfg):
     """Compact indexer state of sequence b before decoding token L-1 (torch gathers of input data)."""
     t = L - 1
