@@ -215,7 +215,7 @@ __device__ __noinline__ void score_rows(const SelArgs& a, float* smem, int b, in
       }
       const float* kt = kb_s + (kc & 1) * kTile * kKS;
       const float* qk = q_s + static_cast<size_t>(kc * kKC) * kRows * kHI + warp * kHI;
-#pragma unroll 4
+#pragma unroll  // the whole chunk: loads of later dims in flight while earlier ones multiply
       for (int kp = 0; kp < kKC / 2; ++kp) {  // two dims per step: 16 key values, 16 query values, 128 FMAs in 64 pair FMAs
         float2 kv[8];
 #pragma unroll
