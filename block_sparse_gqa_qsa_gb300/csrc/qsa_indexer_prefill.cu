@@ -183,14 +183,18 @@ __device__ __noinline__ void score_rows(const SelArgs& a, float* smem, int b, in
   // so a block's score does not depend on where the block sits in a tile.
   const __half* kb_g = a.kbar + static_cast<size_t>(b) * a.nbmax * DI;
   const int ntiles = (n_hi + kTile - 1) / kTile;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  // the first chunk of each tile is fetched during the previous tile's last chunk
+  uint4 pre0 = tid < n_hi ? __ldg(reinterpret_cast<const uint4*>(kb_g + static_cast<size_t>(tid) * DI)) : zero;
+  uint4 pre1 = tid < n_hi ? __ldg(reinterpret_cast<const uint4*>(kb_g + static_cast<size_t>(tid) * DI) + 1) : zero;
   for (int tile = 0; tile < ntiles; ++tile) {
     const int gbase = tile * kTile;
     const int gl = gbase + tid;  // block staged by this thread
     const bool gok = gl < n_hi;
     const uint4* src = reinterpret_cast<const uint4*>(kb_g + static_cast<size_t>(gok ? gl : 0) * DI);
-    const uint4 zero = make_uint4(0, 0, 0, 0);
-    uint4 pre0 = gok ? __ldg(src) : zero;
-    uint4 pre1 = gok ? __ldg(src + 1) : zero;
+    const int gn = gl + kTile;  // this thread's block of the next tile
+    const bool nok = tile + 1 < ntiles && gn < n_hi;
+    const uint4* nsrc = reinterpret_cast<const uint4*>(kb_g + static_cast<size_t>(nok ? gn : 0) * DI);
     uint64_t acc[8][kHI / 2];  // heads (2j, 2j+1) of block lane + 32 m as one fp32 pair
 #pragma unroll
     for (int m = 0; m < 8; ++m)
@@ -212,6 +216,9 @@ __device__ __noinline__ void score_rows(const SelArgs& a, float* smem, int b, in
       if (kc + 1 < DI / kKC) {
         pre0 = gok ? __ldg(src + 2 * (kc + 1)) : zero;
         pre1 = gok ? __ldg(src + 2 * (kc + 1) + 1) : zero;
+      } else {
+        pre0 = nok ? __ldg(nsrc) : zero;
+        pre1 = nok ? __ldg(nsrc + 1) : zero;
       }
       const float* kt = kb_s + (kc & 1) * kTile * kKS;
       const float* qk = q_s + static_cast<size_t>(kc * kKC) * kRows * kHI + warp * kHI;
