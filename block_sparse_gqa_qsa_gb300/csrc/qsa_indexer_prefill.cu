@@ -16,7 +16,7 @@
 //                          whole CTA: index-query prep (fp32, angles reduced
 //                          in integer turns), block scores on the CUDA cores
 //                          (fp32 FMA, a register-tiled contraction of 8 rows x
-//                          8 heads against 256-block tiles staged in shared
+//                          8 heads against 128-block tiles staged in shared
 //                          memory, heads paired in fp32x2 FMAs), the
 //                          relu/head sum into the CTA's own score
 //                          slot and a 256-bin histogram of the score bits per
@@ -80,9 +80,10 @@ struct SelArgs {
 
 constexpr int kRows = kPrefillRowsPerCta;  // rows per work item (one warp each)
 constexpr int kThreads = 256;
-constexpr int kTile = 256;                  // blocks per score tile (8 per lane)
-constexpr int kKC = 16;                     // key dims staged per step
-constexpr int kKS = kKC + 2;                // padded row stride: float2 reads and writes are conflict-free
+constexpr int kTile = 128;                  // blocks per score tile (4 per lane)
+constexpr int kBPL = kTile / 32;            // blocks per lane
+constexpr int kKC = 32;                     // key dims staged per step
+constexpr int kKS = kKC + 2;                // padded row stride (17 x 8 bytes): float2 reads are conflict-free
 constexpr int kHI = 8;                      // heads per thread tile (Hi <= 8, extra heads are zero)
 constexpr int kBins = 256;                  // per-row histogram of the score bits, filled while scoring
 constexpr int kBinBase = 123 * 16;          // (bits >> 19) of 2^-4: bin 0 holds smaller scores, bin 255 2^12 and up
@@ -108,7 +109,7 @@ constexpr size_t select_smem_bytes() {
   return sizeof(float) * (static_cast<size_t>(DI) * kRows * kHI + 2 * kTile * kKS + kRows * DI + kRows * 128 +
                           kRows * kBins);
 }
-static_assert(kRows * kCandCap <= 2 * kTile * kKS, "candidate keys reuse the key tiles");
+static_assert(kRows * kCandCap <= 64 * kRows * kHI + 2 * kTile * kKS, "candidate keys reuse the query and key tiles");
 
 // Index-query prep and block scores of the live rows [t0, t0 + nlive) of
 // sequence b against blocks [0, n_hi): each warp owns one row; the rows that
@@ -178,32 +179,33 @@ __device__ __noinline__ void score_rows(const SelArgs& a, float* smem, int b, in
   __syncthreads();
 
   // ---------------------------------------------------------- block scores
-  // Lane owns blocks lane + 32 m (m < 8) of the tile, for its warp's row
-  // and all kHI heads: 64 accumulators, each a plain ascending-k FMA chain,
+  // Lane owns blocks lane + 32 m (m < kBPL) of the tile, for its warp's row
+  // and all kHI heads: 32 accumulators, each a plain ascending-k FMA chain,
   // so a block's score does not depend on where the block sits in a tile.
   const __half* kb_g = a.kbar + static_cast<size_t>(b) * a.nbmax * DI;
   const int ntiles = (n_hi + kTile - 1) / kTile;
   const uint4 zero = make_uint4(0, 0, 0, 0);
   // the first chunk of each tile is fetched during the previous tile's last chunk
-  uint4 pre0 = tid < n_hi ? __ldg(reinterpret_cast<const uint4*>(kb_g + static_cast<size_t>(tid) * DI)) : zero;
-  uint4 pre1 = tid < n_hi ? __ldg(reinterpret_cast<const uint4*>(kb_g + static_cast<size_t>(tid) * DI) + 1) : zero;
+  const uint4* src0 = reinterpret_cast<const uint4*>(kb_g + static_cast<size_t>(tid >> 1) * DI) + 2 * (tid & 1);
+  uint4 pre0 = (tid >> 1) < n_hi ? __ldg(src0) : zero;
+  uint4 pre1 = (tid >> 1) < n_hi ? __ldg(src0 + 1) : zero;
   for (int tile = 0; tile < ntiles; ++tile) {
     const int gbase = tile * kTile;
-    const int gl = gbase + tid;  // block staged by this thread
+    const int gl = gbase + (tid >> 1);  // block this thread stages 8 dims (half a chunk) of
     const bool gok = gl < n_hi;
-    const uint4* src = reinterpret_cast<const uint4*>(kb_g + static_cast<size_t>(gok ? gl : 0) * DI);
+    const uint4* src = reinterpret_cast<const uint4*>(kb_g + static_cast<size_t>(gok ? gl : 0) * DI) + 2 * (tid & 1);
     const int gn = gl + kTile;  // this thread's block of the next tile
     const bool nok = tile + 1 < ntiles && gn < n_hi;
-    const uint4* nsrc = reinterpret_cast<const uint4*>(kb_g + static_cast<size_t>(nok ? gn : 0) * DI);
-    uint64_t acc[8][kHI / 2];  // heads (2j, 2j+1) of block lane + 32 m as one fp32 pair
+    const uint4* nsrc = reinterpret_cast<const uint4*>(kb_g + static_cast<size_t>(nok ? gn : 0) * DI) + 2 * (tid & 1);
+    uint64_t acc[kBPL][kHI / 2];  // heads (2j, 2j+1) of block lane + 32 m as one fp32 pair
 #pragma unroll
-    for (int m = 0; m < 8; ++m)
+    for (int m = 0; m < kBPL; ++m)
 #pragma unroll
       for (int j = 0; j < kHI / 2; ++j) acc[m][j] = 0ull;
 
 #pragma unroll 1
     for (int kc = 0; kc < DI / kKC; ++kc) {
-      float2* dst = reinterpret_cast<float2*>(kb_s + (kc & 1) * kTile * kKS + tid * kKS);
+      float2* dst = reinterpret_cast<float2*>(kb_s + (kc & 1) * kTile * kKS + (tid >> 1) * kKS + (tid & 1) * 16);
       dst[0] = bits_to_float2(pre0.x);
       dst[1] = bits_to_float2(pre0.y);
       dst[2] = bits_to_float2(pre0.z);
@@ -214,8 +216,8 @@ __device__ __noinline__ void score_rows(const SelArgs& a, float* smem, int b, in
       dst[7] = bits_to_float2(pre1.w);
       __syncthreads();
       if (kc + 1 < DI / kKC) {
-        pre0 = gok ? __ldg(src + 2 * (kc + 1)) : zero;
-        pre1 = gok ? __ldg(src + 2 * (kc + 1) + 1) : zero;
+        pre0 = gok ? __ldg(src + 4 * (kc + 1)) : zero;
+        pre1 = gok ? __ldg(src + 4 * (kc + 1) + 1) : zero;
       } else {
         pre0 = nok ? __ldg(nsrc) : zero;
         pre1 = nok ? __ldg(nsrc + 1) : zero;
@@ -224,9 +226,9 @@ __device__ __noinline__ void score_rows(const SelArgs& a, float* smem, int b, in
       const float* qk = q_s + static_cast<size_t>(kc * kKC) * kRows * kHI + warp * kHI;
 #pragma unroll  // the whole chunk: loads of later dims in flight while earlier ones multiply
       for (int kp = 0; kp < kKC / 2; ++kp) {  // two dims per step: 16 key values, 16 query values, 128 FMAs in 64 pair FMAs
-        float2 kv[8];
+        float2 kv[kBPL];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) kv[m] = *reinterpret_cast<const float2*>(kt + (lane + 32 * m) * kKS + kp * 2);
+        for (int m = 0; m < kBPL; ++m) kv[m] = *reinterpret_cast<const float2*>(kt + (lane + 32 * m) * kKS + kp * 2);
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
           // the 8 heads' query values as 4 fp32 pairs; each pair FMA is two independent fp32 FMAs,
@@ -234,7 +236,7 @@ __device__ __noinline__ void score_rows(const SelArgs& a, float* smem, int b, in
           const ulonglong2* qp = reinterpret_cast<const ulonglong2*>(qk + (kp * 2 + kk) * kRows * kHI);
           const ulonglong2 qa = qp[0], qb = qp[1];
 #pragma unroll
-          for (int m = 0; m < 8; ++m) {
+          for (int m = 0; m < kBPL; ++m) {
             const float kval = kk == 0 ? kv[m].x : kv[m].y;
             const uint64_t k2 = pack_f2(kval, kval);
             acc[m][0] = ffma2(qa.x, k2, acc[m][0]);
@@ -247,7 +249,7 @@ __device__ __noinline__ void score_rows(const SelArgs& a, float* smem, int b, in
     }
     if (srow) {
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
+      for (int m = 0; m < kBPL; ++m) {
         const int g = gbase + lane + 32 * m;
         if (g < n_c) {
           float sc = 0.f;
@@ -499,7 +501,7 @@ __device__ __forceinline__ void write_row(const SelArgs& a, int32_t* out, int t,
 // first and the run ends on rows that only write lists.  Each warp owns one
 // row of the group.  A group whose last live row sees more than `budget`
 // complete blocks is scored by the whole CTA (query prep, then the register
-// tiled contraction against 256-block tiles of fp32 keys staged in shared
+// tiled contraction against 128-block tiles of fp32 keys staged in shared
 // memory); each selecting row's scores go to the CTA's own slot of the
 // workspace and into its warp's 256-bin histogram.  Each warp then finds its
 // row's cut (the bin from the histogram, then narrowing passes over the
@@ -515,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_select_kernel(const SelAr
   const int ratio = R > 0 ? R : a.ratio;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint32_t* hist = hist_s + warp * kBins;
-  uint32_t* cand = reinterpret_cast<uint32_t*>(kb_s) + warp * kCandCap;  // valid once scoring is done
+  uint32_t* cand = reinterpret_cast<uint32_t*>(smem) + warp * kCandCap;  // query and key tiles, free once scored
   float* srow = a.scores + (static_cast<size_t>(blockIdx.x) * kRows + warp) * a.nbmax;
   if (tid == 0) item_s[0] = atomicAdd(a.queue, 1);
   __syncthreads();
@@ -538,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_select_kernel(const SelAr
 #pragma unroll
       for (int j = 0; j < kBins / 32; ++j) hist[lane * (kBins / 32) + j] = 0u;
       score_rows<DI>(a, smem, b, t0, nlive, n_hi, selects ? srow : nullptr, n_c, hist);
-      __syncthreads();  // the key tiles are free: they hold the candidate keys from here on
+      __syncthreads();  // the query and key tiles are free: they hold the candidate keys from here on
       if (selects) row_cut(srow, n_c, a.budget, hist, cand, cut, quota);
     }
     if (t < a.S) write_row<R>(a, a.indices + (static_cast<size_t>(b) * a.S + t) * a.topK, t, L, srow, cut, quota);
