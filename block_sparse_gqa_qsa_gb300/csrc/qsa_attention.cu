@@ -34,6 +34,12 @@ constexpr int kOStride = 132;  // padded fp32 row of the warp-merge buffer
 // Byte offset of 16-byte chunk `c` of row `r` in a [rows][256 B] tile (XOR swizzle
 // over 8-row groups so ldmatrix reads are bank-conflict free).
 __device__ __forceinline__ uint32_t swz(int r, int c) { return r * 256 + ((c ^ (r & 7)) << 4); }
+// K and V tiles: two planes of 64 rows x 128 bytes (dims 0..63, then 64..127),
+// chunk c & 7 of row r at 16-byte slot (c & 7) ^ (r & 7) of its 128-byte row;
+// 8 consecutive rows of one chunk sit in 8 different bank groups.
+__device__ __forceinline__ uint32_t kv_off(int r, int c) {
+  return (c >> 3) * (kKeys * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
 
 // The element type of Q/K/V/O: fp16, or bf16 (kBf16).  Copies move the 16-bit
 // values as they are; only the MMA, the rounding of P and the output differ.
@@ -110,7 +116,7 @@ __device__ __forceinline__ void attend16(WarpAcc<NT>& A, uint32_t k_tile, uint32
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     uint32_t a[4];
-    ldsm_x4(k_tile + swz(kr0 + (lane & 7) + 8 * (mi & 1), 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
+    ldsm_x4(k_tile + kv_off(kr0 + (lane & 7) + 8 * (mi & 1), 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) mma_tile<kBf16>(s[nt], a, qf[nt][ks][0], qf[nt][ks][1]);
   }
@@ -148,7 +154,7 @@ __device__ __forceinline__ void attend16(WarpAcc<NT>& A, uint32_t k_tile, uint32
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
     uint32_t a[4];
-    ldsm_x4_t(v_tile + swz(kr0 + (lane & 7) + 8 * (mi >> 1), 2 * mt + (mi & 1)), a[0], a[1], a[2], a[3]);
+    ldsm_x4_t(v_tile + kv_off(kr0 + (lane & 7) + 8 * (mi >> 1), 2 * mt + (mi & 1)), a[0], a[1], a[2], a[3]);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) mma_tile<kBf16>(A.o[mt][nt], a, pb[nt][0], pb[nt][1]);
   }
@@ -294,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_
   const __half* kbase = a.k + head_off;
   const __half* vbase = a.v + head_off;
   const int tok_stride = a.Hkv * kD;                   // elements between consecutive tokens
-  const uint32_t slot0 = swz(tid >> 4, ch);           // key r*8 + tid/16 sits at slot0 + r * 2048
+  const uint32_t slot0 = kv_off(tid >> 4, ch);        // key r*8 + tid/16 sits at slot0 + r * 1024
   auto issue = [&](int tile, int stage) {
     const uint32_t kdst = ring + stage * 2 * kTileBytes + slot0;
     const uint32_t vdst = kdst + kTileBytes;
@@ -306,8 +312,8 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_
       const int j = idv[r];
       const bool ok = j >= 0;
       const size_t off = static_cast<size_t>(ok ? j : 0) * tok_stride;
-      cp_async16(kdst + r * 8 * 256, kbase + off, ok);
-      cp_async16(vdst + r * 8 * 256, vbase + off, ok);
+      cp_async16(kdst + r * 8 * 128, kbase + off, ok);
+      cp_async16(vdst + r * 8 * 128, vbase + off, ok);
     }
   };
   uint32_t qf[NT][8][2];
@@ -477,8 +483,8 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_k
         const int key = (4 * hf + rr) * 8 + (tid >> 4);
         const long long ko = kov[rr], vo = vov[rr];
         const bool ok = ko >= 0;
-        cp_async16(kdst + swz(key, ch), a.pool + (ok ? ko : 0) + ch * 8, ok);
-        cp_async16(vdst + swz(key, ch), a.pool + (ok ? vo : 0) + ch * 8, ok);
+        cp_async16(kdst + kv_off(key, ch), a.pool + (ok ? ko : 0) + ch * 8, ok);
+        cp_async16(vdst + kv_off(key, ch), a.pool + (ok ? vo : 0) + ch * 8, ok);
       }
     }
   };
