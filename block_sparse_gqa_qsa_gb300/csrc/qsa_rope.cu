@@ -206,7 +206,9 @@ __global__ void __launch_bounds__(kRopeThreads) rope_qkv_kernel(const RopeArgs a
     cp_async_wait<kRopeStages - 1>();  // this thread's chunks of token n have landed
     __syncwarp();                      // the warp's coefficients are visible
     const uint4* row = ring + (n % kRopeStages) * nchunk;
-    // warp-uniform trip count: every lane takes part in the group shuffles; lanes past the end carry zeros
+    // warp-uniform trip count: every lane takes part in the group shuffles; lanes past the end carry zeros.
+    // Two chunks at a time interleave their shuffle chains.
+#pragma unroll 2
     for (int c0 = warp * 32; c0 < nchunk; c0 += kRopeThreads) {
       const int c = c0 + lane;
       const bool in = c < nchunk;
