@@ -58,8 +58,8 @@ def f32(x):
 # DRAM read+write bytes of one sparse_prefill_kernel launch on the headline workload, from the ncu
 # capture summarised under profiles/.  Reported only while the kernel's sources hash to the value
 # they had when the counters were taken (None: no capture of the current sources yet).
-PROFILED_TRAFFIC = {"bytes": 823_700_992 + 514_093_056, "sources": ("qsa_attention.cu", "qsa_device.cuh"),
-                    "sha256": "ea3d6a75382ea17fa4468b1acd6a75a7a2deafbf89647787561d162ffa0dd71f"}
+PROFILED_TRAFFIC = {"bytes": 823_797_504 + 514_002_176, "sources": ("qsa_attention.cu", "qsa_device.cuh"),
+                    "sha256": "32c8a3847dc1800258207f861ef2d1d3c2c072ae26ae00bcf9c4b6b4fd1357ee"}
 
 
 def profiled_traffic():
@@ -470,46 +470,53 @@ def run_ours(args, rank, world, dev):
     ifma = indexer_fma(cfg, ctx)
 
     # End to end through the C ABI: every step copies its inputs from pinned host memory and its output back.
-    # Two device buffer sets; a copy stream moves step i+1's inputs and step i's output while step i computes
-    # on the compute stream (events order the reuse of each set).
+    # Two device buffer sets; one copy stream moves step i+1's inputs and another step i's output while step i
+    # computes on the compute stream, so the two directions use separate copy engines (events order the reuse
+    # of each set).
     pinned = {k: v.pin_memory() for k, v in pf.host.items()}
     out_host = [torch.empty(pf.out.shape, dtype=pf.out.dtype).pin_memory() for _ in range(2)]
     dev_in = [{k: torch.empty_like(v, device=dev) for k, v in pf.host.items()} for _ in range(2)]
     dev_out = [torch.empty_like(pf.out) for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
     d2h = out_host[0].numel() * out_host[0].element_size()
-    comp, copy = torch.cuda.current_stream(), torch.cuda.Stream()
+    comp, copy_in, copy_out = torch.cuda.current_stream(), torch.cuda.Stream(), torch.cuda.Stream()
     n_e2e = max(args.steps, 4)
 
     def e2e_run(n):
         in_ready = [torch.cuda.Event() for _ in range(2)]
         done = [torch.cuda.Event() for _ in range(2)]
+        out_done = [torch.cuda.Event() for _ in range(2)]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        copy.wait_stream(comp)
-        e0.record(copy)
+        copy_in.wait_stream(comp)
+        copy_out.wait_stream(comp)
+        e0.record(copy_in)
 
         def h2d_step(i):
-            with torch.cuda.stream(copy):
+            with torch.cuda.stream(copy_in):
                 if i >= 2:
-                    copy.wait_event(done[i % 2])  # set i % 2 was read by step i - 2
+                    copy_in.wait_event(done[i % 2])  # set i % 2 was read by step i - 2
                 for k in dev_in[i % 2]:
                     dev_in[i % 2][k].copy_(pinned[k], non_blocking=True)
-                in_ready[i % 2].record(copy)
+                in_ready[i % 2].record(copy_in)
 
         h2d_step(0)
         for i in range(n):
             if i + 1 < n:
                 h2d_step(i + 1)
             comp.wait_event(in_ready[i % 2])
+            if i >= 2:
+                comp.wait_event(out_done[i % 2])  # step i - 2's output has left dev_out[i % 2]
             pf.indexer(dev_in[i % 2])
             pf.attention(dev_in[i % 2], dev_out[i % 2])
             done[i % 2].record(comp)
-            with torch.cuda.stream(copy):
-                copy.wait_event(done[i % 2])
+            with torch.cuda.stream(copy_out):
+                copy_out.wait_event(done[i % 2])
                 out_host[i % 2].copy_(dev_out[i % 2], non_blocking=True)
-        e1.record(copy)
+                out_done[i % 2].record(copy_out)
+        copy_out.wait_stream(copy_in)
+        e1.record(copy_out)
         e1.synchronize()
-        comp.wait_stream(copy)
+        comp.wait_stream(copy_out)
         return e0.elapsed_time(e1) / n
 
     e2e_run(3)  # warm-up
@@ -784,8 +791,8 @@ def main():
             "attention_impl_ab": r["attention_impl_ab"],
             "rope_qkv": r["rope_qkv"],
             "e2e": {"value": r["e2e"], "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
-                    "note": "each step copies its inputs from pinned host memory and its output back; a second "
-                            "stream overlaps step i+1's input copy and step i's output copy with step i's kernels"},
+                    "note": "each step copies its inputs from pinned host memory and its output back; two more "
+                            "streams overlap step i+1's input copy and step i's output copy with step i's kernels"},
             "cpu_baseline": cpu, "clocks": r["clocks"], "gpu_launches": r["launches"],
         }
         print(json.dumps(line), flush=True)
