@@ -628,10 +628,8 @@ __device__ __forceinline__ int f2ord(float x) {
 }
 __device__ __forceinline__ float ord2f(int o) { return __int_as_float(o >= 0 ? o : o ^ 0x7fffffff); }
 
-// Byte offset of 16-byte chunk c (dims 8c .. 8c+7) of key row r in a two-half SW128 tile.
-__device__ __forceinline__ uint32_t sw128h(int r, int c) {
-  return (c >> 3) * kTcHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4);
-}
+// The tcgen05 tiles use the same two-plane SW128 layout as the mma.sync kernels (kv_off, kTcKeys == kKeys).
+static_assert(kTcKeys == kKeys && kTcHalf == kKeys * 128, "one K/V tile layout for both prefill kernels");
 
 template <int NT, bool kBf16>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 6 : 5) sparse_prefill_tc_kernel(const PrefillArgs a) {
@@ -701,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 6 : 5) sparse_prefill_tc_k
   const __half* kbase = a.k + head_off;
   const __half* vbase = a.v + head_off;
   const int tok_stride = a.Hkv * kD;
-  const uint32_t slot0 = sw128h(rsub, ch);
+  const uint32_t slot0 = kv_off(rsub, ch);
   int rows[kTcKeys / 8];  // token ids of this thread's rows of a tile, -1 when skipped
   int key_id;             // lanes 0..15: the id of key 16 w + lane of a tile
   auto load_ids = [&](int tile) {
@@ -822,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 6 : 5) sparse_prefill_tc_k
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       uint32_t av[4];
-      ldsm_x4_t(vt + sw128h(kr0 + (lane & 7) + 8 * (mi >> 1), 2 * mt + (mi & 1)), av[0], av[1], av[2], av[3]);
+      ldsm_x4_t(vt + kv_off(kr0 + (lane & 7) + 8 * (mi >> 1), 2 * mt + (mi & 1)), av[0], av[1], av[2], av[3]);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) mma_tile<kBf16>(o[mt][nt], av, pb[nt][0], pb[nt][1]);
     }
