@@ -137,14 +137,24 @@ __device__ __noinline__ void score_rows(const SelArgs& a, float* smem, int b, in
   {
     constexpr int PER = DI / 32;
     const int r = warp;
+    // every head's raw query and the norm weights, loaded before any is used: one round trip, not kHI
+    float xv[kHI][PER], wv[PER];
+    const __half* xr = a.idxQ + (static_cast<size_t>(b) * a.S + t0 + r) * a.Hi * DI;
+#pragma unroll
+    for (int p = 0; p < PER; ++p) wv[p] = a.wq[lane + 32 * p];
+#pragma unroll
+    for (int h = 0; h < kHI; ++h)
+#pragma unroll
+      for (int p = 0; p < PER; ++p)
+        xv[h][p] = r < nlive && h < a.Hi ? __half2float(xr[h * DI + lane + 32 * p]) : 0.f;
+#pragma unroll
     for (int h = 0; h < kHI; ++h) {
       if (r < nlive && h < a.Hi) {
-        const __half* x = a.idxQ + ((static_cast<size_t>(b) * a.S + t0 + r) * a.Hi + h) * DI;
         float y[PER];
         float ss = 0.f;
 #pragma unroll
         for (int p = 0; p < PER; ++p) {
-          y[p] = __half2float(x[lane + 32 * p]);
+          y[p] = xv[h][p];
           ss = fmaf(y[p], y[p], ss);
         }
 #pragma unroll
@@ -153,7 +163,7 @@ __device__ __noinline__ void score_rows(const SelArgs& a, float* smem, int b, in
 #pragma unroll
         for (int p = 0; p < PER; ++p) {
           const int i = lane + 32 * p;
-          y[p] = y[p] * inv * (1.0f + a.wq[i]);
+          y[p] = y[p] * inv * (1.0f + wv[p]);
           ys_s[r * DI + i] = y[p];
         }
         __syncwarp();
