@@ -101,6 +101,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2)
     ap.add_argument("--B", type=int, default=None, help="override the batch size")
     ap.add_argument("--ctx", type=int, default=None, help="decode: every sequence gets this total length")
+    ap.add_argument("--Hkv", type=int, default=None,
+                    help="decode: KV heads of the pool (Hq becomes 8 * Hkv); fewer heads make the pool smaller with "
+                         "the same block-key stream per sequence")
     ap.add_argument("--impl", choices=("mma", "tcgen05"), default="mma",
                     help="prefill attention: qsa_sparse_prefill (mma.sync) or qsa_sparse_prefill_tcgen05")
     ap.add_argument("--op", choices=("path", "rope", "handoff", "gather"), default="path",
@@ -122,6 +125,8 @@ def main(argv=None):
     elif isinstance(cfg, syn.DecodeConfig):
         if args.ctx is not None:
             cfg = dataclasses.replace(cfg, ctx_lo=args.ctx, ctx_hi=args.ctx, max_ctx=max(args.ctx, 1), ctx_list=None)
+        if args.Hkv is not None:
+            cfg = dataclasses.replace(cfg, Hkv=args.Hkv, Hq=8 * args.Hkv)
         _decode_steps(cfg, args.steps)
     else:
         _prefill_steps(cfg, args.steps, args.impl)
