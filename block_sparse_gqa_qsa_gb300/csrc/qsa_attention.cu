@@ -4,8 +4,9 @@
 //                          BSND Q/K/V ("Cute Dsl Qsa Sparse Runner",
 //                          QsaSparsePrefillParams)
 //   sparse_decode_kernel   one CTA per (split, KV head, sequence) over the paged
-//                          pool, fp32 partials, and the last split to finish
-//                          merges them and resets its counter
+//                          pool, up to 8 splits (fewer when they fit one wave
+//                          of CTAs and 8 do not), fp32 partials, and the last
+//                          split to finish merges them and resets its counter
 //                          (QsaSparseDecodeParams, kMaxSplits = 8,
 //                          kPartialRows = 16)
 //
@@ -17,6 +18,9 @@
 // softmax in fp32 (log2 domain), and O^T += V^T P^T with P^T formed from the S
 // fragments by an in-register 8x8 transpose.  Warps keep independent running
 // (m, l, O) and are merged once at the end.
+#include <algorithm>
+#include <atomic>
+
 #include "qsa_device.cuh"
 #include "qsa_internal.h"
 #include "qsa_tcgen05.cuh"
@@ -394,6 +398,7 @@ struct DecodeArgs {
   int32_t* counters;
   int32_t* status;  // optional error word
   int Hq, Hkv, G, poolHeadDim, numFlatPages, maxPagesPerSeq, topK;
+  int nsplit;                     // slices per (sequence, KV head), 1..kMaxSplits
   int tilesPerSplit, extraTiles;  // split s owns tilesPerSplit (+1 for s < extraTiles) whole 64-key tiles
   int slicePad;                   // slots of the longest slice
   float sl2;
@@ -558,10 +563,10 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_k
       pS[kPartialRows + h] = Lsum;
     }
   }
-  // Last split to arrive merges the kMaxSplits partials and re-arms the counter.
+  // Last split to arrive merges the nsplit partials and re-arms the counter.
   __threadfence();
   __syncthreads();
-  if (tid == 0) misc[4] = atomicAdd(a.counters + b * a.Hkv + kvh, 1) == kMaxSplits - 1;
+  if (tid == 0) misc[4] = atomicAdd(a.counters + b * a.Hkv + kvh, 1) == a.nsplit - 1;
   __syncthreads();
   if (!misc[4]) return;
   __threadfence();
@@ -570,16 +575,24 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_decode_k
   __half* out = a.o + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(kvh) * a.G) * kD;
   for (int e = tid; e < a.G * (kD / 2); e += kThreads) {
     const int h = e / (kD / 2), d = 2 * (e % (kD / 2));
+    // Every slot's loads are issued unconditionally (slots past nsplit re-read
+    // the last one and are weighted 0), so they are all in flight together.
+    float m[kMaxSplits];
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) {
+      const float v = __ldcg(pS0 + min(s, a.nsplit - 1) * 2 * kPartialRows + h);
+      m[s] = s < a.nsplit ? v : -INFINITY;
+    }
     float M = -INFINITY;
 #pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s) M = fmaxf(M, __ldcg(pS0 + s * 2 * kPartialRows + h));
+    for (int s = 0; s < kMaxSplits; ++s) M = fmaxf(M, m[s]);
     float Lsum = 0.f, o0 = 0.f, o1 = 0.f;
 #pragma unroll
     for (int s = 0; s < kMaxSplits; ++s) {
-      const float m = __ldcg(pS0 + s * 2 * kPartialRows + h);
-      const float f = m == -INFINITY ? 0.f : exp2f(m - M);
-      Lsum += f * __ldcg(pS0 + s * 2 * kPartialRows + kPartialRows + h);
-      const float2 ov = __ldcg(reinterpret_cast<const float2*>(pO0 + (s * kPartialRows + h) * kD + d));
+      const int sc = min(s, a.nsplit - 1);
+      const float f = m[s] == -INFINITY ? 0.f : exp2f(m[s] - M);
+      Lsum += f * __ldcg(pS0 + sc * 2 * kPartialRows + kPartialRows + h);
+      const float2 ov = __ldcg(reinterpret_cast<const float2*>(pO0 + (sc * kPartialRows + h) * kD + d));
       o0 += f * ov.x;
       o1 += f * ov.y;
     }
@@ -908,14 +921,57 @@ cudaError_t prefill_nt(const PrefillArgs& a, long long nblocks, cudaStream_t st)
   return cudaGetLastError();
 }
 
+// The list of a (sequence, KV head) is cut into nsplit slices of whole 64-key
+// tiles.  nsplit is kMaxSplits unless that grid needs more than one wave of
+// resident CTAs and a smaller count fits in one: a CTA's list resolution and
+// its partial write take as long as a tile or two, so a second, partial wave
+// of short CTAs costs more than longer slices in a single wave.  It is then
+// lowered to the fewest slices with the same longest slice (33 tiles: 7
+// slices of at most 5 rather than 8), which saves CTAs and partials without
+// lengthening any CTA's chain.
 template <int NT, bool kBf16>
-cudaError_t decode_nt(const DecodeArgs& a, int B, cudaStream_t st) {
-  const size_t smem = decode_smem<NT>(a.slicePad);
-  static const cudaError_t attr = cudaFuncSetAttribute(sparse_decode_kernel<NT, kRingStagesFor<NT>, kBf16>,
-                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+cudaError_t decode_nt(DecodeArgs a, int B, cudaStream_t st) {
+  auto kernel = sparse_decode_kernel<NT, kRingStagesFor<NT>, kBf16>;
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
   if (attr != cudaSuccess) return attr;
-  dim3 grid(kMaxSplits, a.Hkv, B);
-  sparse_decode_kernel<NT, kRingStagesFor<NT>, kBf16><<<grid, kThreads, smem, st>>>(a);
+  const int tiles = (a.topK + kKeys - 1) / kKeys;  // <= kMaxTiles (the list width is validated)
+  auto slice_pad = [&](int ns) { return kKeys * ((tiles + ns - 1) / ns); };
+  // Resident CTAs per SM for a slice of n tiles (its list offsets live in
+  // shared memory): 0 = not queried yet, -1 = does not fit.
+  constexpr int kMaxTiles = 256;
+  static std::atomic<int> per_sm[kMaxTiles + 1];
+  auto slots = [&](int ns) -> long long {
+    const int n = (tiles + ns - 1) / ns;
+    if (n > kMaxTiles) return 0;
+    int r = per_sm[n].load(std::memory_order_relaxed);
+    if (r == 0) {
+      const size_t smem = decode_smem<NT>(slice_pad(ns));
+      int blocks = 0;
+      if (smem > static_cast<size_t>(kMaxDynSmem) ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, kThreads, smem) != cudaSuccess || blocks < 1)
+        r = -1;
+      else
+        r = blocks;
+      per_sm[n].store(r, std::memory_order_relaxed);
+    }
+    return r > 0 ? static_cast<long long>(sm_count()) * r : 0;
+  };
+  const long long pairs = static_cast<long long>(B) * a.Hkv;
+  int ns = std::min(kMaxSplits, tiles);
+  if (pairs * ns > slots(ns))
+    for (int c = ns - 1; c >= 1; --c)
+      if (pairs * c <= slots(c)) {
+        ns = c;
+        break;
+      }
+  ns = (tiles + (tiles + ns - 1) / ns - 1) / ((tiles + ns - 1) / ns);
+  a.nsplit = ns;
+  a.tilesPerSplit = tiles / ns;
+  a.extraTiles = tiles % ns;
+  a.slicePad = slice_pad(ns);
+  dim3 grid(ns, a.Hkv, B);
+  kernel<<<grid, kThreads, decode_smem<NT>(a.slicePad), st>>>(a);
   return cudaGetLastError();
 }
 
@@ -994,10 +1050,6 @@ cudaError_t launch_sparse_decode(const QsaSparseDecodeParams& p, bool bf16) {
   a.numFlatPages = p.numFlatPages;
   a.maxPagesPerSeq = p.maxPagesPerSeq;
   a.topK = p.topK;
-  const int tiles = (p.topK + kKeys - 1) / kKeys;
-  a.tilesPerSplit = tiles / kMaxSplits;
-  a.extraTiles = tiles % kMaxSplits;
-  a.slicePad = kKeys * (a.tilesPerSplit + (a.extraTiles > 0 ? 1 : 0));
   a.sl2 = p.attentionScale * kLog2e;
   cudaStream_t st = static_cast<cudaStream_t>(p.stream);
   if (bf16) return a.G <= 8 ? decode_nt<1, true>(a, p.batchSize, st) : decode_nt<2, true>(a, p.batchSize, st);

@@ -270,9 +270,12 @@ typedef struct {
  * QsaSparseDecodeParams, field for field).  One query token per sequence;
  * K/V rows come from the pool through the page table, and only columns
  * [0, headDim) of a pool row are read.  The list of each (sequence, KV head)
- * is cut into kMaxSplits = 8 contiguous slices; each slice writes an fp32
- * partial (O, m, l) and the last slice to finish merges the eight partials
- * into oPtr and resets its counter to zero.  splitCounters MUST be zero on
+ * is cut into at most kMaxSplits = 8 contiguous slices of whole 64-entry
+ * tiles (fewer when B * numKVHeads * 8 CTAs would not fit in one wave on the
+ * GPU and a smaller count does); each slice writes an fp32 partial (O, m, l)
+ * and the last slice to finish merges the partials into oPtr and resets its
+ * counter to zero.  The slice count depends only on the shapes and the GPU,
+ * so repeated calls give identical bits.  splitCounters MUST be zero on
  * entry (zero-fill the buffer once; every call leaves it zeroed).
  * status (not on the pages; may be NULL): a device int32 that the kernels OR
  * error bits into and never clear -- bit 1 (value 2): a list entry's page id
