@@ -107,8 +107,9 @@ def test_noalloc_matches_workspace_entry_twice(binding, cfg):
 
 @pytest.mark.gpu
 def test_noalloc_small_after_capacity(binding):
-    """The shared scratch after a call at full capacity (256 pairs, 8 splits
-    each): a smaller call with other shapes must find its counters at zero and
+    """The shared scratch after a call at full capacity (256 (sequence, KV
+    head) pairs, the most its partial slots hold): a smaller call with other
+    shapes, and so another slice count, must find its counters at zero and
     match the workspace entry."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
