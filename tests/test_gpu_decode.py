@@ -287,6 +287,36 @@ def test_sparse_decode_parity(Hq, Hkv):
     assert torch.equal(out3.view(torch.int16), out.view(torch.int16))
 
 
+@pytest.mark.parametrize("B", [40, 80, 96, 300])
+def test_sparse_decode_slice_count_follows_the_batch(B):
+    """The slices per (sequence, KV head) follow the batch: at most 8, as many
+    as fit one wave of resident CTAs, then the fewest with the same longest
+    slice.  With a 4-tile list these batches take 4, 2, 1 and (past one wave
+    at any count) 4 slices on a 152-SM GPU.  Each matches the oracle, leaves
+    its counters at zero and repeats bit for bit."""
+    cfg = dataclasses.replace(syn.DECODE_PARITY, name=f"slices_B{B}", B=B, Hq=32, Hkv=4, Hi=4, di=64, rot=32,
+                              budget=63, ctx_lo=1, ctx_hi=300, max_ctx=384, ctx_list=None, seed=60 + B)
+    assert cfg.topK == 255
+    d = syn.make_decode(cfg, device=DEV)
+    d_dev = _to_dev(d)
+    pool, pt = d_dev["pool"], d_dev["page_table"]
+    ctx = d["ctx"].numpy()
+    rng = np.random.default_rng(B)
+    lists = np.full((B, cfg.topK), -1, np.int32)
+    for b in range(B):
+        L = int(ctx[b])
+        lists[b, :min(L, cfg.topK)] = np.sort(rng.permutation(L)[:cfg.topK])
+    lists_dev = torch.from_numpy(lists[:, None, :].copy()).to(DEV)
+    out, ws = _gpu_attention(d_dev, lists_dev, cfg, f32(cfg.scale))
+    o, q = to_np(out)[:, 0], to_np(d_dev["q"])[:, 0]
+    for b in range(B):
+        kr, vr = _rows(pool, pt, b, lists[b], cfg)
+        check_attention(o[b], oracle.attend_rows(q[b], kr, vr, f32(cfg.scale)), f"B={B} seq {b}")
+    assert int(ws[2].abs().sum()) == 0, "split counters must be re-armed to zero"
+    out2, _ = _gpu_attention(d_dev, lists_dev, cfg, f32(cfg.scale), ws)
+    assert torch.equal(out2.view(torch.int16), out.view(torch.int16)), "back-to-back calls must agree bitwise"
+
+
 def test_sparse_decode_page_permutation_and_empty():
     cfg = dataclasses.replace(syn.DECODE_PARITY, B=3, ctx_list=(0, 700, 1500), max_ctx=1536, seed=5)
     d = syn.make_decode(cfg)
