@@ -470,15 +470,24 @@ def run_ours(args, rank, world, dev):
     ifma = indexer_fma(cfg, ctx)
 
     # End to end through the C ABI: every step copies its inputs from pinned host memory and its output back.
-    # Two device buffer sets; one copy stream moves step i+1's inputs and another step i's output while step i
-    # computes on the compute stream, so the two directions use separate copy engines (events order the reuse
-    # of each set).
+    # The inputs are the live rows of the [B, S, ...] tensors (rows t >= L are padding that no kernel reads),
+    # the norm weights and the lengths; the output is the live rows of O.  Two device buffer sets; one copy
+    # stream moves step i+1's inputs and another step i's output while step i computes on the compute stream,
+    # so the two directions use separate copy engines (events order the reuse of each set).
     pinned = {k: v.pin_memory() for k, v in pf.host.items()}
     out_host = [torch.empty(pf.out.shape, dtype=pf.out.dtype).pin_memory() for _ in range(2)]
     dev_in = [{k: torch.empty_like(v, device=dev) for k, v in pf.host.items()} for _ in range(2)]
     dev_out = [torch.empty_like(pf.out) for _ in range(2)]
-    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
-    d2h = out_host[0].numel() * out_host[0].element_size()
+
+    def live_pairs(dst, src):  # (destination, source) views of one tensor's step copy
+        if src.dim() >= 2 and tuple(src.shape[:2]) == (cfg.B, cfg.S):
+            return [(dst[b, :L], src[b, :L]) for b, L in enumerate(ctx) if L > 0]
+        return [(dst, src)]
+
+    in_pairs = [[p for k in pinned for p in live_pairs(dev_in[j][k], pinned[k])] for j in range(2)]
+    out_pairs = [live_pairs(out_host[j], dev_out[j]) for j in range(2)]
+    h2d = sum(s_.numel() * s_.element_size() for _, s_ in in_pairs[0])
+    d2h = sum(s_.numel() * s_.element_size() for _, s_ in out_pairs[0])
     comp, copy_in, copy_out = torch.cuda.current_stream(), torch.cuda.Stream(), torch.cuda.Stream()
     n_e2e = max(args.steps, 4)
 
@@ -495,8 +504,8 @@ def run_ours(args, rank, world, dev):
             with torch.cuda.stream(copy_in):
                 if i >= 2:
                     copy_in.wait_event(done[i % 2])  # set i % 2 was read by step i - 2
-                for k in dev_in[i % 2]:
-                    dev_in[i % 2][k].copy_(pinned[k], non_blocking=True)
+                for d_, s_ in in_pairs[i % 2]:
+                    d_.copy_(s_, non_blocking=True)
                 in_ready[i % 2].record(copy_in)
 
         h2d_step(0)
@@ -511,7 +520,8 @@ def run_ours(args, rank, world, dev):
             done[i % 2].record(comp)
             with torch.cuda.stream(copy_out):
                 copy_out.wait_event(done[i % 2])
-                out_host[i % 2].copy_(dev_out[i % 2], non_blocking=True)
+                for d_, s_ in out_pairs[i % 2]:
+                    d_.copy_(s_, non_blocking=True)
                 out_done[i % 2].record(copy_out)
         copy_out.wait_stream(copy_in)
         e1.record(copy_out)
@@ -527,7 +537,7 @@ def run_ours(args, rank, world, dev):
         e2e_ms = e2e_run(n_e2e)
     torch.cuda.synchronize()
     e2e_value = whole_job_rate(tok, world, max_over_ranks(e2e_ms, world, dev))
-    del pinned, out_host, dev_in, dev_out
+    del pinned, out_host, dev_in, dev_out, in_pairs, out_pairs
 
     # bf16 surface of the prefill attention: the same workload and lists with bfloat16 Q/K/V/O
     t16 = {n: pf.t[n].to(torch.bfloat16) for n in ("q", "k", "v")}
@@ -791,8 +801,10 @@ def main():
             "attention_impl_ab": r["attention_impl_ab"],
             "rope_qkv": r["rope_qkv"],
             "e2e": {"value": r["e2e"], "unit": UNIT, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
-                    "note": "each step copies its inputs from pinned host memory and its output back; two more "
-                            "streams overlap step i+1's input copy and step i's output copy with step i's kernels"},
+                    "note": "each step copies its inputs from pinned host memory (the live rows of q/k/v/idxQ/idxK, "
+                            "the norm weights and the lengths; rows at or past a sequence's length are padding no "
+                            "kernel reads) and the live rows of O back; two more streams overlap step i+1's input "
+                            "copy and step i's output copy with step i's kernels"},
             "cpu_baseline": cpu, "clocks": r["clocks"], "gpu_launches": r["launches"],
         }
         print(json.dumps(line), flush=True)
