@@ -222,7 +222,15 @@ def _rows(pool, pt, b, lst, cfg):
     return to_np(kr), to_np(vr)
 
 
-@pytest.mark.parametrize("cfg", [syn.DECODE_32, syn.DECODE_LONG], ids=lambda c: c.name)
+# The largest decode batch (1024): every 16th sequence holds ~2000 tokens and the others 1-3, which have
+# no complete block.  A scorer CTA's pages then span up to 17 sequences, so the queries of those past its
+# shared-memory cache of 8 are read from the workspace.
+DECODE_SPARSE = dataclasses.replace(
+    syn.DECODE_PARITY, name="decode_B1024_sparse_pages", B=1024, max_ctx=2048, seed=71,
+    ctx_list=tuple(2000 + b % 5 if b % 16 == 0 else 1 + b % 3 for b in range(1024)))
+
+
+@pytest.mark.parametrize("cfg", [syn.DECODE_32, syn.DECODE_LONG, DECODE_SPARSE], ids=lambda c: c.name)
 def test_decode_full_size(cfg):
     d = syn.make_decode(cfg, device=DEV)
     d_dev = _to_dev(d)
