@@ -291,6 +291,23 @@ def test_sparse_prefill_group_sizes_and_list_shapes(Hq, Hkv, impl):
     _check_rows(out, t_np, lists, cfg, rows, f32(0.1), "non-causal")
 
 
+def test_prefill_many_sequences():
+    """Forty sequences of random length up to 1100, four of them 0, 1, 3 and 4 tokens long: the indexer's
+    work items cycle over every sequence (lists checked on every row) and both attention kernels run the
+    indexer's own lists (checked on every seventh row)."""
+    cfg = dataclasses.replace(syn.PREFILL_PARITY, name="many_seqs", B=40, S=1100, budget=64, ctx_lo=0,
+                              ctx_hi=1100, seed=9)
+    t_np, t_dev = _inputs(cfg)
+    t_np["ctx"][:4] = (0, 1, 3, 4)  # rows past these lengths keep data: they are never read either way
+    t_dev["ctx"] = torch.from_numpy(t_np["ctx"]).to(DEV)
+    ind, _ = _check_indexer(cfg, t_np, t_dev)
+    lists = to_np(ind)
+    rows = np.arange(0, cfg.B * cfg.S, 7, dtype=np.int64)
+    for impl in IMPLS:
+        out = _gpu_attention(t_dev, ind, cfg, f32(cfg.scale), impl)
+        _check_rows(out, t_np, lists, cfg, rows, f32(cfg.scale), f"many sequences ({impl})")
+
+
 @pytest.mark.parametrize("impl", IMPLS)
 def test_sparse_prefill_special_lists(impl):
     cfg = dataclasses.replace(syn.PREFILL_PARITY, B=1, S=300, ctx_lo=None, ctx_hi=None)
