@@ -320,7 +320,7 @@ struct GlobalKeys {
   template <class F>
   __device__ __forceinline__ void each(F&& f) const {
     const int lane = threadIdx.x & 31;
-    constexpr int U = 8;
+    constexpr int U = 16;
     for (int g0 = 0; g0 < n; g0 += 32 * U) {
       uint32_t k[U];
 #pragma unroll
@@ -395,7 +395,7 @@ __device__ __forceinline__ void row_cut(const float* srow, int n_c, int budget, 
   // stage the range's nT <= kCandCap keys, then narrow in shared memory
   {
     int at = 0;
-    constexpr int U = 8;
+    constexpr int U = 16;
     for (int g0 = 0; g0 < n_c; g0 += 32 * U) {
       uint32_t k[U];
 #pragma unroll
@@ -469,7 +469,7 @@ __device__ __forceinline__ void write_row(const SelArgs& a, int32_t* out, int t,
   }
   const unsigned below = (1u << lane) - 1u;
   int pos = 0;
-  constexpr int U = 4;
+  constexpr int U = 16;
   for (int g0 = 0; g0 < n_c; g0 += 32 * U) {
     uint32_t k[U];
 #pragma unroll
