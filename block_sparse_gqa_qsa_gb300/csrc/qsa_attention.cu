@@ -264,19 +264,19 @@ __global__ void __launch_bounds__(kThreads, STAGES == 1 ? 5 : 3) sparse_prefill_
     cp_async16(q_tile + swz(r, c), qsrc + (ok ? r : 0) * kD + c * 8, ok);
   }
   cp_async_commit();
-  // Stage the list, four loads per thread in flight; entries outside [0, L) are skipped.
+  // Stage the list, eight loads per thread in flight; entries outside [0, L) are skipped.
   const int32_t* lst = a.indices + static_cast<size_t>(bt) * a.topK;
   int last = -1;
   bool bad = false;
-  for (int i0 = tid; i0 < a.topKpad; i0 += 4 * kThreads) {
-    int jv[4];
+  for (int i0 = tid; i0 < a.topKpad; i0 += 8 * kThreads) {
+    int jv[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
       const int i = i0 + u * kThreads;
       jv[u] = i < a.topK ? __ldg(lst + i) : -1;
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
       const int i = i0 + u * kThreads;
       if (i < a.topKpad) {
         const bool ok = static_cast<unsigned>(jv[u]) < static_cast<unsigned>(L);
