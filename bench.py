@@ -419,6 +419,15 @@ def time_prefill(pf, flush, clk, steps):
     return t_idx, t_att, t_step
 
 
+def live_copies(cfg, ctx, dst, src):
+    """(destination, source) views of one tensor's copy in an end-to-end step: the live rows
+    [0, L) of each sequence for the [B, S, ...] tensors (rows at or past L are padding that no
+    kernel reads), the whole tensor otherwise."""
+    if src.dim() >= 2 and tuple(src.shape[:2]) == (cfg.B, cfg.S):
+        return [(dst[b, :L], src[b, :L]) for b, L in enumerate(ctx) if L > 0]
+    return [(dst, src)]
+
+
 def attention_roofline(gbytes, flops, att_ms, l2_gbs, hbm_peak, mma_peak, traffic):
     """The attention kernel against the resource that binds it: its gathered K/V rows come from L2
     (one sequence's K/V is at most 16.8 MB here), so achieved = algorithmic bytes / kernel time is set
@@ -479,13 +488,8 @@ def run_ours(args, rank, world, dev):
     dev_in = [{k: torch.empty_like(v, device=dev) for k, v in pf.host.items()} for _ in range(2)]
     dev_out = [torch.empty_like(pf.out) for _ in range(2)]
 
-    def live_pairs(dst, src):  # (destination, source) views of one tensor's step copy
-        if src.dim() >= 2 and tuple(src.shape[:2]) == (cfg.B, cfg.S):
-            return [(dst[b, :L], src[b, :L]) for b, L in enumerate(ctx) if L > 0]
-        return [(dst, src)]
-
-    in_pairs = [[p for k in pinned for p in live_pairs(dev_in[j][k], pinned[k])] for j in range(2)]
-    out_pairs = [live_pairs(out_host[j], dev_out[j]) for j in range(2)]
+    in_pairs = [[p for k in pinned for p in live_copies(cfg, ctx, dev_in[j][k], pinned[k])] for j in range(2)]
+    out_pairs = [live_copies(cfg, ctx, out_host[j], dev_out[j]) for j in range(2)]
     h2d = sum(s_.numel() * s_.element_size() for _, s_ in in_pairs[0])
     d2h = sum(s_.numel() * s_.element_size() for _, s_ in out_pairs[0])
     comp, copy_in, copy_out = torch.cuda.current_stream(), torch.cuda.Stream(), torch.cuda.Stream()

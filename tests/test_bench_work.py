@@ -64,3 +64,25 @@ def test_decode_work_matches_the_oracle_lists():
     assert kbar == sum((L // cfg.ratio) * cfg.di * 2 for L in ctx)
     assert kv == cfg.Hkv * live * 2 * cfg.D * 2, "gathered rows must be the oracle lists' entries"
     assert total == kbar + kv + cfg.B * (2 * cfg.Hq * cfg.D * 2 + cfg.Hi * cfg.di * 2 + cfg.topK * 4 * 2)
+
+
+def test_end_to_end_copies_cover_exactly_the_live_rows():
+    import torch
+    cfg = _ragged_tiny()
+    t = syn.make_prefill(cfg)  # rows at or past each length are NaN
+    ctx = [int(x) for x in t["ctx"]]
+    dst = {k: torch.full_like(v, -7) for k, v in t.items()}
+    pairs = [p for k in t for p in bench.live_copies(cfg, ctx, dst[k], t[k])]
+    for d, s_ in pairs:
+        assert d.is_contiguous() and s_.is_contiguous()
+        d.copy_(s_)
+    want = sum(v.numel() * v.element_size() for k, v in t.items() if k in ("wq", "wk", "ctx"))
+    for k in ("q", "k", "v", "idxQ", "idxK"):
+        row = t[k][0, 0].numel() * t[k].element_size()
+        want += sum(ctx) * row
+        for b, L in enumerate(ctx):
+            assert torch.equal(dst[k][b, :L], t[k][b, :L]), f"{k}: live rows of sequence {b} not copied"
+            assert torch.all(dst[k][b, L:] == -7), f"{k}: padded rows of sequence {b} were copied"
+    assert sum(s_.numel() * s_.element_size() for _, s_ in pairs) == want
+    for k in ("wq", "wk", "ctx"):
+        assert torch.equal(dst[k], t[k])
