@@ -58,8 +58,8 @@ def f32(x):
 # DRAM read+write bytes of one sparse_prefill_kernel launch on the headline workload, from the ncu
 # capture summarised under profiles/.  Reported only while the kernel's sources hash to the value
 # they had when the counters were taken (None: no capture of the current sources yet).
-PROFILED_TRAFFIC = {"bytes": 824_506_112 + 514_541_824, "sources": ("qsa_attention.cu", "qsa_device.cuh"),
-                    "sha256": "bd97fe18ff7feed1f14c793195f1bd694e6b1c26faf73d31481c8378ab312189"}
+PROFILED_TRAFFIC = {"bytes": 823_708_160 + 514_016_000, "sources": ("qsa_attention.cu", "qsa_device.cuh"),
+                    "sha256": "3ce07eda46bb9934e1a396ba9a9eb5df759ba968a49b4f70b5cbe3374d543f5e"}
 
 
 def profiled_traffic():

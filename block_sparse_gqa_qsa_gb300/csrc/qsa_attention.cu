@@ -948,11 +948,14 @@ cudaError_t decode_nt(DecodeArgs a, int B, cudaStream_t st) {
     if (r == 0) {
       const size_t smem = decode_smem<NT>(slice_pad(ns));
       int blocks = 0;
-      if (smem > static_cast<size_t>(kMaxDynSmem) ||
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, kThreads, smem) != cudaSuccess || blocks < 1)
+      if (smem > static_cast<size_t>(kMaxDynSmem)) {
         r = -1;
-      else
-        r = blocks;
+      } else if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, kThreads, smem) != cudaSuccess) {
+        (void)cudaGetLastError();  // a failed query is not the launch's error: this count is just not used
+        r = -1;
+      } else {
+        r = blocks < 1 ? -1 : blocks;
+      }
       per_sm[n].store(r, std::memory_order_relaxed);
     }
     return r > 0 ? static_cast<long long>(sm_count()) * r : 0;
