@@ -218,6 +218,16 @@ def test_validation_rejects_before_launch(binding):
     assert _call(binding, "qsa_sparse_decode", sd) == binding.QSA_ERR_WORKSPACE
     sd.partialO, sd.poolHeadDim = fake, 100
     assert _call(binding, "qsa_sparse_decode", sd) == binding.QSA_ERR_INVALID_ARG
+    sd.poolHeadDim, sd.numQHeads = 256, 60
+    assert _call(binding, "qsa_sparse_decode", sd) == binding.QSA_ERR_INVALID_ARG  # 60 % 8 != 0
+    sd.numQHeads, sd.numKVHeads = 64, 2
+    assert _call(binding, "qsa_sparse_decode", sd) == binding.QSA_ERR_UNSUPPORTED  # a GQA group of 32
+    sd.numKVHeads, sd.topK = 8, 16385
+    assert _call(binding, "qsa_sparse_decode", sd) == binding.QSA_ERR_UNSUPPORTED  # the list of a slice on chip
+    sd.topK, sd.qPtr = 2051, fake + 4
+    assert _call(binding, "qsa_sparse_decode", sd) == binding.QSA_ERR_INVALID_ARG  # q not 16-byte aligned
+    sd.qPtr, sd.indices = fake, None
+    assert _call(binding, "qsa_sparse_decode_bf16", sd) == binding.QSA_ERR_INVALID_ARG
 
 
 def test_binding_refuses_cpu_tensors(binding):
